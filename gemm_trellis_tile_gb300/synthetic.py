@@ -1,0 +1,101 @@
+"""Seeded synthetic inputs for trellis-coded layers.
+
+This module only draws random numbers; it holds none of the method's
+arithmetic.  The same arrays feed the CUDA library and the CPU oracle.
+
+Recipe (per layer): code words uniform over int16; rin, rout ~ N(1, 0.1)
+rounded to fp16; s_in, s_out ~ U(0.98, 1.02) fp32; activations ~ N(0, 1)
+rounded to fp16.  Multi-layer workloads (the gated MLP and the MoE) scale each
+matrix's rout by an exact power of two 2^-k, k = round(log2(sqrt(in) * 1.2441)),
+so that intermediate activations stay inside the fp16 range; 1.2441 is the
+standard deviation of the cb=1 codebook over all 65536 states.
+"""
+
+import math
+import numpy as np
+
+CODEBOOK_STD = 1.2441
+
+
+def overflow_guard_shift(in_features):
+    """k such that rout * 2^-k keeps a random-code layer's output near unit scale."""
+    return int(round(math.log2(math.sqrt(in_features) * CODEBOOK_STD)))
+
+
+def make_linear(rng, in_features, out_features, bits, guard=False):
+    """One trellis-coded linear layer as host numpy arrays."""
+    assert in_features % 128 == 0 and out_features % 128 == 0
+    code = rng.integers(-32768, 32768, size=(in_features // 16, out_features // 16, 16 * bits),
+                        dtype=np.int16)
+    rin = rng.normal(1.0, 0.1, in_features).astype(np.float16)
+    rout = rng.normal(1.0, 0.1, out_features)
+    if guard:
+        rout = rout * 2.0 ** (-overflow_guard_shift(in_features))
+    rout = rout.astype(np.float16)
+    s_in = rng.uniform(0.98, 1.02, in_features).astype(np.float32)
+    s_out = rng.uniform(0.98, 1.02, out_features).astype(np.float32)
+    config = np.array([16, bits, 1, 1, in_features, out_features], dtype=np.int32)
+    return dict(code=code, rin=rin, rout=rout, s_in=s_in, s_out=s_out, config=config,
+                bits=bits, in_features=in_features, out_features=out_features)
+
+
+def make_activations(rng, m, features):
+    return rng.normal(0.0, 1.0, (m, features)).astype(np.float16)
+
+
+def make_mlp(rng, hidden, inter, bits_gate, bits_up, bits_down):
+    """Gated MLP down(silu(gate x) * up x) with the fp16 range guard on every matrix."""
+    return dict(gate=make_linear(rng, hidden, inter, bits_gate, guard=True),
+                up=make_linear(rng, hidden, inter, bits_up, guard=True),
+                down=make_linear(rng, inter, hidden, bits_down, guard=True))
+
+
+def make_moe(rng, num_experts, hidden, inter, bits_choices=(2, 3, 4)):
+    """Routed-expert stack with one shared hidden-side rotation.
+
+    Every expert gets one width b_e drawn uniformly from bits_choices for all
+    three of its matrices.  The hidden side (gate/up input, down output) uses
+    one shared rin/s_in and one shared rout/s_out for all experts; the
+    intermediate side is per expert.
+    """
+    bits = rng.choice(np.asarray(bits_choices, dtype=np.int32), size=num_experts)
+    experts = []
+    for e in range(num_experts):
+        b = int(bits[e])
+        g = make_linear(rng, hidden, inter, b, guard=True)
+        u = make_linear(rng, hidden, inter, b, guard=True)
+        d = make_linear(rng, inter, hidden, b, guard=True)
+        experts.append(dict(gate=g, up=u, down=d, bits=b))
+    shared = make_linear(rng, hidden, hidden, 2)  # only its side vectors are used
+    gk = overflow_guard_shift(inter)
+    return dict(experts=experts, bits=bits, hidden=hidden, inter=inter,
+                rin_hidden=shared["rin"], s_in_hidden=shared["s_in"],
+                rout_hidden=(shared["rout"].astype(np.float64) * 2.0 ** (-gk)).astype(np.float16),
+                s_out_hidden=shared["s_out"])
+
+
+def make_routing(rng, m, num_experts, topk=8):
+    """topk distinct experts per token, uniform; weights = softmax of N(0,1) logits."""
+    ids = np.stack([rng.choice(num_experts, size=topk, replace=False) for _ in range(m)]).astype(np.int32)
+    logits = rng.normal(0.0, 1.0, (m, topk))
+    w = np.exp(logits - logits.max(axis=1, keepdims=True))
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    return ids, w
+
+
+# The five workloads, by shape (seed = 1000 + index).
+WORKLOADS = {
+    0: dict(name="linear 512x512 2-bit", kind="linear", in_features=512, out_features=512, bits=2),
+    1: dict(name="dense gated MLP 5120->17408->5120 (gate 2-bit, up 3-bit, down 3-bit)",
+            kind="mlp", hidden=5120, inter=17408, bits=(2, 3, 3)),
+    2: dict(name="decode sweep: 5120->10240 2-bit and 6144->5120 2-bit",
+            kind="sweep", shapes=((5120, 10240, 2), (6144, 5120, 2)), m=(1, 2, 4, 8, 16)),
+    3: dict(name="routed MoE: 256 experts, 6144->2048->6144, 2/3/4-bit per expert, top-8",
+            kind="moe", experts=256, hidden=6144, inter=2048, topk=8, m=(1, 2, 4, 8)),
+    4: dict(name="prefill M=2048: 5120->17408 3-bit and 17408->5120 3-bit",
+            kind="prefill", m=2048, shapes=((5120, 17408, 3), (17408, 5120, 3))),
+}
+
+
+def seed_for(workload_index, extra=0):
+    return 1000 + workload_index + 100000 * extra

@@ -1,0 +1,336 @@
+"""Plain CPU oracle for EXL3-style trellis-coded linear layers.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import this module:
+only the tests, the package smoke check and the benchmark's CPU-baseline leg use
+it.  It shares no code with the CUDA library and is deliberately slow and literal:
+every step is written the way the source pages define it, in numpy, with fp64
+arithmetic except where fp16 rounding is itself part of the definition.
+
+Sources (web pages, cited by title and section):
+  [FMT]   "The escha W2 format, recovered and verified" -- sections "Tensor
+          mapping", "Reconstruction", "Codebook: cb=1 (MCG), verified",
+          "Bit layout: the part that is easy to get wrong", "How each claim
+          was verified".
+  [MLX]   "Escha-W2 runs on Metal" -- the tensor table, the activation-side
+          reconstruction, the three-instruction codebook, the tile packing
+          paragraph with the closed-form permutation inverse.
+  [EXLR8] the EXLR8 format page -- the shared per-layer rotation ("The sharing
+          trick"), the 16x16 tile packing, expert shapes.
+
+Readings taken where the pages are silent or ambiguous (each also listed in the
+design notes):
+  * Bit stream.  A tile's 16*bits int16 words are paired little-endian into
+    8*bits uint32 words; the stream is those words in order, each read from its
+    most significant bit down.  State s is the 16 stream bits ending at bit
+    bits*(s+1)-1, circularly (tail-biting).  For bits=2 this is exactly the
+    decoder printed in [FMT] "Bit layout"; for bits=3 and 4 the pages give no
+    decoder, and a constant window offset cannot be seen by the overlap
+    invariant, so the bits=3/4 window origin is PARITY UNPINNED.
+  * Codebook sum.  "fp16_lo + fp16_hi" is one IEEE fp16 addition, i.e. the
+    exact sum rounded once to fp16, round-to-nearest-even.
+  * Permutation.  [MLX] prints the inverse map (tile position -> lane pair t
+    and half e); the symbol index is s = 2*t + e.  The forward map used for
+    placement ("tile[perm] = values", [FMT]) is the inverse of that.
+  * Hadamard.  Natural (Sylvester) order, normalised by 1/sqrt(128), applied to
+    each consecutive block of 128 channels.
+
+The fp16 <-> float conversions use numpy's IEEE half type.
+"""
+
+import numpy as np
+
+TILE = 16                       # [FMT] "Tensor mapping": 16x16 tiles
+SYMBOLS_PER_TILE = TILE * TILE  # 256 trellis states per tile
+HAD_BLOCK = 128                 # [FMT] "Reconstruction": Hadamard of size 128
+
+MCG_MULT = 0xCBAC1FED           # [FMT] "Codebook: cb=1 (MCG)"
+MCG_MASK = 0x8FFF8FFF
+MCG_XOR = 0x3B603B60
+
+SUPPORTED_BITS = (2, 3, 4)
+
+
+# ----------------------------------------------------------------------------
+# Bit stream and trellis states  ([FMT] "Bit layout", [MLX] tile packing)
+# ----------------------------------------------------------------------------
+
+def words_per_tile(bits):
+    """int16 words per tile: 256 symbols x bits / 16 ([FMT] "Tensor mapping")."""
+    return SYMBOLS_PER_TILE * bits // 16
+
+
+def tile_u32_words(tile_code):
+    """Pair the tile's int16 words little-endian into uint32 words.
+
+    tile_code: int16 [..., 16*bits].  Returns uint64 [..., 8*bits] (values < 2^32).
+    """
+    u16 = np.asarray(tile_code).view(np.uint16).astype(np.uint64)
+    return u16[..., 0::2] | (u16[..., 1::2] << np.uint64(16))
+
+
+def tile_stream_bits(tile_code):
+    """The tile's bit stream, one uint8 per bit, words in order, MSB first."""
+    w = tile_u32_words(tile_code)
+    shifts = np.arange(31, -1, -1, dtype=np.uint64)           # MSB first
+    bits = (w[..., :, None] >> shifts) & np.uint64(1)
+    return bits.reshape(*w.shape[:-1], -1).astype(np.uint8)
+
+
+def window_positions(bits):
+    """Stream positions of each state's 16-bit window, MSB first: [256, 16].
+
+    State s ends at stream bit bits*(s+1)-1; the stream is circular.
+    """
+    n = SYMBOLS_PER_TILE * bits
+    s = np.arange(SYMBOLS_PER_TILE)[:, None]
+    i = np.arange(16)[None, :]
+    return (bits * (s + 1) - 16 + i) % n
+
+
+def tile_states(tile_code, bits):
+    """All 256 16-bit trellis states of each tile (stream model): uint32 [..., 256]."""
+    assert bits in SUPPORTED_BITS
+    stream = tile_stream_bits(tile_code)
+    assert stream.shape[-1] == SYMBOLS_PER_TILE * bits
+    window = stream[..., window_positions(bits)]              # [..., 256, 16]
+    place = (1 << np.arange(15, -1, -1)).astype(np.uint32)      # MSB first
+    return (window.astype(np.uint32) * place).sum(axis=-1).astype(np.uint32)
+
+
+def tile_states_k2_printed(tile_code):
+    """bits=2 states by the decoder printed in [FMT] "Bit layout".
+
+    Lane L handles symbols t = 8L .. 8L+7.  It forms a 64-bit value from the
+    word pair (i0, i1), shifts it right by 16 when bit 3 of t is clear, and
+    symbol t+j is the 16-bit window at shift 14-2j.  Independent of the stream
+    model above; the two must agree.
+    """
+    u32 = tile_u32_words(tile_code)
+    assert u32.shape[-1] == 16
+    out = np.zeros(u32.shape[:-1] + (SYMBOLS_PER_TILE,), dtype=np.uint32)
+    for lane in range(32):
+        t = 8 * lane
+        i1 = t >> 4
+        i0 = (i1 + 15) & 15
+        b = (u32[..., i0] << np.uint64(32)) | u32[..., i1]
+        b = b >> np.uint64(((~t) & 8) << 1)
+        for j in range(8):
+            out[..., t + j] = ((b >> np.uint64(14 - 2 * j)) & np.uint64(0xFFFF)).astype(np.uint32)
+    return out
+
+
+def pack_stream_bits(stream_bits):
+    """Test helper: pack a 256*bits-bit stream (uint8 per bit) into int16 words.
+
+    The inverse of tile_stream_bits: words MSB first, uint32 split into two
+    little-endian int16 words.  Used to build tiles from hand-chosen streams.
+    """
+    stream_bits = np.asarray(stream_bits, dtype=np.uint64)
+    nbits = stream_bits.shape[-1]
+    assert nbits % 32 == 0
+    w = stream_bits.reshape(*stream_bits.shape[:-1], nbits // 32, 32)
+    place = np.uint64(1) << np.arange(31, -1, -1, dtype=np.uint64)
+    u32 = (w * place).sum(axis=-1).astype(np.uint64)
+    lo = (u32 & np.uint64(0xFFFF)).astype(np.uint16)
+    hi = (u32 >> np.uint64(16)).astype(np.uint16)
+    u16 = np.stack([lo, hi], axis=-1).reshape(*u32.shape[:-1], -1)
+    return u16.view(np.int16)
+
+
+# ----------------------------------------------------------------------------
+# Codebook cb=1 ("3INST")  ([FMT] "Codebook: cb=1 (MCG), verified"; [MLX])
+# ----------------------------------------------------------------------------
+
+def mcg_word(states):
+    """v = state * 0xCBAC1FED (mod 2^32); v = (v & 0x8FFF8FFF) ^ 0x3B603B60."""
+    v = (np.asarray(states, dtype=np.uint64) * np.uint64(MCG_MULT)) & np.uint64(0xFFFFFFFF)
+    v = (v & np.uint64(MCG_MASK)) ^ np.uint64(MCG_XOR)
+    return v
+
+
+def codebook_halves(states):
+    """The two fp16 numbers of the codebook word: (low half, high half), as float16."""
+    v = mcg_word(states)
+    lo = (v & np.uint64(0xFFFF)).astype(np.uint16).view(np.float16)
+    hi = (v >> np.uint64(16)).astype(np.uint16).view(np.float16)
+    return lo, hi
+
+
+def codebook_value(states):
+    """fp16_lo + fp16_hi as one fp16 addition: exact sum, rounded once (RNE)."""
+    lo, hi = codebook_halves(states)
+    exact = lo.astype(np.float64) + hi.astype(np.float64)
+    return exact.astype(np.float16)
+
+
+# ----------------------------------------------------------------------------
+# Tensor-core permutation  ([MLX] closed-form inverse; [FMT] "tile[perm] = values")
+# ----------------------------------------------------------------------------
+
+def perm_symbol_of(r, c):
+    """Closed-form inverse: tile row r (input channel), column c (output) -> symbol s.
+
+    t = 4*(4*(c&7) + q) + 2*((c>>3)&1) + rh with q = (r>>1)&3, rh = r>>3,
+    e = r&1, and s = 2*t + e.
+    """
+    q = (r >> 1) & 3
+    rh = r >> 3
+    e = r & 1
+    t = 4 * (4 * (c & 7) + q) + 2 * ((c >> 3) & 1) + rh
+    return 2 * t + e
+
+
+def perm_forward():
+    """perm[s] = flat tile index r*16 + c where symbol s lands (inverse of the above)."""
+    perm = np.full(SYMBOLS_PER_TILE, -1, dtype=np.int64)
+    for r in range(TILE):
+        for c in range(TILE):
+            s = perm_symbol_of(r, c)
+            perm[s] = r * TILE + c
+    return perm
+
+
+# ----------------------------------------------------------------------------
+# Decode: code tensor -> W_inner  ([FMT] "Tensor mapping", "Bit layout")
+# ----------------------------------------------------------------------------
+
+def decode_tiles(tile_codes, bits):
+    """Decode tiles: int16 [..., 16*bits] -> float16 [..., 16, 16] (row = input channel)."""
+    values = codebook_value(tile_states(tile_codes, bits))     # [..., 256]
+    perm = perm_forward()
+    flat = np.empty(values.shape, dtype=np.float16)
+    flat[..., perm] = values                                    # tile[perm] = values
+    return flat.reshape(*values.shape[:-1], TILE, TILE)
+
+
+def decode_matrix(code, bits, chunk=4096):
+    """W_inner fp16 [in, out] from the code tensor int16 [in/16, out/16, 16*bits].
+
+    code[i, j] holds W_inner[16i:16i+16, 16j:16j+16] (K-tile index major).
+    """
+    kt, nt, nw = code.shape
+    assert nw == words_per_tile(bits)
+    flat = code.reshape(kt * nt, nw)
+    tiles = np.empty((kt * nt, TILE, TILE), dtype=np.float16)
+    for a in range(0, kt * nt, chunk):
+        tiles[a:a + chunk] = decode_tiles(flat[a:a + chunk], bits)
+    return tiles.reshape(kt, nt, TILE, TILE).transpose(0, 2, 1, 3).reshape(kt * TILE, nt * TILE)
+
+
+def decode_columns(code, bits, cols):
+    """W_inner[:, cols] (fp16) decoding only the tile columns that hold `cols`."""
+    cols = np.asarray(cols)
+    kt = code.shape[0]
+    out = np.empty((kt * TILE, cols.size), dtype=np.float16)
+    for jt in np.unique(cols // TILE):
+        tiles = decode_tiles(code[:, jt, :], bits)              # [kt, 16, 16]
+        strip = tiles.reshape(kt * TILE, TILE)
+        sel = np.nonzero(cols // TILE == jt)[0]
+        out[:, sel] = strip[:, cols[sel] % TILE]
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Blockwise Hadamard-128  ([FMT] "Reconstruction"; [EXLR8] rotation)
+# ----------------------------------------------------------------------------
+
+def sylvester_hadamard(n):
+    """Unnormalised Sylvester Hadamard matrix of order n (power of 2), natural order."""
+    h = np.ones((1, 1))
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    assert h.shape[0] == n
+    return h
+
+
+def had128_matrix():
+    """H_128 / sqrt(128): symmetric and orthogonal."""
+    return sylvester_hadamard(HAD_BLOCK) / np.sqrt(HAD_BLOCK)
+
+
+def had_blockwise(x):
+    """Apply H_128/sqrt(128) to each consecutive 128-block of the last axis (fp64)."""
+    x = np.asarray(x, dtype=np.float64)
+    n = x.shape[-1]
+    assert n % HAD_BLOCK == 0
+    xb = x.reshape(*x.shape[:-1], n // HAD_BLOCK, HAD_BLOCK)
+    return (xb @ had128_matrix()).reshape(x.shape)
+
+
+def blockdiag_hadamard(n):
+    """Dense block-diagonal matrix diag(H128, ..., H128)/sqrt(128) of order n."""
+    h = had128_matrix()
+    out = np.zeros((n, n))
+    for b in range(0, n, HAD_BLOCK):
+        out[b:b + HAD_BLOCK, b:b + HAD_BLOCK] = h
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Layers  ([MLX] activation-side reconstruction; [FMT] "Reconstruction")
+# ----------------------------------------------------------------------------
+
+def fold_scales(r, s):
+    """su = rin * s_in  or  sv = rout * s_out, in fp64 ([MLX])."""
+    return np.asarray(r).astype(np.float64) * np.asarray(s).astype(np.float64)
+
+
+def linear_forward(x, w_inner, su, sv):
+    """y = had(had(x * su) @ W_inner) * sv, fp64 throughout.
+
+    x: [M, in] (any float dtype); w_inner: [in, out]; su: [in]; sv: [out].
+    """
+    x = np.asarray(x).astype(np.float64)
+    xh = had_blockwise(x * su)
+    y_pre = xh @ np.asarray(w_inner).astype(np.float64)
+    return had_blockwise(y_pre) * sv
+
+
+def linear_forward_columns(x, code, bits, su, sv, blocks):
+    """Output columns of the 128-blocks `blocks` only (decodes just those columns)."""
+    x = np.asarray(x).astype(np.float64)
+    xh = had_blockwise(x * su)
+    cols = np.concatenate([np.arange(b * HAD_BLOCK, (b + 1) * HAD_BLOCK) for b in blocks])
+    w = decode_columns(code, bits, cols).astype(np.float64)
+    y_pre = xh @ w
+    y = had_blockwise(y_pre) * sv[cols]
+    return cols, y
+
+
+def reconstruct_weight(w_inner, su, sv):
+    """Weight-side route ([FMT] "Reconstruction"): W [in, out] such that y = x @ W.
+
+    W = had_l(W_inner); W *= su[:, None]; W = had_r(W); W *= sv[None, :].
+    """
+    k, n = w_inner.shape
+    w = blockdiag_hadamard(k) @ np.asarray(w_inner).astype(np.float64)
+    w = w * np.asarray(su)[:, None]
+    w = w @ blockdiag_hadamard(n)
+    return w * np.asarray(sv)[None, :]
+
+
+def silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def mlp_forward(x, gate, up, down):
+    """down(silu(gate(x)) * up(x)); each layer is a dict(w=W_inner, su=, sv=)."""
+    g = linear_forward(x, gate["w"], gate["su"], gate["sv"])
+    u = linear_forward(x, up["w"], up["su"], up["sv"])
+    return linear_forward(silu(g) * u, down["w"], down["su"], down["sv"])
+
+
+def moe_forward(x, experts, ids, weights):
+    """sum_k w[m,k] * mlp_{ids[m,k]}(x[m]) per token ([EXLR8] routed experts).
+
+    experts[e] = (gate, up, down) layer dicts; gate/up share the hidden-side su
+    and down shares the hidden-side sv across experts ("The sharing trick").
+    """
+    x = np.asarray(x).astype(np.float64)
+    m, hidden = x.shape
+    y = np.zeros((m, hidden))
+    for t in range(m):
+        for k in range(ids.shape[1]):
+            gate, up, down = experts[int(ids[t, k])]
+            y[t] += float(weights[t, k]) * mlp_forward(x[t:t + 1], gate, up, down)[0]
+    return y

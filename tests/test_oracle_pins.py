@@ -1,0 +1,401 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Every check here compares the oracle with something other than itself: a
+decoder printed on the pages, a value printed on the pages, a library routine
+(torch fp16 arithmetic, scipy's Hadamard), the PTX ISA fragment table, a
+closed form, an invariant, or brute force on tiny inputs.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import torch
+
+from oracle import escha_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_constants.json")
+
+
+def golden(key):
+    with open(GOLDEN) as f:
+        return json.load(f)[key]["value"]
+
+
+def random_tiles(rng, n, bits):
+    return rng.integers(-32768, 32768, size=(n, 16 * bits), dtype=np.int16)
+
+
+# ---------------------------------------------------------------- fp16 helpers
+
+def test_numpy_half_decode_matches_torch_all_bit_patterns():
+    u16 = np.arange(65536, dtype=np.uint16)
+    ours = u16.view(np.float16).astype(np.float64)
+    ref = torch.from_numpy(u16.view(np.int16)).view(torch.float16).double().numpy()
+    finite = np.isfinite(ref)
+    assert np.array_equal(ours[finite], ref[finite])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+
+
+def test_numpy_double_to_half_rounds_correctly():
+    """numpy's fp64 -> fp16 is one round-to-nearest-even step.
+
+    Checked against Python's struct 'e' packing (a correctly rounded
+    double -> half conversion), including exact ties and values just off a tie.
+    torch is only used for fp32 inputs: its fp64 -> fp16 goes through fp32.
+    """
+    import struct
+    rng = np.random.default_rng(1)
+    x = rng.normal(0, 2, 50000)
+    h = np.arange(0x3000, 0x4400, dtype=np.uint16).view(np.float16).astype(np.float64)
+    ties = (h[:-1] + h[1:]) / 2
+    x = np.concatenate([x, ties, -ties, np.nextafter(ties, 0), np.nextafter(ties, 10)])
+    ours = x.astype(np.float16).view(np.uint16)
+    ref = np.array([struct.unpack('<H', struct.pack('<e', v))[0] for v in x], dtype=np.uint16)
+    assert np.array_equal(ours, ref)
+    x32 = x.astype(np.float32)
+    t = torch.from_numpy(x32).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(x32.astype(np.float16).view(np.uint16), t)
+
+
+# ---------------------------------------------------------------- codebook
+
+def test_codebook_equals_torch_fp16_add_all_states():
+    """fp16_lo + fp16_hi as an fp16 addition, checked with torch's CPU half add."""
+    states = np.arange(65536)
+    lo, hi = O.codebook_halves(states)
+    ref = (torch.from_numpy(lo.view(np.int16)).view(torch.float16)
+           + torch.from_numpy(hi.view(np.int16)).view(torch.float16))
+    ours = O.codebook_value(states)
+    assert np.array_equal(ours.view(np.uint16), ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_codebook_state_zero_by_hand():
+    # v = 0 -> (0 & mask) ^ 0x3B603B60: both halves 0x3B60 = 2^-1 * (1 + 864/1024)
+    half = 0.5 * (1 + 864 / 1024)
+    assert O.codebook_value(np.array([0]))[0] == np.float16(2 * half)
+    # state 1: v = 0xCBAC1FED -> masked 0x8BAC0FED -> xor -> 0xB0CC348D
+    v = ((0xCBAC1FED & 0x8FFF8FFF) ^ 0x3B603B60)
+    assert v == 0xB0CC348D
+    lo = np.uint16(v & 0xFFFF).view(np.float16).astype(np.float64)
+    hi = np.uint16(v >> 16).view(np.float16).astype(np.float64)
+    assert O.codebook_value(np.array([1]))[0] == np.float16(lo + hi)
+
+
+def test_codebook_halves_have_forced_exponent():
+    """The mask/xor forces each half's exponent to 12..15: |half| in [0.125, 2)."""
+    lo, hi = O.codebook_halves(np.arange(65536))
+    for h in (lo, hi):
+        a = np.abs(h.astype(np.float64))
+        assert a.min() >= 0.125 and a.max() < 2.0
+
+
+def test_codebook_std_matches_printed_codebook_scale():
+    """Std of the decoded values over all states vs EXL3's codebook_scale 1.24371088."""
+    vals = O.codebook_value(np.arange(65536)).astype(np.float64)
+    scale = golden("codebook_scale")
+    assert abs(vals.std() - scale) / scale < 1e-3
+    # the page's measured inner-domain std (1.2318) is within 1% as well
+    assert abs(vals.std() - golden("inner_domain_std_measured")) / vals.std() < 0.01
+
+
+def _hand_value(state):
+    """Codebook value of one state computed by hand from the printed constants."""
+    v = (state * 0xCBAC1FED) & 0xFFFFFFFF
+    v = (v & 0x8FFF8FFF) ^ 0x3B603B60
+    return np.float16(np.uint16(v & 0xFFFF).view(np.float16).astype(np.float64)
+                      + np.uint16(v >> 16).view(np.float16).astype(np.float64))
+
+
+@pytest.mark.parametrize("mutation", ["mult", "mask", "xor_forced_bits", "xor_free_bits", "nosum"])
+def test_codebook_pins_reject_plausible_mistakes(mutation, monkeypatch):
+    """Each plausible slip in the codebook fails at least one of the pins above.
+
+    A changed multiplier or a changed XOR in bits the mask lets through only
+    permutes the value multiset (the std cannot see it); the by-hand values of
+    states 0 and 1 can.  A changed mask, a changed XOR in the forced exponent
+    bits, or a dropped half moves the std off the printed codebook scale.
+    """
+    if mutation == "mult":
+        monkeypatch.setattr(O, "MCG_MULT", 0xCBAC1FEB)
+    elif mutation == "mask":
+        monkeypatch.setattr(O, "MCG_MASK", 0x9FFF9FFF)
+    elif mutation == "xor_forced_bits":
+        monkeypatch.setattr(O, "MCG_XOR", 0x2B602B60)
+    elif mutation == "xor_free_bits":
+        monkeypatch.setattr(O, "MCG_XOR", 0x3C603C60)
+    states = np.arange(65536)
+    if mutation == "nosum":
+        lo, _ = O.codebook_halves(states)
+        vals = lo.astype(np.float64)
+    else:
+        vals = O.codebook_value(states).astype(np.float64)
+    scale = golden("codebook_scale")
+    std_off = abs(vals.std() - scale) / scale > 5e-3
+    hand_off = (O.codebook_value(np.array([0]))[0] != _hand_value(0)
+                or O.codebook_value(np.array([1]))[0] != _hand_value(1))
+    if mutation == "nosum":
+        assert std_off
+    else:
+        assert std_off or hand_off
+
+
+# ---------------------------------------------------------------- bit layout
+
+def test_words_per_tile_printed():
+    printed = golden("code_words_per_tile")
+    for b, w in printed.items():
+        assert O.words_per_tile(int(b)) == w
+
+
+def test_stream_model_equals_printed_k2_decoder():
+    rng = np.random.default_rng(2)
+    tiles = random_tiles(rng, 512, 2)
+    assert np.array_equal(O.tile_states(tiles, 2), O.tile_states_k2_printed(tiles))
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_overlap_invariant_including_wrap(bits):
+    """Low 16-bits bits of state t equal the high 16-bits bits of state t+1 (255 -> 0 too)."""
+    rng = np.random.default_rng(3 + bits)
+    st = O.tile_states(random_tiles(rng, 256, bits), bits).astype(np.int64)
+    nxt = np.roll(st, -1, axis=-1)
+    mask = (1 << (16 - bits)) - 1
+    assert np.array_equal(st & mask, nxt >> bits)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_single_bit_flip_locality(bits):
+    """Flipping stream bit p changes exactly the states whose window covers p, at the right bit."""
+    rng = np.random.default_rng(10 + bits)
+    n = 256 * bits
+    base_bits = rng.integers(0, 2, size=n).astype(np.uint8)
+    base = O.tile_states(O.pack_stream_bits(base_bits), bits).astype(np.int64)
+    for p in list(range(0, n, 37)) + [0, n - 1, n - 16, 15]:
+        flipped_bits = base_bits.copy()
+        flipped_bits[p] ^= 1
+        st = O.tile_states(O.pack_stream_bits(flipped_bits), bits).astype(np.int64)
+        diff = st ^ base
+        for s in range(256):
+            start = (bits * (s + 1) - 16) % n
+            offset = (p - start) % n
+            if offset < 16:
+                assert diff[s] == 1 << (15 - offset), (p, s)
+            else:
+                assert diff[s] == 0, (p, s)
+
+
+def test_k2_word_pairing_by_hand():
+    """A lone set bit at the MSB of uint32 word 0 (high int16 of the first pair).
+
+    That is stream bit 0.  At bits=2 state s ends at bit 2s+1, so bit 0 lies in the
+    windows of states 0..7 (state 0 ends at bit 1) and wraps for state 255.
+    The printed decoder gives the same.
+    """
+    code = np.zeros((1, 32), dtype=np.uint16)
+    code[0, 1] = 0x8000           # word 0 = u16[0] | u16[1] << 16 -> bit 31
+    tiles = code.view(np.int16)
+    st = O.tile_states(tiles, 2)[0]
+    expect = np.zeros(256, dtype=np.int64)
+    for s in range(256):
+        start = (2 * (s + 1) - 16) % 512
+        off = (0 - start) % 512
+        if off < 16:
+            expect[s] = 1 << (15 - off)
+    assert np.array_equal(st, expect)
+    assert np.array_equal(O.tile_states_k2_printed(tiles)[0], expect)
+    assert expect[0] == 1 << 1 and expect[7] == 1 << 15 and expect[255] == 0
+
+
+# ---------------------------------------------------------------- permutation
+
+def test_perm_is_bijection():
+    perm = O.perm_forward()
+    assert sorted(perm.tolist()) == list(range(256))
+
+
+def test_perm_matches_ptx_m16n8k16_b_fragments():
+    """Lane L = 4g + t holds symbols 8L..8L+7 = the B fragments of two m16n8k16 MMAs.
+
+    PTX ISA, mma.m16n8k16 .f16 B fragment: b0 = (B[2t][g], B[2t+1][g]),
+    b1 = (B[2t+8][g], B[2t+9][g]); the second MMA covers columns 8..15.
+    Tile rows are B's k (input channel), columns its n (output channel).
+    """
+    perm = O.perm_forward()
+    for lane in range(32):
+        g, t = lane // 4, lane % 4
+        for j in range(8):
+            nh, reg, half = j // 4, (j // 2) % 2, j % 2
+            k = 2 * t + half + 8 * reg
+            n = g + 8 * nh
+            assert perm[8 * lane + j] == k * 16 + n
+
+
+def test_perm_closed_form_row_pairs():
+    """[MLX]: r = 8*rh + 2*q + {0,1}; e = r & 1; both rows of a lane pair map to one t."""
+    for c in range(16):
+        for q in range(4):
+            for rh in range(2):
+                t = 4 * (4 * (c & 7) + q) + 2 * ((c >> 3) & 1) + rh
+                for e in range(2):
+                    r = 8 * rh + 2 * q + e
+                    assert O.perm_symbol_of(r, c) == 2 * t + e
+
+
+def test_decode_matrix_tile_placement():
+    """code[i, j] lands at W_inner[16i:16i+16, 16j:16j+16], K-tile index major."""
+    rng = np.random.default_rng(5)
+    code = rng.integers(-32768, 32768, size=(3, 5, 32), dtype=np.int16)
+    w = O.decode_matrix(code, 2)
+    assert w.shape == (48, 80)
+    for i in range(3):
+        for j in range(5):
+            tile = O.decode_tiles(code[i, j], 2)
+            assert np.array_equal(w[16 * i:16 * i + 16, 16 * j:16 * j + 16].view(np.uint16),
+                                  tile.view(np.uint16))
+    cols = np.array([0, 17, 33, 79])
+    assert np.array_equal(O.decode_columns(code, 2, cols).view(np.uint16),
+                          w[:, cols].view(np.uint16))
+
+
+def test_decode_tile_brute_force_single_symbol():
+    """Build a tile whose stream makes one state distinctive and find its value by hand."""
+    bits = 3
+    n = 256 * bits
+    rng = np.random.default_rng(6)
+    stream = rng.integers(0, 2, size=n).astype(np.uint8)
+    tile = O.pack_stream_bits(stream)
+    w = O.decode_tiles(tile, bits)
+    for s in (0, 1, 77, 255):
+        start = bits * (s + 1) - 16
+        state = 0
+        for i in range(16):
+            state = (state << 1) | int(stream[(start + i) % n])
+        v = (state * 0xCBAC1FED) & 0xFFFFFFFF
+        v = (v & 0x8FFF8FFF) ^ 0x3B603B60
+        val = np.float16(np.uint16(v & 0xFFFF).view(np.float16).astype(np.float64)
+                         + np.uint16(v >> 16).view(np.float16).astype(np.float64))
+        lane, j = s // 8, s % 8
+        g, t = lane // 4, lane % 4
+        k = 2 * t + (j % 2) + 8 * ((j // 2) % 2)
+        c = g + 8 * (j // 4)
+        assert w[k, c] == val
+
+
+# ---------------------------------------------------------------- Hadamard
+
+def test_hadamard_matches_scipy_and_closed_form():
+    h = O.sylvester_hadamard(128)
+    assert np.array_equal(h, scipy.linalg.hadamard(128).astype(np.float64))
+    a = np.arange(128)
+    pc = np.vectorize(lambda v: bin(v).count("1"))(a[:, None] & a[None, :])
+    assert np.array_equal(h, (-1.0) ** pc)
+
+
+def test_hadamard_symmetric_orthogonal_self_inverse():
+    h = O.had128_matrix()
+    assert np.array_equal(h, h.T)
+    assert np.allclose(h @ h, np.eye(128), atol=1e-13)
+    rng = np.random.default_rng(7)
+    x = rng.normal(size=(3, 384))
+    assert np.allclose(O.had_blockwise(O.had_blockwise(x)), x, atol=1e-12)
+    assert np.allclose(np.linalg.norm(O.had_blockwise(x), axis=1), np.linalg.norm(x, axis=1))
+    assert np.allclose(O.had_blockwise(x), x @ O.blockdiag_hadamard(384), atol=1e-12)
+
+
+def test_hadamard_blocks_are_independent():
+    x = np.zeros((1, 256))
+    x[0, 130] = 1.0
+    y = O.had_blockwise(x)
+    assert np.all(y[0, :128] == 0) and np.allclose(np.abs(y[0, 128:]), 1 / np.sqrt(128))
+
+
+# ---------------------------------------------------------------- layers
+
+def make_small_layer(rng, k, n, bits):
+    code = rng.integers(-32768, 32768, size=(k // 16, n // 16, 16 * bits), dtype=np.int16)
+    rin = rng.normal(1, 0.1, k).astype(np.float16)
+    rout = rng.normal(1, 0.1, n).astype(np.float16)
+    s_in = rng.uniform(0.98, 1.02, k).astype(np.float32)
+    s_out = rng.uniform(0.98, 1.02, n).astype(np.float32)
+    return code, rin, rout, s_in, s_out
+
+
+@pytest.mark.parametrize("k,n,bits", [(128, 128, 2), (256, 384, 3), (384, 256, 4)])
+def test_activation_route_equals_weight_route(k, n, bits):
+    rng = np.random.default_rng(8 + bits)
+    code, rin, rout, s_in, s_out = make_small_layer(rng, k, n, bits)
+    w_inner = O.decode_matrix(code, bits)
+    su, sv = O.fold_scales(rin, s_in), O.fold_scales(rout, s_out)
+    x = rng.normal(size=(5, k)).astype(np.float16)
+    y_act = O.linear_forward(x, w_inner, su, sv)
+    y_w = x.astype(np.float64) @ O.reconstruct_weight(w_inner, su, sv)
+    assert np.allclose(y_act, y_w, rtol=1e-10, atol=1e-9)
+
+
+def test_layer_brute_force_loops():
+    """Per-element loops on a 128x128 layer, one token."""
+    rng = np.random.default_rng(9)
+    code, rin, rout, s_in, s_out = make_small_layer(rng, 128, 128, 2)
+    w = O.decode_matrix(code, 2).astype(np.float64)
+    su, sv = O.fold_scales(rin, s_in), O.fold_scales(rout, s_out)
+    x = rng.normal(size=128)
+    H = [[(-1.0) ** bin(a & b).count("1") / np.sqrt(128) for b in range(128)] for a in range(128)]
+    xh = [sum(x[a] * su[a] * H[a][k] for a in range(128)) for k in range(128)]
+    yp = [sum(xh[k] * w[k, n] for k in range(128)) for n in range(128)]
+    y = [sum(yp[b] * H[b][n] for b in range(128)) * sv[n] for n in range(128)]
+    assert np.allclose(O.linear_forward(x[None, :], w, su, sv)[0], y, rtol=1e-10, atol=1e-10)
+
+
+def test_layer_rejects_transposed_weight():
+    rng = np.random.default_rng(10)
+    code, rin, rout, s_in, s_out = make_small_layer(rng, 128, 128, 2)
+    w = O.decode_matrix(code, 2)
+    su, sv = O.fold_scales(rin, s_in), O.fold_scales(rout, s_out)
+    x = rng.normal(size=(2, 128))
+    assert not np.allclose(O.linear_forward(x, w, su, sv), O.linear_forward(x, w.T, su, sv))
+
+
+def test_linear_forward_columns_matches_full():
+    rng = np.random.default_rng(11)
+    code, rin, rout, s_in, s_out = make_small_layer(rng, 256, 512, 3)
+    su, sv = O.fold_scales(rin, s_in), O.fold_scales(rout, s_out)
+    x = rng.normal(size=(3, 256))
+    full = O.linear_forward(x, O.decode_matrix(code, 3), su, sv)
+    cols, part = O.linear_forward_columns(x, code, 3, su, sv, [1, 3])
+    assert np.allclose(full[:, cols], part, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_single_output_rotation_by_linearity():
+    """sum_k w_k had(y_k) sv == had(sum_k w_k y_k) sv: one rotation serves all experts."""
+    rng = np.random.default_rng(12)
+    ys = rng.normal(size=(8, 256))
+    w = rng.random(8)
+    sv = rng.uniform(0.5, 1.5, 256)
+    a = sum(w[k] * O.had_blockwise(ys[k:k + 1])[0] * sv for k in range(8))
+    b = O.had_blockwise((w[:, None] * ys).sum(0, keepdims=True))[0] * sv
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_forward_reduces_to_mlp():
+    rng = np.random.default_rng(13)
+
+    def layer(k, n, b):
+        code, rin, rout, s_in, s_out = make_small_layer(rng, k, n, b)
+        return dict(w=O.decode_matrix(code, b), su=O.fold_scales(rin, s_in),
+                    sv=O.fold_scales(rout, s_out))
+    experts = [(layer(128, 256, 2), layer(128, 256, 2), layer(256, 128, 2)) for _ in range(3)]
+    x = rng.normal(size=(2, 128))
+    ids = np.array([[1, 2], [0, 1]])
+    wts = np.array([[1.0, 0.0], [0.25, 0.75]])
+    y = O.moe_forward(x, experts, ids, wts)
+    assert np.allclose(y[0], O.mlp_forward(x[0:1], *experts[1])[0])
+    ref1 = 0.25 * O.mlp_forward(x[1:2], *experts[0])[0] + 0.75 * O.mlp_forward(x[1:2], *experts[1])[0]
+    assert np.allclose(y[1], ref1)
+
+
+def test_silu_closed_form():
+    z = np.array([0.0, 1.0, -1.0, 20.0])
+    assert np.allclose(O.silu(z), [0.0, 1 / (1 + np.exp(-1)), -1 / (1 + np.e), 20.0], atol=1e-7)
