@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of the trellis decode-and-multiply path on one GB300 (sm_103a).
+
+Default workload: the dense gated MLP at decode, 5120 -> 17408 -> 5120 with
+gate 2-bit, up 3-bit and down 3-bit trellis codes, one token.  One step is one
+full MLP application (input rotations, two trellis GEMV launches, the fused
+SiLU-gate middle, the output rotation) on device-resident inputs.
+
+Prints ONE JSON line.  `value` is decode GEMV throughput in GB/s of
+algorithmic bytes (code words + side vectors + activations) per step;
+`roofline` rates the dominant kernel (the trellis GEMV) against the measured
+HBM copy bandwidth; `e2e` is the same metric through the C ABI with host
+buffers and the copies inside the timed region; `cpu_baseline` is the CPU
+oracle on a bounded sample of the same workload.
+
+Other workloads (--workload linear512 | sweep) print the same line for their
+own shapes.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gemm_trellis_tile_gb300 import synthetic as S  # noqa: E402
+from gemm_trellis_tile_gb300 import workloads as WL  # noqa: E402
+
+L2_FALLBACK_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="escha", choices=["escha", "reference"])
+    p.add_argument("--workload", default="mlp", choices=["mlp", "linear512", "sweep"])
+    p.add_argument("--m", type=int, default=1, help="tokens per step")
+    p.add_argument("--shape", default="5120x10240", help="sweep shape in x out")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- environment
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "escha_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workloads
+
+def workload_spec(args):
+    """Layers of one step as (in, out, bits) and a description."""
+    if args.workload == "mlp":
+        layers = WL.mlp_layers(5120, 17408, (2, 3, 3))
+        name = "dense gated MLP 5120->17408->5120, gate 2-bit / up 3-bit / down 3-bit, M=%d" % args.m
+        return dict(kind="mlp", layers=layers, name=name, seed=S.seed_for(1))
+    if args.workload == "linear512":
+        return dict(kind="linear", layers=[(512, 512, 2)], seed=S.seed_for(0),
+                    name="single linear 512x512 2-bit, M=%d" % args.m)
+    k, n = (int(v) for v in args.shape.split("x"))
+    return dict(kind="linear", layers=[(k, n, 2)], seed=S.seed_for(2, k),
+                name="decode sweep linear %dx%d 2-bit, M=%d" % (k, n, args.m))
+
+
+def step_bytes(spec, m):
+    return sum(WL.layer_bytes(m, i, o, b) for i, o, b in spec["layers"])
+
+
+def make_instance(spec, seed):
+    rng = np.random.default_rng(seed)
+    if spec["kind"] == "mlp":
+        hidden, inter = spec["layers"][0][0], spec["layers"][0][1]
+        bits = tuple(b for _, _, b in spec["layers"])
+        return S.make_mlp(rng, hidden, inter, *bits)
+    k, n, b = spec["layers"][0]
+    return dict(layer=S.make_linear(rng, k, n, b))
+
+
+def instance_matrices(spec, inst):
+    return [inst["gate"], inst["up"], inst["down"]] if spec["kind"] == "mlp" else [inst["layer"]]
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample_rate(spec, m, seconds, seed=7):
+    """Run the CPU oracle on 128-output column blocks of the workload's matrices
+    until `seconds` of work; return (GB/s of algorithmic bytes, effective cores,
+    sample description)."""
+    from oracle import escha_oracle as O
+    mats = instance_matrices(spec, make_instance(spec, spec["seed"]))
+    rng = np.random.default_rng(seed)
+    done_bytes = 0
+    blocks = 0
+    t0 = time.perf_counter()
+    c0 = time.process_time()
+    while True:
+        lay = mats[blocks % len(mats)]
+        k, n = lay["in_features"], lay["out_features"]
+        blk = int(rng.integers(n // 128))
+        x = S.make_activations(rng, m, k)
+        su = O.fold_scales(lay["rin"], lay["s_in"])
+        sv = O.fold_scales(lay["rout"], lay["s_out"])
+        O.linear_forward_columns(x, lay["code"], lay["bits"], su, sv, [blk])
+        done_bytes += WL.layer_bytes(m, k, 128, lay["bits"])
+        blocks += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    return (done_bytes / wall / 1e9, round(cpu / wall, 2),
+            "%d column blocks of 128 outputs (full input depth) across the workload's matrices, "
+            "%.1f s" % (blocks, wall))
+
+
+def run_reference(args, spec, rank):
+    """--impl reference: the CPU oracle, as it stands, on a bounded sample per step."""
+    if rank != 0:
+        return 0
+    from oracle import escha_oracle as O
+    mats = instance_matrices(spec, make_instance(spec, spec["seed"]))
+    rng = np.random.default_rng(11)
+    budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
+    probe = mats[0]
+    t0 = time.perf_counter()
+    O.decode_columns(probe["code"][:8], probe["bits"], np.arange(128))
+    per_ktile = max(1e-6, (time.perf_counter() - t0) / 8)
+    ktiles = max(8, int(budget / per_ktile) // 8 * 8)
+
+    def one_step(i):
+        lay = mats[i % len(mats)]
+        k, n, b = lay["in_features"], lay["out_features"], lay["bits"]
+        kt = min(ktiles, k // 16)
+        blk = int(rng.integers(n // 128))
+        kk = kt * 16
+        x = S.make_activations(rng, args.m, kk)
+        w = O.decode_columns(lay["code"][:kt], b, np.arange(blk * 128, blk * 128 + 128))
+        su = O.fold_scales(lay["rin"][:kk], lay["s_in"][:kk])
+        y_pre = O.had_blockwise(x * su) @ w.astype(np.float64)
+        _ = O.had_blockwise(y_pre) * O.fold_scales(lay["rout"], lay["s_out"])[blk * 128:blk * 128 + 128]
+        return WL.layer_bytes(args.m, kk, 128, b)
+
+    for i in range(args.warmup):
+        one_step(i)
+    t0 = time.perf_counter()
+    c0 = time.process_time()
+    total = 0
+    for i in range(args.steps):
+        total += one_step(i)
+    wall = time.perf_counter() - t0
+    cores = round((time.process_time() - c0) / wall, 2)
+    value = total / wall / 1e9
+    depth = min(ktiles, max(lay["in_features"] // 16 for lay in mats))
+    sample = ("per step: one 128-output column block of one matrix (cycling through the "
+              "workload's matrices), %d k-tiles deep" % depth)
+    line = {"impl": "reference", "metric": "decode GEMV compressed-weight GB/s", "value": value,
+            "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec["name"]},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def make_handles(spec, inst):
+    from gemm_trellis_tile_gb300 import escha
+    if spec["kind"] == "mlp":
+        g = escha.Linear.from_arrays(inst["gate"])
+        u = escha.Linear.from_arrays(inst["up"])
+        d = escha.Linear.from_arrays(inst["down"])
+        return escha.MLP(g, u, d), (g, u, d)
+    lin = escha.Linear.from_arrays(inst["layer"])
+    return lin, (lin,)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    spec = workload_spec(args)
+    if args.impl == "reference":
+        return run_reference(args, spec, rank)
+
+    import torch
+    from gemm_trellis_tile_gb300 import build, escha
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    build.build()
+    escha.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or L2_FALLBACK_BYTES
+    m = args.m
+    k_in = spec["layers"][0][0]
+    n_out = spec["layers"][-1][1]
+    launches_per_step = 5 if spec["kind"] == "mlp" else 3
+    gemv_launches_per_step = 2 if spec["kind"] == "mlp" else 1
+
+    # Rotating weight sets, together more than 4x L2, so no step finds its
+    # code words in L2 from an earlier step.
+    code_per_inst = sum(WL.code_bytes(i, o, b) for i, o, b in spec["layers"])
+    n_inst = max(2, int(np.ceil(4.0 * l2 / code_per_inst)))
+    handles = []
+    for r in range(n_inst):
+        inst = make_instance(spec, spec["seed"] + 7919 * r + 1000003 * rank)
+        handles.append(make_handles(spec, inst))
+        del inst
+    rng = np.random.default_rng(spec["seed"] + 17)
+    x_host = torch.from_numpy(S.make_activations(rng, m, k_in)).pin_memory()
+    x = x_host.to(dev)
+    y = torch.empty((m, n_out), dtype=torch.float16, device=dev)
+
+    def step(i):
+        handles[i % n_inst][0].gemv(x, y)
+
+    for i in range(max(args.warmup, n_inst)):
+        step(i)
+    torch.cuda.synchronize()
+    for h, _ in handles:
+        if h.check() != 0:
+            raise SystemExit("device error flag set during warm-up")
+        h.profile(True)
+    for i in range(2 * n_inst):   # fills each handle's event pool outside capture
+        step(i)
+    torch.cuda.synchronize()
+    for h, _ in handles:
+        h.collect()
+
+    # CUDA graphs: one graph per pass over the weight sets, plus a remainder.
+    per_graph = n_inst
+    full, rem = divmod(args.steps, per_graph)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g_main = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_main, stream=side):
+            for i in range(per_graph):
+                step(i)
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g_rem, stream=side):
+                for i in range(rem):
+                    step(i)
+    torch.cuda.synchronize()
+    for i in range(3):
+        g_main.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(full):
+        g_main.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    t_end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # Dominant kernel: the trellis GEMV launches recorded inside the graphs
+    # (their events hold the durations of the last replay of each graph).
+    k_ms = 0.0
+    k_n = 0
+    for h, _ in handles:
+        a, n = h.collect()
+        k_ms += a
+        k_n += n
+        h.profile(False)
+    steps_covered = k_n / gemv_launches_per_step
+    k_bytes = WL.gemv_kernel_bytes(m, spec["layers"]) * steps_covered
+    achieved = k_bytes / (k_ms / 1e3) / 1e9 if k_ms > 0 else None
+
+    # End to end through the C ABI: host input copied in, result copied out.
+    y_host = torch.empty((m, n_out), dtype=torch.float16).pin_memory()
+    e2e_steps = min(args.steps, 2000)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        x.copy_(x_host, non_blocking=True)
+        handles[i % n_inst][0].gemv(x, y)
+        y_host.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    for h, _ in handles:
+        st = h.check()
+        if st != 0:
+            raise SystemExit("device error flag set: status %d" % st)
+
+    sbytes = step_bytes(spec, m)
+    value = world * args.steps * sbytes / (ms / 1e3) / 1e9
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    line = {
+        "metric": "decode GEMV compressed-weight GB/s (algorithmic bytes: codes + side vectors + activations)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "us_per_layer": 1e3 * ms / args.steps / len(spec["layers"]),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded uniform code words, N(1,0.1) scales, N(0,1) activations)",
+        "config": {"workload": spec["name"], "tokens": m,
+                   "bytes_per_step": sbytes,
+                   "l2": "%d rotating weight sets, %.0f MB of code words (> 4x L2)"
+                         % (n_inst, n_inst * code_per_inst / 1e6),
+                   "timing": "CUDA graphs of the public API calls, CUDA events"},
+        "roofline": {"bound": "hbm", "kernel": "trellis_gemv",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": None,
+                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": e2e_steps * sbytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(y_host.numel() * 2)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = oracle_sample_rate(spec, m, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

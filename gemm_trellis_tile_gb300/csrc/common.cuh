@@ -1,0 +1,136 @@
+// Device-side helpers shared by the libescha kernels: mbarrier waits with a
+// time limit, 1-D bulk copies (TMA engine), the in-register Hadamard-128
+// butterflies and fp16 bit helpers.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace escha {
+
+constexpr int kHad = 128;                          // Hadamard block size
+constexpr float kHadScale = 0.08838834764831845f;  // 1/sqrt(128)
+
+// Default limit of a bounded device wait (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void set_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up after
+// limit_ns of wall time (or 2^30 polls), returning false; never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------- bulk copy
+
+// 1-D bulk copy global -> shared, completing on an mbarrier (TMA engine).
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority hint (streamed once: evict first).
+__device__ __forceinline__ void bulk_g2s_evict_first(uint32_t dst, const void* src, uint32_t bytes,
+                                                     uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------- Hadamard
+
+// Fast Walsh-Hadamard transform of one 128-block held by a warp, four
+// consecutive elements per lane (element 4*lane + r in v[r]); natural
+// (Sylvester) order, unnormalised.  Two butterfly stages in registers, five
+// across lanes.
+__device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
+  const float a0 = v[0] + v[1], a1 = v[0] - v[1];
+  const float a2 = v[2] + v[3], a3 = v[2] - v[3];
+  v[0] = a0 + a2;
+  v[2] = a0 - a2;
+  v[1] = a1 + a3;
+  v[3] = a1 - a3;
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int m = 1 << s;
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[r], m);
+      v[r] = upper ? (o - v[r]) : (v[r] + o);
+    }
+  }
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t b) {
+  return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ uint16_t float_to_half_bits(float f) {
+  return __half_as_ushort(__float2half_rn(f));
+}
+
+}  // namespace escha

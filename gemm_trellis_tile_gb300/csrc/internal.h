@@ -1,0 +1,86 @@
+// Host-side internals of libescha shared between translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+namespace escha {
+
+// Device error codes written to a handle's error word.
+constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrBadRoute = 2;
+
+// ---------------------------------------------------------------- GEMV schedule
+//
+// A launch of the trellis GEMV kernel contracts one or more matrices ("jobs").
+// Job j's work is cut into units: unit (g, kt) = k-tile row kt of output group
+// g (128 output channels = 8 tiles of 16).  Units are numbered job-major, then
+// group-major, then k.  The launch's units are split into `grid` contiguous,
+// near-equal ranges, one per persistent CTA (CTA c owns [c*U/G, (c+1)*U/G)).
+// Where a CTA's range covers a group only partly, it writes its fp32 partial
+// sums to slot (c - first CTA of that group); the output kernel sums the slots.
+
+struct GemvJob {
+  const uint8_t* code;   // tiles, [KT][NT][32*bits bytes]
+  const uint4* xfrag;    // rotated activations in fragment order, [KT][TB][32] x uint4
+  float* part;           // partial sums, [slots][mpad][N]
+  long long unit_begin;  // first unit of this job within the launch
+  int bits;
+  int KT;                // in / 16
+  int NG;                // out / 128
+  int N;                 // out
+};
+
+struct GemvSchedule {
+  std::vector<GemvJob> jobs;
+  GemvJob* d_jobs = nullptr;
+  long long units = 0;
+  int grid = 0;
+  int max_slots = 0;
+};
+
+constexpr int kGemvMaxTokens = 16;
+constexpr int kMinUnitsPerCta = 8;
+
+int gemv_ctas_per_sm();
+// Fill unit_begin, units, grid and max_slots for the given jobs.
+void plan_gemv(GemvSchedule& s, int num_sms, int ctas_per_sm);
+int gemv_slots_for_group(const GemvSchedule& s, int job, int g);
+
+cudaError_t launch_gemv(const GemvSchedule& s, int M, int* err, cudaStream_t st);
+cudaError_t launch_decode(const int16_t* code, int bits, int K, int N, uint16_t* w,
+                          cudaStream_t st);
+cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);
+
+// ---------------------------------------------------------------- rotations
+
+struct RotInJob {
+  const uint16_t* x;  // [M, K] fp16
+  const float* su;    // [K]
+  uint32_t* xfrag;    // [K/16][TB][32][4]
+  int K;
+};
+
+// Slot bookkeeping the output kernels need to sum a group's partial sums.
+struct PartRef {
+  const float* part;
+  long long unit_begin;
+  int KT;
+  int N;
+};
+
+cudaError_t launch_fold_scales(const uint16_t* r, const float* s, float* out, int n,
+                               cudaStream_t st);
+cudaError_t launch_rotate_in_xfrag(const RotInJob* jobs, int njobs, int M, int TB,
+                                   cudaStream_t st);
+cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t* xh, int M,
+                                   int K, cudaStream_t st);
+cudaError_t launch_rotate_out(const PartRef& pr, long long units, int grid, const float* sv,
+                              uint16_t* y, int M, int mpad, cudaStream_t st);
+cudaError_t launch_mlp_mid(const PartRef& gate, const PartRef& up, long long units, int grid,
+                           const float* sv_gate, const float* sv_up, const float* su_down,
+                           uint32_t* xfrag_down, int M, int TB, cudaStream_t st);
+
+}  // namespace escha

@@ -1,0 +1,198 @@
+// Host orchestration of the dense trellis layer and the gated MLP at decode.
+//
+// Dense layer, 1..16 tokens (three launches on the caller's stream):
+//   1. rotate_in:  xfrag = fp16(had128(x * su)) in the GEMV's fragment order
+//   2. trellis GEMV: fp32 partial sums of xh @ W_inner (decode in registers)
+//   3. rotate_out: y = fp16(had128(sum of partials) * sv)
+// Gated MLP (five launches): both input rotations in one launch, gate and up
+// contracted in one GEMV launch, one fused middle kernel (output rotations,
+// silu(g)*u, the down layer's input rotation), the down GEMV, and the output
+// rotation.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "api_internal.h"
+
+namespace escha {
+
+template <typename T>
+escha_status_t dev_alloc(T** p, size_t count) {
+  *p = nullptr;
+  if (count == 0) return ESCHA_OK;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return e == cudaErrorMemoryAllocation ? ESCHA_ERR_OOM : ESCHA_ERR_CUDA;
+  }
+  return ESCHA_OK;
+}
+template escha_status_t dev_alloc<int>(int**, size_t);
+template escha_status_t dev_alloc<float>(float**, size_t);
+template escha_status_t dev_alloc<uint32_t>(uint32_t**, size_t);
+template escha_status_t dev_alloc<uint16_t>(uint16_t**, size_t);
+template escha_status_t dev_alloc<GemvJob>(GemvJob**, size_t);
+
+namespace {
+
+GemvJob make_job(const escha_linear_s* h, const uint32_t* xfrag, float* part) {
+  GemvJob j;
+  j.code = reinterpret_cast<const uint8_t*>(h->code);
+  j.xfrag = reinterpret_cast<const uint4*>(xfrag);
+  j.part = part;
+  j.unit_begin = 0;
+  j.bits = h->bits;
+  j.KT = h->K / 16;
+  j.NG = h->N / 128;
+  j.N = h->N;
+  return j;
+}
+
+size_t xfrag_words(int K) { return (size_t)(K / 16) * 2 * 32 * 4; }
+
+PartRef part_ref(const GemvSchedule& s, int job) {
+  PartRef r;
+  r.part = s.jobs[job].part;
+  r.unit_begin = s.jobs[job].unit_begin;
+  r.KT = s.jobs[job].KT;
+  r.N = s.jobs[job].N;
+  return r;
+}
+
+}  // namespace
+
+escha_status_t linear_init(escha_linear_s* h, const int16_t* code, int bits, int K, int N,
+                           const uint16_t* rin, const uint16_t* rout, const float* s_in,
+                           const float* s_out, cudaStream_t st) {
+  escha_status_t s = device_info(&h->device, &h->num_sms);
+  if (s != ESCHA_OK) return s;
+  h->K = K;
+  h->N = N;
+  h->bits = bits;
+  h->code = code;
+  if ((s = dev_alloc(&h->su, K)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->sv, N)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->xfrag, xfrag_words(K))) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->err, 1)) != ESCHA_OK) return s;
+  if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return ESCHA_ERR_CUDA;
+
+  if (launch_fold_scales(rin, s_in, h->su, K, st) != cudaSuccess) return ESCHA_ERR_CUDA;
+  if (launch_fold_scales(rout, s_out, h->sv, N, st) != cudaSuccess) return ESCHA_ERR_CUDA;
+
+  h->sched.jobs.assign(1, make_job(h, h->xfrag, nullptr));
+  plan_gemv(h->sched, h->num_sms, gemv_ctas_per_sm());
+  if ((s = dev_alloc(&h->part, (size_t)h->sched.max_slots * kGemvMaxTokens * N)) != ESCHA_OK)
+    return s;
+  h->sched.jobs[0].part = h->part;
+  if ((s = upload_jobs(h->sched)) != ESCHA_OK) return s;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ESCHA_ERR_CUDA;
+  return ESCHA_OK;
+}
+
+void linear_free(escha_linear_s* h) {
+  cudaFree(h->su);
+  cudaFree(h->sv);
+  cudaFree(h->xfrag);
+  cudaFree(h->part);
+  cudaFree(h->err);
+  cudaFree(h->sched.d_jobs);
+  cudaFree(h->xh);
+  h->su = h->sv = nullptr;
+  h->xfrag = nullptr;
+  h->part = nullptr;
+  h->err = nullptr;
+  h->sched.d_jobs = nullptr;
+  h->xh = nullptr;
+}
+
+escha_status_t linear_gemv(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
+                           cudaStream_t st) {
+  const int TB = M <= 8 ? 1 : 2;
+  RotInJob rj{x, h->su, h->xfrag, h->K};
+  cudaError_t e = launch_rotate_in_xfrag(&rj, 1, M, TB, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  h->prof.begin(st);
+  e = launch_gemv(h->sched, M, h->err, st);
+  h->prof.end(st);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_rotate_out(part_ref(h->sched, 0), h->sched.units, h->sched.grid, h->sv, y, M,
+                        kGemvMaxTokens, st);
+  return from_cuda(e);
+}
+
+escha_status_t mlp_init(escha_mlp_s* m, escha_linear_s* gate, escha_linear_s* up,
+                        escha_linear_s* down) {
+  m->gate = gate;
+  m->up = up;
+  m->down = down;
+  escha_status_t s;
+  if ((s = dev_alloc(&m->xfrag_gate, xfrag_words(gate->K))) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&m->xfrag_up, xfrag_words(up->K))) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&m->xfrag_down, xfrag_words(down->K))) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&m->err, 1)) != ESCHA_OK) return s;
+  if (cudaMemset(m->err, 0, sizeof(int)) != cudaSuccess) return ESCHA_ERR_CUDA;
+
+  const int cps = gemv_ctas_per_sm();
+  m->s_gate_up.jobs = {make_job(gate, m->xfrag_gate, nullptr), make_job(up, m->xfrag_up, nullptr)};
+  plan_gemv(m->s_gate_up, gate->num_sms, cps);
+  m->s_down.jobs = {make_job(down, m->xfrag_down, nullptr)};
+  plan_gemv(m->s_down, down->num_sms, cps);
+  const size_t rows = (size_t)kGemvMaxTokens;
+  if ((s = dev_alloc(&m->part_gate, m->s_gate_up.max_slots * rows * gate->N)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&m->part_up, m->s_gate_up.max_slots * rows * up->N)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&m->part_down, m->s_down.max_slots * rows * down->N)) != ESCHA_OK) return s;
+  m->s_gate_up.jobs[0].part = m->part_gate;
+  m->s_gate_up.jobs[1].part = m->part_up;
+  m->s_down.jobs[0].part = m->part_down;
+  if ((s = upload_jobs(m->s_gate_up)) != ESCHA_OK) return s;
+  if ((s = upload_jobs(m->s_down)) != ESCHA_OK) return s;
+  return ESCHA_OK;
+}
+
+void mlp_free(escha_mlp_s* m) {
+  cudaFree(m->xfrag_gate);
+  cudaFree(m->xfrag_up);
+  cudaFree(m->xfrag_down);
+  cudaFree(m->part_gate);
+  cudaFree(m->part_up);
+  cudaFree(m->part_down);
+  cudaFree(m->err);
+  cudaFree(m->s_gate_up.d_jobs);
+  cudaFree(m->s_down.d_jobs);
+}
+
+escha_status_t mlp_gemv(escha_mlp_s* m, const uint16_t* x, uint16_t* y, int M, cudaStream_t st) {
+  const int TB = M <= 8 ? 1 : 2;
+  RotInJob rj[2] = {{x, m->gate->su, m->xfrag_gate, m->gate->K},
+                    {x, m->up->su, m->xfrag_up, m->up->K}};
+  cudaError_t e = launch_rotate_in_xfrag(rj, 2, M, TB, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  m->prof.begin(st);
+  e = launch_gemv(m->s_gate_up, M, m->err, st);
+  m->prof.end(st);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_mlp_mid(part_ref(m->s_gate_up, 0), part_ref(m->s_gate_up, 1), m->s_gate_up.units,
+                     m->s_gate_up.grid, m->gate->sv, m->up->sv, m->down->su, m->xfrag_down, M, TB,
+                     st);
+  if (e != cudaSuccess) return from_cuda(e);
+  m->prof.begin(st);
+  e = launch_gemv(m->s_down, M, m->err, st);
+  m->prof.end(st);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_rotate_out(part_ref(m->s_down, 0), m->s_down.units, m->s_down.grid, m->down->sv, y,
+                        M, kGemvMaxTokens, st);
+  return from_cuda(e);
+}
+
+Profiler* profiler_of(void* handle, int kind) {
+  if (!handle) return nullptr;
+  switch (kind) {
+    case ESCHA_KIND_LINEAR: return &static_cast<escha_linear_s*>(handle)->prof;
+    case ESCHA_KIND_MLP: return &static_cast<escha_mlp_s*>(handle)->prof;
+    default: return nullptr;
+  }
+}
+
+}  // namespace escha

@@ -1,0 +1,246 @@
+// Activation-side transforms of a trellis layer: the input rotation
+// xh = had128(x * su) and the output rotation y = had128(y_pre) * sv.
+// "Escha-W2 runs on Metal" (activation-side reconstruction): the scales sit
+// outside the Hadamard, so both transforms are cheap elementwise+butterfly
+// passes on activations; the Hadamard never touches the weights.
+//
+// Every kernel here maps one warp to one 128-channel block of one token: lane
+// l holds elements 4l..4l+3, two butterfly stages run in registers and five
+// across lanes (fwht128_warp), all in fp32, rounded to fp16 once at the end.
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace escha {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__host__ __device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
+  return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+// Store one rotated activation (fp16 bits) at its place in the GEMV's
+// B-fragment layout: per k-tile, token block and lane (g = token % 8, t), four
+// words (x[2t], 0), (x[2t+8], 0), (x[2t+1], 0), (x[2t+9], 0).
+__device__ __forceinline__ void xfrag_store(uint32_t* xf, int TB, int m, int k, uint16_t hb) {
+  const int kt = k >> 4, kk = k & 15;
+  const int t = (kk & 7) >> 1, odd = kk & 1, hi8 = kk >> 3;
+  const int reg = 2 * odd + hi8;
+  const int tb = m >> 3, g = m & 7;
+  xf[(((size_t)kt * TB + tb) * 32 + 4 * g + t) * 4 + reg] = hb;
+}
+
+__device__ __forceinline__ void load4_half(const uint16_t* p, float (&v)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  v[0] = half_bits_to_float(raw.x & 0xFFFF);
+  v[1] = half_bits_to_float(raw.x >> 16);
+  v[2] = half_bits_to_float(raw.y & 0xFFFF);
+  v[3] = half_bits_to_float(raw.y >> 16);
+}
+
+__device__ __forceinline__ void store4_half(uint16_t* p, const float (&v)[4]) {
+  uint2 raw;
+  raw.x = float_to_half_bits(v[0]) | (uint32_t(float_to_half_bits(v[1])) << 16);
+  raw.y = float_to_half_bits(v[2]) | (uint32_t(float_to_half_bits(v[3])) << 16);
+  *reinterpret_cast<uint2*>(p) = raw;
+}
+
+// Sum a group's partial-sum slots for token m, channels 128g + 4l .. +3.
+__device__ __forceinline__ void sum_slots(const PartRef& pr, long long U, int G, int mpad, int m,
+                                          int g, int lane, float (&v)[4]) {
+  const long long ub = pr.unit_begin + (long long)g * pr.KT;
+  const int ns = cta_of_unit(ub + pr.KT - 1, U, G) - cta_of_unit(ub, U, G) + 1;
+  v[0] = v[1] = v[2] = v[3] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float4 p = *reinterpret_cast<const float4*>(
+        pr.part + ((size_t)s * mpad + m) * pr.N + 128 * g + 4 * lane);
+    v[0] += p.x;
+    v[1] += p.y;
+    v[2] += p.z;
+    v[3] += p.w;
+  }
+}
+
+__global__ void fold_scales_kernel(const uint16_t* r, const float* s, float* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = half_bits_to_float(r[i]) * (s ? s[i] : 1.0f);
+}
+
+struct RotInArgs {
+  RotInJob jobs[2];
+  int njobs;
+  int M;
+  int TB;
+};
+
+// xfrag = fp16(had128(x * su)) for tokens 0..8TB-1 (zeros past M).
+__global__ void rotate_in_xfrag_kernel(const RotInArgs a) {
+  const int lane = threadIdx.x & 31;
+  long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int mp = 8 * a.TB;
+  int j = 0;
+  for (; j < a.njobs; ++j) {
+    const long long n = (long long)mp * (a.jobs[j].K / kHad);
+    if (wid < n) break;
+    wid -= n;
+  }
+  if (j >= a.njobs) return;
+  const RotInJob J = j == 0 ? a.jobs[0] : a.jobs[1];
+  const int nb = J.K / kHad;
+  const int m = static_cast<int>(wid / nb);
+  const int kb = static_cast<int>(wid - (long long)m * nb);
+  const int k0 = kb * kHad + 4 * lane;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (m < a.M) {
+    load4_half(J.x + (size_t)m * J.K + k0, v);
+    const float4 su = *reinterpret_cast<const float4*>(J.su + k0);
+    v[0] *= su.x;
+    v[1] *= su.y;
+    v[2] *= su.z;
+    v[3] *= su.w;
+    fwht128_warp(v, lane);
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    xfrag_store(J.xfrag, a.TB, m, k0 + r, float_to_half_bits(v[r] * kHadScale));
+}
+
+// xh[m, k] = fp16(had128(x * su)), plain row-major (the GEMM's A operand).
+__global__ void rotate_in_plain_kernel(const uint16_t* x, const float* su, uint16_t* xh, int M,
+                                       int K) {
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int nb = K / kHad;
+  if (wid >= (long long)M * nb) return;
+  const int m = static_cast<int>(wid / nb);
+  const int kb = static_cast<int>(wid - (long long)m * nb);
+  const int k0 = kb * kHad + 4 * lane;
+  float v[4];
+  load4_half(x + (size_t)m * K + k0, v);
+  const float4 s = *reinterpret_cast<const float4*>(su + k0);
+  v[0] *= s.x;
+  v[1] *= s.y;
+  v[2] *= s.z;
+  v[3] *= s.w;
+  fwht128_warp(v, lane);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) v[r] *= kHadScale;
+  store4_half(xh + (size_t)m * K + k0, v);
+}
+
+// y = fp16(had128(sum of partial slots) * sv).
+__global__ void rotate_out_kernel(const PartRef pr, long long U, int G, const float* sv,
+                                  uint16_t* y, int M, int mpad) {
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int NG = pr.N / kHad;
+  if (wid >= (long long)M * NG) return;
+  const int m = static_cast<int>(wid / NG);
+  const int g = static_cast<int>(wid - (long long)m * NG);
+  float v[4];
+  sum_slots(pr, U, G, mpad, m, g, lane, v);
+  fwht128_warp(v, lane);
+  const int n0 = g * kHad + 4 * lane;
+  const float4 s = *reinterpret_cast<const float4*>(sv + n0);
+  v[0] *= kHadScale * s.x;
+  v[1] *= kHadScale * s.y;
+  v[2] *= kHadScale * s.z;
+  v[3] *= kHadScale * s.w;
+  store4_half(y + (size_t)m * pr.N + n0, v);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Gated-MLP middle: g = had(gate_pre)*sv_g, u = had(up_pre)*sv_u, h = silu(g)*u,
+// then the down layer's input rotation had(h * su_down) into its fragments.
+__global__ void mlp_mid_kernel(const PartRef gate, const PartRef up, long long U, int G,
+                               const float* sv_gate, const float* sv_up, const float* su_down,
+                               uint32_t* xfrag_down, int M, int TB) {
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int NG = gate.N / kHad;
+  const int mp = 8 * TB;
+  if (wid >= (long long)mp * NG) return;
+  const int m = static_cast<int>(wid / NG);
+  const int g = static_cast<int>(wid - (long long)m * NG);
+  const int n0 = g * kHad + 4 * lane;
+  float h[4] = {0.f, 0.f, 0.f, 0.f};
+  if (m < M) {
+    float gv[4], uv[4];
+    sum_slots(gate, U, G, kGemvMaxTokens, m, g, lane, gv);
+    sum_slots(up, U, G, kGemvMaxTokens, m, g, lane, uv);
+    fwht128_warp(gv, lane);
+    fwht128_warp(uv, lane);
+    const float4 sg = *reinterpret_cast<const float4*>(sv_gate + n0);
+    const float4 su = *reinterpret_cast<const float4*>(sv_up + n0);
+    const float4 sd = *reinterpret_cast<const float4*>(su_down + n0);
+    const float sgv[4] = {sg.x, sg.y, sg.z, sg.w};
+    const float suv[4] = {su.x, su.y, su.z, su.w};
+    const float sdv[4] = {sd.x, sd.y, sd.z, sd.w};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float gg = gv[r] * kHadScale * sgv[r];
+      const float uu = uv[r] * kHadScale * suv[r];
+      h[r] = silu(gg) * uu * sdv[r];
+    }
+    fwht128_warp(h, lane);
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    xfrag_store(xfrag_down, TB, m, n0 + r, float_to_half_bits(h[r] * kHadScale));
+}
+
+unsigned blocks_for(long long warps) {
+  return static_cast<unsigned>((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
+}
+
+}  // namespace
+
+cudaError_t launch_fold_scales(const uint16_t* r, const float* s, float* out, int n,
+                               cudaStream_t st) {
+  fold_scales_kernel<<<(n + 255) / 256, 256, 0, st>>>(r, s, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_in_xfrag(const RotInJob* jobs, int njobs, int M, int TB,
+                                   cudaStream_t st) {
+  RotInArgs a;
+  long long warps = 0;
+  for (int j = 0; j < njobs; ++j) {
+    a.jobs[j] = jobs[j];
+    warps += (long long)8 * TB * (jobs[j].K / kHad);
+  }
+  a.njobs = njobs;
+  a.M = M;
+  a.TB = TB;
+  rotate_in_xfrag_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t* xh, int M,
+                                   int K, cudaStream_t st) {
+  const long long warps = (long long)M * (K / kHad);
+  rotate_in_plain_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(x, su, xh, M, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_out(const PartRef& pr, long long units, int grid, const float* sv,
+                              uint16_t* y, int M, int mpad, cudaStream_t st) {
+  const long long warps = (long long)M * (pr.N / kHad);
+  rotate_out_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(pr, units, grid, sv, y, M,
+                                                                       mpad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mlp_mid(const PartRef& gate, const PartRef& up, long long units, int grid,
+                           const float* sv_gate, const float* sv_up, const float* su_down,
+                           uint32_t* xfrag_down, int M, int TB, cudaStream_t st) {
+  const long long warps = (long long)8 * TB * (gate.N / kHad);
+  mlp_mid_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(
+      gate, up, units, grid, sv_gate, sv_up, su_down, xfrag_down, M, TB);
+  return cudaGetLastError();
+}
+
+}  // namespace escha

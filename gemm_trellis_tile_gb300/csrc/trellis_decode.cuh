@@ -1,0 +1,122 @@
+// Trellis tile decode in registers.
+//
+// A 16x16 tile of `BITS`-bit weights is 8*BITS little-endian uint32 words.
+// Read MSB first, word after word, they form a circular stream of 256*BITS
+// bits; state s is the 16-bit window ending at stream bit BITS*(s+1)-1
+// ("The escha W2 format, recovered and verified", section "Bit layout"; the
+// Metal page calls it the window at offset i*K, tail-biting).
+//
+// Lane L of a warp decodes symbols 8L..8L+7.  All eight windows lie inside one
+// 64-bit pair of consecutive words (i0, i1), where i1 holds the last bit of
+// symbol 8L+7.  After one funnel shift by sh7 the windows sit at the fixed
+// offsets BITS*(7-j), so the per-symbol work is a constant-offset extraction.
+//
+// Each state goes through the cb=1 MCG codebook (section "Codebook: cb=1"):
+//   v = state * 0xCBAC1FED; v = (v & 0x8FFF8FFF) ^ 0x3B603B60;
+//   w = fp16(v.lo) + fp16(v.hi)   -- one fp16 addition, round to nearest even.
+//
+// Placement: lane L = 4g + t, symbol j of the lane sits at tile row (input
+// channel) r = 2t + (j&1) + 8((j>>1)&1) and column (output channel)
+// c = g + 8(j>>2): the m16n8k16 B-fragment order (Metal page, closed-form
+// inverse of the tensor-core permutation).  Seen as W^T (rows = output
+// channel), the same eight values are the lane's m16n8k16 A fragment:
+//   a0 <- j=0,1   a1 <- j=4,5   a2 <- j=2,3   a3 <- j=6,7.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace escha {
+
+constexpr uint32_t kMcgMult = 0xCBAC1FEDu;
+constexpr uint32_t kMcgMask = 0x8FFF8FFFu;
+constexpr uint32_t kMcgXor = 0x3B603B60u;
+
+struct LaneWindow {
+  int i0;    // word holding the start of the lane's bit span
+  int i1;    // word holding the last bit of symbol 8L+7
+  int sh7;   // right shift of (w[i0]:w[i1]) that puts symbol 7's window at bit 0
+};
+
+template <int BITS>
+__device__ __forceinline__ LaneWindow lane_window(int lane) {
+  const int nwords = 8 * BITS;
+  const int e7 = BITS * (8 * lane + 8) - 1;  // stream bit ending symbol 8L+7
+  LaneWindow lw;
+  lw.i1 = e7 >> 5;
+  lw.i0 = (lw.i1 + nwords - 1) % nwords;     // circular: tail-biting
+  lw.sh7 = 31 - (e7 & 31);
+  return lw;
+}
+
+// Codebook value of one state, replicated into both fp16 halves: one HADD2
+// with both operands broadcast from the word, (lo,lo) + (hi,hi).
+__device__ __forceinline__ uint32_t mcg_decode_dup(uint32_t state) {
+  uint32_t v = state * kMcgMult;
+  v = (v & kMcgMask) ^ kMcgXor;
+  const __half2 h = *reinterpret_cast<const __half2*>(&v);
+  const __half2 s = __hadd2(__low2half2(h), __high2half2(h));
+  return *reinterpret_cast<const uint32_t*>(&s);
+}
+
+// 16-bit field starting at byte `b` (0..2) of x, zero-extended (one PRMT).
+__device__ __forceinline__ uint32_t field16_at_byte(uint32_t x, int b) {
+  return __byte_perm(x, 0u, b == 0 ? 0x4410 : (b == 1 ? 0x4421 : 0x4432));
+}
+
+// The lane's eight 16-bit states.  (lo, hi) is the lane's 64-bit span shifted
+// so that symbol 7's window starts at bit 0; symbol j's window starts at bit
+// BITS*(7-j).  At 2 and 4 bits every window is byte aligned in one of a few
+// pre-shifted copies of the span, so each state costs one byte permute.
+template <int BITS>
+__device__ __forceinline__ void lane_states(uint32_t lo, uint32_t hi, uint32_t (&st)[8]) {
+  if (BITS == 2) {
+    // offsets 14, 12, ..., 0: copies shifted by 0, 2, 4, 6
+    const uint32_t r[4] = {lo, lo >> 2, lo >> 4, lo >> 6};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s = 2 * (7 - j);
+      st[j] = field16_at_byte(r[(s & 7) >> 1], s >> 3);
+    }
+  } else if (BITS == 4) {
+    // offsets 28, 24, ..., 0
+    const uint32_t l4 = __funnelshift_r(lo, hi, 4);
+    const uint32_t m16 = __funnelshift_r(lo, hi, 16);
+    const uint32_t m20 = __funnelshift_r(lo, hi, 20);
+    st[7] = field16_at_byte(lo, 0);   // 0
+    st[6] = field16_at_byte(l4, 0);   // 4
+    st[5] = field16_at_byte(lo, 1);   // 8
+    st[4] = field16_at_byte(l4, 1);   // 12
+    st[3] = field16_at_byte(lo, 2);   // 16
+    st[2] = field16_at_byte(l4, 2);   // 20
+    st[1] = field16_at_byte(m16, 1);  // 24
+    st[0] = field16_at_byte(m20, 1);  // 28
+  } else {
+    // 3 bits: offsets 21, 18, ..., 0 have eight different residues mod 8
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int s = BITS * (7 - j);
+      st[j] = (s + 16 <= 32) ? ((lo >> s) & 0xFFFFu) : (__funnelshift_r(lo, hi, s) & 0xFFFFu);
+    }
+  }
+}
+
+// Decode the lane's eight symbols from its word pair.  out[j] holds symbol
+// 8L+j's fp16 value in both halves.
+template <int BITS>
+__device__ __forceinline__ void decode8(uint32_t w0, uint32_t w1, int sh7, uint32_t (&out)[8]) {
+  const uint32_t lo = __funnelshift_r(w1, w0, sh7);
+  const uint32_t hi = w0 >> sh7;
+  uint32_t st[8];
+  lane_states<BITS>(lo, hi, st);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[j] = mcg_decode_dup(st[j]);
+}
+
+// Tile coordinates of lane symbol j (row = input channel, col = output channel).
+__device__ __forceinline__ int sym_row(int lane, int j) {
+  return 2 * (lane & 3) + (j & 1) + 8 * ((j >> 1) & 1);
+}
+__device__ __forceinline__ int sym_col(int lane, int j) { return (lane >> 2) + 8 * (j >> 2); }
+
+}  // namespace escha

@@ -1,0 +1,269 @@
+"""Python binding of libescha (include/escha.h): argument marshalling only.
+
+Every computation runs in the CUDA library; this module converts torch
+tensors to device pointers and status codes to exceptions.  There is no CPU
+fallback: if libescha.so is missing, loading fails loudly.
+
+The raw C entry points are exposed under their C names (escha_linear_create,
+escha_linear_gemv, ...) taking integer pointers; the classes Linear and MLP
+wrap them for torch CUDA tensors.
+"""
+
+import ctypes
+import os
+import re
+
+from . import build as _build
+
+ESCHA_OK = 0
+STATUS_NAMES = {0: "ESCHA_OK", 1: "ESCHA_ERR_INVALID_ARG", 2: "ESCHA_ERR_UNSUPPORTED",
+                3: "ESCHA_ERR_CUDA", 4: "ESCHA_ERR_OOM", 5: "ESCHA_ERR_TIMEOUT"}
+KIND_LINEAR, KIND_MLP, KIND_MOE = 0, 1, 2
+
+HEADER_PATH = os.path.join(os.path.dirname(_build.HERE), "include", "escha.h")
+
+
+class EschaError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (what, STATUS_NAMES.get(status, "?"), status))
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "escha_status_string": (ctypes.c_char_p, [_I]),
+    "escha_version": (_I, []),
+    "escha_linear_create": (_I, [ctypes.POINTER(_P), _P, _P, _P, _P, _P, _P, _I, _P]),
+    "escha_linear_destroy": (_I, [_P]),
+    "escha_linear_shape": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "escha_linear_decode": (_I, [_P, _P, _P]),
+    "escha_linear_gemv": (_I, [_P, _P, _P, _I, _P]),
+    "escha_linear_gemm": (_I, [_P, _P, _P, _I, _P]),
+    "escha_linear_reserve": (_I, [_P, _I]),
+    "escha_mlp_create": (_I, [ctypes.POINTER(_P), _P, _P, _P]),
+    "escha_mlp_destroy": (_I, [_P]),
+    "escha_mlp_gemv": (_I, [_P, _P, _P, _I, _P]),
+    "escha_moe_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _P, _P, _P, _P,
+                              _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "escha_moe_destroy": (_I, [_P]),
+    "escha_linear_moe_gemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
+    "escha_linear_check": (_I, [_P, _P]),
+    "escha_moe_check": (_I, [_P, _P]),
+    "escha_profile_enable": (_I, [_P, _I, _I]),
+    "escha_profile_collect": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
+    "escha_selftest_wait_timeout": (_I, [_I, _P]),
+}
+
+
+def lib_path():
+    return _build.LIB_PATH
+
+
+def load():
+    """Load libescha.so (built in-tree by gemm_trellis_tile_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError("libescha.so is not built (%s); run gemm_trellis_tile_gb300.build.build()"
+                           % path)
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def declared_functions():
+    """Names of the functions declared in include/escha.h."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(escha_[a-z0-9_]+)\s*\(", text)))
+
+
+def check(status, what):
+    if status != ESCHA_OK:
+        raise EschaError(status, what)
+
+
+def __getattr__(name):
+    # raw C entry points under their own names
+    if name.startswith("escha_") and name in _SIGS:
+        return getattr(load(), name)
+    raise AttributeError(name)
+
+
+# ---------------------------------------------------------------- torch wrappers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype, shape=None):
+    """Validate a device tensor argument."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("expected a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError("expected dtype %s, got %s" % (dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("expected shape %s, got %s" % (tuple(shape), tuple(t.shape)))
+    return t
+
+
+def _collect(handle, kind):
+    ms = ctypes.c_double()
+    n = _I()
+    check(load().escha_profile_collect(handle, kind, ctypes.byref(ms), ctypes.byref(n)),
+          "escha_profile_collect")
+    return ms.value, n.value
+
+
+class Linear:
+    """Dense trellis-coded linear layer on the current CUDA device.
+
+    Tensors: code int16 [in/16, out/16, 16*bits]; rin, rout fp16; s_in, s_out
+    fp32 (optional); config int32 [6] or [9] (host or device tensor).  code must
+    stay alive as long as the layer (it is borrowed, not copied).
+    """
+
+    def __init__(self, code, rin, rout, s_in=None, s_out=None, config=None, stream=None):
+        torch = _torch()
+        lib = load()
+        if config is None:
+            kt, nt, w = code.shape
+            config = torch.tensor([16, w // 16, 1, 1, kt * 16, nt * 16], dtype=torch.int32)
+        self._keep = (code, rin, rout, s_in, s_out, config)
+        h = ctypes.c_void_p()
+        cfg_ptr = ctypes.c_void_p(config.data_ptr())
+        check(lib.escha_linear_create(ctypes.byref(h), _ptr(code), _ptr(rin), _ptr(rout), _ptr(s_in),
+                                      _ptr(s_out), cfg_ptr, int(config.numel()), _stream(stream)),
+              "escha_linear_create")
+        self.handle = h
+        a, b, c = _I(), _I(), _I()
+        check(lib.escha_linear_shape(h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+              "escha_linear_shape")
+        self.in_features, self.out_features, self.bits = a.value, b.value, c.value
+
+    @classmethod
+    def from_arrays(cls, layer, device="cuda"):
+        """Build from host numpy arrays (code, rin, rout, s_in, s_out, config)."""
+        torch = _torch()
+        t = {k: torch.from_numpy(layer[k]).to(device) for k in ("code", "rin", "rout", "s_in", "s_out")}
+        return cls(t["code"], t["rin"], t["rout"], t["s_in"], t["s_out"],
+                   torch.from_numpy(layer["config"]))
+
+    def gemv(self, x, y=None, stream=None):
+        torch = _torch()
+        _dev(x, torch.float16)
+        m = x.shape[0]
+        if y is None:
+            y = torch.empty((m, self.out_features), dtype=torch.float16, device=x.device)
+        check(load().escha_linear_gemv(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
+              "escha_linear_gemv")
+        return y
+
+    def gemm(self, x, y=None, stream=None):
+        torch = _torch()
+        _dev(x, torch.float16)
+        m = x.shape[0]
+        if y is None:
+            y = torch.empty((m, self.out_features), dtype=torch.float16, device=x.device)
+        check(load().escha_linear_gemm(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
+              "escha_linear_gemm")
+        return y
+
+    def reserve(self, max_m):
+        check(load().escha_linear_reserve(self.handle, int(max_m)), "escha_linear_reserve")
+
+    def decode(self, stream=None):
+        torch = _torch()
+        w = torch.empty((self.in_features, self.out_features), dtype=torch.float16, device="cuda")
+        check(load().escha_linear_decode(self.handle, _ptr(w), _stream(stream)), "escha_linear_decode")
+        return w
+
+    def check(self, stream=None):
+        return load().escha_linear_check(self.handle, _stream(stream))
+
+    def profile(self, on=True):
+        check(load().escha_profile_enable(self.handle, KIND_LINEAR, int(on)), "escha_profile_enable")
+
+    def collect(self):
+        return _collect(self.handle, KIND_LINEAR)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            load().escha_linear_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MLP:
+    """Gated MLP down(silu(gate x) * up x) over three Linear layers (borrowed)."""
+
+    def __init__(self, gate, up, down):
+        self._layers = (gate, up, down)
+        h = ctypes.c_void_p()
+        check(load().escha_mlp_create(ctypes.byref(h), gate.handle, up.handle, down.handle),
+              "escha_mlp_create")
+        self.handle = h
+        self.hidden = gate.in_features
+
+    def gemv(self, x, y=None, stream=None):
+        torch = _torch()
+        _dev(x, torch.float16)
+        m = x.shape[0]
+        if y is None:
+            y = torch.empty((m, self.hidden), dtype=torch.float16, device=x.device)
+        check(load().escha_mlp_gemv(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
+              "escha_mlp_gemv")
+        return y
+
+    def check(self, stream=None):
+        return max(layer.check(stream) for layer in self._layers)
+
+    def profile(self, on=True):
+        check(load().escha_profile_enable(self.handle, KIND_MLP, int(on)), "escha_profile_enable")
+
+    def collect(self):
+        return _collect(self.handle, KIND_MLP)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            load().escha_mlp_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def selftest_wait_timeout(limit_us=10000, stream=None):
+    """Run the bounded-wait self test; returns the status code (5 = timed out as designed)."""
+    return load().escha_selftest_wait_timeout(int(limit_us), _stream(stream))

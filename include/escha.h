@@ -1,0 +1,214 @@
+/*
+ * escha.h -- C ABI of libescha: trellis-coded (EXL3-style, cb=1) linear layers on
+ * one sm_103a GPU.
+ *
+ * What is computed.  A layer stores W_inner [in, out] as 16x16 tiles, each tile a
+ * tail-biting stream of 256 16-bit trellis states packed at `bits` bits per weight
+ * (2, 3 or 4).  Each state decodes through the cb=1 MCG codebook
+ *     v = state * 0xCBAC1FED;  v = (v & 0x8FFF8FFF) ^ 0x3B603B60;
+ *     w = fp16(v.lo) + fp16(v.hi)            (one fp16 addition)
+ * and lands in the tile at its tensor-core position.  The layer is applied on the
+ * activation side:
+ *     su = rin * s_in;  sv = rout * s_out
+ *     y  = had128( had128(x * su) @ W_inner ) * sv
+ * where had128 is the normalised Sylvester Hadamard H_128/sqrt(128) applied to
+ * each consecutive block of 128 channels.
+ * Sources: "The escha W2 format, recovered and verified" (sections "Tensor
+ * mapping", "Reconstruction", "Codebook: cb=1 (MCG), verified", "Bit layout");
+ * "Escha-W2 runs on Metal" (activation-side reconstruction, three-instruction
+ * codebook, tile packing and the closed-form permutation inverse); the EXLR8
+ * format page (shared per-layer rotation for routed experts, tile packing).
+ *
+ * Conventions for every call.
+ *   - Tensor arguments are DEVICE pointers unless stated otherwise, row-major and
+ *     contiguous, 16-byte aligned.  fp16 tensors are passed as uint16_t bit
+ *     patterns (IEEE binary16).
+ *   - Borrowing: code words and the caller's x / y buffers are borrowed, never
+ *     copied; the caller keeps code alive for the handle's lifetime.  rin, rout,
+ *     s_in, s_out are read once at create time (folded into su, sv).  The handle
+ *     owns its folded scales and scratch memory.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every compute call is asynchronous on that stream; create and
+ *     destroy synchronise.
+ *   - Errors: every call returns an escha_status_t; nothing is thrown across the
+ *     ABI.  Argument errors are detected on the host before any launch.
+ *     Asynchronous CUDA errors surface as ESCHA_ERR_CUDA on a later call.  A
+ *     device-side wait that exceeds its time limit sets the handle's error flag;
+ *     escha_linear_check() reports it as ESCHA_ERR_TIMEOUT.
+ *   - Shapes: in and out must be multiples of 128; bits in {2,3,4}; cb == 1;
+ *     tile == 16.  Anything else is ESCHA_ERR_UNSUPPORTED.
+ *   - No CPU fallback exists: without a usable sm_103a device every compute call
+ *     fails with ESCHA_ERR_CUDA.
+ */
+#ifndef ESCHA_H
+#define ESCHA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ESCHA_OK = 0,
+  ESCHA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad handle */
+  ESCHA_ERR_UNSUPPORTED = 2,  /* well-formed but outside what is implemented */
+  ESCHA_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  ESCHA_ERR_OOM = 4,          /* device allocation failed */
+  ESCHA_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out */
+} escha_status_t;
+
+typedef struct escha_linear_s* escha_linear_t;
+typedef struct escha_mlp_s* escha_mlp_t;
+typedef struct escha_moe_s* escha_moe_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* escha_status_string(escha_status_t status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int escha_version(void);
+
+/*
+ * Create a dense trellis-coded linear layer.
+ *   code    int16 [in/16, out/16, 16*bits]: tile (i, j) holds
+ *           W_inner[16i:16i+16, 16j:16j+16] ("Tensor mapping": escha_code / EXL3
+ *           trellis; K-tile index major).
+ *   rin     fp16 [in]  per-input-channel scale (EXL3 suh).
+ *   rout    fp16 [out] per-output-channel scale (EXL3 svh).
+ *   s_in    fp32 [in], s_out fp32 [out]: escha's extra scales (may be NULL = 1.0).
+ *   config  int32 [config_len], host OR device pointer, either layout:
+ *           [6] = [16, bits, cb, 1, in, out]          ("Tensor mapping")
+ *           [9] = [16, K, bits, mcg, E, in, out, in_p, out_p]  (Metal page tensor
+ *                 table; E must be 1, K must equal bits or 16*bits, mcg 1,
+ *                 in_p == in, out_p == out).
+ * The handle borrows `code`; scales are folded into owned fp32 su/sv.
+ */
+escha_status_t escha_linear_create(escha_linear_t* out, const int16_t* code,
+                                   const uint16_t* rin, const uint16_t* rout,
+                                   const float* s_in, const float* s_out,
+                                   const int32_t* config, int config_len, void* stream);
+
+escha_status_t escha_linear_destroy(escha_linear_t h);
+
+/* Shape of a handle (any output pointer may be NULL). */
+escha_status_t escha_linear_shape(escha_linear_t h, int* in_features, int* out_features, int* bits);
+
+/*
+ * Decode the whole W_inner into fp16 [in, out] (test and inspection entry).
+ * Uses the same device decode routine as the GEMV and GEMM kernels.
+ * Source: "Bit layout" (stream, windows, lane L holds symbols 8L..8L+7) and the
+ * tile packing paragraph of the Metal page (closed-form permutation inverse).
+ */
+escha_status_t escha_linear_decode(escha_linear_t h, uint16_t* w_inner, void* stream);
+
+/*
+ * Decode-time layer: y[M, out] = had(had(x * su) @ W_inner) * sv for 1 <= M <= 16.
+ *   x  fp16 [M, in];  y  fp16 [M, out] (may not alias x).
+ * Fused decode-and-multiply: the codes stream from HBM once; weights are decoded
+ * in registers and never written anywhere.  Source: Metal page, activation-side
+ * reconstruction (xh = had(x*su); y_pre = xh @ W; y = had(y_pre)*sv).
+ */
+escha_status_t escha_linear_gemv(escha_linear_t h, const uint16_t* x, uint16_t* y, int M,
+                                 void* stream);
+
+/*
+ * Prefill layer for any M >= 1: the same function as escha_linear_gemv, computed
+ * with tiles decoded into shared memory feeding tcgen05 fp16 MMAs (fp32 TMEM
+ * accumulators) and the output rotation fused into the epilogue.
+ * The handle keeps a workspace for the rotated activations; it grows on demand
+ * (a call with a larger M than any before allocates).  escha_linear_reserve()
+ * sizes it up front.
+ */
+escha_status_t escha_linear_gemm(escha_linear_t h, const uint16_t* x, uint16_t* y, int M,
+                                 void* stream);
+escha_status_t escha_linear_reserve(escha_linear_t h, int max_m);
+
+/*
+ * Gated MLP at decode: y = down( silu(gate(x)) * up(x) ), each matrix a dense
+ * trellis layer with its own rin/rout/s_in/s_out.  gate and up map in -> inter,
+ * down maps inter -> in.  The three handles are borrowed.  1 <= M <= 16.
+ * Source: model layout in the Qwen3.8-27B ANE notes, section 1 (MLP 5120->17408);
+ * each matrix is the activation-side layer above.
+ */
+escha_status_t escha_mlp_create(escha_mlp_t* out, escha_linear_t gate, escha_linear_t up,
+                                escha_linear_t down);
+escha_status_t escha_mlp_destroy(escha_mlp_t m);
+escha_status_t escha_mlp_gemv(escha_mlp_t m, const uint16_t* x, uint16_t* y, int M, void* stream);
+
+/*
+ * Routed-expert layer (EXLR8 page, "The sharing trick" and the GLM-5.3 expert
+ * shapes): E experts, each with gate/up [hidden -> inter] and down [inter ->
+ * hidden] trellis matrices at its own width bits[e] in {2,3,4}.  The hidden side
+ * is shared by all experts: gate/up use one su_hidden = rin_hidden * s_in_hidden
+ * and down uses one sv_hidden = rout_hidden * s_out_hidden, so a token is rotated
+ * once and one rotated activation serves every routed expert.  The intermediate
+ * side is per expert.
+ *   gate_code/up_code/down_code: HOST arrays [E] of DEVICE pointers to each
+ *     expert's int16 code tensor ([hidden/16, inter/16, 16*b] and
+ *     [inter/16, hidden/16, 16*b]).  Borrowed.
+ *   bits: HOST int32 [E].
+ *   rin_hidden fp16 [hidden], s_in_hidden fp32 [hidden] (NULL = 1.0)
+ *   rout_gate, rout_up fp16 [E, inter]; s_out_gate, s_out_up fp32 [E, inter]
+ *   rin_down fp16 [E, inter]; s_in_down fp32 [E, inter]
+ *   rout_hidden fp16 [hidden]; s_out_hidden fp32 [hidden]
+ */
+escha_status_t escha_moe_create(escha_moe_t* out, int num_experts, int hidden, int inter,
+                                const int16_t* const* gate_code, const int16_t* const* up_code,
+                                const int16_t* const* down_code, const int32_t* bits,
+                                const uint16_t* rin_hidden, const float* s_in_hidden,
+                                const uint16_t* rout_gate, const float* s_out_gate,
+                                const uint16_t* rout_up, const float* s_out_up,
+                                const uint16_t* rin_down, const float* s_in_down,
+                                const uint16_t* rout_hidden, const float* s_out_hidden,
+                                void* stream);
+escha_status_t escha_moe_destroy(escha_moe_t m);
+
+/*
+ * y[m] = sum_k expert_w[m,k] * down_e( silu(gate_e(x[m])) * up_e(x[m]) ),
+ * e = expert_ids[m,k].  1 <= M <= 8, 1 <= topk <= 8; ids in [0, E) and distinct
+ * within a token (duplicates are summed, out-of-range ids are skipped and set
+ * the handle's error flag).
+ *   x fp16 [M, hidden]; expert_ids int32 [M, topk]; expert_w fp32 [M, topk];
+ *   y fp16 [M, hidden].  All device pointers; routing is read on the device.
+ */
+escha_status_t escha_linear_moe_gemv(escha_moe_t m, const uint16_t* x, const int32_t* expert_ids,
+                                     const float* expert_w, uint16_t* y, int M, int topk,
+                                     void* stream);
+
+/*
+ * Synchronise `stream` and report the handle's device error flag:
+ * ESCHA_ERR_TIMEOUT if a bounded wait in one of its kernels ran out,
+ * ESCHA_ERR_INVALID_ARG if routing ids were out of range, ESCHA_ERR_CUDA on an
+ * asynchronous CUDA error, else ESCHA_OK.  The flag is cleared by the read.
+ */
+escha_status_t escha_linear_check(escha_linear_t h, void* stream);
+escha_status_t escha_moe_check(escha_moe_t m, void* stream);
+
+/*
+ * Per-kernel timing of the trellis contraction launches (the dominant kernel).
+ * When enabled on a handle, every trellis GEMV/GEMM launch made for it is
+ * bracketed by CUDA events on the launching stream (inside stream capture the
+ * events become graph nodes that fire on every replay).  collect() synchronises
+ * those events and returns the summed milliseconds and the number of launches
+ * since the previous collect(), then resets.  kind selects the handle type.
+ */
+escha_status_t escha_profile_enable(void* handle, int kind, int on);
+escha_status_t escha_profile_collect(void* handle, int kind, double* ms_total, int* launches);
+#define ESCHA_KIND_LINEAR 0
+#define ESCHA_KIND_MLP 1
+#define ESCHA_KIND_MOE 2
+
+/*
+ * Self-test of the bounded device wait: launches one block that waits on an
+ * mbarrier no one arrives at, with a limit of `limit_us` microseconds (1..1e6).
+ * Returns ESCHA_ERR_TIMEOUT when the kernel gave up and reported it (the expected
+ * outcome), ESCHA_OK if the wait unexpectedly completed.  The context stays usable.
+ */
+escha_status_t escha_selftest_wait_timeout(int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ESCHA_H */
