@@ -55,6 +55,7 @@ _SIGS = {
     "escha_profile_enable": (_I, [_P, _I, _I]),
     "escha_profile_collect": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "escha_selftest_wait_timeout": (_I, [_I, _P]),
+    "escha_linear_gemv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P]),
 }
 
 

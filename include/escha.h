@@ -200,6 +200,37 @@ escha_status_t escha_profile_collect(void* handle, int kind, double* ms_total, i
 #define ESCHA_KIND_MOE 2
 
 /*
+ * Allocation-free dense layer at decode.  The source pages have no counterpart:
+ * this entry point is for callers that must not allocate device memory, such as
+ * runtimes that reserve all device memory for their own pool up front, or code
+ * running where a cudaMalloc would synchronise the device or is not allowed.
+ * It computes the same y[M, out] = had(had(x * su) @ W_inner) * sv as
+ * escha_linear_gemv, with the same kernels, but takes the layer's tensors
+ * directly (no handle, no create) and allocates nothing: its scratch (folded
+ * scales, rotated activations, partial sums) lives in one fixed device array
+ * of ESCHA_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits.
+ *   code, rin, rout, s_in, s_out: as for escha_linear_create (device pointers;
+ *     s_in / s_out may be NULL = 1.0); in_features, out_features multiples of
+ *     128; bits in {2,3,4}; x fp16 [M, in], y fp16 [M, out]; 1 <= M <= 16.
+ * Returns ESCHA_ERR_UNSUPPORTED, before launching anything, when the layer
+ * needs more scratch than the fixed array holds (folded scales 4*(in+out)
+ * bytes, rotated activations 64*in bytes and fp32 partial sums 64*out bytes
+ * per partial-sum slot, plus 512 bytes).  The first call on a device looks up
+ * the array's device address; make that first call before any stream capture.
+ * Every call reuses the same array: calls whose work overlaps on the GPU (on
+ * other streams or from other host threads) race and must be ordered by the
+ * caller.  The call is asynchronous on `stream`; it reports argument and
+ * launch errors only (there is no handle whose error flag could be read).
+ */
+#define ESCHA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const uint16_t* rin,
+                                         const uint16_t* rout, const float* s_in,
+                                         const float* s_out, int in_features, int out_features,
+                                         int bits, const uint16_t* x, uint16_t* y, int M,
+                                         void* stream);
+
+/*
  * Self-test of the bounded device wait: launches one block that waits on an
  * mbarrier no one arrives at, with a limit of `limit_us` microseconds (1..1e6).
  * Returns ESCHA_ERR_TIMEOUT when the kernel gave up and reported it (the expected
