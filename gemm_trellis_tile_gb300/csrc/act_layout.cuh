@@ -1,0 +1,67 @@
+// Activation-side helpers shared by the rotation, MLP and MoE kernels: the
+// GEMV's fragment layout for rotated activations, fp16 vector loads/stores,
+// and the sum over a 128-channel group's partial-sum slots.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace escha {
+
+// CTA that owns unit u when U units are split into G near-equal contiguous
+// ranges (CTA c owns [c*U/G, (c+1)*U/G)).
+__host__ __device__ __forceinline__ int owner_cta(long long u, long long U, int G) {
+  return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
+// Store one rotated activation (fp16 bits) at its place in the GEMV's
+// B-fragment layout: per k-tile, token block and lane (g = token % 8, t), four
+// words (x[2t], 0), (x[2t+8], 0), (x[2t+1], 0), (x[2t+9], 0).
+__device__ __forceinline__ void xfrag_store(uint32_t* xf, int TB, int m, int k, uint16_t hb) {
+  const int kt = k >> 4, kk = k & 15;
+  const int t = (kk & 7) >> 1, odd = kk & 1, hi8 = kk >> 3;
+  const int reg = 2 * odd + hi8;
+  const int tb = m >> 3, g = m & 7;
+  xf[(((size_t)kt * TB + tb) * 32 + 4 * g + t) * 4 + reg] = hb;
+}
+
+__device__ __forceinline__ void load4_half(const uint16_t* p, float (&v)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  v[0] = half_bits_to_float(raw.x & 0xFFFF);
+  v[1] = half_bits_to_float(raw.x >> 16);
+  v[2] = half_bits_to_float(raw.y & 0xFFFF);
+  v[3] = half_bits_to_float(raw.y >> 16);
+}
+
+__device__ __forceinline__ void store4_half(uint16_t* p, const float (&v)[4]) {
+  uint2 raw;
+  raw.x = float_to_half_bits(v[0]) | (uint32_t(float_to_half_bits(v[1])) << 16);
+  raw.y = float_to_half_bits(v[2]) | (uint32_t(float_to_half_bits(v[3])) << 16);
+  *reinterpret_cast<uint2*>(p) = raw;
+}
+
+__device__ __forceinline__ float4 load4_f32(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+
+// Sum a group's partial-sum slots for token m, channels 128g + 4*lane .. +3.
+// The group's KT units start at unit `ub`; slot s belongs to the s-th CTA
+// that covers them.
+__device__ __forceinline__ void sum_slots(const float* part, long long ub, int KT, int N,
+                                          long long U, int G, int mpad, int m, int g, int lane,
+                                          float (&v)[4]) {
+  const long long gb = ub + (long long)g * KT;
+  const int ns = owner_cta(gb + KT - 1, U, G) - owner_cta(gb, U, G) + 1;
+  v[0] = v[1] = v[2] = v[3] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float4 p = load4_f32(part + ((size_t)s * mpad + m) * N + 128 * g + 4 * lane);
+    v[0] += p.x;
+    v[1] += p.y;
+    v[2] += p.z;
+    v[3] += p.w;
+  }
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace escha

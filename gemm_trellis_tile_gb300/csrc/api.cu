@@ -324,19 +324,64 @@ escha_status_t escha_linear_reserve(escha_linear_t h, int max_m) {
   (void)h; (void)max_m;
   return ESCHA_ERR_UNSUPPORTED;
 }
-escha_status_t escha_moe_create(escha_moe_t* out, int, int, int, const int16_t* const*,
-                                const int16_t* const*, const int16_t* const*, const int32_t*,
-                                const uint16_t*, const float*, const uint16_t*, const float*,
-                                const uint16_t*, const float*, const uint16_t*, const float*,
-                                const uint16_t*, const float*, void*) {
-  if (out) *out = nullptr;
-  return ESCHA_ERR_UNSUPPORTED;
+escha_status_t escha_moe_create(escha_moe_t* out, int num_experts, int hidden, int inter,
+                                const int16_t* const* gate_code, const int16_t* const* up_code,
+                                const int16_t* const* down_code, const int32_t* bits,
+                                const uint16_t* rin_hidden, const float* s_in_hidden,
+                                const uint16_t* rout_gate, const float* s_out_gate,
+                                const uint16_t* rout_up, const float* s_out_up,
+                                const uint16_t* rin_down, const float* s_in_down,
+                                const uint16_t* rout_hidden, const float* s_out_hidden,
+                                void* stream) {
+  if (!out) return ESCHA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (num_experts < 1 || hidden <= 0 || inter <= 0) return ESCHA_ERR_INVALID_ARG;
+  if (num_experts > kMoeMaxExperts) return ESCHA_ERR_UNSUPPORTED;
+  if (hidden % 128 != 0 || inter % 128 != 0) return ESCHA_ERR_UNSUPPORTED;
+  if (!gate_code || !up_code || !down_code || !bits || !rin_hidden || !rout_gate || !rout_up ||
+      !rin_down || !rout_hidden)
+    return ESCHA_ERR_INVALID_ARG;
+  for (int e = 0; e < num_experts; ++e) {
+    if (!gate_code[e] || !up_code[e] || !down_code[e]) return ESCHA_ERR_INVALID_ARG;
+    if (!aligned16(gate_code[e]) || !aligned16(up_code[e]) || !aligned16(down_code[e]))
+      return ESCHA_ERR_INVALID_ARG;
+    if (bits[e] < 2 || bits[e] > 4) return ESCHA_ERR_UNSUPPORTED;
+  }
+  escha_moe_s* h = new (std::nothrow) escha_moe_s();
+  if (!h) return ESCHA_ERR_OOM;
+  escha_status_t s = moe_init(h, num_experts, hidden, inter, gate_code, up_code, down_code, bits,
+                              rin_hidden, s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up,
+                              rin_down, s_in_down, rout_hidden, s_out_hidden,
+                              static_cast<cudaStream_t>(stream));
+  if (s != ESCHA_OK) {
+    moe_free(h);
+    delete h;
+    return s;
+  }
+  *out = h;
+  return ESCHA_OK;
 }
-escha_status_t escha_moe_destroy(escha_moe_t) { return ESCHA_ERR_INVALID_ARG; }
-escha_status_t escha_linear_moe_gemv(escha_moe_t, const uint16_t*, const int32_t*, const float*,
-                                     uint16_t*, int, int, void*) {
-  return ESCHA_ERR_UNSUPPORTED;
+
+escha_status_t escha_moe_destroy(escha_moe_t m) {
+  if (!m) return ESCHA_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  moe_free(m);
+  delete m;
+  return ESCHA_OK;
 }
-escha_status_t escha_moe_check(escha_moe_t, void*) { return ESCHA_ERR_INVALID_ARG; }
+
+escha_status_t escha_linear_moe_gemv(escha_moe_t m, const uint16_t* x, const int32_t* expert_ids,
+                                     const float* expert_w, uint16_t* y, int M, int topk,
+                                     void* stream) {
+  if (!m || !x || !expert_ids || !expert_w || !y) return ESCHA_ERR_INVALID_ARG;
+  if (M < 1 || M > kMoeMaxTokens || topk < 1 || topk > kMoeMaxTopk) return ESCHA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return ESCHA_ERR_INVALID_ARG;
+  return moe_gemv(m, x, expert_ids, expert_w, y, M, topk, static_cast<cudaStream_t>(stream));
+}
+
+escha_status_t escha_moe_check(escha_moe_t m, void* stream) {
+  if (!m) return ESCHA_ERR_INVALID_ARG;
+  return read_and_clear_error(m->err, static_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"

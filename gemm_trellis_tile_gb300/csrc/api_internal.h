@@ -62,7 +62,45 @@ struct escha_mlp_s {
   escha::Profiler prof;
 };
 
+struct escha_moe_s {
+  int device = 0;
+  int num_sms = 0;
+  int E = 0, hidden = 0, inter = 0;
+  const uint8_t** gate_code = nullptr;  // device [E] tables of borrowed code pointers
+  const uint8_t** up_code = nullptr;
+  const uint8_t** down_code = nullptr;
+  int* bits = nullptr;                  // device [E]
+  float* su_hidden = nullptr;           // shared input side of gate/up [hidden]
+  float* sv_hidden = nullptr;           // shared output side of down [hidden]
+  float* sv_gate = nullptr;             // per expert [E][inter]
+  float* sv_up = nullptr;
+  float* su_down = nullptr;
+  uint32_t* xfrag_hidden = nullptr;     // rotated token(s), fragment order
+  uint32_t* xfrag_down = nullptr;       // per distinct expert slot
+  float* part1 = nullptr;               // gate/up partial sums per job
+  float* part2 = nullptr;               // down partial sums per distinct expert
+  escha::GemvJob* jobs1 = nullptr;      // written on the device each call
+  escha::GemvJob* jobs2 = nullptr;
+  unsigned char* route = nullptr;       // device routing state
+  int* err = nullptr;
+  size_t xdown_stride = 0, part1_stride = 0, part2_stride = 0;
+  int grid_max = 0;
+  escha::Profiler prof;
+};
+
 namespace escha {
+
+escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
+                        const int16_t* const* gate_code, const int16_t* const* up_code,
+                        const int16_t* const* down_code, const int32_t* bits,
+                        const uint16_t* rin_hidden, const float* s_in_hidden,
+                        const uint16_t* rout_gate, const float* s_out_gate,
+                        const uint16_t* rout_up, const float* s_out_up,
+                        const uint16_t* rin_down, const float* s_in_down,
+                        const uint16_t* rout_hidden, const float* s_out_hidden, cudaStream_t st);
+void moe_free(escha_moe_s* h);
+escha_status_t moe_gemv(escha_moe_s* h, const uint16_t* x, const int32_t* ids, const float* w,
+                        uint16_t* y, int M, int topk, cudaStream_t st);
 
 escha_status_t linear_init(escha_linear_s* h, const int16_t* code, int bits, int K, int N,
                            const uint16_t* rin, const uint16_t* rout, const float* s_in,

@@ -49,6 +49,8 @@ struct GemvArgs {
   const GemvJob* jobs;
   long long units;
   int grid;
+  const long long* dev_units;  // when set, units and grid are read from device memory
+  const int* dev_grid;         // (a schedule built on the device, e.g. by MoE routing)
   int M;
   int mpad;
   int* err;
@@ -99,7 +101,11 @@ struct ChunkIter {
     u1 = end;
     j = 0;
     load(jobs);
-    while (u >= ue && u < u1) {
+    if (u >= u1) {  // empty range: nothing to walk
+      g = kt = 0;
+      return;
+    }
+    while (u >= ue) {
       ++j;
       load(jobs);
     }
@@ -184,6 +190,13 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
   uint64_t* bars = reinterpret_cast<uint64_t*>(xfs + kStages * xf_stage_bytes<TB>());
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  long long U = a.units;
+  int G = a.grid;
+  if (a.dev_units != nullptr) {
+    U = *a.dev_units;
+    G = *a.dev_grid;
+  }
+  if (static_cast<int>(blockIdx.x) >= G) return;  // launched for the worst case; not needed
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -196,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
 
   const int c = blockIdx.x;
   ChunkIter it;
-  it.init(a.jobs, cta_start(c, a.units, a.grid), cta_start(c + 1, a.units, a.grid));
+  it.init(a.jobs, cta_start(c, U, G), cta_start(c + 1, U, G));
   Chunk ch;
 
   if (warp == kCW) {
@@ -269,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
     }
     if (ch.seg_end) {
       const long long gb = it.ub + (long long)ch.g * it.KT;
-      const int slot = c - cta_of_unit(gb, a.units, a.grid);
+      const int slot = c - cta_of_unit(gb, U, G);
       const int n0 = 128 * ch.g + 16 * warp + (lane >> 2);
       const int t2 = 2 * (lane & 3);
 #pragma unroll
@@ -339,6 +352,8 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   a.jobs = s.d_jobs;
   a.units = s.units;
   a.grid = s.grid;
+  a.dev_units = nullptr;
+  a.dev_grid = nullptr;
   a.M = M;
   a.mpad = kGemvMaxTokens;
   a.err = err;
@@ -386,6 +401,27 @@ int gemv_slots_for_group(const GemvSchedule& s, int job, int g) {
 cudaError_t launch_gemv(const GemvSchedule& s, int M, int* err, cudaStream_t st) {
   if (M <= 8) return launch_gemv_tb<1>(s, M, err, st);
   return launch_gemv_tb<2>(s, M, err, st);
+}
+
+cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* d_units,
+                                        const int* d_grid, int max_grid, int M, int mpad,
+                                        int* err, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(trellis_gemv_kernel<1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       gemv_smem_bytes<1>());
+  if (e != cudaSuccess) return e;
+  GemvArgs a;
+  a.jobs = d_jobs;
+  a.units = 0;
+  a.grid = max_grid;
+  a.dev_units = d_units;
+  a.dev_grid = d_grid;
+  a.M = M;
+  a.mpad = mpad;
+  a.err = err;
+  a.limit_ns = kWaitLimitNs;
+  trellis_gemv_kernel<1><<<max_grid, kThreads, gemv_smem_bytes<1>(), st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const int16_t* code, int bits, int K, int N, uint16_t* w,

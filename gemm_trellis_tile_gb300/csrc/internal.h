@@ -42,6 +42,13 @@ struct GemvSchedule {
 };
 
 constexpr int kGemvMaxTokens = 16;
+
+// Routed-expert limits: tokens per call, experts per token, distinct experts
+// per call (kMoeMaxTokens * kMoeMaxTopk), experts per layer.
+constexpr int kMoeMaxTokens = 8;
+constexpr int kMoeMaxTopk = 8;
+constexpr int kMoeMaxDistinct = kMoeMaxTokens * kMoeMaxTopk;
+constexpr int kMoeMaxExperts = 4096;
 constexpr int kMinUnitsPerCta = 8;
 
 int gemv_ctas_per_sm();
@@ -50,6 +57,11 @@ void plan_gemv(GemvSchedule& s, int num_sms, int ctas_per_sm);
 int gemv_slots_for_group(const GemvSchedule& s, int job, int g);
 
 cudaError_t launch_gemv(const GemvSchedule& s, int M, int* err, cudaStream_t st);
+// Up to 8 tokens, with the job table, unit count and grid size written on the
+// device (the grid is launched at max_grid; CTAs past the device grid exit).
+cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* d_units,
+                                        const int* d_grid, int max_grid, int M, int mpad,
+                                        int* err, cudaStream_t st);
 cudaError_t launch_decode(const int16_t* code, int bits, int K, int N, uint16_t* w,
                           cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);

@@ -34,6 +34,8 @@ template escha_status_t dev_alloc<float>(float**, size_t);
 template escha_status_t dev_alloc<uint32_t>(uint32_t**, size_t);
 template escha_status_t dev_alloc<uint16_t>(uint16_t**, size_t);
 template escha_status_t dev_alloc<GemvJob>(GemvJob**, size_t);
+template escha_status_t dev_alloc<const uint8_t*>(const uint8_t***, size_t);
+template escha_status_t dev_alloc<unsigned char>(unsigned char**, size_t);
 
 namespace {
 
@@ -191,6 +193,7 @@ Profiler* profiler_of(void* handle, int kind) {
   switch (kind) {
     case ESCHA_KIND_LINEAR: return &static_cast<escha_linear_s*>(handle)->prof;
     case ESCHA_KIND_MLP: return &static_cast<escha_mlp_s*>(handle)->prof;
+    case ESCHA_KIND_MOE: return &static_cast<escha_moe_s*>(handle)->prof;
     default: return nullptr;
   }
 }

@@ -8,6 +8,7 @@
 // l holds elements 4l..4l+3, two butterfly stages run in registers and five
 // across lanes (fwht128_warp), all in fp32, rounded to fp16 once at the end.
 
+#include "act_layout.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -17,50 +18,10 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
-__host__ __device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
-  return static_cast<int>(((u + 1) * G - 1) / U);
-}
-
-// Store one rotated activation (fp16 bits) at its place in the GEMV's
-// B-fragment layout: per k-tile, token block and lane (g = token % 8, t), four
-// words (x[2t], 0), (x[2t+8], 0), (x[2t+1], 0), (x[2t+9], 0).
-__device__ __forceinline__ void xfrag_store(uint32_t* xf, int TB, int m, int k, uint16_t hb) {
-  const int kt = k >> 4, kk = k & 15;
-  const int t = (kk & 7) >> 1, odd = kk & 1, hi8 = kk >> 3;
-  const int reg = 2 * odd + hi8;
-  const int tb = m >> 3, g = m & 7;
-  xf[(((size_t)kt * TB + tb) * 32 + 4 * g + t) * 4 + reg] = hb;
-}
-
-__device__ __forceinline__ void load4_half(const uint16_t* p, float (&v)[4]) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(p);
-  v[0] = half_bits_to_float(raw.x & 0xFFFF);
-  v[1] = half_bits_to_float(raw.x >> 16);
-  v[2] = half_bits_to_float(raw.y & 0xFFFF);
-  v[3] = half_bits_to_float(raw.y >> 16);
-}
-
-__device__ __forceinline__ void store4_half(uint16_t* p, const float (&v)[4]) {
-  uint2 raw;
-  raw.x = float_to_half_bits(v[0]) | (uint32_t(float_to_half_bits(v[1])) << 16);
-  raw.y = float_to_half_bits(v[2]) | (uint32_t(float_to_half_bits(v[3])) << 16);
-  *reinterpret_cast<uint2*>(p) = raw;
-}
-
 // Sum a group's partial-sum slots for token m, channels 128g + 4l .. +3.
-__device__ __forceinline__ void sum_slots(const PartRef& pr, long long U, int G, int mpad, int m,
-                                          int g, int lane, float (&v)[4]) {
-  const long long ub = pr.unit_begin + (long long)g * pr.KT;
-  const int ns = cta_of_unit(ub + pr.KT - 1, U, G) - cta_of_unit(ub, U, G) + 1;
-  v[0] = v[1] = v[2] = v[3] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float4 p = *reinterpret_cast<const float4*>(
-        pr.part + ((size_t)s * mpad + m) * pr.N + 128 * g + 4 * lane);
-    v[0] += p.x;
-    v[1] += p.y;
-    v[2] += p.z;
-    v[3] += p.w;
-  }
+__device__ __forceinline__ void sum_part_slots(const PartRef& pr, long long U, int G, int mpad,
+                                               int m, int g, int lane, float (&v)[4]) {
+  sum_slots(pr.part, pr.unit_begin, pr.KT, pr.N, U, G, mpad, m, g, lane, v);
 }
 
 __global__ void fold_scales_kernel(const uint16_t* r, const float* s, float* out, int n) {
@@ -140,7 +101,7 @@ __global__ void rotate_out_kernel(const PartRef pr, long long U, int G, const fl
   const int m = static_cast<int>(wid / NG);
   const int g = static_cast<int>(wid - (long long)m * NG);
   float v[4];
-  sum_slots(pr, U, G, mpad, m, g, lane, v);
+  sum_part_slots(pr, U, G, mpad, m, g, lane, v);
   fwht128_warp(v, lane);
   const int n0 = g * kHad + 4 * lane;
   const float4 s = *reinterpret_cast<const float4*>(sv + n0);
@@ -150,8 +111,6 @@ __global__ void rotate_out_kernel(const PartRef pr, long long U, int G, const fl
   v[3] *= kHadScale * s.w;
   store4_half(y + (size_t)m * pr.N + n0, v);
 }
-
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // Gated-MLP middle: g = had(gate_pre)*sv_g, u = had(up_pre)*sv_u, h = silu(g)*u,
 // then the down layer's input rotation had(h * su_down) into its fragments.
@@ -169,8 +128,8 @@ __global__ void mlp_mid_kernel(const PartRef gate, const PartRef up, long long U
   float h[4] = {0.f, 0.f, 0.f, 0.f};
   if (m < M) {
     float gv[4], uv[4];
-    sum_slots(gate, U, G, kGemvMaxTokens, m, g, lane, gv);
-    sum_slots(up, U, G, kGemvMaxTokens, m, g, lane, uv);
+    sum_part_slots(gate, U, G, kGemvMaxTokens, m, g, lane, gv);
+    sum_part_slots(up, U, G, kGemvMaxTokens, m, g, lane, uv);
     fwht128_warp(gv, lane);
     fwht128_warp(uv, lane);
     const float4 sg = *reinterpret_cast<const float4*>(sv_gate + n0);

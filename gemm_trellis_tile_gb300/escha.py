@@ -265,6 +265,95 @@ class MLP:
             pass
 
 
+class MoE:
+    """Routed-expert layer with one shared hidden-side rotation.
+
+    gate_codes / up_codes / down_codes: lists of E int16 CUDA tensors (they may
+    alias one another for experts that are never routed); bits: E widths.
+    Side vectors are CUDA tensors: rin_hidden, rout_hidden fp16 [hidden];
+    s_in_hidden, s_out_hidden fp32 [hidden]; rout_gate, rout_up, rin_down fp16
+    [E, inter]; s_out_gate, s_out_up, s_in_down fp32 [E, inter].
+    """
+
+    def __init__(self, hidden, inter, gate_codes, up_codes, down_codes, bits, rin_hidden,
+                 s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up, rin_down, s_in_down,
+                 rout_hidden, s_out_hidden, stream=None):
+        E = len(bits)
+        self._keep = (gate_codes, up_codes, down_codes, rin_hidden, s_in_hidden, rout_gate,
+                      s_out_gate, rout_up, s_out_up, rin_down, s_in_down, rout_hidden, s_out_hidden)
+        ptrs = ctypes.c_void_p * E
+        g = ptrs(*[t.data_ptr() for t in gate_codes])
+        u = ptrs(*[t.data_ptr() for t in up_codes])
+        d = ptrs(*[t.data_ptr() for t in down_codes])
+        b = (ctypes.c_int32 * E)(*[int(v) for v in bits])
+        self._tables = (g, u, d, b)
+        h = ctypes.c_void_p()
+        check(load().escha_moe_create(
+            ctypes.byref(h), E, hidden, inter, ctypes.cast(g, _P), ctypes.cast(u, _P),
+            ctypes.cast(d, _P), ctypes.cast(b, _P), _ptr(rin_hidden), _ptr(s_in_hidden),
+            _ptr(rout_gate), _ptr(s_out_gate), _ptr(rout_up), _ptr(s_out_up), _ptr(rin_down),
+            _ptr(s_in_down), _ptr(rout_hidden), _ptr(s_out_hidden), _stream(stream)),
+            "escha_moe_create")
+        self.handle = h
+        self.hidden = hidden
+
+    @classmethod
+    def from_arrays(cls, spec, expert_codes, device="cuda"):
+        """Build from host arrays: spec holds the side vectors and widths (see
+        synthetic.make_moe_spec); expert_codes maps expert id -> (gate, up, down)
+        int16 arrays.  Experts without codes point at one zero-filled stand-in
+        buffer (never read unless routed to)."""
+        torch = _torch()
+        E, hidden, inter = spec["num_experts"], spec["hidden"], spec["inter"]
+        dev = {e: tuple(torch.from_numpy(c).to(device) for c in codes)
+               for e, codes in expert_codes.items()}
+        stand_in = torch.zeros(hidden * inter // 2, dtype=torch.int16, device=device)
+        gates = [dev[e][0] if e in dev else stand_in for e in range(E)]
+        ups = [dev[e][1] if e in dev else stand_in for e in range(E)]
+        downs = [dev[e][2] if e in dev else stand_in for e in range(E)]
+        t = {k: torch.from_numpy(spec[k]).to(device) for k in (
+            "rin_hidden", "s_in_hidden", "rout_gate", "s_out_gate", "rout_up", "s_out_up",
+            "rin_down", "s_in_down", "rout_hidden", "s_out_hidden")}
+        obj = cls(hidden, inter, gates, ups, downs, spec["bits"], t["rin_hidden"],
+                  t["s_in_hidden"], t["rout_gate"], t["s_out_gate"], t["rout_up"], t["s_out_up"],
+                  t["rin_down"], t["s_in_down"], t["rout_hidden"], t["s_out_hidden"])
+        obj._keep_dev = (dev, stand_in, t)
+        return obj
+
+    def gemv(self, x, expert_ids, expert_w, y=None, stream=None):
+        torch = _torch()
+        _dev(x, torch.float16)
+        _dev(expert_ids, torch.int32)
+        _dev(expert_w, torch.float32)
+        m, topk = expert_ids.shape
+        if y is None:
+            y = torch.empty((m, self.hidden), dtype=torch.float16, device=x.device)
+        check(load().escha_linear_moe_gemv(self.handle, _ptr(x), _ptr(expert_ids), _ptr(expert_w),
+                                           _ptr(y), m, topk, _stream(stream)),
+              "escha_linear_moe_gemv")
+        return y
+
+    def check(self, stream=None):
+        return load().escha_moe_check(self.handle, _stream(stream))
+
+    def profile(self, on=True):
+        check(load().escha_profile_enable(self.handle, KIND_MOE, int(on)), "escha_profile_enable")
+
+    def collect(self):
+        return _collect(self.handle, KIND_MOE)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            load().escha_moe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def selftest_wait_timeout(limit_us=10000, stream=None):
     """Run the bounded-wait self test; returns the status code (5 = timed out as designed)."""
     return load().escha_selftest_wait_timeout(int(limit_us), _stream(stream))

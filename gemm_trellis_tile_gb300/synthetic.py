@@ -50,28 +50,49 @@ def make_mlp(rng, hidden, inter, bits_gate, bits_up, bits_down):
                 down=make_linear(rng, inter, hidden, bits_down, guard=True))
 
 
-def make_moe(rng, num_experts, hidden, inter, bits_choices=(2, 3, 4)):
-    """Routed-expert stack with one shared hidden-side rotation.
+def make_moe_spec(seed, num_experts, hidden, inter, bits_choices=(2, 3, 4)):
+    """Routed-expert stack: widths, shared hidden-side vectors and per-expert
+    intermediate-side vectors.  Code words are drawn per expert on demand
+    (make_moe_expert_codes), so a test can build only the experts it routes to.
 
     Every expert gets one width b_e drawn uniformly from bits_choices for all
     three of its matrices.  The hidden side (gate/up input, down output) uses
-    one shared rin/s_in and one shared rout/s_out for all experts; the
-    intermediate side is per expert.
+    one shared rin/s_in and one shared rout/s_out; the intermediate side is per
+    expert.  rout vectors carry the fp16 range guard of their matrix.
     """
-    bits = rng.choice(np.asarray(bits_choices, dtype=np.int32), size=num_experts)
-    experts = []
-    for e in range(num_experts):
-        b = int(bits[e])
-        g = make_linear(rng, hidden, inter, b, guard=True)
-        u = make_linear(rng, hidden, inter, b, guard=True)
-        d = make_linear(rng, inter, hidden, b, guard=True)
-        experts.append(dict(gate=g, up=u, down=d, bits=b))
-    shared = make_linear(rng, hidden, hidden, 2)  # only its side vectors are used
-    gk = overflow_guard_shift(inter)
-    return dict(experts=experts, bits=bits, hidden=hidden, inter=inter,
-                rin_hidden=shared["rin"], s_in_hidden=shared["s_in"],
-                rout_hidden=(shared["rout"].astype(np.float64) * 2.0 ** (-gk)).astype(np.float16),
-                s_out_hidden=shared["s_out"])
+    rng = np.random.default_rng([seed, 0])
+    E = num_experts
+    bits = rng.choice(np.asarray(bits_choices, dtype=np.int32), size=E).astype(np.int32)
+    kg = overflow_guard_shift(hidden)   # gate/up: hidden -> inter
+    kd = overflow_guard_shift(inter)    # down: inter -> hidden
+
+    def f16(a):
+        return a.astype(np.float16)
+
+    return dict(
+        seed=seed, num_experts=E, hidden=hidden, inter=inter, bits=bits,
+        rin_hidden=f16(rng.normal(1.0, 0.1, hidden)),
+        s_in_hidden=rng.uniform(0.98, 1.02, hidden).astype(np.float32),
+        rout_hidden=f16(rng.normal(1.0, 0.1, hidden) * 2.0 ** (-kd)),
+        s_out_hidden=rng.uniform(0.98, 1.02, hidden).astype(np.float32),
+        rout_gate=f16(rng.normal(1.0, 0.1, (E, inter)) * 2.0 ** (-kg)),
+        s_out_gate=rng.uniform(0.98, 1.02, (E, inter)).astype(np.float32),
+        rout_up=f16(rng.normal(1.0, 0.1, (E, inter)) * 2.0 ** (-kg)),
+        s_out_up=rng.uniform(0.98, 1.02, (E, inter)).astype(np.float32),
+        rin_down=f16(rng.normal(1.0, 0.1, (E, inter))),
+        s_in_down=rng.uniform(0.98, 1.02, (E, inter)).astype(np.float32),
+    )
+
+
+def make_moe_expert_codes(spec, e):
+    """Code words of expert e: (gate, up, down) int16 tensors."""
+    rng = np.random.default_rng([spec["seed"], 1, int(e)])
+    b = int(spec["bits"][e])
+    h, i = spec["hidden"], spec["inter"]
+    gate = rng.integers(-32768, 32768, size=(h // 16, i // 16, 16 * b), dtype=np.int16)
+    up = rng.integers(-32768, 32768, size=(h // 16, i // 16, 16 * b), dtype=np.int16)
+    down = rng.integers(-32768, 32768, size=(i // 16, h // 16, 16 * b), dtype=np.int16)
+    return gate, up, down
 
 
 def make_routing(rng, m, num_experts, topk=8):
