@@ -42,9 +42,10 @@ def parse_args():
     p.add_argument("--steps", type=int, default=4000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="escha", choices=["escha", "reference"])
-    p.add_argument("--workload", default="mlp", choices=["mlp", "linear512", "sweep"])
+    p.add_argument("--workload", default="mlp", choices=["mlp", "linear512", "sweep", "prefill"])
     p.add_argument("--m", type=int, default=1, help="tokens per step")
-    p.add_argument("--shape", default="5120x10240", help="sweep shape in x out")
+    p.add_argument("--shape", default=None, help="in x out (sweep: default 5120x10240; "
+                   "prefill: default 5120x17408)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
@@ -134,7 +135,11 @@ def workload_spec(args):
     if args.workload == "linear512":
         return dict(kind="linear", layers=[(512, 512, 2)], seed=S.seed_for(0),
                     name="single linear 512x512 2-bit, M=%d" % args.m)
-    k, n = (int(v) for v in args.shape.split("x"))
+    if args.workload == "prefill":
+        k, n = (int(v) for v in (args.shape or "5120x17408").split("x"))
+        return dict(kind="prefill", layers=[(k, n, 3)], seed=S.seed_for(4, k),
+                    name="prefill GEMM %dx%d 3-bit, M=%d tokens" % (k, n, args.m))
+    k, n = (int(v) for v in (args.shape or "5120x10240").split("x"))
     return dict(kind="linear", layers=[(k, n, 2)], seed=S.seed_for(2, k),
                 name="decode sweep linear %dx%d 2-bit, M=%d" % (k, n, args.m))
 
@@ -244,6 +249,111 @@ def run_reference(args, spec, rank):
 
 # ---------------------------------------------------------------- GPU leg
 
+def run_prefill(args, spec, rank, world, local):
+    """Prefill GEMM: TFLOP/s of 2*M*in*out per step against the tensor peak."""
+    import torch
+    from gemm_trellis_tile_gb300 import build, escha
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    build.build()
+    escha.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    m = args.m
+    k, n, b = spec["layers"][0]
+    n_inst = 4   # rotating weight sets: 4 x code + activations + outputs > L2
+    lins = []
+    for r in range(n_inst):
+        lins.append(escha.Linear.from_arrays(S.make_linear(np.random.default_rng(
+            spec["seed"] + 7919 * r + 1000003 * rank), k, n, b)))
+    rng = np.random.default_rng(spec["seed"] + 17)
+    x_host = torch.from_numpy(S.make_activations(rng, m, k)).pin_memory()
+    x = x_host.to(dev)
+    y = torch.empty((m, n), dtype=torch.float16, device=dev)
+    for lin in lins:
+        lin.reserve(m)
+    for i in range(max(args.warmup, 3)):
+        lins[i % n_inst].gemm(x, y)
+    torch.cuda.synchronize()
+    for lin in lins:
+        if lin.check() != 0:
+            raise SystemExit("device error flag set during warm-up")
+        lin.profile(True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        lins[i % n_inst].gemm(x, y)
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    k_ms, k_n = 0.0, 0
+    for lin in lins:
+        a, c = lin.collect()
+        k_ms += a
+        k_n += c
+        lin.profile(False)
+    flops = WL.layer_flops(m, k, n)
+    achieved = flops * k_n / (k_ms / 1e3) / 1e12 if k_ms > 0 else None
+    # e2e: host activations in, host result out, through the public call
+    y_host = torch.empty((m, n), dtype=torch.float16).pin_memory()
+    e_steps = min(args.steps, 20)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e_steps):
+        x.copy_(x_host, non_blocking=True)
+        lins[i % n_inst].gemm(x, y)
+        y_host.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    for lin in lins:
+        if lin.check() != 0:
+            raise SystemExit("device error flag set")
+    peaks, src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    value = world * args.steps * flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "prefill TFLOP/s (2*M*in*out per step)", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded uniform code words)",
+        "config": {"workload": spec["name"], "tokens": m,
+                   "l2": "4 rotating weight sets; activations %.0f MB, output %.0f MB per step"
+                         % (m * k * 2 / 1e6, m * n * 2 / 1e6),
+                   "timing": "CUDA events around back-to-back public API calls"},
+        "roofline": {"bound": "tensor", "kernel": "trellis_gemm", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak if achieved else None, "traffic": None,
+                     "peak_source": src + " (MEASURED_PEAKS.json bf16_tflops burst; fp16 has "
+                                    "the same nominal dense rate)"},
+        "e2e": {"value": e_steps * flops / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(y_host.numel() * 2)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def make_handles(spec, inst):
     from gemm_trellis_tile_gb300 import escha
     if spec["kind"] == "mlp":
@@ -258,9 +368,13 @@ def make_handles(spec, inst):
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.workload == "prefill" and args.m == 1:
+        args.m = 2048
     spec = workload_spec(args)
     if args.impl == "reference":
         return run_reference(args, spec, rank)
+    if spec["kind"] == "prefill":
+        return run_prefill(args, spec, rank, world, local)
 
     import torch
     from gemm_trellis_tile_gb300 import build, escha

@@ -314,15 +314,17 @@ escha_status_t escha_selftest_wait_timeout(int limit_us, void* stream) {
   return s;
 }
 
-// Entry points whose kernels are not built yet report that plainly.
 escha_status_t escha_linear_gemm(escha_linear_t h, const uint16_t* x, uint16_t* y, int M,
                                  void* stream) {
-  (void)h; (void)x; (void)y; (void)M; (void)stream;
-  return ESCHA_ERR_UNSUPPORTED;
+  if (!h || !x || !y) return ESCHA_ERR_INVALID_ARG;
+  if (M < 1) return ESCHA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return ESCHA_ERR_INVALID_ARG;
+  return linear_gemm(h, x, y, M, static_cast<cudaStream_t>(stream));
 }
+
 escha_status_t escha_linear_reserve(escha_linear_t h, int max_m) {
-  (void)h; (void)max_m;
-  return ESCHA_ERR_UNSUPPORTED;
+  if (!h || max_m < 1) return ESCHA_ERR_INVALID_ARG;
+  return linear_reserve(h, max_m);
 }
 escha_status_t escha_moe_create(escha_moe_t* out, int num_experts, int hidden, int inter,
                                 const int16_t* const* gate_code, const int16_t* const* up_code,

@@ -108,6 +108,9 @@ escha_status_t linear_init(escha_linear_s* h, const int16_t* code, int bits, int
 void linear_free(escha_linear_s* h);
 escha_status_t linear_gemv(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
                            cudaStream_t st);
+escha_status_t linear_reserve(escha_linear_s* h, int rows);
+escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
+                           cudaStream_t st);
 escha_status_t mlp_init(escha_mlp_s* m, escha_linear_s* gate, escha_linear_s* up,
                         escha_linear_s* down);
 void mlp_free(escha_mlp_s* m);

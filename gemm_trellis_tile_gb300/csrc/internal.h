@@ -62,6 +62,10 @@ cudaError_t launch_gemv(const GemvSchedule& s, int M, int* err, cudaStream_t st)
 cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* d_units,
                                         const int* d_grid, int max_grid, int M, int mpad,
                                         int* err, cudaStream_t st);
+// Prefill GEMM on tcgen05: y = fp16(had128(xh @ W_inner) * sv) for any M >= 1;
+// xh is fp16 [M, K], 16-byte aligned.
+cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, int M, int K,
+                                int N, const float* sv, uint16_t* y, int* err, cudaStream_t st);
 cudaError_t launch_decode(const int16_t* code, int bits, int K, int N, uint16_t* w,
                           cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);

@@ -124,6 +124,32 @@ escha_status_t linear_gemv(escha_linear_s* h, const uint16_t* x, uint16_t* y, in
   return from_cuda(e);
 }
 
+escha_status_t linear_reserve(escha_linear_s* h, int rows) {
+  if (rows <= h->xh_rows) return ESCHA_OK;
+  if (h->xh) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ESCHA_ERR_CUDA;
+    cudaFree(h->xh);
+    h->xh = nullptr;
+    h->xh_rows = 0;
+  }
+  escha_status_t s = dev_alloc(&h->xh, (size_t)rows * h->K);
+  if (s != ESCHA_OK) return s;
+  h->xh_rows = rows;
+  return ESCHA_OK;
+}
+
+escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
+                           cudaStream_t st) {
+  escha_status_t s = linear_reserve(h, M);
+  if (s != ESCHA_OK) return s;
+  cudaError_t e = launch_rotate_in_plain(x, h->su, h->xh, M, h->K, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  h->prof.begin(st);
+  e = launch_trellis_gemm(h->xh, h->code, h->bits, M, h->K, h->N, h->sv, y, h->err, st);
+  h->prof.end(st);
+  return from_cuda(e);
+}
+
 escha_status_t mlp_init(escha_mlp_s* m, escha_linear_s* gate, escha_linear_s* up,
                         escha_linear_s* down) {
   m->gate = gate;
