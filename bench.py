@@ -42,7 +42,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=4000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="escha", choices=["escha", "reference"])
-    p.add_argument("--workload", default="mlp", choices=["mlp", "linear512", "sweep", "prefill"])
+    p.add_argument("--workload", default="mlp", choices=["mlp", "linear512", "sweep", "prefill", "moe"])
     p.add_argument("--m", type=int, default=1, help="tokens per step")
     p.add_argument("--shape", default=None, help="in x out (sweep: default 5120x10240; "
                    "prefill: default 5120x17408)")
@@ -135,6 +135,10 @@ def workload_spec(args):
     if args.workload == "linear512":
         return dict(kind="linear", layers=[(512, 512, 2)], seed=S.seed_for(0),
                     name="single linear 512x512 2-bit, M=%d" % args.m)
+    if args.workload == "moe":
+        return dict(kind="moe", layers=WL.mlp_layers(6144, 2048, (3, 3, 3)), seed=S.seed_for(3),
+                    name="routed MoE 256 experts 6144->2048->6144, 2/3/4-bit per expert, top-8, "
+                         "M=%d" % args.m)
     if args.workload == "prefill":
         k, n = (int(v) for v in (args.shape or "5120x17408").split("x"))
         return dict(kind="prefill", layers=[(k, n, 3)], seed=S.seed_for(4, k),
@@ -248,6 +252,148 @@ def run_reference(args, spec, rank):
 
 
 # ---------------------------------------------------------------- GPU leg
+
+def run_moe(args, spec, rank, world, local):
+    """Routed experts at decode: GB/s of the algorithmic bytes of each step's
+    distinct routed experts (their code words and side vectors, the shared
+    hidden vectors, activations), over 64 cycled seeded routings."""
+    import torch
+    from gemm_trellis_tile_gb300 import build, escha
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    build.build()
+    escha.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    E, hidden, inter, m = 256, 6144, 2048, args.m
+    mspec = S.make_moe_spec(spec["seed"] + 1000003 * rank, E, hidden, inter)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(spec["seed"] + 1000003 * rank)
+    codes = []
+    for e in range(E):
+        b = int(mspec["bits"][e])
+        shapes = [(hidden // 16, inter // 16, 16 * b)] * 2 + [(inter // 16, hidden // 16, 16 * b)]
+        codes.append(tuple(torch.randint(-32768, 32768, sh, dtype=torch.int16, device=dev,
+                                         generator=gen) for sh in shapes))
+    t = {k: torch.from_numpy(mspec[k]).to(dev) for k in (
+        "rin_hidden", "s_in_hidden", "rout_gate", "s_out_gate", "rout_up", "s_out_up",
+        "rin_down", "s_in_down", "rout_hidden", "s_out_hidden")}
+    moe = escha.MoE(hidden, inter, [c[0] for c in codes], [c[1] for c in codes],
+                    [c[2] for c in codes], mspec["bits"], t["rin_hidden"], t["s_in_hidden"],
+                    t["rout_gate"], t["s_out_gate"], t["rout_up"], t["s_out_up"], t["rin_down"],
+                    t["s_in_down"], t["rout_hidden"], t["s_out_hidden"])
+    rng = np.random.default_rng(spec["seed"] + 29)
+    R = 64
+    routes = [S.make_routing(rng, m, E, 8) for _ in range(R)]
+    ids_d = [torch.from_numpy(r[0]).to(dev) for r in routes]
+    w_d = [torch.from_numpy(r[1]).to(dev) for r in routes]
+
+    def route_bytes(ids):
+        tot = WL.side_bytes(hidden, 0) + WL.side_bytes(0, hidden) + 2 * m * 2 * hidden
+        for e in sorted(set(ids.reshape(-1).tolist())):
+            b = int(mspec["bits"][e])
+            tot += 2 * WL.code_bytes(hidden, inter, b) + WL.code_bytes(inter, hidden, b)
+            tot += 3 * 6 * inter
+        return tot
+    rbytes = [route_bytes(r[0]) for r in routes]
+    x_host = torch.from_numpy(S.make_activations(rng, m, hidden)).pin_memory()
+    x = x_host.to(dev)
+    y = torch.empty((m, hidden), dtype=torch.float16, device=dev)
+
+    def step(i):
+        moe.gemv(x, ids_d[i % R], w_d[i % R], y)
+
+    for i in range(max(args.warmup, R)):
+        step(i)
+    torch.cuda.synchronize()
+    if moe.check() != 0:
+        raise SystemExit("device error flag set during warm-up")
+    moe.profile(True)
+    for i in range(2 * R):
+        step(i)
+    torch.cuda.synchronize()
+    moe.collect()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g_main = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_main, stream=side):
+            for i in range(R):
+                step(i)
+    torch.cuda.synchronize()
+    g_main.replay()
+    torch.cuda.synchronize()
+    moe.collect()
+    reps = max(1, args.steps // R)
+    steps = reps * R
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        g_main.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1)
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    k_ms, k_n = moe.collect()
+    moe.profile(False)
+    per_pass = sum(rbytes)
+    gemv_bytes = per_pass - R * (WL.side_bytes(hidden, 0) + WL.side_bytes(0, hidden))
+    achieved = gemv_bytes / (k_ms / 1e3) / 1e9 if k_ms > 0 else None
+    y_host = torch.empty((m, hidden), dtype=torch.float16).pin_memory()
+    e_steps = min(steps, 2 * R)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e_steps):
+        x.copy_(x_host, non_blocking=True)
+        step(i)
+        y_host.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    if moe.check() != 0:
+        raise SystemExit("device error flag set")
+    peaks, src = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    value = world * reps * per_pass / (ms / 1e3) / 1e9
+    line = {
+        "metric": "decode GEMV compressed-weight GB/s (algorithmic bytes of the routed experts)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded device-generated code "
+        "words, 64 cycled uniform top-8 routings)",
+        "config": {"workload": spec["name"], "tokens": m, "bytes_per_step": per_pass / R,
+                   "l2": "256 experts, %.1f GB of code words; 64 routings cycled"
+                         % (sum(c.numel() * 2 for cc in codes for c in cc) / 1e9),
+                   "timing": "CUDA graph of 64 public API calls, CUDA events"},
+        "roofline": {"bound": "hbm", "kernel": "trellis_gemv (MoE jobs)", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak if achieved else None,
+                     "traffic": None, "peak_source": src + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": e_steps * (per_pass / R) / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(y_host.numel() * 2)},
+        "gpu_launches": 6 * steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
 
 def run_prefill(args, spec, rank, world, local):
     """Prefill GEMM: TFLOP/s of 2*M*in*out per step against the tensor peak."""
@@ -375,6 +521,8 @@ def main():
         return run_reference(args, spec, rank)
     if spec["kind"] == "prefill":
         return run_prefill(args, spec, rank, world, local)
+    if spec["kind"] == "moe":
+        return run_moe(args, spec, rank, world, local)
 
     import torch
     from gemm_trellis_tile_gb300 import build, escha

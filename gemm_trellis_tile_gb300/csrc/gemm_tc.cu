@@ -14,7 +14,7 @@
 //              tcgen05.mma kind::f16 instructions (2 accumulators x 4 K-steps)
 //              once a stage's A has landed and its B is decoded; a
 //              tcgen05.commit frees the stage.
-//   warps 2-9  decoders: each decodes 4 tiles per block in registers and
+//   warps 2-17 decoders: each decodes 2 tiles per block in registers and
 //              stores fp16 pairs straight into the canonical K-major
 //              128B-swizzled B layout; then the epilogue: TMEM -> registers ->
 //              shared stash, 128-point Hadamard across each row's 128 output
@@ -38,8 +38,8 @@ constexpr int kBM = 256;          // rows per CTA (two M=128 MMAs)
 constexpr int kBN = 128;          // output channels per CTA (= one Hadamard block)
 constexpr int kBK = 64;           // K per pipeline stage (128 bytes of fp16)
 constexpr int kStagesG = 4;
-constexpr int kThreadsG = 320;    // 10 warps
-constexpr int kDecWarps = 8;
+constexpr int kThreadsG = 576;    // 18 warps
+constexpr int kDecWarps = 16;
 constexpr int kTmemCols = 256;
 
 constexpr int kABytes = kBM * kBK * 2;           // 32 KB
@@ -253,9 +253,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     }
   } else {
     // ---------------------------------------------------------- decoders
-    const int dw = warp - 2;          // 0..7
-    const int kt_local = dw >> 1;     // k-tile row within the block
-    const int nt_base = (dw & 1) * 4; // 4 n-tiles per warp
+    const int dw = warp - 2;          // 0..15
+    const int kt_local = dw >> 2;     // k-tile row within the block
+    const int nt_base = (dw & 3) * 2; // 2 n-tiles per warp
     const LaneWindow lw = lane_window<BITS>(lane);
     const int g = lane >> 2, t = lane & 3;
     bool ok = true;
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       const uint8_t* codes = stage_code(s);
       uint8_t* bt = smem + (stage_b(s) - base);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i) {
         const int nt = nt_base + i;
         const uint32_t* tw = reinterpret_cast<const uint32_t*>(codes + (kt_local * 8 + nt) * T);
         uint32_t h[8];
@@ -291,8 +291,10 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     }
 
     // ---------------------------------------------------------- epilogue
-    const int acc = dw >> 2;          // warps 2-5: rows 0-127, warps 6-9: rows 128-255
+    // Pass 1: each (accumulator, TMEM lane quadrant, 64-column half) is one warp.
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+    const int acc = (dw >> 2) & 1;
+    const int half = dw >> 3;
     __syncwarp();
     const bool have = ok && mbar_wait(bar(12), 0, a.limit_ns);
     if (!have && ok) set_error(a.err, kDevErrTimeout);
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     if (have) {
       const int row = acc * 128 + quad * 32 + lane;
 #pragma unroll
-      for (int c = 0; c < kBN; c += 32) {
+      for (int c = 64 * half; c < 64 * half + 64; c += 32) {
         uint32_t r[32];
         tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kBN + c, r);
         tmem_wait_ld();
@@ -311,21 +313,22 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     }
     tc_fence_before();
     named_barrier(1, kDecWarps * 32);
+    // Pass 2: one warp per row, element lane + 32*q in v[q].
     if (have) {
-      const float4 svv = load4_f32(a.sv + n0 + 4 * lane);
-      for (int rr = 0; rr < 32; ++rr) {
-        const int row = dw * 32 + rr;
+      float svv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) svv[q] = a.sv[n0 + lane + 32 * q] * kHadScale;
+      for (int rr = 0; rr < kBM / kDecWarps; ++rr) {
+        const int row = dw * (kBM / kDecWarps) + rr;
         const int m = m0 + row;
         if (m >= a.M) break;
         float v[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = stash[row * kStashStride + 4 * lane + q];
-        fwht128_warp(v, lane);
-        v[0] *= kHadScale * svv.x;
-        v[1] *= kHadScale * svv.y;
-        v[2] *= kHadScale * svv.z;
-        v[3] *= kHadScale * svv.w;
-        store4_half(a.y + (size_t)m * a.N + n0 + 4 * lane, v);
+        for (int q = 0; q < 4; ++q) v[q] = stash[row * kStashStride + lane + 32 * q];
+        fwht128_warp_strided(v, lane);
+        uint16_t* yr = a.y + (size_t)m * a.N + n0 + lane;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) yr[32 * q] = float_to_half_bits(v[q] * svv[q]);
       }
     }
   }
