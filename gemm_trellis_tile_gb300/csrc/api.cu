@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <new>
 #include <utility>
@@ -17,8 +18,12 @@ using namespace escha;
 
 namespace escha {
 
+static thread_local char g_last_error[256] = "";
+
 escha_status_t from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return ESCHA_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+           cudaGetErrorString(e));
   if (e == cudaErrorMemoryAllocation) return ESCHA_ERR_OOM;
   return ESCHA_ERR_CUDA;
 }
@@ -177,6 +182,8 @@ const char* escha_status_string(escha_status_t s) {
 }
 
 int escha_version(void) { return 100; }
+
+const char* escha_last_error_string(void) { return g_last_error; }
 
 escha_status_t escha_linear_create(escha_linear_t* out, const int16_t* code, const uint16_t* rin,
                                    const uint16_t* rout, const float* s_in, const float* s_out,

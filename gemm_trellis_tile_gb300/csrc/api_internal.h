@@ -45,6 +45,7 @@ struct escha_linear_s {
   escha::GemvSchedule sched;  // one job: this matrix
   uint16_t* xh = nullptr;     // prefill workspace: rotated activations [xh_rows, K]
   int xh_rows = 0;
+  float* gemm_ws = nullptr;   // prefill partial sums of tiles shared between CTAs
   escha::Profiler prof;
 };
 

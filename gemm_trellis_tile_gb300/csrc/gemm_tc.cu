@@ -3,24 +3,30 @@
 // (activation-side reconstruction, "Escha-W2 runs on Metal"; decode as in
 // "The escha W2 format, recovered and verified", "Bit layout" / "Codebook").
 //
-// One CTA computes a 256 x 128 output tile (two M=128 accumulators in TMEM
-// sharing one decoded B tile, so each weight is decoded once per 256 rows).
-// The K loop runs in blocks of 64 (one 128-byte swizzle row of fp16) through
-// a 4-stage shared-memory ring:
-//   warp 0     producer: TMA tiled load of the A block (256 x 64, 128B
-//              swizzle, rows past M zero-filled) and 1-D bulk copies of the
-//              4 x 8 code tiles of the block, on one mbarrier.
-//   warp 1     owns TMEM (256 columns) and, from one lane, issues the
-//              tcgen05.mma kind::f16 instructions (2 accumulators x 4 K-steps)
-//              once a stage's A has landed and its B is decoded; a
-//              tcgen05.commit frees the stage.
-//   warps 2-17 decoders: each decodes 2 tiles per block in registers and
-//              stores fp16 pairs straight into the canonical K-major
-//              128B-swizzled B layout; then the epilogue: TMEM -> registers ->
-//              shared stash, 128-point Hadamard across each row's 128 output
-//              channels (one warp per row), * sv, coalesced fp16 stores.
+// Tiles are 512 x 128 (rows x output channels): four M=128 accumulators in
+// TMEM (all 512 columns) share one decoded 128 x 64 B block per K step, so each
+// weight is decoded once per 512 rows.  The kernel is persistent: the grid's
+// CTAs split the (tile, K-block) units evenly and contiguously (stream-K).  A
+// CTA whose range covers a whole tile runs the fused epilogue; where a tile is
+// shared between CTAs each writes its fp32 partial sums and a fix-up kernel
+// sums them and applies the epilogue.
+//
+// Warp roles (19 warps):
+//   warp 0      A producer: TMA tiled loads of the 512 x 64 activation block
+//               (two 256-row boxes, 128B swizzle, rows past M zero-filled)
+//               into a 2-stage ring.
+//   warp 1      code producer: 1-D bulk copies of the block's 4 x 8 code tiles
+//               into a 4-stage ring.
+//   warp 2      owns TMEM; one lane issues tcgen05.mma kind::f16 (4 accumulators
+//               x 4 K16 steps per block) and the commits that free the rings.
+//   warps 3-18  decoders: two tiles per warp per block, decoded in registers
+//               and stored as fp16 pairs into the canonical K-major 128B-swizzled
+//               B layout (3-stage ring); then, per tile, the epilogue: the
+//               128-point Hadamard over each row is done in registers (two
+//               64-point halves written back to TMEM, then the last stage),
+//               * sv, fp16 stores -- or the raw fp32 partial sums.
 // Every mbarrier wait is bounded; a wait that runs out sets the error word and
-// the CTA unwinds without hanging (TMEM is always released).
+// the CTA unwinds (TMEM is always released, in-flight copies are drained).
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -34,30 +40,50 @@ namespace escha {
 
 namespace {
 
-constexpr int kBM = 256;          // rows per CTA (two M=128 MMAs)
-constexpr int kBN = 128;          // output channels per CTA (= one Hadamard block)
-constexpr int kBK = 64;           // K per pipeline stage (128 bytes of fp16)
-constexpr int kStagesG = 4;
-constexpr int kThreadsG = 576;    // 18 warps
+constexpr int kBM = 512;          // rows per tile (four M=128 accumulators)
+constexpr int kBN = 128;          // output channels per tile (= one Hadamard block)
+constexpr int kBK = 64;           // K per block (128 bytes of fp16)
+constexpr int kAStages = 2;
+constexpr int kBStages = 3;
+constexpr int kCStages = 4;
 constexpr int kDecWarps = 16;
-constexpr int kTmemCols = 256;
+constexpr int kFirstDec = 3;
+constexpr int kThreadsG = (kFirstDec + kDecWarps) * 32;  // 608
+constexpr int kTmemCols = 512;
 
-constexpr int kABytes = kBM * kBK * 2;           // 32 KB
-constexpr int kBBytes = kBN * kBK * 2;           // 16 KB
-constexpr int kCodeBytes = 4 * 8 * 128;          // 4 k-tiles x 8 n-tiles, sized for 4 bits
-constexpr int kStageBytes = kABytes + kBBytes + kCodeBytes;
-constexpr int kStashStride = kBN + 1;            // floats per stashed row (bank-conflict free)
-constexpr int kSmemBytes = kStagesG * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
-static_assert(kBM * kStashStride * 4 <= kStagesG * kStageBytes, "stash must fit the ring");
+constexpr int kABytes = kBM * kBK * 2;  // 64 KB
+constexpr int kBBytes = kBN * kBK * 2;  // 16 KB
+constexpr int kCBytes = 4 * 8 * 128;    // 4 k-tiles x 8 n-tiles, sized for 4 bits
+constexpr int kOffB = kAStages * kABytes;
+constexpr int kOffC = kOffB + kBStages * kBBytes;
+constexpr int kOffBar = kOffC + kCStages * kCBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+
+// barrier indices
+constexpr int kBarAFull = 0, kBarAEmpty = 2, kBarCFull = 4, kBarCEmpty = 8, kBarBFull = 12,
+              kBarBEmpty = 15, kBarAcc = 18, kBarTmemFree = 19, kBarDrain = 20, kNumBars = 21;
 
 struct GemmArgs {
   const uint8_t* code;
   const float* sv;
   uint16_t* y;
+  float* ws;             // partial sums: [grid][2][kBM][kBN] fp32
   int M, N, K;
+  int n_blocks;          // N / kBN
+  int kb_per_tile;       // K / kBK
+  long long units;       // tiles * kb_per_tile
+  int grid;
   int* err;
   uint64_t limit_ns;
 };
+
+__host__ __device__ __forceinline__ long long range_start(long long c, long long U, int G) {
+  return (c * U) / G;
+}
+
+__host__ __device__ __forceinline__ int owner(long long u, long long U, int G) {
+  return static_cast<int>(((u + 1) * G - 1) / U);
+}
 
 // ---------------------------------------------------------------- PTX wrappers
 
@@ -110,7 +136,8 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
       "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -120,13 +147,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-
-__device__ __forceinline__ void named_barrier(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand whose rows are 128 bytes
@@ -143,11 +202,59 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
 
 // Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D,
 // M = 128, N = 128.
-constexpr uint32_t kIdesc = (1u << 4)            // D format: f32
-                            | (0u << 7)          // A format: f16
-                            | (0u << 10)         // B format: f16
-                            | ((kBN >> 3) << 17) // N / 8
+constexpr uint32_t kIdesc = (1u << 4)              // D format: f32
+                            | (0u << 7)            // A format: f16
+                            | (0u << 10)           // B format: f16
+                            | ((kBN >> 3) << 17)   // N / 8
                             | ((128 >> 4) << 24);  // M / 16
+
+// Walsh-Hadamard butterflies (natural order, unnormalised) over 32 values
+// held in registers.
+__device__ __forceinline__ void fwht32_regs(float (&v)[32]) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((i & h) == 0) {
+        const float p = v[i], q = v[i + h];
+        v[i] = p + q;
+        v[i + h] = p - q;
+      }
+    }
+  }
+}
+
+// Position in a ring of S stages: stage index and phase parity.
+template <int S>
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void advance() {
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// One tile segment of a CTA's range: tile index and K-block range [kb0, kb1).
+struct Segment {
+  int tile, kb0, kb1;
+};
+
+struct SegIter {
+  long long u, u1;
+  int KB;
+  __device__ __forceinline__ bool next(Segment& s) {
+    if (u >= u1) return false;
+    s.tile = static_cast<int>(u / KB);
+    s.kb0 = static_cast<int>(u - (long long)s.tile * KB);
+    const long long left = u1 - u;
+    s.kb1 = (left >= KB - s.kb0) ? KB : s.kb0 + static_cast<int>(left);
+    u += s.kb1 - s.kb0;
+    return true;
+  }
+};
 
 // ---------------------------------------------------------------- kernel
 
@@ -158,35 +265,37 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  // ring: per stage [A 32 KB][B 16 KB][codes 4 KB]; then barriers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStagesG * kStageBytes);
-  // bars[0..3] load_full, [4..7] b_full, [8..11] empty, [12] acc_full, [13] mma_done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  auto stage_a = [&](int s) { return base + s * kStageBytes; };
-  auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
-  auto stage_code = [&](int s) { return smem + s * kStageBytes + kABytes + kBBytes; };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars + 1);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_block = blockIdx.x;
-  const int m0 = blockIdx.y * kBM;
-  const int n0 = n_block * kBN;
-  const int num_kb = a.K / kBK;
   constexpr int T = 32 * BITS;
   const int NT = a.N / 16;
+  const int c = blockIdx.x;
+  const long long u_begin = range_start(c, a.units, a.grid);
+  const long long u_end = range_start(c + 1, a.units, a.grid);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesG; ++s) {
-      mbar_init(bar(s), 1);              // load_full: producer arrive + tx bytes
-      mbar_init(bar(4 + s), kDecWarps);  // b_full: one arrive per decoder warp
-      mbar_init(bar(8 + s), 1);          // empty: tcgen05.commit
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(bar(kBarAFull + s), 1);
+      mbar_init(bar(kBarAEmpty + s), 1);
     }
-    mbar_init(bar(12), 1);  // acc_full
-    mbar_init(bar(13), 1);  // mma_done (unwinding)
+    for (int s = 0; s < kCStages; ++s) {
+      mbar_init(bar(kBarCFull + s), 1);
+      mbar_init(bar(kBarCEmpty + s), kDecWarps);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(bar(kBarBFull + s), kDecWarps);
+      mbar_init(bar(kBarBEmpty + s), 1);
+    }
+    mbar_init(bar(kBarAcc), 1);
+    mbar_init(bar(kBarTmemFree), kDecWarps);
+    mbar_init(bar(kBarDrain), 1);
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 2) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
     tc_fence_before();
@@ -195,150 +304,299 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  SegIter it{u_begin, u_end, a.kb_per_tile};
+  Segment seg;
+
   if (warp == 0) {
-    // ---------------------------------------------------------- producer
+    // ---------------------------------------------------------- A producer
     if (lane == 0) {
-      int armed[kStagesG];
-      for (int s = 0; s < kStagesG; ++s) armed[s] = -1;
+      int armed[kAStages] = {-1, -1};
       bool ok = true;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % kStagesG;
-        const uint32_t ph = (kb / kStagesG) & 1;
-        if (!mbar_wait(bar(8 + s), ph ^ 1u, a.limit_ns)) {
-          set_error(a.err, kDevErrTimeout);
-          ok = false;
-          break;
+      Ring<kAStages> ra;
+      while (ok && it.next(seg)) {
+        const int m0 = (seg.tile / a.n_blocks) * kBM;
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb, ra.advance()) {
+          const int s = ra.stage;
+          const uint32_t ph = ra.phase;
+          if (!mbar_wait(bar(kBarAEmpty + s), ph ^ 1u, a.limit_ns)) {
+            set_error(a.err, kDevErrTimeout);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarAFull + s), kABytes);
+          const uint32_t dst = base + s * kABytes;
+          tma_load_2d(dst, &tmap_a, kb * kBK, m0, bar(kBarAFull + s));
+          tma_load_2d(dst + kABytes / 2, &tmap_a, kb * kBK, m0 + kBM / 2, bar(kBarAFull + s));
+          armed[s] = static_cast<int>(ph);
         }
-        const uint32_t row_bytes = 8 * T;
-        mbar_arrive_expect_tx(bar(s), kABytes + 4 * row_bytes);
-        tma_load_2d(stage_a(s), &tmap_a, kb * kBK, m0, bar(s));
-        const uint32_t cdst = smem_u32(stage_code(s));
-        for (int r = 0; r < 4; ++r) {
-          const uint8_t* src = a.code + ((size_t)(4 * kb + r) * NT + 8 * n_block) * T;
-          bulk_g2s(cdst + r * row_bytes, src, row_bytes, bar(s));
-        }
-        armed[s] = static_cast<int>(ph);
       }
-      if (!ok) {
-        for (int s = 0; s < kStagesG; ++s)
-          if (armed[s] >= 0) mbar_wait(bar(s), static_cast<uint32_t>(armed[s]), a.limit_ns);
-      }
+      if (!ok)
+        for (int s = 0; s < kAStages; ++s)
+          if (armed[s] >= 0)
+            mbar_wait(bar(kBarAFull + s), static_cast<uint32_t>(armed[s]), a.limit_ns);
     }
   } else if (warp == 1) {
+    // ---------------------------------------------------------- code producer
+    if (lane == 0) {
+      int armed[kCStages] = {-1, -1, -1, -1};
+      bool ok = true;
+      Ring<kCStages> rc;
+      const uint32_t row_bytes = 8 * T;
+      while (ok && it.next(seg)) {
+        const int nb = seg.tile % a.n_blocks;
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb, rc.advance()) {
+          const int s = rc.stage;
+          const uint32_t ph = rc.phase;
+          if (!mbar_wait(bar(kBarCEmpty + s), ph ^ 1u, a.limit_ns)) {
+            set_error(a.err, kDevErrTimeout);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarCFull + s), 4 * row_bytes);
+          const uint32_t dst = base + kOffC + s * kCBytes;
+          for (int r = 0; r < 4; ++r) {
+            const uint8_t* src = a.code + ((size_t)(4 * kb + r) * NT + 8 * nb) * T;
+            bulk_g2s(dst + r * row_bytes, src, row_bytes, bar(kBarCFull + s));
+          }
+          armed[s] = static_cast<int>(ph);
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < kCStages; ++s)
+          if (armed[s] >= 0)
+            mbar_wait(bar(kBarCFull + s), static_cast<uint32_t>(armed[s]), a.limit_ns);
+    }
+  } else if (warp == 2) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % kStagesG;
-        const uint32_t ph = (kb / kStagesG) & 1;
-        if (!mbar_wait(bar(s), ph, a.limit_ns) || !mbar_wait(bar(4 + s), ph, a.limit_ns)) {
+      bool ok = true;
+      Ring<kAStages> ra;
+      Ring<kBStages> rb;
+      int nseg = 0;
+      while (ok && it.next(seg)) {
+        if (nseg > 0 && !mbar_wait(bar(kBarTmemFree), (nseg - 1) & 1, a.limit_ns)) {
           set_error(a.err, kDevErrTimeout);
           break;
         }
         tc_fence_after();
-        const uint32_t sa = stage_a(s), sb = stage_b(s);
-#pragma unroll
-        for (int acc = 0; acc < 2; ++acc) {
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = smem_desc_k128(sa + acc * (kABytes / 2) + kk * 32);
-            const uint64_t bd = smem_desc_k128(sb + kk * 32);
-            mma_f16(tmem_base + acc * kBN, ad, bd, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb, ra.advance(), rb.advance()) {
+          const int sa = ra.stage;
+          const uint32_t pa = ra.phase;
+          const int sb = rb.stage;
+          const uint32_t pb = rb.phase;
+          if (!mbar_wait(bar(kBarAFull + sa), pa, a.limit_ns) ||
+              !mbar_wait(bar(kBarBFull + sb), pb, a.limit_ns)) {
+            set_error(a.err, kDevErrTimeout);
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          const uint32_t as = base + sa * kABytes;
+          const uint32_t bs = base + kOffB + sb * kBBytes;
+#pragma unroll
+          for (int acc = 0; acc < 4; ++acc) {
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t ad = smem_desc_k128(as + acc * (kABytes / 4) + kk * 32);
+              const uint64_t bd = smem_desc_k128(bs + kk * 32);
+              mma_f16(tmem_base + acc * kBN, ad, bd, kIdesc,
+                      (kb > seg.kb0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(bar(kBarAEmpty + sa));
+          mma_commit(bar(kBarBEmpty + sb));
         }
-        mma_commit(bar(8 + s));  // stage s may be refilled once these MMAs are done
+        if (!ok) break;
+        mma_commit(bar(kBarAcc));  // this segment's accumulators are complete
+        ++nseg;
       }
-      mma_commit(bar(12));  // accumulators complete
-      mma_commit(bar(13));
-      mbar_wait(bar(13), 0, a.limit_ns);  // nothing left in flight before TMEM is released
+      mma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, a.limit_ns);  // nothing in flight before TMEM is released
     }
   } else {
-    // ---------------------------------------------------------- decoders
-    const int dw = warp - 2;          // 0..15
-    const int kt_local = dw >> 2;     // k-tile row within the block
-    const int nt_base = (dw & 3) * 2; // 2 n-tiles per warp
+    // ---------------------------------------------------------- decoders + epilogue
+    const int dw = warp - kFirstDec;   // 0..15
+    const int kt_local = dw >> 2;      // k-tile row of the block this warp decodes
+    const int nt_base = (dw & 3) * 2;  // its two n-tiles
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
+    const int acc = dw >> 2;           // accumulator (128-row slice) it finishes
     const LaneWindow lw = lane_window<BITS>(lane);
     const int g = lane >> 2, t = lane & 3;
     bool ok = true;
-    for (int kb = 0; kb < num_kb && ok; ++kb) {
-      const int s = kb % kStagesG;
-      const uint32_t ph = (kb / kStagesG) & 1;
-      // B[s] must be free (previous MMAs on it done) and the codes must have landed.
-      if (!mbar_wait(bar(8 + s), ph ^ 1u, a.limit_ns) || !mbar_wait(bar(s), ph, a.limit_ns)) {
+    Ring<kCStages> rc;
+    Ring<kBStages> rb;
+    int nseg = 0;
+    while (ok && it.next(seg)) {
+      const int nb = seg.tile % a.n_blocks;
+      const int m0 = (seg.tile / a.n_blocks) * kBM;
+      for (int kb = seg.kb0; kb < seg.kb1; ++kb, rc.advance(), rb.advance()) {
+        const int sc = rc.stage;
+        const uint32_t pc = rc.phase;
+        const int sb = rb.stage;
+        const uint32_t pb = rb.phase;
+        if (!mbar_wait(bar(kBarCFull + sc), pc, a.limit_ns) ||
+            !mbar_wait(bar(kBarBEmpty + sb), pb ^ 1u, a.limit_ns)) {
+          set_error(a.err, kDevErrTimeout);
+          ok = false;
+          break;
+        }
+        const uint8_t* codes = smem + kOffC + sc * kCBytes;
+        uint8_t* bt = smem + kOffB + sb * kBBytes;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int nt = nt_base + i;
+          const uint32_t* tw = reinterpret_cast<const uint32_t*>(codes + (kt_local * 8 + nt) * T);
+          uint32_t h[8];
+          decode8<BITS>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const int rh = p & 1, nh = p >> 1;
+            const int n = 16 * nt + g + 8 * nh;
+            const int chunk = (2 * kt_local + rh) ^ g;
+            const uint32_t pair = __byte_perm(h[2 * p], h[2 * p + 1], 0x5410);
+            *reinterpret_cast<uint32_t*>(bt + n * 128 + chunk * 16 + 4 * t) = pair;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(kBarBFull + sb));
+          mbar_arrive(bar(kBarCEmpty + sc));
+        }
+      }
+      if (!ok) break;
+
+      // ---- epilogue of this segment: row acc*128 + quad*32 + lane of the tile
+      __syncwarp();
+      if (!mbar_wait(bar(kBarAcc), nseg & 1, a.limit_ns)) {
         set_error(a.err, kDevErrTimeout);
         ok = false;
         break;
       }
-      const uint8_t* codes = stage_code(s);
-      uint8_t* bt = smem + (stage_b(s) - base);
+      tc_fence_after();
+      const uint32_t tl = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kBN;
+      const int row = acc * 128 + quad * 32 + lane;
+      const int m = m0 + row;
+      const long long t_first = (long long)seg.tile * a.kb_per_tile;
+      const bool fused =
+          owner(t_first, a.units, a.grid) == owner(t_first + a.kb_per_tile - 1, a.units, a.grid);
+      const int n0 = nb * kBN;
+      if (fused) {
+        // index bits 0..4: a 32-point transform on each 32-column chunk, in TMEM
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          float w[32];
+          tmem_ld32(tl + 32 * q, w);
+          tmem_wait_ld();
+          fwht32_regs(w);
+          tmem_st32(tl + 32 * q, w);
+        }
+        tmem_wait_st();
+        // index bits 5 and 6 across the four chunks, then * sv / sqrt(128), fp16
+#pragma unroll 1
+        for (int c16 = 0; c16 < 32; c16 += 16) {
+          float x0[16], x1[16], x2[16], x3[16];
+          tmem_ld16(tl + c16, x0);
+          tmem_ld16(tl + c16 + 32, x1);
+          tmem_ld16(tl + c16 + 64, x2);
+          tmem_ld16(tl + c16 + 96, x3);
+          tmem_wait_ld();
+          if (m < a.M) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int nt = nt_base + i;
-        const uint32_t* tw = reinterpret_cast<const uint32_t*>(codes + (kt_local * 8 + nt) * T);
-        uint32_t h[8];
-        decode8<BITS>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
+            for (int j = 0; j < 16; ++j) {
+              const float a0 = x0[j] + x1[j], a1 = x0[j] - x1[j];
+              const float a2 = x2[j] + x3[j], a3 = x2[j] - x3[j];
+              x0[j] = a0 + a2;
+              x2[j] = a0 - a2;
+              x1[j] = a1 + a3;
+              x3[j] = a1 - a3;
+            }
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int rh = p & 1, nh = p >> 1;
-          const int n = 16 * nt + g + 8 * nh;
-          const int chunk = (2 * kt_local + rh) ^ g;
-          const uint32_t pair = __byte_perm(h[2 * p], h[2 * p + 1], 0x5410);
-          *reinterpret_cast<uint32_t*>(bt + n * 128 + chunk * 16 + 4 * t) = pair;
+            for (int qq = 0; qq < 4; ++qq) {
+              const float(&w)[16] = qq == 0 ? x0 : (qq == 1 ? x1 : (qq == 2 ? x2 : x3));
+              const int col = n0 + c16 + 32 * qq;
+              uint4* dst = reinterpret_cast<uint4*>(a.y + (size_t)m * a.N + col);
+#pragma unroll
+              for (int h8 = 0; h8 < 2; ++h8) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int j = 8 * h8 + 2 * e;
+                  const float s0 = __ldg(a.sv + col + j) * kHadScale;
+                  const float s1 = __ldg(a.sv + col + j + 1) * kHadScale;
+                  pk[e] = float_to_half_bits(w[j] * s0) |
+                          (uint32_t(float_to_half_bits(w[j + 1] * s1)) << 16);
+                }
+                dst[h8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              }
+            }
+          }
+        }
+      } else {
+        // partial sums of a shared tile: slot 0 = this CTA's first tile, slot 1 = a later one
+        const int which = (t_first <= u_begin) ? 0 : 1;
+        float* wrow = a.ws + ((size_t)(2 * c + which) * kBM + row) * kBN;
+#pragma unroll
+        for (int c32 = 0; c32 < kBN; c32 += 32) {
+          float u[32];
+          tmem_ld32(tl + c32, u);
+          tmem_wait_ld();
+          float4* d = reinterpret_cast<float4*>(wrow + c32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d[q] = make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
         }
       }
-      fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(4 + s));
-    }
-
-    // ---------------------------------------------------------- epilogue
-    // Pass 1: each (accumulator, TMEM lane quadrant, 64-column half) is one warp.
-    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int acc = (dw >> 2) & 1;
-    const int half = dw >> 3;
-    __syncwarp();
-    const bool have = ok && mbar_wait(bar(12), 0, a.limit_ns);
-    if (!have && ok) set_error(a.err, kDevErrTimeout);
-    tc_fence_after();
-    float* stash = reinterpret_cast<float*>(smem);
-    if (have) {
-      const int row = acc * 128 + quad * 32 + lane;
-#pragma unroll
-      for (int c = 64 * half; c < 64 * half + 64; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quad * 32) << 16) + acc * kBN + c, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) stash[row * kStashStride + c + j] = __uint_as_float(r[j]);
-      }
-    }
-    tc_fence_before();
-    named_barrier(1, kDecWarps * 32);
-    // Pass 2: one warp per row, element lane + 32*q in v[q].
-    if (have) {
-      float svv[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) svv[q] = a.sv[n0 + lane + 32 * q] * kHadScale;
-      for (int rr = 0; rr < kBM / kDecWarps; ++rr) {
-        const int row = dw * (kBM / kDecWarps) + rr;
-        const int m = m0 + row;
-        if (m >= a.M) break;
-        float v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = stash[row * kStashStride + lane + 32 * q];
-        fwht128_warp_strided(v, lane);
-        uint16_t* yr = a.y + (size_t)m * a.N + n0 + lane;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) yr[32 * q] = float_to_half_bits(v[q] * svv[q]);
-      }
+      if (lane == 0) mbar_arrive(bar(kBarTmemFree));
+      ++nseg;
     }
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+// Fix-up for tiles shared by several CTAs: y = fp16(had128(sum of partials) * sv).
+// One warp per (listed tile, row); element lane + 32*q in v[q].
+constexpr int kMaxSplitTiles = 512;
+struct FixupArgs {
+  const float* ws;
+  const float* sv;
+  uint16_t* y;
+  int M, N, n_blocks, kb_per_tile, grid, count;
+  long long units;
+  int tiles[kMaxSplitTiles];
+};
+
+__global__ void gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int tile = f.tiles[blockIdx.x];
+  const int m = (tile / f.n_blocks) * kBM + row;
+  if (m >= f.M) return;
+  const int n0 = (tile % f.n_blocks) * kBN;
+  const long long t_first = (long long)tile * f.kb_per_tile;
+  const int c0 = owner(t_first, f.units, f.grid);
+  const int c1 = owner(t_first + f.kb_per_tile - 1, f.units, f.grid);
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = c0; c <= c1; ++c) {
+    const long long cb = range_start(c, f.units, f.grid);
+    const int which = (t_first <= cb) ? 0 : 1;
+    const float* wrow = f.ws + ((size_t)(2 * c + which) * kBM + row) * kBN;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] += wrow[lane + 32 * q];
+  }
+  fwht128_warp_strided(v, lane);
+  uint16_t* yr = f.y + (size_t)m * f.N + n0 + lane;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    yr[32 * q] = float_to_half_bits(v[q] * kHadScale * f.sv[n0 + lane + 32 * q]);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -369,41 +627,82 @@ cudaError_t launch_gemm_bits(const CUtensorMap& map, const GemmArgs& a, cudaStre
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(a.N / kBN, (a.M + kBM - 1) / kBM);
-  trellis_gemm_kernel<BITS><<<grid, kThreadsG, kSmemBytes, st>>>(map, a);
+  trellis_gemm_kernel<BITS><<<a.grid, kThreadsG, kSmemBytes, st>>>(map, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// xh: rotated activations fp16 [M, K] (16-byte aligned, K a multiple of 128).
+size_t gemm_workspace_floats(int num_sms) { return (size_t)num_sms * 2 * kBM * kBN; }
+
+// xh: rotated activations fp16 [M, K] (16-byte aligned, K a multiple of 128);
+// ws: gemm_workspace_floats(num_sms) fp32.
 cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, int M, int K,
-                                int N, const float* sv, uint16_t* y, int* err, cudaStream_t st) {
+                                int N, const float* sv, uint16_t* y, float* ws, int num_sms,
+                                int* err, cudaStream_t st) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {kBK, kBM};
+  const cuuint32_t box[2] = {kBK, kBM / 2};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xh), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xh), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   GemmArgs a;
   a.code = reinterpret_cast<const uint8_t*>(code);
   a.sv = sv;
   a.y = y;
+  a.ws = ws;
   a.M = M;
   a.N = N;
   a.K = K;
+  a.n_blocks = N / kBN;
+  a.kb_per_tile = K / kBK;
+  const long long tiles = (long long)((M + kBM - 1) / kBM) * a.n_blocks;
+  a.units = tiles * a.kb_per_tile;
+  // at least 16 K-blocks per CTA, at most one CTA per SM
+  long long g = a.units / 16;
+  if (g < 1) g = 1;
+  if (g > num_sms) g = num_sms;
+  a.grid = static_cast<int>(g);
   a.err = err;
   a.limit_ns = kWaitLimitNs;
-  switch (bits) {
-    case 2: return launch_gemm_bits<2>(map, a, st);
-    case 3: return launch_gemm_bits<3>(map, a, st);
-    default: return launch_gemm_bits<4>(map, a, st);
+
+  FixupArgs f;
+  f.ws = ws;
+  f.sv = sv;
+  f.y = y;
+  f.M = M;
+  f.N = N;
+  f.n_blocks = a.n_blocks;
+  f.kb_per_tile = a.kb_per_tile;
+  f.grid = a.grid;
+  f.units = a.units;
+  f.count = 0;
+  for (long long t = 0; t < tiles; ++t) {
+    const long long t0 = t * a.kb_per_tile;
+    if (owner(t0, a.units, a.grid) != owner(t0 + a.kb_per_tile - 1, a.units, a.grid)) {
+      if (f.count >= kMaxSplitTiles) return cudaErrorInvalidValue;
+      f.tiles[f.count++] = static_cast<int>(t);
+    }
   }
+
+  cudaError_t e;
+  switch (bits) {
+    case 2: e = launch_gemm_bits<2>(map, a, st); break;
+    case 3: e = launch_gemm_bits<3>(map, a, st); break;
+    default: e = launch_gemm_bits<4>(map, a, st); break;
+  }
+  if (e != cudaSuccess) return e;
+  if (f.count > 0) {
+    dim3 grid(f.count, kBM / 8);
+    gemm_fixup_kernel<<<grid, 256, 0, st>>>(f);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace escha

@@ -63,9 +63,12 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
                                         const int* d_grid, int max_grid, int M, int mpad,
                                         int* err, cudaStream_t st);
 // Prefill GEMM on tcgen05: y = fp16(had128(xh @ W_inner) * sv) for any M >= 1;
-// xh is fp16 [M, K], 16-byte aligned.
+// xh is fp16 [M, K], 16-byte aligned; ws holds gemm_workspace_floats(num_sms)
+// fp32 for tiles shared between CTAs.
+size_t gemm_workspace_floats(int num_sms);
 cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, int M, int K,
-                                int N, const float* sv, uint16_t* y, int* err, cudaStream_t st);
+                                int N, const float* sv, uint16_t* y, float* ws, int num_sms,
+                                int* err, cudaStream_t st);
 cudaError_t launch_decode(const int16_t* code, int bits, int K, int N, uint16_t* w,
                           cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);

@@ -101,6 +101,8 @@ void linear_free(escha_linear_s* h) {
   cudaFree(h->err);
   cudaFree(h->sched.d_jobs);
   cudaFree(h->xh);
+  cudaFree(h->gemm_ws);
+  h->gemm_ws = nullptr;
   h->su = h->sv = nullptr;
   h->xfrag = nullptr;
   h->part = nullptr;
@@ -135,6 +137,8 @@ escha_status_t linear_reserve(escha_linear_s* h, int rows) {
   escha_status_t s = dev_alloc(&h->xh, (size_t)rows * h->K);
   if (s != ESCHA_OK) return s;
   h->xh_rows = rows;
+  if (!h->gemm_ws && (s = dev_alloc(&h->gemm_ws, gemm_workspace_floats(h->num_sms))) != ESCHA_OK)
+    return s;
   return ESCHA_OK;
 }
 
@@ -145,7 +149,8 @@ escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, in
   cudaError_t e = launch_rotate_in_plain(x, h->su, h->xh, M, h->K, st);
   if (e != cudaSuccess) return from_cuda(e);
   h->prof.begin(st);
-  e = launch_trellis_gemm(h->xh, h->code, h->bits, M, h->K, h->N, h->sv, y, h->err, st);
+  e = launch_trellis_gemm(h->xh, h->code, h->bits, M, h->K, h->N, h->sv, y, h->gemm_ws,
+                          h->num_sms, h->err, st);
   h->prof.end(st);
   return from_cuda(e);
 }

@@ -36,6 +36,7 @@ _I = ctypes.c_int
 _SIGS = {
     "escha_status_string": (ctypes.c_char_p, [_I]),
     "escha_version": (_I, []),
+    "escha_last_error_string": (ctypes.c_char_p, []),
     "escha_linear_create": (_I, [ctypes.POINTER(_P), _P, _P, _P, _P, _P, _P, _I, _P]),
     "escha_linear_destroy": (_I, [_P]),
     "escha_linear_shape": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
@@ -90,7 +91,8 @@ def declared_functions():
 
 def check(status, what):
     if status != ESCHA_OK:
-        raise EschaError(status, what)
+        detail = load().escha_last_error_string().decode() if status == 3 else ""
+        raise EschaError(status, what + (" [%s]" % detail if detail else ""))
 
 
 def __getattr__(name):

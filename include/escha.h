@@ -66,6 +66,10 @@ typedef struct escha_moe_s* escha_moe_t;
 /* Human-readable name of a status code (static string, never NULL). */
 const char* escha_status_string(escha_status_t status);
 
+/* Name and description of the last CUDA error this thread saw inside the
+ * library ("" if none); the string stays valid until the thread's next call. */
+const char* escha_last_error_string(void);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int escha_version(void);
 
