@@ -164,6 +164,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -494,16 +504,16 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         tmem_wait_st();
         // index bits 5 and 6 across the four chunks, then * sv / sqrt(128), fp16
 #pragma unroll 1
-        for (int c16 = 0; c16 < 32; c16 += 16) {
-          float x0[16], x1[16], x2[16], x3[16];
-          tmem_ld16(tl + c16, x0);
-          tmem_ld16(tl + c16 + 32, x1);
-          tmem_ld16(tl + c16 + 64, x2);
-          tmem_ld16(tl + c16 + 96, x3);
+        for (int c8 = 0; c8 < 32; c8 += 8) {
+          float x0[8], x1[8], x2[8], x3[8];
+          tmem_ld8(tl + c8, x0);
+          tmem_ld8(tl + c8 + 32, x1);
+          tmem_ld8(tl + c8 + 64, x2);
+          tmem_ld8(tl + c8 + 96, x3);
           tmem_wait_ld();
           if (m < a.M) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 8; ++j) {
               const float a0 = x0[j] + x1[j], a1 = x0[j] - x1[j];
               const float a2 = x2[j] + x3[j], a3 = x2[j] - x3[j];
               x0[j] = a0 + a2;
@@ -513,22 +523,18 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             }
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
-              const float(&w)[16] = qq == 0 ? x0 : (qq == 1 ? x1 : (qq == 2 ? x2 : x3));
-              const int col = n0 + c16 + 32 * qq;
-              uint4* dst = reinterpret_cast<uint4*>(a.y + (size_t)m * a.N + col);
+              const float(&w)[8] = qq == 0 ? x0 : (qq == 1 ? x1 : (qq == 2 ? x2 : x3));
+              const int col = n0 + c8 + 32 * qq;
+              uint32_t pk[4];
 #pragma unroll
-              for (int h8 = 0; h8 < 2; ++h8) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int j = 8 * h8 + 2 * e;
-                  const float s0 = __ldg(a.sv + col + j) * kHadScale;
-                  const float s1 = __ldg(a.sv + col + j + 1) * kHadScale;
-                  pk[e] = float_to_half_bits(w[j] * s0) |
-                          (uint32_t(float_to_half_bits(w[j + 1] * s1)) << 16);
-                }
-                dst[h8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              for (int e = 0; e < 4; ++e) {
+                const float s0 = __ldg(a.sv + col + 2 * e) * kHadScale;
+                const float s1 = __ldg(a.sv + col + 2 * e + 1) * kHadScale;
+                pk[e] = float_to_half_bits(w[2 * e] * s0) |
+                        (uint32_t(float_to_half_bits(w[2 * e + 1] * s1)) << 16);
               }
+              *reinterpret_cast<uint4*>(a.y + (size_t)m * a.N + col) =
+                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
           }
         }
@@ -536,14 +542,14 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         // partial sums of a shared tile: slot 0 = this CTA's first tile, slot 1 = a later one
         const int which = (t_first <= u_begin) ? 0 : 1;
         float* wrow = a.ws + ((size_t)(2 * c + which) * kBM + row) * kBN;
-#pragma unroll
-        for (int c32 = 0; c32 < kBN; c32 += 32) {
-          float u[32];
-          tmem_ld32(tl + c32, u);
+#pragma unroll 1
+        for (int c16 = 0; c16 < kBN; c16 += 16) {
+          float u[16];
+          tmem_ld16(tl + c16, u);
           tmem_wait_ld();
-          float4* d = reinterpret_cast<float4*>(wrow + c32);
+          float4* d = reinterpret_cast<float4*>(wrow + c16);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
+          for (int q = 0; q < 4; ++q)
             d[q] = make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
         }
       }
