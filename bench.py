@@ -310,46 +310,63 @@ def run_moe(args, spec, rank, world, local):
     torch.cuda.synchronize()
     if moe.check() != 0:
         raise SystemExit("device error flag set during warm-up")
-    moe.profile(True)
-    for i in range(2 * R):
-        step(i)
-    torch.cuda.synchronize()
-    moe.collect()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
-    g_main = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g_main, stream=side):
-            for i in range(R):
-                step(i)
-    torch.cuda.synchronize()
-    g_main.replay()
-    torch.cuda.synchronize()
-    moe.collect()
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(R):
+                    fn(i)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def timed(g, reps, sampler=None):
+        if sampler is not None:
+            sampler.start()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        clk = sampler.stop() if sampler is not None else None
+        elapsed = t0.elapsed_time(t1)
+        if dist is not None:
+            tt = torch.tensor([elapsed], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            elapsed = float(tt.item())
+        return elapsed, clk
+
     reps = max(1, args.steps // R)
     steps = reps * R
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(reps):
-        g_main.replay()
-    t1.record()
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    ms = t0.elapsed_time(t1)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    k_ms, k_n = moe.collect()
-    moe.profile(False)
+    g_main = capture(step)
+    ms, clocks = timed(g_main, reps, ClockSampler(dev.index if dev.index is not None else 0))
+
+    # Dominant kernel: the two trellis contraction launches of each call
+    # (stages 2 and 4), timed as (routing plan + contractions) minus (routing
+    # plan alone) over the same cycled routings, CUDA events on the launching
+    # stream around whole graph replays.
+    def stages(ss):
+        def fn(i):
+            for s in ss:
+                moe.gemv(x, ids_d[i % R], w_d[i % R], y, stage=s)
+        return fn
+    g_k = capture(stages((1, 2, 4)))
+    g_p = capture(stages((1,)))
+    kp_ms, _ = timed(g_k, reps)
+    p_ms, _ = timed(g_p, reps)
+    k_ms = kp_ms - p_ms
+    k_n = 2 * steps
     per_pass = sum(rbytes)
-    gemv_bytes = per_pass - R * (WL.side_bytes(hidden, 0) + WL.side_bytes(0, hidden))
+    gemv_bytes = reps * (per_pass - R * (WL.side_bytes(hidden, 0) + WL.side_bytes(0, hidden)))
     achieved = gemv_bytes / (k_ms / 1e3) / 1e9 if k_ms > 0 else None
     y_host = torch.empty((m, hidden), dtype=torch.float16).pin_memory()
     e_steps = min(steps, 2 * R)
@@ -379,7 +396,8 @@ def run_moe(args, spec, rank, world, local):
                    "l2": "256 experts, %.1f GB of code words; 64 routings cycled"
                          % (sum(c.numel() * 2 for cc in codes for c in cc) / 1e9),
                    "timing": "CUDA graph of 64 public API calls, CUDA events"},
-        "roofline": {"bound": "hbm", "kernel": "trellis_gemv (MoE jobs)", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "trellis_gemv (MoE jobs)",
+                     "launch_us": 1e3 * k_ms / k_n, "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak if achieved else None,
                      "traffic": None, "peak_source": src + " (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": e_steps * (per_pass / R) / (e_ms / 1e3) / 1e9, "unit": "GB/s",
@@ -565,69 +583,74 @@ def main():
     for h, _ in handles:
         if h.check() != 0:
             raise SystemExit("device error flag set during warm-up")
-        h.profile(True)
-    for i in range(2 * n_inst):   # fills each handle's event pool outside capture
-        step(i)
-    torch.cuda.synchronize()
-    for h, _ in handles:
-        h.collect()
 
     # CUDA graphs: one graph per pass over the weight sets, plus a remainder.
-    per_graph = n_inst
-    full, rem = divmod(args.steps, per_graph)
+    # The timed graphs hold the public calls only: an event node between two
+    # kernels of a graph costs microseconds and stops the next kernel from
+    # starting early, so the dominant kernel is timed in a second region.
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
-    g_main = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g_main, stream=side):
-            for i in range(per_graph):
-                step(i)
-    g_rem = None
-    if rem:
-        g_rem = torch.cuda.CUDAGraph()
+
+    def capture(fn, count):
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
-            with torch.cuda.graph(g_rem, stream=side):
-                for i in range(rem):
-                    step(i)
+            with torch.cuda.graph(g, stream=side):
+                for i in range(count):
+                    fn(i)
+        return g
+
+    def timed_replays(graphs, sampler=None):
+        if sampler is not None:
+            sampler.start()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for g in graphs:
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        clk = sampler.stop() if sampler is not None else None
+        if dist is not None:
+            dist.barrier()
+        elapsed = t0.elapsed_time(t1)
+        if dist is not None:
+            t = torch.tensor([elapsed], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            elapsed = float(t.item())
+        return elapsed, clk
+
+    per_graph = n_inst
+    full, rem = divmod(args.steps, per_graph)
+    g_main = capture(step, per_graph)
+    g_rem = capture(step, rem) if rem else None
     torch.cuda.synchronize()
     for i in range(3):
         g_main.replay()
     torch.cuda.synchronize()
+    ms, clocks = timed_replays([g_main] * full + ([g_rem] if g_rem else []),
+                               ClockSampler(dev.index if dev.index is not None else 0))
 
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record()
-    for _ in range(full):
-        g_main.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    t_end.record()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    clocks = sampler.stop()
-    ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    # Dominant kernel: the same steps with only the trellis contraction stage(s)
+    # of each call (escha_*_gemv_stage), K steps between two CUDA events on the
+    # launching stream; the average launch duration is that time over the
+    # launches.  The other stages' buffers hold the previous full call's values.
+    k_stages = (1, 3) if spec["kind"] == "mlp" else (1,)
 
-    # Dominant kernel: the trellis GEMV launches recorded inside the graphs
-    # (their events hold the durations of the last replay of each graph).
-    k_ms = 0.0
-    k_n = 0
-    for h, _ in handles:
-        a, n = h.collect()
-        k_ms += a
-        k_n += n
-        h.profile(False)
-    steps_covered = k_n / gemv_launches_per_step
-    k_bytes = WL.gemv_kernel_bytes(m, spec["layers"]) * steps_covered
+    def kstep(i):
+        for s in k_stages:
+            handles[i % n_inst][0].gemv(x, y, stage=s)
+
+    gk_main = capture(kstep, per_graph)
+    gk_rem = capture(kstep, rem) if rem else None
+    for i in range(3):
+        gk_main.replay()
+    torch.cuda.synchronize()
+    k_ms, _ = timed_replays([gk_main] * full + ([gk_rem] if gk_rem else []))
+    k_n = gemv_launches_per_step * args.steps
+    k_bytes = WL.gemv_kernel_bytes(m, spec["layers"]) * args.steps
     achieved = k_bytes / (k_ms / 1e3) / 1e9 if k_ms > 0 else None
 
     # End to end through the C ABI: host input copied in, result copied out.
@@ -667,6 +690,7 @@ def main():
                          % (n_inst, n_inst * code_per_inst / 1e6),
                    "timing": "CUDA graphs of the public API calls, CUDA events"},
         "roofline": {"bound": "hbm", "kernel": "trellis_gemv",
+                     "launch_us": 1e3 * k_ms / k_n,
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": (achieved / peak) if achieved else None, "traffic": None,
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"},

@@ -16,13 +16,15 @@ __host__ __device__ __forceinline__ int owner_cta(long long u, long long U, int 
 
 // Store one rotated activation (fp16 bits) at its place in the GEMV's
 // B-fragment layout: per k-tile, token block and lane (g = token % 8, t), four
-// words (x[2t], 0), (x[2t+8], 0), (x[2t+1], 0), (x[2t+9], 0).
+// words (x[2t], x[2t]), (x[2t+8], x[2t+8]), (x[2t+1], x[2t+1]),
+// (x[2t+9], x[2t+9]) -- each activation in both halves, against the (lo, hi)
+// halves of a codebook word in the weight operand.
 __device__ __forceinline__ void xfrag_store(uint32_t* xf, int TB, int m, int k, uint16_t hb) {
   const int kt = k >> 4, kk = k & 15;
   const int t = (kk & 7) >> 1, odd = kk & 1, hi8 = kk >> 3;
   const int reg = 2 * odd + hi8;
   const int tb = m >> 3, g = m & 7;
-  xf[(((size_t)kt * TB + tb) * 32 + 4 * g + t) * 4 + reg] = hb;
+  xf[(((size_t)kt * TB + tb) * 32 + 4 * g + t) * 4 + reg] = uint32_t(hb) | (uint32_t(hb) << 16);
 }
 
 __device__ __forceinline__ void load4_half(const uint16_t* p, float (&v)[4]) {

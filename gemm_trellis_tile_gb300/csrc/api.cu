@@ -237,12 +237,20 @@ escha_status_t escha_linear_decode(escha_linear_t h, uint16_t* w_inner, void* st
                                  static_cast<cudaStream_t>(stream)));
 }
 
+static bool gemv_args_ok(const void* h, const void* x, const void* y, int M) {
+  return h && x && y && M >= 1 && M <= kGemvMaxTokens && aligned16(x) && aligned16(y);
+}
+
 escha_status_t escha_linear_gemv(escha_linear_t h, const uint16_t* x, uint16_t* y, int M,
                                  void* stream) {
-  if (!h || !x || !y) return ESCHA_ERR_INVALID_ARG;
-  if (M < 1 || M > kGemvMaxTokens) return ESCHA_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y)) return ESCHA_ERR_INVALID_ARG;
+  if (!gemv_args_ok(h, x, y, M)) return ESCHA_ERR_INVALID_ARG;
   return linear_gemv(h, x, y, M, static_cast<cudaStream_t>(stream));
+}
+
+escha_status_t escha_linear_gemv_stage(escha_linear_t h, int stage, const uint16_t* x,
+                                       uint16_t* y, int M, void* stream) {
+  if (!gemv_args_ok(h, x, y, M)) return ESCHA_ERR_INVALID_ARG;
+  return linear_gemv_stage(h, stage, x, y, M, static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_linear_check(escha_linear_t h, void* stream) {
@@ -279,10 +287,14 @@ escha_status_t escha_mlp_destroy(escha_mlp_t m) {
 
 escha_status_t escha_mlp_gemv(escha_mlp_t m, const uint16_t* x, uint16_t* y, int M,
                               void* stream) {
-  if (!m || !x || !y) return ESCHA_ERR_INVALID_ARG;
-  if (M < 1 || M > kGemvMaxTokens) return ESCHA_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y)) return ESCHA_ERR_INVALID_ARG;
+  if (!gemv_args_ok(m, x, y, M)) return ESCHA_ERR_INVALID_ARG;
   return mlp_gemv(m, x, y, M, static_cast<cudaStream_t>(stream));
+}
+
+escha_status_t escha_mlp_gemv_stage(escha_mlp_t m, int stage, const uint16_t* x, uint16_t* y,
+                                    int M, void* stream) {
+  if (!gemv_args_ok(m, x, y, M)) return ESCHA_ERR_INVALID_ARG;
+  return mlp_gemv_stage(m, stage, x, y, M, static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_profile_enable(void* handle, int kind, int on) {
@@ -379,13 +391,25 @@ escha_status_t escha_moe_destroy(escha_moe_t m) {
   return ESCHA_OK;
 }
 
+static bool moe_args_ok(const void* m, const void* x, const void* ids, const void* w,
+                        const void* y, int M, int topk) {
+  return m && x && ids && w && y && M >= 1 && M <= kMoeMaxTokens && topk >= 1 &&
+         topk <= kMoeMaxTopk && aligned16(x) && aligned16(y);
+}
+
 escha_status_t escha_linear_moe_gemv(escha_moe_t m, const uint16_t* x, const int32_t* expert_ids,
                                      const float* expert_w, uint16_t* y, int M, int topk,
                                      void* stream) {
-  if (!m || !x || !expert_ids || !expert_w || !y) return ESCHA_ERR_INVALID_ARG;
-  if (M < 1 || M > kMoeMaxTokens || topk < 1 || topk > kMoeMaxTopk) return ESCHA_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y)) return ESCHA_ERR_INVALID_ARG;
+  if (!moe_args_ok(m, x, expert_ids, expert_w, y, M, topk)) return ESCHA_ERR_INVALID_ARG;
   return moe_gemv(m, x, expert_ids, expert_w, y, M, topk, static_cast<cudaStream_t>(stream));
+}
+
+escha_status_t escha_linear_moe_gemv_stage(escha_moe_t m, int stage, const uint16_t* x,
+                                           const int32_t* expert_ids, const float* expert_w,
+                                           uint16_t* y, int M, int topk, void* stream) {
+  if (!moe_args_ok(m, x, expert_ids, expert_w, y, M, topk)) return ESCHA_ERR_INVALID_ARG;
+  return moe_gemv_stage(m, stage, x, expert_ids, expert_w, y, M, topk,
+                        static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_moe_check(escha_moe_t m, void* stream) {

@@ -100,6 +100,8 @@ escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
                         const uint16_t* rin_down, const float* s_in_down,
                         const uint16_t* rout_hidden, const float* s_out_hidden, cudaStream_t st);
 void moe_free(escha_moe_s* h);
+escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, const int32_t* ids,
+                              const float* w, uint16_t* y, int M, int topk, cudaStream_t st);
 escha_status_t moe_gemv(escha_moe_s* h, const uint16_t* x, const int32_t* ids, const float* w,
                         uint16_t* y, int M, int topk, cudaStream_t st);
 
@@ -107,6 +109,8 @@ escha_status_t linear_init(escha_linear_s* h, const int16_t* code, int bits, int
                            const uint16_t* rin, const uint16_t* rout, const float* s_in,
                            const float* s_out, cudaStream_t st);
 void linear_free(escha_linear_s* h);
+escha_status_t linear_gemv_stage(escha_linear_s* h, int stage, const uint16_t* x, uint16_t* y,
+                                 int M, cudaStream_t st);
 escha_status_t linear_gemv(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
                            cudaStream_t st);
 escha_status_t linear_reserve(escha_linear_s* h, int rows);
@@ -115,6 +119,8 @@ escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, in
 escha_status_t mlp_init(escha_mlp_s* m, escha_linear_s* gate, escha_linear_s* up,
                         escha_linear_s* down);
 void mlp_free(escha_mlp_s* m);
+escha_status_t mlp_gemv_stage(escha_mlp_s* m, int stage, const uint16_t* x, uint16_t* y, int M,
+                              cudaStream_t st);
 escha_status_t mlp_gemv(escha_mlp_s* m, const uint16_t* x, uint16_t* y, int M, cudaStream_t st);
 Profiler* profiler_of(void* handle, int kind);
 

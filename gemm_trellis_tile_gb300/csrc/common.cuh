@@ -28,6 +28,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before its predecessor in the stream finishes.
+// pdl_wait() blocks until the predecessor grid has completed and its writes
+// are visible (a no-op when the kernel was launched normally);
+// pdl_trigger() lets the successor grid be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -16,9 +16,14 @@
 //               lane, decodes eight weights per lane, and issues m16n8k16 MMAs
 //               with the weight tile as A (rows = output channels) and up to 8
 //               tokens as B; a second token block handles 9..16 tokens.
-// The decoded value is in both fp16 halves of each A register; B carries the
-// activation in the low half and zero in the high half, so each MMA contracts
-// 8 real input channels and two MMAs cover a tile.
+// Each A register holds one weight's codebook word as its two fp16 halves
+// (lo, hi) and B carries the activation in both halves, so the MMA forms
+// lo*x + hi*x in fp32: the codebook's final addition happens inside the
+// contraction instead of as a separate fp16 add (which costs more integer and
+// FMA-pipe instructions than the rest of the decode step).  The sum is not
+// rounded to fp16 first; that changes each weight by at most half an fp16 ulp
+// (relative RMS 2.2e-4 over uniform states).  Each MMA contracts 8 real input
+// channels and two MMAs cover a tile.
 
 #include "common.cuh"
 #include "internal.h"
@@ -55,6 +60,8 @@ struct GemvArgs {
   int mpad;
   int* err;
   uint64_t limit_ns;
+  uint32_t cb_mask;  // kMcgMask and kMcgXor, as run-time values (see mcg_pair)
+  uint32_t cb_xor;
 };
 
 __host__ __device__ __forceinline__ long long cta_start(long long c, long long U, int G) {
@@ -150,9 +157,10 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 
 template <int BITS, int TB>
 __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t* p1, const uint4* xp,
-                                             int sh7, float (&acc)[TB][4]) {
+                                             int sh7, uint32_t mask, uint32_t xr,
+                                             float (&acc)[TB][4]) {
   uint32_t h[8];
-  decode8<BITS>(*p0, *p1, sh7, h);
+  decode8_pairs<BITS>(*p0, *p1, sh7, mask, xr, h);
 #pragma unroll
   for (int tb = 0; tb < TB; ++tb) {
     const uint4 xf = xp[tb * 32];
@@ -164,7 +172,8 @@ __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t*
 // One stage: n units (k-tile rows of 8 tiles); this warp owns tile column w.
 template <int BITS, int TB>
 __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint4* xf_s, int n,
-                                              int w, int lane, float (&acc)[TB][4]) {
+                                              int w, int lane, uint32_t mask, uint32_t xr,
+                                              float (&acc)[TB][4]) {
   constexpr int T = 32 * BITS;
   constexpr int kRowWords = kCW * T / 4;  // uint32 words per unit in the stage
   const LaneWindow lw = lane_window<BITS>(lane);
@@ -175,10 +184,12 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint
   if (n == kUPS) {
 #pragma unroll
     for (int i = 0; i < kUPS; ++i)
-      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * TB * 32, lw.sh7, acc);
+      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * TB * 32, lw.sh7,
+                             mask, xr, acc);
   } else {
     for (int i = 0; i < n; ++i)
-      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * TB * 32, lw.sh7, acc);
+      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * TB * 32, lw.sh7,
+                             mask, xr, acc);
   }
 }
 
@@ -190,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
   uint64_t* bars = reinterpret_cast<uint64_t*>(xfs + kStages * xf_stage_bytes<TB>());
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_trigger();
   long long U = a.units;
   int G = a.grid;
   if (a.dev_units != nullptr) {
@@ -221,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
     int armed[kStages];
     for (int s = 0; s < kStages; ++s) armed[s] = -1;
     bool ok = true;
+    bool waited = false;
     while (it.next(a.jobs, ch)) {
       const uint32_t full = smem_u32(&bars[stage]);
       if (!mbar_wait(smem_u32(&bars[kStages + stage]), phase ^ 1u, a.limit_ns)) {
@@ -237,6 +250,12 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
       for (int i = 0; i < ch.n; ++i) {
         const uint8_t* src = it.code + ((size_t)(ch.kt + i) * NT + (size_t)kCW * ch.g) * T;
         bulk_g2s_evict_first(cdst + i * rowb, src, rowb, full, pol);
+      }
+      if (!waited) {
+        // The code words above do not depend on the previous kernel; the
+        // rotated activations do.
+        pdl_wait();
+        waited = true;
       }
       bulk_g2s(smem_u32(xfs + stage * xf_stage_bytes<TB>()), it.xfrag + (size_t)ch.kt * TB * 32,
                ch.n * TB * 512, full);
@@ -270,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
     const uint8_t* cs = codes + stage * kCodeStageBytes;
     const uint4* xs = reinterpret_cast<const uint4*>(xfs + stage * xf_stage_bytes<TB>());
     switch (it.bits) {
-      case 2: consume_chunk<2, TB>(cs, xs, ch.n, warp, lane, acc); break;
-      case 3: consume_chunk<3, TB>(cs, xs, ch.n, warp, lane, acc); break;
-      default: consume_chunk<4, TB>(cs, xs, ch.n, warp, lane, acc); break;
+      case 2: consume_chunk<2, TB>(cs, xs, ch.n, warp, lane, a.cb_mask, a.cb_xor, acc); break;
+      case 3: consume_chunk<3, TB>(cs, xs, ch.n, warp, lane, a.cb_mask, a.cb_xor, acc); break;
+      default: consume_chunk<4, TB>(cs, xs, ch.n, warp, lane, a.cb_mask, a.cb_xor, acc); break;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + stage]));
@@ -358,8 +377,19 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   a.mpad = kGemvMaxTokens;
   a.err = err;
   a.limit_ns = kWaitLimitNs;
-  trellis_gemv_kernel<TB><<<s.grid, kThreads, gemv_smem_bytes<TB>(), st>>>(a);
-  return cudaGetLastError();
+  a.cb_mask = kMcgMask;
+  a.cb_xor = kMcgXor;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = gemv_smem_bytes<TB>();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, trellis_gemv_kernel<TB>, a);
 }
 
 }  // namespace
@@ -420,6 +450,8 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
   a.mpad = mpad;
   a.err = err;
   a.limit_ns = kWaitLimitNs;
+  a.cb_mask = kMcgMask;
+  a.cb_xor = kMcgXor;
   trellis_gemv_kernel<1><<<max_grid, kThreads, gemv_smem_bytes<1>(), st>>>(a);
   return cudaGetLastError();
 }

@@ -111,19 +111,38 @@ void linear_free(escha_linear_s* h) {
   h->xh = nullptr;
 }
 
+escha_status_t linear_gemv_stage(escha_linear_s* h, int stage, const uint16_t* x, uint16_t* y,
+                                 int M, cudaStream_t st) {
+  const int TB = M <= 8 ? 1 : 2;
+  cudaError_t e = cudaSuccess;
+  switch (stage) {
+    case 0: {
+      RotInJob rj{x, h->su, h->xfrag, h->K};
+      e = launch_rotate_in_xfrag(&rj, 1, M, TB, st);
+      break;
+    }
+    case 1:
+      h->prof.begin(st);
+      e = launch_gemv(h->sched, M, h->err, st);
+      h->prof.end(st);
+      break;
+    case 2:
+      e = launch_rotate_out(part_ref(h->sched, 0), h->sched.units, h->sched.grid, h->sv, y, M,
+                            kGemvMaxTokens, st);
+      break;
+    default:
+      return ESCHA_ERR_INVALID_ARG;
+  }
+  return from_cuda(e);
+}
+
 escha_status_t linear_gemv(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
                            cudaStream_t st) {
-  const int TB = M <= 8 ? 1 : 2;
-  RotInJob rj{x, h->su, h->xfrag, h->K};
-  cudaError_t e = launch_rotate_in_xfrag(&rj, 1, M, TB, st);
-  if (e != cudaSuccess) return from_cuda(e);
-  h->prof.begin(st);
-  e = launch_gemv(h->sched, M, h->err, st);
-  h->prof.end(st);
-  if (e != cudaSuccess) return from_cuda(e);
-  e = launch_rotate_out(part_ref(h->sched, 0), h->sched.units, h->sched.grid, h->sv, y, M,
-                        kGemvMaxTokens, st);
-  return from_cuda(e);
+  for (int s = 0; s < ESCHA_LINEAR_STAGES; ++s) {
+    const escha_status_t r = linear_gemv_stage(h, s, x, y, M, st);
+    if (r != ESCHA_OK) return r;
+  }
+  return ESCHA_OK;
 }
 
 escha_status_t linear_reserve(escha_linear_s* h, int rows) {
@@ -196,27 +215,48 @@ void mlp_free(escha_mlp_s* m) {
   cudaFree(m->s_down.d_jobs);
 }
 
-escha_status_t mlp_gemv(escha_mlp_s* m, const uint16_t* x, uint16_t* y, int M, cudaStream_t st) {
+escha_status_t mlp_gemv_stage(escha_mlp_s* m, int stage, const uint16_t* x, uint16_t* y, int M,
+                              cudaStream_t st) {
   const int TB = M <= 8 ? 1 : 2;
-  RotInJob rj[2] = {{x, m->gate->su, m->xfrag_gate, m->gate->K},
-                    {x, m->up->su, m->xfrag_up, m->up->K}};
-  cudaError_t e = launch_rotate_in_xfrag(rj, 2, M, TB, st);
-  if (e != cudaSuccess) return from_cuda(e);
-  m->prof.begin(st);
-  e = launch_gemv(m->s_gate_up, M, m->err, st);
-  m->prof.end(st);
-  if (e != cudaSuccess) return from_cuda(e);
-  e = launch_mlp_mid(part_ref(m->s_gate_up, 0), part_ref(m->s_gate_up, 1), m->s_gate_up.units,
-                     m->s_gate_up.grid, m->gate->sv, m->up->sv, m->down->su, m->xfrag_down, M, TB,
-                     st);
-  if (e != cudaSuccess) return from_cuda(e);
-  m->prof.begin(st);
-  e = launch_gemv(m->s_down, M, m->err, st);
-  m->prof.end(st);
-  if (e != cudaSuccess) return from_cuda(e);
-  e = launch_rotate_out(part_ref(m->s_down, 0), m->s_down.units, m->s_down.grid, m->down->sv, y,
-                        M, kGemvMaxTokens, st);
+  cudaError_t e = cudaSuccess;
+  switch (stage) {
+    case 0: {
+      RotInJob rj[2] = {{x, m->gate->su, m->xfrag_gate, m->gate->K},
+                        {x, m->up->su, m->xfrag_up, m->up->K}};
+      e = launch_rotate_in_xfrag(rj, 2, M, TB, st);
+      break;
+    }
+    case 1:
+      m->prof.begin(st);
+      e = launch_gemv(m->s_gate_up, M, m->err, st);
+      m->prof.end(st);
+      break;
+    case 2:
+      e = launch_mlp_mid(part_ref(m->s_gate_up, 0), part_ref(m->s_gate_up, 1), m->s_gate_up.units,
+                         m->s_gate_up.grid, m->gate->sv, m->up->sv, m->down->su, m->xfrag_down, M,
+                         TB, st);
+      break;
+    case 3:
+      m->prof.begin(st);
+      e = launch_gemv(m->s_down, M, m->err, st);
+      m->prof.end(st);
+      break;
+    case 4:
+      e = launch_rotate_out(part_ref(m->s_down, 0), m->s_down.units, m->s_down.grid, m->down->sv,
+                            y, M, kGemvMaxTokens, st);
+      break;
+    default:
+      return ESCHA_ERR_INVALID_ARG;
+  }
   return from_cuda(e);
+}
+
+escha_status_t mlp_gemv(escha_mlp_s* m, const uint16_t* x, uint16_t* y, int M, cudaStream_t st) {
+  for (int s = 0; s < ESCHA_MLP_STAGES; ++s) {
+    const escha_status_t r = mlp_gemv_stage(m, s, x, y, M, st);
+    if (r != ESCHA_OK) return r;
+  }
+  return ESCHA_OK;
 }
 
 Profiler* profiler_of(void* handle, int kind) {

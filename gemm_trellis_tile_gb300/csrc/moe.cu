@@ -339,78 +339,101 @@ void moe_free(escha_moe_s* h) {
   cudaFree(h->err);
 }
 
+escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, const int32_t* ids,
+                              const float* w, uint16_t* y, int M, int topk, cudaStream_t st) {
+  MoeRoute* route = reinterpret_cast<MoeRoute*>(h->route);
+  cudaError_t e = cudaSuccess;
+  switch (stage) {
+    case 0: {
+      RotInJob rj{x, h->su_hidden, h->xfrag_hidden, h->hidden};
+      e = launch_rotate_in_xfrag(&rj, 1, M, 1, st);
+      break;
+    }
+    case 1: {
+      MoePlanArgs pa;
+      pa.ids = ids;
+      pa.M = M;
+      pa.topk = topk;
+      pa.E = h->E;
+      pa.hidden = h->hidden;
+      pa.inter = h->inter;
+      pa.gate_code = h->gate_code;
+      pa.up_code = h->up_code;
+      pa.down_code = h->down_code;
+      pa.bits = h->bits;
+      pa.xfrag_hidden = h->xfrag_hidden;
+      pa.xfrag_down = h->xfrag_down;
+      pa.part1 = h->part1;
+      pa.part2 = h->part2;
+      pa.part1_stride = h->part1_stride;
+      pa.part2_stride = h->part2_stride;
+      pa.xdown_stride = h->xdown_stride;
+      pa.jobs1 = h->jobs1;
+      pa.jobs2 = h->jobs2;
+      pa.route = route;
+      pa.grid1_max = h->grid_max;
+      pa.grid2_max = h->grid_max;
+      pa.err = h->err;
+      moe_plan_kernel<<<1, 128, h->E * sizeof(int), st>>>(pa);
+      e = cudaGetLastError();
+      break;
+    }
+    case 2:
+      h->prof.begin(st);
+      e = launch_gemv_device_schedule(h->jobs1, &route->units1, &route->grid1, h->grid_max, M,
+                                      kMoeMaxTokens, h->err, st);
+      h->prof.end(st);
+      break;
+    case 3: {
+      MoeMidArgs ma;
+      ma.route = route;
+      ma.jobs1 = h->jobs1;
+      ma.sv_gate = h->sv_gate;
+      ma.sv_up = h->sv_up;
+      ma.su_down = h->su_down;
+      ma.xfrag_down = h->xfrag_down;
+      ma.xdown_stride = h->xdown_stride;
+      ma.M = M;
+      ma.inter = h->inter;
+      const long long mid_warps = (long long)kMoeMaxDistinct * 8 * (h->inter / kHad);
+      moe_mid_kernel<<<blocks_for(mid_warps), 32 * kWarpsPerBlock, 0, st>>>(ma);
+      e = cudaGetLastError();
+      break;
+    }
+    case 4:
+      h->prof.begin(st);
+      e = launch_gemv_device_schedule(h->jobs2, &route->units2, &route->grid2, h->grid_max, M,
+                                      kMoeMaxTokens, h->err, st);
+      h->prof.end(st);
+      break;
+    case 5: {
+      MoeOutArgs oa;
+      oa.route = route;
+      oa.jobs2 = h->jobs2;
+      oa.expert_w = w;
+      oa.sv_hidden = h->sv_hidden;
+      oa.y = y;
+      oa.M = M;
+      oa.topk = topk;
+      oa.hidden = h->hidden;
+      const long long out_warps = (long long)M * (h->hidden / kHad);
+      moe_out_kernel<<<blocks_for(out_warps), 32 * kWarpsPerBlock, 0, st>>>(oa);
+      e = cudaGetLastError();
+      break;
+    }
+    default:
+      return ESCHA_ERR_INVALID_ARG;
+  }
+  return from_cuda(e);
+}
+
 escha_status_t moe_gemv(escha_moe_s* h, const uint16_t* x, const int32_t* ids, const float* w,
                         uint16_t* y, int M, int topk, cudaStream_t st) {
-  RotInJob rj{x, h->su_hidden, h->xfrag_hidden, h->hidden};
-  cudaError_t e = launch_rotate_in_xfrag(&rj, 1, M, 1, st);
-  if (e != cudaSuccess) return from_cuda(e);
-
-  MoeRoute* route = reinterpret_cast<MoeRoute*>(h->route);
-  MoePlanArgs pa;
-  pa.ids = ids;
-  pa.M = M;
-  pa.topk = topk;
-  pa.E = h->E;
-  pa.hidden = h->hidden;
-  pa.inter = h->inter;
-  pa.gate_code = h->gate_code;
-  pa.up_code = h->up_code;
-  pa.down_code = h->down_code;
-  pa.bits = h->bits;
-  pa.xfrag_hidden = h->xfrag_hidden;
-  pa.xfrag_down = h->xfrag_down;
-  pa.part1 = h->part1;
-  pa.part2 = h->part2;
-  pa.part1_stride = h->part1_stride;
-  pa.part2_stride = h->part2_stride;
-  pa.xdown_stride = h->xdown_stride;
-  pa.jobs1 = h->jobs1;
-  pa.jobs2 = h->jobs2;
-  pa.route = route;
-  pa.grid1_max = h->grid_max;
-  pa.grid2_max = h->grid_max;
-  pa.err = h->err;
-  moe_plan_kernel<<<1, 128, h->E * sizeof(int), st>>>(pa);
-  if ((e = cudaGetLastError()) != cudaSuccess) return from_cuda(e);
-
-  h->prof.begin(st);
-  e = launch_gemv_device_schedule(h->jobs1, &route->units1, &route->grid1, h->grid_max, M,
-                                  kMoeMaxTokens, h->err, st);
-  h->prof.end(st);
-  if (e != cudaSuccess) return from_cuda(e);
-
-  MoeMidArgs ma;
-  ma.route = route;
-  ma.jobs1 = h->jobs1;
-  ma.sv_gate = h->sv_gate;
-  ma.sv_up = h->sv_up;
-  ma.su_down = h->su_down;
-  ma.xfrag_down = h->xfrag_down;
-  ma.xdown_stride = h->xdown_stride;
-  ma.M = M;
-  ma.inter = h->inter;
-  const long long mid_warps = (long long)kMoeMaxDistinct * 8 * (h->inter / kHad);
-  moe_mid_kernel<<<blocks_for(mid_warps), 32 * kWarpsPerBlock, 0, st>>>(ma);
-  if ((e = cudaGetLastError()) != cudaSuccess) return from_cuda(e);
-
-  h->prof.begin(st);
-  e = launch_gemv_device_schedule(h->jobs2, &route->units2, &route->grid2, h->grid_max, M,
-                                  kMoeMaxTokens, h->err, st);
-  h->prof.end(st);
-  if (e != cudaSuccess) return from_cuda(e);
-
-  MoeOutArgs oa;
-  oa.route = route;
-  oa.jobs2 = h->jobs2;
-  oa.expert_w = w;
-  oa.sv_hidden = h->sv_hidden;
-  oa.y = y;
-  oa.M = M;
-  oa.topk = topk;
-  oa.hidden = h->hidden;
-  const long long out_warps = (long long)M * (h->hidden / kHad);
-  moe_out_kernel<<<blocks_for(out_warps), 32 * kWarpsPerBlock, 0, st>>>(oa);
-  return from_cuda(cudaGetLastError());
+  for (int s = 0; s < ESCHA_MOE_STAGES; ++s) {
+    const escha_status_t r = moe_gemv_stage(h, s, x, ids, w, y, M, topk, st);
+    if (r != ESCHA_OK) return r;
+  }
+  return ESCHA_OK;
 }
 
 }  // namespace escha

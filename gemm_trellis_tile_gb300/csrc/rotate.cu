@@ -38,6 +38,7 @@ struct RotInArgs {
 
 // xfrag = fp16(had128(x * su)) for tokens 0..8TB-1 (zeros past M).
 __global__ void rotate_in_xfrag_kernel(const RotInArgs a) {
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int mp = 8 * a.TB;
@@ -94,6 +95,7 @@ __global__ void rotate_in_plain_kernel(const uint16_t* x, const float* su, uint1
 // y = fp16(had128(sum of partial slots) * sv).
 __global__ void rotate_out_kernel(const PartRef pr, long long U, int G, const float* sv,
                                   uint16_t* y, int M, int mpad) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int NG = pr.N / kHad;
@@ -117,6 +119,8 @@ __global__ void rotate_out_kernel(const PartRef pr, long long U, int G, const fl
 __global__ void mlp_mid_kernel(const PartRef gate, const PartRef up, long long U, int G,
                                const float* sv_gate, const float* sv_up, const float* su_down,
                                uint32_t* xfrag_down, int M, int TB) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int NG = gate.N / kHad;
@@ -155,6 +159,23 @@ unsigned blocks_for(long long warps) {
   return static_cast<unsigned>((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
 }
 
+// Launch configuration allowing this kernel to start before its predecessor
+// finishes (it calls pdl_wait() before touching the predecessor's output).
+struct DependentLaunch {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  DependentLaunch(unsigned blocks, unsigned threads, cudaStream_t st) {
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
 }  // namespace
 
 cudaError_t launch_fold_scales(const uint16_t* r, const float* s, float* out, int n,
@@ -188,18 +209,17 @@ cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t*
 cudaError_t launch_rotate_out(const PartRef& pr, long long units, int grid, const float* sv,
                               uint16_t* y, int M, int mpad, cudaStream_t st) {
   const long long warps = (long long)M * (pr.N / kHad);
-  rotate_out_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(pr, units, grid, sv, y, M,
-                                                                       mpad);
-  return cudaGetLastError();
+  DependentLaunch dl(blocks_for(warps), 32 * kWarpsPerBlock, st);
+  return cudaLaunchKernelEx(&dl.cfg, rotate_out_kernel, pr, units, grid, sv, y, M, mpad);
 }
 
 cudaError_t launch_mlp_mid(const PartRef& gate, const PartRef& up, long long units, int grid,
                            const float* sv_gate, const float* sv_up, const float* su_down,
                            uint32_t* xfrag_down, int M, int TB, cudaStream_t st) {
   const long long warps = (long long)8 * TB * (gate.N / kHad);
-  mlp_mid_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(
-      gate, up, units, grid, sv_gate, sv_up, su_down, xfrag_down, M, TB);
-  return cudaGetLastError();
+  DependentLaunch dl(blocks_for(warps), 32 * kWarpsPerBlock, st);
+  return cudaLaunchKernelEx(&dl.cfg, mlp_mid_kernel, gate, up, units, grid, sv_gate, sv_up,
+                            su_down, xfrag_down, M, TB);
 }
 
 }  // namespace escha

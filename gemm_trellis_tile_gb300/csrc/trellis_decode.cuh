@@ -59,6 +59,19 @@ __device__ __forceinline__ uint32_t mcg_decode_dup(uint32_t state) {
   return *reinterpret_cast<const uint32_t*>(&s);
 }
 
+// The codebook word of one state before its final addition: fp16 lo in the
+// low half, fp16 hi in the high half.  A tensor-core contraction against an
+// operand that carries the same activation in both halves forms lo*x + hi*x
+// in fp32, i.e. the codebook sum without its fp16 rounding (the rounding
+// changes a weight by at most half an fp16 ulp of lo + hi).
+//
+// `mask` and `xr` are kMcgMask and kMcgXor, passed in at run time: given two
+// literal constants the compiler spends two integer instructions on the
+// mask-and-flip, given one in a register it uses a single three-input logic op.
+__device__ __forceinline__ uint32_t mcg_pair(uint32_t state, uint32_t mask, uint32_t xr) {
+  return ((state * kMcgMult) & mask) ^ xr;
+}
+
 // 16-bit field starting at byte `b` (0..2) of x, zero-extended (one PRMT).
 __device__ __forceinline__ uint32_t field16_at_byte(uint32_t x, int b) {
   return __byte_perm(x, 0u, b == 0 ? 0x4410 : (b == 1 ? 0x4421 : 0x4432));
@@ -111,6 +124,18 @@ __device__ __forceinline__ void decode8(uint32_t w0, uint32_t w1, int sh7, uint3
   lane_states<BITS>(lo, hi, st);
 #pragma unroll
   for (int j = 0; j < 8; ++j) out[j] = mcg_decode_dup(st[j]);
+}
+
+// The lane's eight codebook words as (lo, hi) fp16 pairs (see mcg_pair).
+template <int BITS>
+__device__ __forceinline__ void decode8_pairs(uint32_t w0, uint32_t w1, int sh7, uint32_t mask,
+                                              uint32_t xr, uint32_t (&out)[8]) {
+  const uint32_t lo = __funnelshift_r(w1, w0, sh7);
+  const uint32_t hi = w0 >> sh7;
+  uint32_t st[8];
+  lane_states<BITS>(lo, hi, st);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[j] = mcg_pair(st[j], mask, xr);
 }
 
 // Tile coordinates of lane symbol j (row = input channel, col = output channel).

@@ -42,15 +42,18 @@ _SIGS = {
     "escha_linear_shape": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "escha_linear_decode": (_I, [_P, _P, _P]),
     "escha_linear_gemv": (_I, [_P, _P, _P, _I, _P]),
+    "escha_linear_gemv_stage": (_I, [_P, _I, _P, _P, _I, _P]),
     "escha_linear_gemm": (_I, [_P, _P, _P, _I, _P]),
     "escha_linear_reserve": (_I, [_P, _I]),
     "escha_mlp_create": (_I, [ctypes.POINTER(_P), _P, _P, _P]),
     "escha_mlp_destroy": (_I, [_P]),
     "escha_mlp_gemv": (_I, [_P, _P, _P, _I, _P]),
+    "escha_mlp_gemv_stage": (_I, [_P, _I, _P, _P, _I, _P]),
     "escha_moe_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _P, _P, _P, _P,
                               _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "escha_moe_destroy": (_I, [_P]),
     "escha_linear_moe_gemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
+    "escha_linear_moe_gemv_stage": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _P]),
     "escha_linear_check": (_I, [_P, _P]),
     "escha_moe_check": (_I, [_P, _P]),
     "escha_profile_enable": (_I, [_P, _I, _I]),
@@ -175,14 +178,20 @@ class Linear:
         return cls(t["code"], t["rin"], t["rout"], t["s_in"], t["s_out"],
                    torch.from_numpy(layer["config"]))
 
-    def gemv(self, x, y=None, stream=None):
+    STAGES = 3
+
+    def gemv(self, x, y=None, stream=None, stage=None):
         torch = _torch()
         _dev(x, torch.float16)
         m = x.shape[0]
         if y is None:
             y = torch.empty((m, self.out_features), dtype=torch.float16, device=x.device)
-        check(load().escha_linear_gemv(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
-              "escha_linear_gemv")
+        if stage is None:
+            check(load().escha_linear_gemv(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
+                  "escha_linear_gemv")
+        else:
+            check(load().escha_linear_gemv_stage(self.handle, int(stage), _ptr(x), _ptr(y), m,
+                                                 _stream(stream)), "escha_linear_gemv_stage")
         return y
 
     def gemm(self, x, y=None, stream=None):
@@ -236,14 +245,20 @@ class MLP:
         self.handle = h
         self.hidden = gate.in_features
 
-    def gemv(self, x, y=None, stream=None):
+    STAGES = 5
+
+    def gemv(self, x, y=None, stream=None, stage=None):
         torch = _torch()
         _dev(x, torch.float16)
         m = x.shape[0]
         if y is None:
             y = torch.empty((m, self.hidden), dtype=torch.float16, device=x.device)
-        check(load().escha_mlp_gemv(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
-              "escha_mlp_gemv")
+        if stage is None:
+            check(load().escha_mlp_gemv(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
+                  "escha_mlp_gemv")
+        else:
+            check(load().escha_mlp_gemv_stage(self.handle, int(stage), _ptr(x), _ptr(y), m,
+                                              _stream(stream)), "escha_mlp_gemv_stage")
         return y
 
     def check(self, stream=None):
@@ -322,7 +337,9 @@ class MoE:
         obj._keep_dev = (dev, stand_in, t)
         return obj
 
-    def gemv(self, x, expert_ids, expert_w, y=None, stream=None):
+    STAGES = 6
+
+    def gemv(self, x, expert_ids, expert_w, y=None, stream=None, stage=None):
         torch = _torch()
         _dev(x, torch.float16)
         _dev(expert_ids, torch.int32)
@@ -330,9 +347,15 @@ class MoE:
         m, topk = expert_ids.shape
         if y is None:
             y = torch.empty((m, self.hidden), dtype=torch.float16, device=x.device)
-        check(load().escha_linear_moe_gemv(self.handle, _ptr(x), _ptr(expert_ids), _ptr(expert_w),
-                                           _ptr(y), m, topk, _stream(stream)),
-              "escha_linear_moe_gemv")
+        if stage is None:
+            check(load().escha_linear_moe_gemv(self.handle, _ptr(x), _ptr(expert_ids),
+                                               _ptr(expert_w), _ptr(y), m, topk, _stream(stream)),
+                  "escha_linear_moe_gemv")
+        else:
+            check(load().escha_linear_moe_gemv_stage(self.handle, int(stage), _ptr(x),
+                                                     _ptr(expert_ids), _ptr(expert_w), _ptr(y), m,
+                                                     topk, _stream(stream)),
+                  "escha_linear_moe_gemv_stage")
         return y
 
     def check(self, stream=None):

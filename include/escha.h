@@ -181,6 +181,38 @@ escha_status_t escha_linear_moe_gemv(escha_moe_t m, const uint16_t* x, const int
                                      void* stream);
 
 /*
+ * One stage of a decode-time call, for timing and inspecting the stages one by
+ * one.  Each takes the arguments of its full call (validated the same way)
+ * plus `stage`; running stages 0 .. N-1 in order on one stream with the same
+ * arguments is exactly the full call.  Intermediate results stay in the
+ * handle's own device buffers, so the stages of one pass must not interleave
+ * with another call on the same handle.
+ *   linear (ESCHA_LINEAR_STAGES = 3): 0 input rotation xh = had(x * su);
+ *     1 trellis decode-and-multiply into fp32 partial sums; 2 output rotation
+ *     y = had(sum of partials) * sv.
+ *   mlp (ESCHA_MLP_STAGES = 5): 0 input rotation (shared by gate and up);
+ *     1 gate and up contraction (one launch); 2 output rotations of gate and
+ *     up, silu(gate) * up, input rotation of down; 3 down contraction;
+ *     4 output rotation of down.
+ *   moe (ESCHA_MOE_STAGES = 6): 0 input rotation (shared hidden side);
+ *     1 routing plan (reads expert_ids); 2 gate and up contraction of the
+ *     routed experts; 3 their output rotations, silu(gate) * up and the input
+ *     rotation of down; 4 down contraction; 5 output rotation, weighted sum
+ *     over the routed experts (reads expert_w).
+ * Stage numbers outside [0, N) return ESCHA_ERR_INVALID_ARG.
+ */
+#define ESCHA_LINEAR_STAGES 3
+#define ESCHA_MLP_STAGES 5
+#define ESCHA_MOE_STAGES 6
+escha_status_t escha_linear_gemv_stage(escha_linear_t h, int stage, const uint16_t* x,
+                                       uint16_t* y, int M, void* stream);
+escha_status_t escha_mlp_gemv_stage(escha_mlp_t m, int stage, const uint16_t* x, uint16_t* y,
+                                    int M, void* stream);
+escha_status_t escha_linear_moe_gemv_stage(escha_moe_t m, int stage, const uint16_t* x,
+                                           const int32_t* expert_ids, const float* expert_w,
+                                           uint16_t* y, int M, int topk, void* stream);
+
+/*
  * Synchronise `stream` and report the handle's device error flag:
  * ESCHA_ERR_TIMEOUT if a bounded wait in one of its kernels ran out,
  * ESCHA_ERR_INVALID_ARG if routing ids were out of range, ESCHA_ERR_CUDA on an

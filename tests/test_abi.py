@@ -38,6 +38,10 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
     assert lib.escha_linear_decode(None, None, None) == 1
     assert lib.escha_linear_destroy(None) == 1
     assert lib.escha_mlp_gemv(None, None, None, 1, None) == 1
+    for s in (0, 1, 2, -1, 7):
+        assert lib.escha_linear_gemv_stage(None, s, None, None, 1, None) == 1
+        assert lib.escha_mlp_gemv_stage(None, s, None, None, 1, None) == 1
+        assert lib.escha_linear_moe_gemv_stage(None, s, None, None, None, None, 1, 8, None) == 1
     assert lib.escha_mlp_create(ctypes.byref(h), None, None, None) == 1
     assert lib.escha_linear_check(None, None) == 1
     assert lib.escha_profile_enable(None, 0, 1) == 1

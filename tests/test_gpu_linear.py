@@ -211,3 +211,32 @@ def test_profiler_counts_trellis_launches():
     lin.profile(False)
     lin.gemv(x)
     assert lin.collect() == (0.0, 0)
+
+
+def test_stages_compose_to_the_full_call():
+    """Stages 0..N-1 in order give the full call's output bit for bit."""
+    from gemm_trellis_tile_gb300 import escha
+    rng = np.random.default_rng(61)
+    layer = S.make_linear(rng, 768, 1280, 3)
+    lin, _ = make_linear_handle(layer)
+    mlp = S.make_mlp(rng, 512, 1536, 2, 3, 4)
+    handle, keep = _mlp_handle(mlp)
+    for m in (1, 11):
+        x = S.make_activations(rng, m, 768)
+        xt = torch.from_numpy(x).cuda()
+        full = lin.gemv(xt)
+        staged = torch.empty_like(full)
+        for s in range(escha.Linear.STAGES):
+            lin.gemv(xt, staged, stage=s)
+        assert torch.equal(full, staged)
+        assert rel_l2(staged.cpu().numpy(), oracle_linear(layer, x)) <= REL_L2_TOL
+        xm = torch.from_numpy(S.make_activations(rng, m, 512)).cuda()
+        full = handle.gemv(xm)
+        staged = torch.empty_like(full)
+        for s in range(escha.MLP.STAGES):
+            handle.gemv(xm, staged, stage=s)
+        assert torch.equal(full, staged)
+    for bad in (-1, escha.Linear.STAGES):
+        with pytest.raises(escha.EschaError) as e:
+            lin.gemv(xt, staged[:, :1280], stage=bad)
+        assert e.value.status == 1

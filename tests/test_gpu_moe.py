@@ -154,3 +154,20 @@ def test_moe_glm_shape_full_size_sampled():
                                          sv_h, blocks)
         ref += float(w[0, k]) * yd[0]
     assert rel_l2(y[0, cols], ref) <= REL_L2_TOL
+
+
+def test_moe_stages_compose_to_the_full_call():
+    from gemm_trellis_tile_gb300 import escha
+    spec, moe, experts = _small(3005)
+    rng = np.random.default_rng(3600)
+    x = torch.from_numpy(S.make_activations(rng, 3, spec["hidden"])).cuda()
+    ids, w = S.make_routing(rng, 3, spec["num_experts"], 8)
+    ids, w = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+    full = moe.gemv(x, ids, w)
+    staged = torch.empty_like(full)
+    for s in range(escha.MoE.STAGES):
+        moe.gemv(x, ids, w, staged, stage=s)
+    assert torch.equal(full, staged)
+    with pytest.raises(escha.EschaError) as e:
+        moe.gemv(x, ids, w, staged, stage=escha.MoE.STAGES)
+    assert e.value.status == 1
