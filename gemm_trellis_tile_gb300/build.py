@@ -16,7 +16,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libescha.so")
 
 SOURCES = ["api.cu", "layers.cu", "gemv.cu", "rotate.cu", "moe.cu", "gemm_tc.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "trellis_decode.cuh", "internal.h", "api_internal.h", "act_layout.cuh"]
+HEADERS = ["common.cuh", "trellis_decode.cuh", "internal.h", "api_internal.h", "act_layout.cuh",
+           "tensor_map.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

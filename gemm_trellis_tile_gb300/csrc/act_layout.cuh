@@ -14,17 +14,17 @@ __host__ __device__ __forceinline__ int owner_cta(long long u, long long U, int 
   return static_cast<int>(((u + 1) * G - 1) / U);
 }
 
-// Store one rotated activation (fp16 bits) at its place in the GEMV's
-// B-fragment layout: per k-tile, token block and lane (g = token % 8, t), four
-// words (x[2t], x[2t]), (x[2t+8], x[2t+8]), (x[2t+1], x[2t+1]),
+// Store one rotated activation (fp16 bits) of token m (of M) at its place in
+// the GEMV's B-fragment layout [K/16][M][4][4 words]: per k-tile and token,
+// lane t's four words (x[2t], x[2t]), (x[2t+8], x[2t+8]), (x[2t+1], x[2t+1]),
 // (x[2t+9], x[2t+9]) -- each activation in both halves, against the (lo, hi)
-// halves of a codebook word in the weight operand.
-__device__ __forceinline__ void xfrag_store(uint32_t* xf, int TB, int m, int k, uint16_t hb) {
+// halves of a codebook word in the weight operand.  Only the M real tokens
+// are stored; the GEMV gives lanes of absent tokens zeros.
+__device__ __forceinline__ void xfrag_store(uint32_t* xf, int M, int m, int k, uint16_t hb) {
   const int kt = k >> 4, kk = k & 15;
   const int t = (kk & 7) >> 1, odd = kk & 1, hi8 = kk >> 3;
   const int reg = 2 * odd + hi8;
-  const int tb = m >> 3, g = m & 7;
-  xf[(((size_t)kt * TB + tb) * 32 + 4 * g + t) * 4 + reg] = uint32_t(hb) | (uint32_t(hb) << 16);
+  xf[(((size_t)kt * M + m) * 4 + t) * 4 + reg] = uint32_t(hb) | (uint32_t(hb) << 16);
 }
 
 __device__ __forceinline__ void load4_half(const uint16_t* p, float (&v)[4]) {

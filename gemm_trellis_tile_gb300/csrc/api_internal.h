@@ -39,7 +39,8 @@ struct escha_linear_s {
   const int16_t* code = nullptr;
   float* su = nullptr;        // rin * s_in, fp32 [K]
   float* sv = nullptr;        // rout * s_out, fp32 [N]
-  uint32_t* xfrag = nullptr;  // rotated activations in fragment order, [K/16][2][32][4]
+  CUtensorMap* tmap = nullptr;  // device copy of the GEMV's tensor map of `code`
+  uint32_t* xfrag = nullptr;    // rotated activations in fragment order, [K/16][16][4][4]
   float* part = nullptr;      // GEMV partial sums, [max_slots][16][N]
   int* err = nullptr;         // device error word
   escha::GemvSchedule sched;  // one job: this matrix
@@ -70,6 +71,7 @@ struct escha_moe_s {
   const uint8_t** gate_code = nullptr;  // device [E] tables of borrowed code pointers
   const uint8_t** up_code = nullptr;
   const uint8_t** down_code = nullptr;
+  CUtensorMap* code_maps = nullptr;     // device [3][E]: gate, up, down tensor maps per expert
   int* bits = nullptr;                  // device [E]
   float* su_hidden = nullptr;           // shared input side of gate/up [hidden]
   float* sv_hidden = nullptr;           // shared output side of down [hidden]

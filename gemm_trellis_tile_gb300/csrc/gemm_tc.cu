@@ -34,6 +34,7 @@
 #include "act_layout.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "tensor_map.h"
 #include "trellis_decode.cuh"
 
 namespace escha {
@@ -605,25 +606,6 @@ __global__ void gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
     yr[32 * q] = float_to_half_bits(v[q] * kHadScale * f.sv[n0 + lane + 32 * q]);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 template <int BITS>
 cudaError_t launch_gemm_bits(const CUtensorMap& map, const GemmArgs& a, cudaStream_t st) {
   static bool configured = false;
@@ -646,7 +628,7 @@ size_t gemm_workspace_floats(int num_sms) { return (size_t)num_sms * 2 * kBM * k
 cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, int M, int K,
                                 int N, const float* sv, uint16_t* y, float* ws, int num_sms,
                                 int* err, cudaStream_t st) {
-  EncodeTiledFn enc = encode_fn();
+  EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};

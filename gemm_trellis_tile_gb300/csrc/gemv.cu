@@ -6,27 +6,29 @@
 // ("The escha W2 format, recovered and verified", sections "Bit layout" and
 // "Codebook: cb=1") and fed to the tensor cores.
 //
-// Kernel layout (persistent, several CTAs per SM):
-//   warp 8      producer: one thread streams each unit's row of 8 tiles
-//               (8 x 32*bits bytes, contiguous in HBM) and the matching
-//               activation fragments into a shared-memory ring with 1-D bulk
-//               copies (TMA engine), completing on mbarriers.
-//   warps 0..7  consumers: warp w owns output tile column w of the current
-//               128-channel group.  Per unit it reads its tile's two words per
-//               lane, decodes eight weights per lane, and issues m16n8k16 MMAs
-//               with the weight tile as A (rows = output channels) and up to 8
-//               tokens as B; a second token block handles 9..16 tokens.
-// Each A register holds one weight's codebook word as its two fp16 halves
-// (lo, hi) and B carries the activation in both halves, so the MMA forms
-// lo*x + hi*x in fp32: the codebook's final addition happens inside the
-// contraction instead of as a separate fp16 add (which costs more integer and
-// FMA-pipe instructions than the rest of the decode step).  The sum is not
-// rounded to fp16 first; that changes each weight by at most half an fp16 ulp
-// (relative RMS 2.2e-4 over uniform states).  Each MMA contracts 8 real input
-// channels and two MMAs cover a tile.
-
+// Kernel layout (persistent, one CTA per SM):
+//   warp 0      producer: streams each stage's code words (16 k-tile rows x 8
+//               tile columns, one 2-D TMA copy) and the matching activation
+//               fragments into a shared-memory ring, completing on mbarriers.
+//   warps 1..24 consumers, three groups of eight.  Each group owns one of the
+//               launch's contiguous unit ranges (CTA b of C: ranges b, b + C,
+//               b + 2C) and two ring
+//               stages; in a group, warp w owns output tile column w of the
+//               current 128-channel group.  Per unit it reads its tile's two
+//               words per lane, decodes eight weights per lane, and issues
+//               m16n8k16 MMAs with the weight tile as A (rows = output
+//               channels) and up to 8 tokens as B; a second token block
+//               handles 9..16 tokens.
+// The producer serves the three groups' stages in turn (lanes 0..2 of warp 0,
+// one range each), which keeps them
+// within a stage of each other.  (Separate CTAs on one SM drift apart: the
+// warp scheduler favours the oldest CTA, whose ring runs ahead while the
+// youngest one's work piles up at the end of the launch, when the SM is no
+// longer busy.)  A TMA copy costs the issuing CTA a roughly fixed time however
+// small it is, so each full stage is one 2-D copy of 8-16 KB.
 #include "common.cuh"
 #include "internal.h"
+#include "tensor_map.h"
 #include "trellis_decode.cuh"
 
 #include <algorithm>
@@ -35,12 +37,16 @@ namespace escha {
 
 namespace {
 
-constexpr int kUPS = 8;     // units per pipeline stage
-constexpr int kStages = 4;  // ring depth
-constexpr int kCW = 8;      // consumer warps = tiles per unit
-constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kUPS = 16;    // units per pipeline stage
+constexpr int kCW = 8;      // consumer warps per group = tiles per unit
+constexpr int kGroups = 3;  // consumer groups = unit ranges per CTA
+constexpr int kStages = 6;  // ring depth; stage s serves group s % kGroups
+constexpr int kConsumers = kCW * kGroups * 32;
+constexpr int kThreads = kConsumers + 32;
 constexpr int kCodeStageBytes = kUPS * kCW * 128;  // sized for bits = 4
+static_assert(kStages % kGroups == 0, "a stage must always serve the same group");
 
+// Activation fragments of a stage: kUPS units x M tokens x 64 bytes (M <= 8 TB).
 template <int TB>
 __host__ __device__ constexpr int xf_stage_bytes() {
   return kUPS * TB * 512;
@@ -53,7 +59,7 @@ __host__ __device__ constexpr int gemv_smem_bytes() {
 struct GemvArgs {
   const GemvJob* jobs;
   long long units;
-  int grid;
+  int grid;                    // unit ranges (kGroups per CTA)
   const long long* dev_units;  // when set, units and grid are read from device memory
   const int* dev_grid;         // (a schedule built on the device, e.g. by MoE routing)
   int M;
@@ -86,6 +92,7 @@ struct ChunkIter {
   int g, kt;
   // cached job
   const uint8_t* code;
+  const CUtensorMap* tmap;
   const uint4* xfrag;
   float* part;
   long long ub, ue;
@@ -94,6 +101,7 @@ struct ChunkIter {
   __device__ __forceinline__ void load(const GemvJob* jobs) {
     const GemvJob& J = jobs[j];
     code = J.code;
+    tmap = J.tmap;
     xfrag = J.xfrag;
     part = J.part;
     ub = J.unit_begin;
@@ -155,15 +163,20 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// One unit of this warp's tile column: decode the lane's eight codebook words
+// and contract them with the unit's activation fragments.  xp points at the
+// unit's fragments [M][4] (uint4) plus the lane's (g, t) offset; lanes of
+// tokens at or past M contribute zeros.
 template <int BITS, int TB>
 __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t* p1, const uint4* xp,
-                                             int sh7, uint32_t mask, uint32_t xr,
+                                             int sh7, uint32_t mask, uint32_t xr, int g, int M,
                                              float (&acc)[TB][4]) {
   uint32_t h[8];
   decode8_pairs<BITS>(*p0, *p1, sh7, mask, xr, h);
 #pragma unroll
   for (int tb = 0; tb < TB; ++tb) {
-    const uint4 xf = xp[tb * 32];
+    uint4 xf = make_uint4(0u, 0u, 0u, 0u);
+    if (8 * tb + g < M) xf = xp[tb * 32];
     mma16816(acc[tb], h[0], h[4], h[2], h[6], xf.x, xf.y);
     mma16816(acc[tb], h[1], h[5], h[3], h[7], xf.z, xf.w);
   }
@@ -172,7 +185,7 @@ __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t*
 // One stage: n units (k-tile rows of 8 tiles); this warp owns tile column w.
 template <int BITS, int TB>
 __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint4* xf_s, int n,
-                                              int w, int lane, uint32_t mask, uint32_t xr,
+                                              int w, int lane, int M, uint32_t mask, uint32_t xr,
                                               float (&acc)[TB][4]) {
   constexpr int T = 32 * BITS;
   constexpr int kRowWords = kCW * T / 4;  // uint32 words per unit in the stage
@@ -180,21 +193,25 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint
   const uint32_t* base = reinterpret_cast<const uint32_t*>(codes_s + w * T);
   const uint32_t* p0 = base + lw.i0;
   const uint32_t* p1 = base + lw.i1;
-  const uint4* xp = xf_s + lane;
+  const int g = lane >> 2;
+  const uint4* xp = xf_s + 4 * g + (lane & 3);
+  const int xstride = 4 * M;  // uint4 per unit
   if (n == kUPS) {
+    for (int h = 0; h < kUPS; h += 8) {
 #pragma unroll
-    for (int i = 0; i < kUPS; ++i)
-      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * TB * 32, lw.sh7,
-                             mask, xr, acc);
+      for (int i = h; i < h + 8; ++i)
+        consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * xstride, lw.sh7,
+                               mask, xr, g, M, acc);
+    }
   } else {
     for (int i = 0; i < n; ++i)
-      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * TB * 32, lw.sh7,
-                             mask, xr, acc);
+      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * xstride, lw.sh7,
+                             mask, xr, g, M, acc);
   }
 }
 
 template <int TB>
-__global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* codes = smem;
   uint8_t* xfs = smem + kStages * kCodeStageBytes;
@@ -208,48 +225,67 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
     U = *a.dev_units;
     G = *a.dev_grid;
   }
+  // CTA b works unit ranges b, b + C, b + 2C (C = CTAs launched), one per group.
+  const int C = static_cast<int>(gridDim.x);
   if (static_cast<int>(blockIdx.x) >= G) return;  // launched for the worst case; not needed
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);              // full: producer + tx bytes
-      mbar_init(smem_u32(&bars[kStages + s]), kCW);  // empty: one arrive per consumer warp
+      mbar_init(smem_u32(&bars[kStages + s]), kCW);  // empty: one arrive per warp of its group
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  const int c = blockIdx.x;
-  ChunkIter it;
-  it.init(a.jobs, cta_start(c, U, G), cta_start(c + 1, U, G));
-  Chunk ch;
-
-  if (warp == kCW) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
+    // Lane q < kGroups walks range blockIdx.x + q*C and fills its group's
+    // stages; the lanes advance together, so the groups are served in turn.
+    // A full stage is one tensor copy, a partial one (end of a segment or of
+    // the range) one copy per k-tile row.
+    const int q = lane;
+    const int r = static_cast<int>(blockIdx.x) + q * C;
+    const bool mine = q < kGroups && r < G;
+    ChunkIter it;
+    if (mine) it.init(a.jobs, cta_start(r, U, G), cta_start(r + 1, U, G));
     const uint64_t pol = policy_evict_first();
-    int stage = 0;
+    int slot = 0;  // next stage index within the group's stages
     uint32_t phase = 0;
-    int armed[kStages];
-    for (int s = 0; s < kStages; ++s) armed[s] = -1;
-    bool ok = true;
-    bool waited = false;
-    while (it.next(a.jobs, ch)) {
-      const uint32_t full = smem_u32(&bars[stage]);
+    int armed[kStages / kGroups];
+#pragma unroll
+    for (int s = 0; s < kStages / kGroups; ++s) armed[s] = -1;
+    bool waited = false, ok = true;
+    const CUtensorMap* fenced = nullptr;
+    for (;;) {
+      Chunk ch;
+      const bool has = mine && ok && it.next(a.jobs, ch);
+      if (!__any_sync(0xFFFFFFFFu, has)) break;
+      if (!has) continue;
+      const int stage = q + kGroups * slot;
       if (!mbar_wait(smem_u32(&bars[kStages + stage]), phase ^ 1u, a.limit_ns)) {
         set_error(a.err, kDevErrTimeout);
         ok = false;
-        break;
+        continue;
       }
+      const uint32_t full = smem_u32(&bars[stage]);
       const int T = 32 * it.bits;
       const int rowb = kCW * T;
-      const size_t NT = (size_t)it.NG * kCW;
-      const uint32_t bytes = ch.n * rowb + ch.n * TB * 512;
-      mbar_arrive_expect_tx(full, bytes);
       const uint32_t cdst = smem_u32(codes + stage * kCodeStageBytes);
-      for (int i = 0; i < ch.n; ++i) {
-        const uint8_t* src = it.code + ((size_t)(ch.kt + i) * NT + (size_t)kCW * ch.g) * T;
-        bulk_g2s_evict_first(cdst + i * rowb, src, rowb, full, pol);
+      const uint32_t xbytes = ch.n * a.M * 64;
+      mbar_arrive_expect_tx(full, ch.n * rowb + xbytes);
+      if (ch.n == kUPS) {
+        if (it.tmap != fenced) {
+          tensormap_acquire(it.tmap);
+          fenced = it.tmap;
+        }
+        tma_load_2d_hint(cdst, it.tmap, ch.g * rowb / 4, ch.kt, full, pol);
+      } else {
+        const size_t NT = (size_t)it.NG * kCW;
+        for (int i = 0; i < ch.n; ++i) {
+          const uint8_t* src = it.code + ((size_t)(ch.kt + i) * NT + (size_t)kCW * ch.g) * T;
+          bulk_g2s_evict_first(cdst + i * rowb, src, rowb, full, pol);
+        }
       }
       if (!waited) {
         // The code words above do not depend on the previous kernel; the
@@ -257,31 +293,41 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
         pdl_wait();
         waited = true;
       }
-      bulk_g2s(smem_u32(xfs + stage * xf_stage_bytes<TB>()), it.xfrag + (size_t)ch.kt * TB * 32,
-               ch.n * TB * 512, full);
-      armed[stage] = static_cast<int>(phase);
-      if (++stage == kStages) {
-        stage = 0;
+      bulk_g2s(smem_u32(xfs + stage * xf_stage_bytes<TB>()), it.xfrag + (size_t)ch.kt * a.M * 4,
+               xbytes, full);
+      armed[slot] = static_cast<int>(phase);
+      if (++slot == kStages / kGroups) {
+        slot = 0;
         phase ^= 1u;
       }
     }
-    if (!ok) {
-      // Let every copy already issued land before the CTA's shared memory goes away.
-      for (int s = 0; s < kStages; ++s)
-        if (armed[s] >= 0) mbar_wait(smem_u32(&bars[s]), static_cast<uint32_t>(armed[s]), a.limit_ns);
-    }
+    // Every copy issued must land before the CTA's shared memory goes away
+    // (on the normal path these waits return at once).
+    if (mine)
+#pragma unroll
+      for (int s = 0; s < kStages / kGroups; ++s)
+        if (armed[s] >= 0)
+          mbar_wait(smem_u32(&bars[q + kGroups * s]), static_cast<uint32_t>(armed[s]), a.limit_ns);
     return;
   }
 
   // -------------------------------------------------------------- consumers
+  const int q = (warp - 1) / kCW;       // group: unit range blockIdx.x + q*C
+  const int wt = (warp - 1) - q * kCW;  // tile column within a unit
+  const int r = static_cast<int>(blockIdx.x) + q * C;
+  if (r >= G) return;
+  ChunkIter it;
+  it.init(a.jobs, cta_start(r, U, G), cta_start(r + 1, U, G));
+  Chunk ch;
   float acc[TB][4];
 #pragma unroll
   for (int tb = 0; tb < TB; ++tb)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[tb][q] = 0.f;
-  int stage = 0;
+    for (int i = 0; i < 4; ++i) acc[tb][i] = 0.f;
+  int slot = 0;  // next stage index within the group's stages
   uint32_t phase = 0;
   while (it.next(a.jobs, ch)) {
+    const int stage = q + kGroups * slot;
     if (!mbar_wait(smem_u32(&bars[stage]), phase, a.limit_ns)) {
       set_error(a.err, kDevErrTimeout);
       break;
@@ -289,34 +335,34 @@ __global__ void __launch_bounds__(kThreads, 3) trellis_gemv_kernel(const GemvArg
     const uint8_t* cs = codes + stage * kCodeStageBytes;
     const uint4* xs = reinterpret_cast<const uint4*>(xfs + stage * xf_stage_bytes<TB>());
     switch (it.bits) {
-      case 2: consume_chunk<2, TB>(cs, xs, ch.n, warp, lane, a.cb_mask, a.cb_xor, acc); break;
-      case 3: consume_chunk<3, TB>(cs, xs, ch.n, warp, lane, a.cb_mask, a.cb_xor, acc); break;
-      default: consume_chunk<4, TB>(cs, xs, ch.n, warp, lane, a.cb_mask, a.cb_xor, acc); break;
+      case 2: consume_chunk<2, TB>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 3: consume_chunk<3, TB>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      default: consume_chunk<4, TB>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + stage]));
-    if (++stage == kStages) {
-      stage = 0;
+    if (++slot == kStages / kGroups) {
+      slot = 0;
       phase ^= 1u;
     }
     if (ch.seg_end) {
       const long long gb = it.ub + (long long)ch.g * it.KT;
-      const int slot = c - cta_of_unit(gb, U, G);
-      const int n0 = 128 * ch.g + 16 * warp + (lane >> 2);
+      const int ps = r - cta_of_unit(gb, U, G);  // partial-sum slot
+      const int n0 = 128 * ch.g + 16 * wt + (lane >> 2);
       const int t2 = 2 * (lane & 3);
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int tok = 8 * tb + t2 + q;
+        for (int i = 0; i < 2; ++i) {
+          const int tok = 8 * tb + t2 + i;
           if (tok < a.M) {
-            float* row = it.part + ((size_t)slot * a.mpad + tok) * it.N;
-            row[n0] = acc[tb][q];
-            row[n0 + 8] = acc[tb][2 + q];
+            float* row = it.part + ((size_t)ps * a.mpad + tok) * it.N;
+            row[n0] = acc[tb][i];
+            row[n0 + 8] = acc[tb][2 + i];
           }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[tb][q] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[tb][i] = 0.f;
       }
     }
   }
@@ -380,7 +426,7 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   a.cb_mask = kMcgMask;
   a.cb_xor = kMcgXor;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(s.grid);
+  cfg.gridDim = dim3(s.ctas);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = gemv_smem_bytes<TB>();
   cfg.stream = st;
@@ -394,27 +440,41 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
 
 }  // namespace
 
-int gemv_ctas_per_sm() {
+bool encode_gemv_code_map(CUtensorMap* map, const void* code, int bits, int KT, int NT) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t row_words = (cuuint64_t)NT * 8 * bits;  // a tile is 8*bits words
+  const cuuint64_t dims[2] = {row_words, (cuuint64_t)KT};
+  const cuuint64_t strides[1] = {row_words * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)(kCW * 8 * bits), (cuuint32_t)kUPS};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(code), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemv_ranges_per_sm() {
   int n = 0;
   if (cudaFuncSetAttribute(trellis_gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            gemv_smem_bytes<2>()) != cudaSuccess)
-    return 1;
+    return kGroups;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, trellis_gemv_kernel<2>, kThreads,
                                                     gemv_smem_bytes<2>()) != cudaSuccess)
-    return 1;
-  return std::max(1, n);
+    return kGroups;
+  return kGroups * std::max(1, n);
 }
 
-void plan_gemv(GemvSchedule& s, int num_sms, int ctas_per_sm) {
+void plan_gemv(GemvSchedule& s, int num_sms, int ranges_per_sm) {
   long long u = 0;
   for (auto& j : s.jobs) {
     j.unit_begin = u;
     u += (long long)j.KT * j.NG;
   }
   s.units = u;
-  long long g = std::min<long long>((long long)num_sms * ctas_per_sm,
+  long long g = std::min<long long>((long long)num_sms * ranges_per_sm,
                                     std::max<long long>(1, u / kMinUnitsPerCta));
   s.grid = static_cast<int>(std::max<long long>(1, g));
+  s.ctas = std::min(s.grid, num_sms * std::max(1, ranges_per_sm / kGroups));
   int ms = 1;
   for (size_t j = 0; j < s.jobs.size(); ++j)
     for (int gg = 0; gg < s.jobs[j].NG; ++gg)
@@ -452,7 +512,8 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
   a.limit_ns = kWaitLimitNs;
   a.cb_mask = kMcgMask;
   a.cb_xor = kMcgXor;
-  trellis_gemv_kernel<1><<<max_grid, kThreads, gemv_smem_bytes<1>(), st>>>(a);
+  trellis_gemv_kernel<1><<<(max_grid + kGroups - 1) / kGroups, kThreads, gemv_smem_bytes<1>(),
+                           st>>>(a);
   return cudaGetLastError();
 }
 

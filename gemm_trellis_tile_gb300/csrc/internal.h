@@ -1,6 +1,7 @@
 // Host-side internals of libescha shared between translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -18,13 +19,14 @@ constexpr int kDevErrBadRoute = 2;
 // Job j's work is cut into units: unit (g, kt) = k-tile row kt of output group
 // g (128 output channels = 8 tiles of 16).  Units are numbered job-major, then
 // group-major, then k.  The launch's units are split into `grid` contiguous,
-// near-equal ranges, one per persistent CTA (CTA c owns [c*U/G, (c+1)*U/G)).
-// Where a CTA's range covers a group only partly, it writes its fp32 partial
-// sums to slot (c - first CTA of that group); the output kernel sums the slots.
-
+// near-equal ranges (range r owns [r*U/G, (r+1)*U/G)); persistent CTA b of C
+// works ranges b, b + C and b + 2C, one per consumer warp group.  Where a range covers a
+// group only partly, it writes its fp32 partial sums to slot (r - first range
+// of that group); the output kernel sums the slots.
 struct GemvJob {
-  const uint8_t* code;   // tiles, [KT][NT][32*bits bytes]
-  const uint4* xfrag;    // rotated activations in fragment order, [KT][TB][32] x uint4
+  const uint8_t* code;       // tiles, [KT][NT][32*bits bytes]
+  const CUtensorMap* tmap;   // `code` as a 2-D tensor (encode_gemv_code_map), in device memory
+  const uint4* xfrag;        // rotated activations in fragment order, [KT][M][4] x uint4
   float* part;           // partial sums, [slots][mpad][N]
   long long unit_begin;  // first unit of this job within the launch
   int bits;
@@ -37,7 +39,8 @@ struct GemvSchedule {
   std::vector<GemvJob> jobs;
   GemvJob* d_jobs = nullptr;
   long long units = 0;
-  int grid = 0;
+  int grid = 0;   // unit ranges
+  int ctas = 0;   // CTAs launched (each works up to three ranges)
   int max_slots = 0;
 };
 
@@ -51,14 +54,21 @@ constexpr int kMoeMaxDistinct = kMoeMaxTokens * kMoeMaxTopk;
 constexpr int kMoeMaxExperts = 4096;
 constexpr int kMinUnitsPerCta = 8;
 
-int gemv_ctas_per_sm();
+int gemv_ranges_per_sm();
 // Fill unit_begin, units, grid and max_slots for the given jobs.
-void plan_gemv(GemvSchedule& s, int num_sms, int ctas_per_sm);
+void plan_gemv(GemvSchedule& s, int num_sms, int ranges_per_sm);
 int gemv_slots_for_group(const GemvSchedule& s, int job, int g);
 
 cudaError_t launch_gemv(const GemvSchedule& s, int M, int* err, cudaStream_t st);
+// The 2-D tensor map through which the GEMV loads a stage's rows of code
+// words: `code` [KT][NT][32*bits bytes] seen as uint32 rows of NT*8*bits
+// words, one box = 8 tile columns x 16 k-tile rows.  Host only; false if the
+// driver cannot encode it.
+bool encode_gemv_code_map(CUtensorMap* map, const void* code, int bits, int KT, int NT);
+
 // Up to 8 tokens, with the job table, unit count and grid size written on the
-// device (the grid is launched at max_grid; CTAs past the device grid exit).
+// device (max_grid ranges are launched for; CTAs whose ranges start past the
+// device grid exit).
 cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* d_units,
                                         const int* d_grid, int max_grid, int M, int mpad,
                                         int* err, cudaStream_t st);
@@ -78,7 +88,7 @@ cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);
 struct RotInJob {
   const uint16_t* x;  // [M, K] fp16
   const float* su;    // [K]
-  uint32_t* xfrag;    // [K/16][TB][32][4]
+  uint32_t* xfrag;    // [K/16][M][4][4]
   int K;
 };
 
@@ -92,14 +102,13 @@ struct PartRef {
 
 cudaError_t launch_fold_scales(const uint16_t* r, const float* s, float* out, int n,
                                cudaStream_t st);
-cudaError_t launch_rotate_in_xfrag(const RotInJob* jobs, int njobs, int M, int TB,
-                                   cudaStream_t st);
+cudaError_t launch_rotate_in_xfrag(const RotInJob* jobs, int njobs, int M, cudaStream_t st);
 cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t* xh, int M,
                                    int K, cudaStream_t st);
 cudaError_t launch_rotate_out(const PartRef& pr, long long units, int grid, const float* sv,
                               uint16_t* y, int M, int mpad, cudaStream_t st);
 cudaError_t launch_mlp_mid(const PartRef& gate, const PartRef& up, long long units, int grid,
                            const float* sv_gate, const float* sv_up, const float* su_down,
-                           uint32_t* xfrag_down, int M, int TB, cudaStream_t st);
+                           uint32_t* xfrag_down, int M, cudaStream_t st);
 
 }  // namespace escha

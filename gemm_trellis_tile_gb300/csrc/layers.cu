@@ -36,12 +36,14 @@ template escha_status_t dev_alloc<uint16_t>(uint16_t**, size_t);
 template escha_status_t dev_alloc<GemvJob>(GemvJob**, size_t);
 template escha_status_t dev_alloc<const uint8_t*>(const uint8_t***, size_t);
 template escha_status_t dev_alloc<unsigned char>(unsigned char**, size_t);
+template escha_status_t dev_alloc<CUtensorMap>(CUtensorMap**, size_t);
 
 namespace {
 
 GemvJob make_job(const escha_linear_s* h, const uint32_t* xfrag, float* part) {
   GemvJob j;
   j.code = reinterpret_cast<const uint8_t*>(h->code);
+  j.tmap = h->tmap;
   j.xfrag = reinterpret_cast<const uint4*>(xfrag);
   j.part = part;
   j.unit_begin = 0;
@@ -52,7 +54,7 @@ GemvJob make_job(const escha_linear_s* h, const uint32_t* xfrag, float* part) {
   return j;
 }
 
-size_t xfrag_words(int K) { return (size_t)(K / 16) * 2 * 32 * 4; }
+size_t xfrag_words(int K) { return (size_t)(K / 16) * kGemvMaxTokens * 16; }
 
 PartRef part_ref(const GemvSchedule& s, int job) {
   PartRef r;
@@ -79,12 +81,21 @@ escha_status_t linear_init(escha_linear_s* h, const int16_t* code, int bits, int
   if ((s = dev_alloc(&h->xfrag, xfrag_words(K))) != ESCHA_OK) return s;
   if ((s = dev_alloc(&h->err, 1)) != ESCHA_OK) return s;
   if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return ESCHA_ERR_CUDA;
+  {
+    CUtensorMap map;
+    if (!encode_gemv_code_map(&map, code, bits, K / 16, N / 16)) return ESCHA_ERR_CUDA;
+    unsigned char* d = nullptr;
+    if ((s = dev_alloc(&d, sizeof(CUtensorMap))) != ESCHA_OK) return s;
+    h->tmap = reinterpret_cast<CUtensorMap*>(d);
+    if (cudaMemcpy(h->tmap, &map, sizeof(map), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ESCHA_ERR_CUDA;
+  }
 
   if (launch_fold_scales(rin, s_in, h->su, K, st) != cudaSuccess) return ESCHA_ERR_CUDA;
   if (launch_fold_scales(rout, s_out, h->sv, N, st) != cudaSuccess) return ESCHA_ERR_CUDA;
 
   h->sched.jobs.assign(1, make_job(h, h->xfrag, nullptr));
-  plan_gemv(h->sched, h->num_sms, gemv_ctas_per_sm());
+  plan_gemv(h->sched, h->num_sms, gemv_ranges_per_sm());
   if ((s = dev_alloc(&h->part, (size_t)h->sched.max_slots * kGemvMaxTokens * N)) != ESCHA_OK)
     return s;
   h->sched.jobs[0].part = h->part;
@@ -94,6 +105,7 @@ escha_status_t linear_init(escha_linear_s* h, const int16_t* code, int bits, int
 }
 
 void linear_free(escha_linear_s* h) {
+  cudaFree(h->tmap);
   cudaFree(h->su);
   cudaFree(h->sv);
   cudaFree(h->xfrag);
@@ -105,6 +117,7 @@ void linear_free(escha_linear_s* h) {
   h->gemm_ws = nullptr;
   h->su = h->sv = nullptr;
   h->xfrag = nullptr;
+  h->tmap = nullptr;
   h->part = nullptr;
   h->err = nullptr;
   h->sched.d_jobs = nullptr;
@@ -113,12 +126,11 @@ void linear_free(escha_linear_s* h) {
 
 escha_status_t linear_gemv_stage(escha_linear_s* h, int stage, const uint16_t* x, uint16_t* y,
                                  int M, cudaStream_t st) {
-  const int TB = M <= 8 ? 1 : 2;
   cudaError_t e = cudaSuccess;
   switch (stage) {
     case 0: {
       RotInJob rj{x, h->su, h->xfrag, h->K};
-      e = launch_rotate_in_xfrag(&rj, 1, M, TB, st);
+      e = launch_rotate_in_xfrag(&rj, 1, M, st);
       break;
     }
     case 1:
@@ -186,7 +198,7 @@ escha_status_t mlp_init(escha_mlp_s* m, escha_linear_s* gate, escha_linear_s* up
   if ((s = dev_alloc(&m->err, 1)) != ESCHA_OK) return s;
   if (cudaMemset(m->err, 0, sizeof(int)) != cudaSuccess) return ESCHA_ERR_CUDA;
 
-  const int cps = gemv_ctas_per_sm();
+  const int cps = gemv_ranges_per_sm();
   m->s_gate_up.jobs = {make_job(gate, m->xfrag_gate, nullptr), make_job(up, m->xfrag_up, nullptr)};
   plan_gemv(m->s_gate_up, gate->num_sms, cps);
   m->s_down.jobs = {make_job(down, m->xfrag_down, nullptr)};
@@ -217,13 +229,12 @@ void mlp_free(escha_mlp_s* m) {
 
 escha_status_t mlp_gemv_stage(escha_mlp_s* m, int stage, const uint16_t* x, uint16_t* y, int M,
                               cudaStream_t st) {
-  const int TB = M <= 8 ? 1 : 2;
   cudaError_t e = cudaSuccess;
   switch (stage) {
     case 0: {
       RotInJob rj[2] = {{x, m->gate->su, m->xfrag_gate, m->gate->K},
                         {x, m->up->su, m->xfrag_up, m->up->K}};
-      e = launch_rotate_in_xfrag(rj, 2, M, TB, st);
+      e = launch_rotate_in_xfrag(rj, 2, M, st);
       break;
     }
     case 1:
@@ -234,7 +245,7 @@ escha_status_t mlp_gemv_stage(escha_mlp_s* m, int stage, const uint16_t* x, uint
     case 2:
       e = launch_mlp_mid(part_ref(m->s_gate_up, 0), part_ref(m->s_gate_up, 1), m->s_gate_up.units,
                          m->s_gate_up.grid, m->gate->sv, m->up->sv, m->down->su, m->xfrag_down, M,
-                         TB, st);
+                         st);
       break;
     case 3:
       m->prof.begin(st);

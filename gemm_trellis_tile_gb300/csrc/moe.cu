@@ -56,9 +56,10 @@ struct MoePlanArgs {
   const uint8_t* const* gate_code;
   const uint8_t* const* up_code;
   const uint8_t* const* down_code;
+  const CUtensorMap* code_maps;  // [3][E]: gate, up, down
   const int* bits;
   const uint32_t* xfrag_hidden;
-  uint32_t* xfrag_down;   // [kMoeMaxDistinct][inter/16][1][32][4]
+  uint32_t* xfrag_down;   // [kMoeMaxDistinct][inter/16][M][4][4]
   float* part1;           // [2*kMoeMaxDistinct][slots][8][inter]
   float* part2;           // [kMoeMaxDistinct][slots][8][hidden]
   size_t part1_stride, part2_stride, xdown_stride;  // elements per job / per distinct slot
@@ -69,10 +70,12 @@ struct MoePlanArgs {
   int* err;
 };
 
-__device__ __forceinline__ GemvJob make_job(const uint8_t* code, const uint32_t* xfrag, float* part,
-                                            long long ub, int bits, int KT, int NG, int N) {
+__device__ __forceinline__ GemvJob make_job(const uint8_t* code, const CUtensorMap* tmap,
+                                            const uint32_t* xfrag, float* part, long long ub,
+                                            int bits, int KT, int NG, int N) {
   GemvJob j;
   j.code = code;
+  j.tmap = tmap;
   j.xfrag = reinterpret_cast<const uint4*>(xfrag);
   j.part = part;
   j.unit_begin = ub;
@@ -129,13 +132,15 @@ __global__ void moe_plan_kernel(const MoePlanArgs a) {
   for (int d = threadIdx.x; d < kMoeMaxDistinct; d += blockDim.x) {
     const int e = d < nd ? r->expert[d] : 0;
     const int b = a.bits[e];
-    a.jobs1[2 * d] = make_job(a.gate_code[e], a.xfrag_hidden, a.part1 + (2 * d) * a.part1_stride,
-                              (2 * d) * ug, b, KTg, NGg, a.inter);
-    a.jobs1[2 * d + 1] = make_job(a.up_code[e], a.xfrag_hidden,
+    a.jobs1[2 * d] = make_job(a.gate_code[e], a.code_maps + e, a.xfrag_hidden,
+                              a.part1 + (2 * d) * a.part1_stride, (2 * d) * ug, b, KTg, NGg,
+                              a.inter);
+    a.jobs1[2 * d + 1] = make_job(a.up_code[e], a.code_maps + a.E + e, a.xfrag_hidden,
                                   a.part1 + (2 * d + 1) * a.part1_stride, (2 * d + 1) * ug, b, KTg,
                                   NGg, a.inter);
-    a.jobs2[d] = make_job(a.down_code[e], a.xfrag_down + d * a.xdown_stride,
-                          a.part2 + d * a.part2_stride, d * ud, b, KTd, NGd, a.hidden);
+    a.jobs2[d] = make_job(a.down_code[e], a.code_maps + 2 * a.E + e,
+                          a.xfrag_down + d * a.xdown_stride, a.part2 + d * a.part2_stride, d * ud,
+                          b, KTd, NGd, a.hidden);
   }
   if (threadIdx.x == 0) {
     r->n_distinct = nd;
@@ -170,7 +175,8 @@ __global__ void moe_mid_kernel(const MoeMidArgs a) {
   const MoeRoute* r = a.route;
   if (d >= r->n_distinct) return;
   const int e = r->expert[d];
-  const bool routed = m < a.M && ((r->mask[d] >> m) & 1u);
+  if (m >= a.M) return;
+  const bool routed = (r->mask[d] >> m) & 1u;
   const int n0 = g * kHad + 4 * lane;
   float h[4] = {0.f, 0.f, 0.f, 0.f};
   if (routed) {
@@ -200,7 +206,7 @@ __global__ void moe_mid_kernel(const MoeMidArgs a) {
   }
   uint32_t* xf = a.xfrag_down + d * a.xdown_stride;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) xfrag_store(xf, 1, m, n0 + q, float_to_half_bits(h[q] * kHadScale));
+  for (int q = 0; q < 4; ++q) xfrag_store(xf, a.M, m, n0 + q, float_to_half_bits(h[q] * kHadScale));
 }
 
 struct MoeOutArgs {
@@ -285,6 +291,17 @@ escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
   if ((s = upload(&h->up_code, u.data(), E)) != ESCHA_OK) return s;
   if ((s = upload(&h->down_code, d.data(), E)) != ESCHA_OK) return s;
   if ((s = upload(&h->bits, b.data(), E)) != ESCHA_OK) return s;
+  {
+    // Tensor maps of every expert's three code tensors, [gate | up | down][E].
+    std::vector<CUtensorMap> maps(3 * (size_t)E);
+    for (int e = 0; e < E; ++e) {
+      if (!encode_gemv_code_map(&maps[e], g[e], b[e], hidden / 16, inter / 16) ||
+          !encode_gemv_code_map(&maps[E + e], u[e], b[e], hidden / 16, inter / 16) ||
+          !encode_gemv_code_map(&maps[2 * (size_t)E + e], d[e], b[e], inter / 16, hidden / 16))
+        return ESCHA_ERR_CUDA;
+    }
+    if ((s = upload(&h->code_maps, maps.data(), maps.size())) != ESCHA_OK) return s;
+  }
 
   const size_t ei = (size_t)E * inter;
   if ((s = dev_alloc(&h->su_hidden, hidden)) != ESCHA_OK) return s;
@@ -299,10 +316,11 @@ escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
       launch_fold_scales(rin_down, s_in_down, h->su_down, static_cast<int>(ei), st) != cudaSuccess)
     return ESCHA_ERR_CUDA;
 
-  h->xdown_stride = (size_t)(inter / 16) * 32 * 4;  // words per distinct slot (one token block)
+  h->xdown_stride = (size_t)(inter / 16) * kMoeMaxTokens * 16;  // words per distinct slot
   h->part1_stride = (size_t)kMoeSlots * kMoeMaxTokens * inter;
   h->part2_stride = (size_t)kMoeSlots * kMoeMaxTokens * hidden;
-  if ((s = dev_alloc(&h->xfrag_hidden, (size_t)(hidden / 16) * 32 * 4)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->xfrag_hidden, (size_t)(hidden / 16) * kMoeMaxTokens * 16)) != ESCHA_OK)
+    return s;
   if ((s = dev_alloc(&h->xfrag_down, h->xdown_stride * kMoeMaxDistinct)) != ESCHA_OK) return s;
   if ((s = dev_alloc(&h->part1, h->part1_stride * 2 * kMoeMaxDistinct)) != ESCHA_OK) return s;
   if ((s = dev_alloc(&h->part2, h->part2_stride * kMoeMaxDistinct)) != ESCHA_OK) return s;
@@ -314,12 +332,13 @@ escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
   if ((s = dev_alloc(&h->err, 1)) != ESCHA_OK) return s;
   if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return ESCHA_ERR_CUDA;
   if (cudaMemset(h->route, 0, sizeof(MoeRoute)) != cudaSuccess) return ESCHA_ERR_CUDA;
-  h->grid_max = h->num_sms * gemv_ctas_per_sm();
+  h->grid_max = h->num_sms * gemv_ranges_per_sm();
   if (cudaStreamSynchronize(st) != cudaSuccess) return ESCHA_ERR_CUDA;
   return ESCHA_OK;
 }
 
 void moe_free(escha_moe_s* h) {
+  cudaFree(h->code_maps);
   cudaFree(h->gate_code);
   cudaFree(h->up_code);
   cudaFree(h->down_code);
@@ -346,7 +365,7 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
   switch (stage) {
     case 0: {
       RotInJob rj{x, h->su_hidden, h->xfrag_hidden, h->hidden};
-      e = launch_rotate_in_xfrag(&rj, 1, M, 1, st);
+      e = launch_rotate_in_xfrag(&rj, 1, M, st);
       break;
     }
     case 1: {
@@ -360,6 +379,7 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       pa.gate_code = h->gate_code;
       pa.up_code = h->up_code;
       pa.down_code = h->down_code;
+      pa.code_maps = h->code_maps;
       pa.bits = h->bits;
       pa.xfrag_hidden = h->xfrag_hidden;
       pa.xfrag_down = h->xfrag_down;

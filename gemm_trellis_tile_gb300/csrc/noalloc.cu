@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "api_internal.h"
+#include "common.cuh"
 #include "escha.h"
 #include "internal.h"
 
@@ -38,14 +39,21 @@ struct DeviceState {
   bool ready = false;
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
   int num_sms = 0;
-  int ctas_per_sm = 1;
+  int ranges_per_sm = 1;
   GemvSchedule sched;                // one job; its vector keeps capacity 1
 };
 
 DeviceState g_state[kMaxDevices];
 std::mutex g_mutex;
 
-__global__ void put_job_kernel(GemvJob job, GemvJob* dst) { *dst = job; }
+// Writes the job table and the code tensor map into the scratch array (a
+// kernel, not a copy from host memory, so the call stays capturable).
+__global__ void put_job_kernel(GemvJob job, GemvJob* dst, const __grid_constant__ CUtensorMap map,
+                               CUtensorMap* map_dst) {
+  *dst = job;
+  *map_dst = map;
+  tensormap_release();
+}
 
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
@@ -63,7 +71,7 @@ escha_status_t setup_device(int dev, DeviceState& s) {
   }
   s.scratch = static_cast<unsigned char*>(p);
   s.num_sms = sms;
-  s.ctas_per_sm = gemv_ctas_per_sm();
+  s.ranges_per_sm = gemv_ranges_per_sm();
   s.sched.jobs.reserve(1);
   s.ready = true;
   (void)dev;
@@ -98,6 +106,7 @@ extern "C" escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const u
   const int K = in_features, N = out_features;
   GemvJob job;
   job.code = reinterpret_cast<const uint8_t*>(code);
+  job.tmap = nullptr;
   job.xfrag = nullptr;
   job.part = nullptr;
   job.unit_begin = 0;
@@ -106,12 +115,13 @@ extern "C" escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const u
   job.NG = N / 128;
   job.N = N;
   s.sched.jobs.assign(1, job);
-  plan_gemv(s.sched, s.num_sms, s.ctas_per_sm);
+  plan_gemv(s.sched, s.num_sms, s.ranges_per_sm);
 
   // Scratch layout, each piece on a 256-byte boundary.
   const size_t off_job = 0;
   const size_t off_err = 256;
-  const size_t off_su = 512;
+  const size_t off_map = 512;
+  const size_t off_su = 768;
   const size_t off_sv = off_su + round256((size_t)K * sizeof(float));
   const size_t off_xf = off_sv + round256((size_t)N * sizeof(float));
   const size_t off_part = off_xf + round256((size_t)(K / 16) * 2 * 32 * 4 * sizeof(uint32_t));
@@ -125,20 +135,23 @@ extern "C" escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const u
   float* sv = reinterpret_cast<float*>(base + off_sv);
   uint32_t* xfrag = reinterpret_cast<uint32_t*>(base + off_xf);
   float* part = reinterpret_cast<float*>(base + off_part);
+  CUtensorMap* d_map = reinterpret_cast<CUtensorMap*>(base + off_map);
+  CUtensorMap map;
+  if (!encode_gemv_code_map(&map, code, bits, K / 16, N / 16)) return ESCHA_ERR_CUDA;
+  s.sched.jobs[0].tmap = d_map;
   s.sched.jobs[0].xfrag = reinterpret_cast<const uint4*>(xfrag);
   s.sched.jobs[0].part = part;
   s.sched.d_jobs = reinterpret_cast<GemvJob*>(base + off_job);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int TB = M <= 8 ? 1 : 2;
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), st);
   if (e != cudaSuccess) return from_cuda(e);
-  put_job_kernel<<<1, 1, 0, st>>>(s.sched.jobs[0], s.sched.d_jobs);
+  put_job_kernel<<<1, 1, 0, st>>>(s.sched.jobs[0], s.sched.d_jobs, map, d_map);
   if ((e = cudaGetLastError()) != cudaSuccess) return from_cuda(e);
   if ((e = launch_fold_scales(rin, s_in, su, K, st)) != cudaSuccess) return from_cuda(e);
   if ((e = launch_fold_scales(rout, s_out, sv, N, st)) != cudaSuccess) return from_cuda(e);
   RotInJob rj{x, su, xfrag, K};
-  if ((e = launch_rotate_in_xfrag(&rj, 1, M, TB, st)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_rotate_in_xfrag(&rj, 1, M, st)) != cudaSuccess) return from_cuda(e);
   if ((e = launch_gemv(s.sched, M, err, st)) != cudaSuccess) return from_cuda(e);
   PartRef pr;
   pr.part = part;

@@ -33,15 +33,14 @@ struct RotInArgs {
   RotInJob jobs[2];
   int njobs;
   int M;
-  int TB;
 };
 
-// xfrag = fp16(had128(x * su)) for tokens 0..8TB-1 (zeros past M).
+// xfrag = fp16(had128(x * su)) for tokens 0..M-1.
 __global__ void rotate_in_xfrag_kernel(const RotInArgs a) {
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  const int mp = 8 * a.TB;
+  const int mp = a.M;
   int j = 0;
   for (; j < a.njobs; ++j) {
     const long long n = (long long)mp * (a.jobs[j].K / kHad);
@@ -54,19 +53,17 @@ __global__ void rotate_in_xfrag_kernel(const RotInArgs a) {
   const int m = static_cast<int>(wid / nb);
   const int kb = static_cast<int>(wid - (long long)m * nb);
   const int k0 = kb * kHad + 4 * lane;
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
-  if (m < a.M) {
-    load4_half(J.x + (size_t)m * J.K + k0, v);
-    const float4 su = *reinterpret_cast<const float4*>(J.su + k0);
-    v[0] *= su.x;
-    v[1] *= su.y;
-    v[2] *= su.z;
-    v[3] *= su.w;
-    fwht128_warp(v, lane);
-  }
+  float v[4];
+  load4_half(J.x + (size_t)m * J.K + k0, v);
+  const float4 su = *reinterpret_cast<const float4*>(J.su + k0);
+  v[0] *= su.x;
+  v[1] *= su.y;
+  v[2] *= su.z;
+  v[3] *= su.w;
+  fwht128_warp(v, lane);
 #pragma unroll
   for (int r = 0; r < 4; ++r)
-    xfrag_store(J.xfrag, a.TB, m, k0 + r, float_to_half_bits(v[r] * kHadScale));
+    xfrag_store(J.xfrag, a.M, m, k0 + r, float_to_half_bits(v[r] * kHadScale));
 }
 
 // xh[m, k] = fp16(had128(x * su)), plain row-major (the GEMM's A operand).
@@ -118,19 +115,18 @@ __global__ void rotate_out_kernel(const PartRef pr, long long U, int G, const fl
 // then the down layer's input rotation had(h * su_down) into its fragments.
 __global__ void mlp_mid_kernel(const PartRef gate, const PartRef up, long long U, int G,
                                const float* sv_gate, const float* sv_up, const float* su_down,
-                               uint32_t* xfrag_down, int M, int TB) {
+                               uint32_t* xfrag_down, int M) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int NG = gate.N / kHad;
-  const int mp = 8 * TB;
-  if (wid >= (long long)mp * NG) return;
+  if (wid >= (long long)M * NG) return;
   const int m = static_cast<int>(wid / NG);
   const int g = static_cast<int>(wid - (long long)m * NG);
   const int n0 = g * kHad + 4 * lane;
-  float h[4] = {0.f, 0.f, 0.f, 0.f};
-  if (m < M) {
+  float h[4];
+  {
     float gv[4], uv[4];
     sum_part_slots(gate, U, G, kGemvMaxTokens, m, g, lane, gv);
     sum_part_slots(up, U, G, kGemvMaxTokens, m, g, lane, uv);
@@ -152,7 +148,7 @@ __global__ void mlp_mid_kernel(const PartRef gate, const PartRef up, long long U
   }
 #pragma unroll
   for (int r = 0; r < 4; ++r)
-    xfrag_store(xfrag_down, TB, m, n0 + r, float_to_half_bits(h[r] * kHadScale));
+    xfrag_store(xfrag_down, M, m, n0 + r, float_to_half_bits(h[r] * kHadScale));
 }
 
 unsigned blocks_for(long long warps) {
@@ -184,17 +180,15 @@ cudaError_t launch_fold_scales(const uint16_t* r, const float* s, float* out, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_rotate_in_xfrag(const RotInJob* jobs, int njobs, int M, int TB,
-                                   cudaStream_t st) {
+cudaError_t launch_rotate_in_xfrag(const RotInJob* jobs, int njobs, int M, cudaStream_t st) {
   RotInArgs a;
   long long warps = 0;
   for (int j = 0; j < njobs; ++j) {
     a.jobs[j] = jobs[j];
-    warps += (long long)8 * TB * (jobs[j].K / kHad);
+    warps += (long long)M * (jobs[j].K / kHad);
   }
   a.njobs = njobs;
   a.M = M;
-  a.TB = TB;
   rotate_in_xfrag_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(a);
   return cudaGetLastError();
 }
@@ -215,11 +209,11 @@ cudaError_t launch_rotate_out(const PartRef& pr, long long units, int grid, cons
 
 cudaError_t launch_mlp_mid(const PartRef& gate, const PartRef& up, long long units, int grid,
                            const float* sv_gate, const float* sv_up, const float* su_down,
-                           uint32_t* xfrag_down, int M, int TB, cudaStream_t st) {
-  const long long warps = (long long)8 * TB * (gate.N / kHad);
+                           uint32_t* xfrag_down, int M, cudaStream_t st) {
+  const long long warps = (long long)M * (gate.N / kHad);
   DependentLaunch dl(blocks_for(warps), 32 * kWarpsPerBlock, st);
   return cudaLaunchKernelEx(&dl.cfg, mlp_mid_kernel, gate, up, units, grid, sv_gate, sv_up,
-                            su_down, xfrag_down, M, TB);
+                            su_down, xfrag_down, M);
 }
 
 }  // namespace escha
