@@ -35,6 +35,13 @@ from gemm_trellis_tile_gb300 import workloads as WL  # noqa: E402
 
 L2_FALLBACK_BYTES = 129 * 1024 * 1024
 
+# DRAM bytes per contraction launch (dram__bytes_read.sum + dram__bytes_write.sum
+# from one ncu capture of this kernel, averaged over the step's launches), by
+# workload at M=1; None where no capture of the current kernel exists.
+GEMV_TRAFFIC_BYTES = {
+    "dense gated MLP 5120->17408->5120, gate 2-bit / up 3-bit / down 3-bit, M=1": 44.72e6,
+}
+
 
 def parse_args():
     p = argparse.ArgumentParser()
@@ -692,7 +699,8 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "trellis_gemv",
                      "launch_us": 1e3 * k_ms / k_n,
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": (achieved / peak) if achieved else None, "traffic": None,
+                     "frac": (achieved / peak) if achieved else None,
+                     "traffic": GEMV_TRAFFIC_BYTES.get(spec["name"]) if m == 1 else None,
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": e2e_steps * sbytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
