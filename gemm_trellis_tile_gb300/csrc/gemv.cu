@@ -164,25 +164,26 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // One unit of this warp's tile column: decode the lane's eight codebook words
-// and contract them with the unit's activation fragments.  xp points at the
-// unit's fragments [M][4] (uint4) plus the lane's (g, t) offset; lanes of
-// tokens at or past M contribute zeros.
+// and contract them with the unit's activation fragments.  xq[tb] points at
+// the lane's fragment of token block tb in this unit.
 template <int BITS, int TB>
-__device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t* p1, const uint4* xp,
-                                             int sh7, uint32_t mask, uint32_t xr, int g, int M,
-                                             float (&acc)[TB][4]) {
+__device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t* p1,
+                                             const uint4* const (&xq)[TB], int sh7, uint32_t mask,
+                                             uint32_t xr, float (&acc)[TB][4]) {
   uint32_t h[8];
   decode8_pairs<BITS>(*p0, *p1, sh7, mask, xr, h);
 #pragma unroll
   for (int tb = 0; tb < TB; ++tb) {
-    uint4 xf = make_uint4(0u, 0u, 0u, 0u);
-    if (8 * tb + g < M) xf = xp[tb * 32];
+    const uint4 xf = *xq[tb];
     mma16816(acc[tb], h[0], h[4], h[2], h[6], xf.x, xf.y);
     mma16816(acc[tb], h[1], h[5], h[3], h[7], xf.z, xf.w);
   }
 }
 
 // One stage: n units (k-tile rows of 8 tiles); this warp owns tile column w.
+// The stage holds fragments for the M real tokens only.  A lane whose token
+// (8 tb + g) is at or past M reads token M-1's fragment instead: MMA output
+// column g depends on B column g alone, and those columns are never stored.
 template <int BITS, int TB>
 __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint4* xf_s, int n,
                                               int w, int lane, int M, uint32_t mask, uint32_t xr,
@@ -194,19 +195,26 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint
   const uint32_t* p0 = base + lw.i0;
   const uint32_t* p1 = base + lw.i1;
   const int g = lane >> 2;
-  const uint4* xp = xf_s + 4 * g + (lane & 3);
   const int xstride = 4 * M;  // uint4 per unit
+  const uint4* xq[TB];
+#pragma unroll
+  for (int tb = 0; tb < TB; ++tb) xq[tb] = xf_s + 4 * min(8 * tb + g, M - 1) + (lane & 3);
   if (n == kUPS) {
     for (int h = 0; h < kUPS; h += 8) {
 #pragma unroll
-      for (int i = h; i < h + 8; ++i)
-        consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * xstride, lw.sh7,
-                               mask, xr, g, M, acc);
+      for (int i = 0; i < 8; ++i) {
+        consume_unit<BITS, TB>(p0 + (h + i) * kRowWords, p1 + (h + i) * kRowWords, xq, lw.sh7,
+                               mask, xr, acc);
+#pragma unroll
+        for (int tb = 0; tb < TB; ++tb) xq[tb] += xstride;
+      }
     }
   } else {
-    for (int i = 0; i < n; ++i)
-      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xp + i * xstride, lw.sh7,
-                             mask, xr, g, M, acc);
+    for (int i = 0; i < n; ++i) {
+      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xq, lw.sh7, mask, xr, acc);
+#pragma unroll
+      for (int tb = 0; tb < TB; ++tb) xq[tb] += xstride;
+    }
   }
 }
 
