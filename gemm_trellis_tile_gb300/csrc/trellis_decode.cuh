@@ -79,38 +79,23 @@ __device__ __forceinline__ uint32_t field16_at_byte(uint32_t x, int b) {
 
 // The lane's eight 16-bit states.  (lo, hi) is the lane's 64-bit span shifted
 // so that symbol 7's window starts at bit 0; symbol j's window starts at bit
-// BITS*(7-j).  At 2 and 4 bits every window is byte aligned in one of a few
-// pre-shifted copies of the span, so each state costs one byte permute.
+// s = BITS*(7-j) <= 28.  A window with s <= 16 is moved up to the next byte
+// boundary of lo by a left shift (s + k = 8*ceil(s/8), and the window still
+// ends by bit 32), the others likewise in m = bits 16..47 of the span; one
+// byte permute then extracts it zero-extended.  The left shifts are constant
+// multiplies, which the compiler can issue on the multiply pipe, leaving the
+// integer ALU pipe (the decode's bottleneck) one permute per state.
 template <int BITS>
 __device__ __forceinline__ void lane_states(uint32_t lo, uint32_t hi, uint32_t (&st)[8]) {
-  if (BITS == 2) {
-    // offsets 14, 12, ..., 0: copies shifted by 0, 2, 4, 6
-    const uint32_t r[4] = {lo, lo >> 2, lo >> 4, lo >> 6};
+  const uint32_t m = __funnelshift_r(lo, hi, 16);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int s = 2 * (7 - j);
-      st[j] = field16_at_byte(r[(s & 7) >> 1], s >> 3);
-    }
-  } else if (BITS == 4) {
-    // offsets 28, 24, ..., 0
-    const uint32_t l4 = __funnelshift_r(lo, hi, 4);
-    const uint32_t m16 = __funnelshift_r(lo, hi, 16);
-    const uint32_t m20 = __funnelshift_r(lo, hi, 20);
-    st[7] = field16_at_byte(lo, 0);   // 0
-    st[6] = field16_at_byte(l4, 0);   // 4
-    st[5] = field16_at_byte(lo, 1);   // 8
-    st[4] = field16_at_byte(l4, 1);   // 12
-    st[3] = field16_at_byte(lo, 2);   // 16
-    st[2] = field16_at_byte(l4, 2);   // 20
-    st[1] = field16_at_byte(m16, 1);  // 24
-    st[0] = field16_at_byte(m20, 1);  // 28
-  } else {
-    // 3 bits: offsets 21, 18, ..., 0 have eight different residues mod 8
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int s = BITS * (7 - j);
-      st[j] = (s + 16 <= 32) ? ((lo >> s) & 0xFFFFu) : (__funnelshift_r(lo, hi, s) & 0xFFFFu);
-    }
+  for (int j = 0; j < 8; ++j) {
+    const int s = BITS * (7 - j);
+    const uint32_t src = s <= 16 ? lo : m;
+    const int sr = s <= 16 ? s : s - 16;
+    const int b = (sr + 7) / 8;
+    const int k = 8 * b - sr;
+    st[j] = field16_at_byte(src * (1u << k), b);
   }
 }
 
