@@ -66,6 +66,7 @@ struct GemvArgs {
   int mpad;
   int* err;
   uint64_t limit_ns;
+  int maps_from_device;  // tensor maps were written by a kernel: fence before first use
   uint32_t cb_mask;  // kMcgMask and kMcgXor, as run-time values (see mcg_pair)
   uint32_t cb_xor;
 };
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
       const uint32_t xbytes = ch.n * a.M * 64;
       mbar_arrive_expect_tx(full, ch.n * rowb + xbytes);
       if (ch.n == kUPS) {
-        if (it.tmap != fenced) {
+        if (a.maps_from_device && it.tmap != fenced) {
           tensormap_acquire(it.tmap);
           fenced = it.tmap;
         }
@@ -430,6 +431,7 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   a.M = M;
   a.mpad = kGemvMaxTokens;
   a.err = err;
+  a.maps_from_device = s.maps_from_device ? 1 : 0;
   a.limit_ns = kWaitLimitNs;
   a.cb_mask = kMcgMask;
   a.cb_xor = kMcgXor;
@@ -517,6 +519,7 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
   a.M = M;
   a.mpad = mpad;
   a.err = err;
+  a.maps_from_device = 0;  // copied from the host at creation
   a.limit_ns = kWaitLimitNs;
   a.cb_mask = kMcgMask;
   a.cb_xor = kMcgXor;

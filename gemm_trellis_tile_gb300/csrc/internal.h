@@ -42,6 +42,7 @@ struct GemvSchedule {
   int grid = 0;   // unit ranges
   int ctas = 0;   // CTAs launched (each works up to three ranges)
   int max_slots = 0;
+  bool maps_from_device = false;  // the jobs' tensor maps are written by a kernel
 };
 
 constexpr int kGemvMaxTokens = 16;

@@ -139,6 +139,7 @@ extern "C" escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const u
   CUtensorMap map;
   if (!encode_gemv_code_map(&map, code, bits, K / 16, N / 16)) return ESCHA_ERR_CUDA;
   s.sched.jobs[0].tmap = d_map;
+  s.sched.maps_from_device = true;
   s.sched.jobs[0].xfrag = reinterpret_cast<const uint4*>(xfrag);
   s.sched.jobs[0].part = part;
   s.sched.d_jobs = reinterpret_cast<GemvJob*>(base + off_job);
