@@ -15,7 +15,8 @@ Sources (web pages, cited by title and section):
           reconstruction, the three-instruction codebook, the tile packing
           paragraph with the closed-form permutation inverse.
   [EXLR8] the EXLR8 format page -- the shared per-layer rotation ("The sharing
-          trick"), the 16x16 tile packing, expert shapes.
+          trick"), the 16x16 tile packing, expert shapes, and the E4M3 rounding
+          of every codebook value (round-to-nearest-even, saturating).
 
 Readings taken where the pages are silent or ambiguous (each also listed in the
 design notes):
@@ -33,6 +34,10 @@ design notes):
     placement ("tile[perm] = values", [FMT]) is the inverse of that.
   * Hadamard.  Natural (Sylvester) order, normalised by 1/sqrt(128), applied to
     each consecutive block of 128 channels.
+  * E4M3 variant.  [EXLR8] rounds "every value the codebook produces" to FP8
+    E4M3; the value rounded is the codebook's fp16 value (after its one fp16
+    addition), to the nearest E4M3 value, ties to even mantissa, magnitudes
+    above 448 clamped to 448 (saturating; E4M3 has no infinities).
 
 The fp16 <-> float conversions use numpy's IEEE half type.
 """
@@ -164,6 +169,46 @@ def codebook_value(states):
 
 
 # ----------------------------------------------------------------------------
+# E4M3 rounding of codebook values  ([EXLR8] "Every value the codebook produces
+# is rounded to E4M3 (round-to-nearest-even, saturating)")
+# ----------------------------------------------------------------------------
+
+E4M3_MAX = 448.0        # largest finite FP8 E4M3 value: 1.75 * 2^8
+E4M3_MIN_EXP = -6       # exponent of the smallest normal value (bias 7)
+E4M3_MANT_BITS = 3
+
+
+def e4m3_round(x):
+    """Nearest FP8 E4M3 value (ties to even mantissa), saturating at +-448.
+
+    The spacing of E4M3 values in the binade [2^e, 2^(e+1)) is 2^(e-3); below
+    2^-6 (subnormals) it stays 2^-9.  Rounding |x| / spacing to the nearest
+    integer, halves to even, is round-to-nearest-even on the mantissa.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, E4M3_MIN_EXP)
+    q = np.exp2(e - E4M3_MANT_BITS)
+    r = np.minimum(np.round(a / q) * q, E4M3_MAX)
+    return np.copysign(r, x)
+
+
+def codebook_value_e4m3(states):
+    """The codebook's fp16 value rounded to E4M3 (returned as float16, exactly)."""
+    return e4m3_round(codebook_value(states).astype(np.float64)).astype(np.float16)
+
+
+def codebook(states, rounding="fp16"):
+    """Weight value of each state: the fp16 codebook value, or its E4M3 rounding."""
+    if rounding == "fp16":
+        return codebook_value(states)
+    if rounding == "e4m3":
+        return codebook_value_e4m3(states)
+    raise ValueError(rounding)
+
+
+# ----------------------------------------------------------------------------
 # Tensor-core permutation  ([MLX] closed-form inverse; [FMT] "tile[perm] = values")
 # ----------------------------------------------------------------------------
 
@@ -194,16 +239,16 @@ def perm_forward():
 # Decode: code tensor -> W_inner  ([FMT] "Tensor mapping", "Bit layout")
 # ----------------------------------------------------------------------------
 
-def decode_tiles(tile_codes, bits):
+def decode_tiles(tile_codes, bits, rounding="fp16"):
     """Decode tiles: int16 [..., 16*bits] -> float16 [..., 16, 16] (row = input channel)."""
-    values = codebook_value(tile_states(tile_codes, bits))     # [..., 256]
+    values = codebook(tile_states(tile_codes, bits), rounding)  # [..., 256]
     perm = perm_forward()
     flat = np.empty(values.shape, dtype=np.float16)
     flat[..., perm] = values                                    # tile[perm] = values
     return flat.reshape(*values.shape[:-1], TILE, TILE)
 
 
-def decode_matrix(code, bits, chunk=4096):
+def decode_matrix(code, bits, chunk=4096, rounding="fp16"):
     """W_inner fp16 [in, out] from the code tensor int16 [in/16, out/16, 16*bits].
 
     code[i, j] holds W_inner[16i:16i+16, 16j:16j+16] (K-tile index major).
@@ -213,17 +258,17 @@ def decode_matrix(code, bits, chunk=4096):
     flat = code.reshape(kt * nt, nw)
     tiles = np.empty((kt * nt, TILE, TILE), dtype=np.float16)
     for a in range(0, kt * nt, chunk):
-        tiles[a:a + chunk] = decode_tiles(flat[a:a + chunk], bits)
+        tiles[a:a + chunk] = decode_tiles(flat[a:a + chunk], bits, rounding)
     return tiles.reshape(kt, nt, TILE, TILE).transpose(0, 2, 1, 3).reshape(kt * TILE, nt * TILE)
 
 
-def decode_columns(code, bits, cols):
+def decode_columns(code, bits, cols, rounding="fp16"):
     """W_inner[:, cols] (fp16) decoding only the tile columns that hold `cols`."""
     cols = np.asarray(cols)
     kt = code.shape[0]
     out = np.empty((kt * TILE, cols.size), dtype=np.float16)
     for jt in np.unique(cols // TILE):
-        tiles = decode_tiles(code[:, jt, :], bits)              # [kt, 16, 16]
+        tiles = decode_tiles(code[:, jt, :], bits, rounding)    # [kt, 16, 16]
         strip = tiles.reshape(kt * TILE, TILE)
         sel = np.nonzero(cols // TILE == jt)[0]
         out[:, sel] = strip[:, cols[sel] % TILE]
@@ -286,12 +331,12 @@ def linear_forward(x, w_inner, su, sv):
     return had_blockwise(y_pre) * sv
 
 
-def linear_forward_columns(x, code, bits, su, sv, blocks):
+def linear_forward_columns(x, code, bits, su, sv, blocks, rounding="fp16"):
     """Output columns of the 128-blocks `blocks` only (decodes just those columns)."""
     x = np.asarray(x).astype(np.float64)
     xh = had_blockwise(x * su)
     cols = np.concatenate([np.arange(b * HAD_BLOCK, (b + 1) * HAD_BLOCK) for b in blocks])
-    w = decode_columns(code, bits, cols).astype(np.float64)
+    w = decode_columns(code, bits, cols, rounding).astype(np.float64)
     y_pre = xh @ w
     y = had_blockwise(y_pre) * sv[cols]
     return cols, y

@@ -399,3 +399,75 @@ def test_moe_forward_reduces_to_mlp():
 def test_silu_closed_form():
     z = np.array([0.0, 1.0, -1.0, 20.0])
     assert np.allclose(O.silu(z), [0.0, 1 / (1 + np.exp(-1)), -1 / (1 + np.e), 20.0], atol=1e-7)
+
+
+# ---------------------------------------------------------------- E4M3 rounding (EXLR8)
+
+def _e4m3_table():
+    """All finite FP8 E4M3 values, decoded from their bit patterns (bias 7,
+    three mantissa bits, exponent field 0 = subnormal, S.1111.111 = NaN)."""
+    vals = []
+    for code in range(256):
+        s, e, m = code >> 7, (code >> 3) & 15, code & 7
+        if e == 15 and m == 7:
+            continue                                     # NaN
+        mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        vals.append(-mag if s else mag)
+    return np.array(sorted(set(vals)))
+
+
+def test_e4m3_table_extremes():
+    t = _e4m3_table()
+    assert t.max() == 448.0 and t.min() == -448.0        # 1.75 * 2^8
+    assert np.min(t[t > 0]) == 2.0 ** -9                 # smallest subnormal
+
+
+def test_e4m3_round_matches_torch_float8_on_every_fp16_in_range():
+    v = np.arange(65536, dtype=np.uint16).view(np.float16).astype(np.float64)
+    v = v[np.isfinite(v) & (np.abs(v) <= 448)]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.e4m3_round(v), ref)
+
+
+def test_e4m3_round_fixes_every_e4m3_value_and_breaks_ties_to_even():
+    t = _e4m3_table()
+    assert np.array_equal(O.e4m3_round(t), t)
+    pos = t[t >= 0]
+    mids = (pos[:-1] + pos[1:]) / 2
+    got = O.e4m3_round(mids)
+    # the tie goes to the neighbour whose mantissa field is even
+    for lo_v, hi_v, g in zip(pos[:-1], pos[1:], got):
+        def mant(v):
+            if v < 2.0 ** -6:
+                return int(round(v / 2.0 ** -9))
+            return int(round((v / 2.0 ** np.floor(np.log2(v)) - 1) * 8))
+        want = lo_v if mant(lo_v) % 2 == 0 else hi_v
+        assert g == want, (lo_v, hi_v, g)
+
+
+def test_e4m3_round_saturates():
+    got = O.e4m3_round(np.array([449.0, 464.0, 1e4, -500.0, 65504.0]))
+    assert np.array_equal(got, [448.0, 448.0, 448.0, -448.0, 448.0])
+
+
+def test_e4m3_codebook_rounds_the_fp16_value_and_never_saturates():
+    st = np.arange(65536, dtype=np.uint32)
+    w = O.codebook_value(st).astype(np.float64)
+    w8 = O.codebook_value_e4m3(st).astype(np.float64)
+    table = _e4m3_table()
+    assert np.all(np.isin(w8, table))
+    assert np.abs(w).max() < 4.0                         # far below 448
+    # every value is the nearest table entry to the fp16 value
+    idx = np.searchsorted(table, w)
+    lo = table[np.clip(idx - 1, 0, table.size - 1)]
+    hi = table[np.clip(idx, 0, table.size - 1)]
+    assert np.all(np.minimum(np.abs(w - lo), np.abs(w - hi)) == np.abs(w - w8))
+
+
+def test_decode_e4m3_is_rounding_of_decode_fp16():
+    rng = np.random.default_rng(77)
+    code = rng.integers(-32768, 32768, size=(3, 4, 48), dtype=np.int16)
+    w = O.decode_matrix(code, 3).astype(np.float64)
+    w8 = O.decode_matrix(code, 3, rounding="e4m3").astype(np.float64)
+    ref = torch.from_numpy(w).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(w8, ref)
