@@ -53,6 +53,8 @@ def parse_args():
     p.add_argument("--m", type=int, default=1, help="tokens per step")
     p.add_argument("--shape", default=None, help="in x out (sweep: default 5120x10240; "
                    "prefill: default 5120x17408)")
+    p.add_argument("--rounding", default="fp16", choices=["fp16", "e4m3"],
+                   help="codebook rounding: fp16 values, or the EXLR8 E4M3 variant")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
@@ -134,7 +136,15 @@ class ClockSampler:
 # ---------------------------------------------------------------- workloads
 
 def workload_spec(args):
-    """Layers of one step as (in, out, bits) and a description."""
+    """Layers of one step as (in, out, bits), a description and the codebook rounding."""
+    spec = _workload_spec(args)
+    spec["rounding"] = args.rounding
+    if args.rounding == "e4m3":
+        spec["name"] += ", E4M3 codebook rounding"
+    return spec
+
+
+def _workload_spec(args):
     if args.workload == "mlp":
         layers = WL.mlp_layers(5120, 17408, (2, 3, 3))
         name = "dense gated MLP 5120->17408->5120, gate 2-bit / up 3-bit / down 3-bit, M=%d" % args.m
@@ -193,7 +203,8 @@ def oracle_sample_rate(spec, m, seconds, seed=7):
         x = S.make_activations(rng, m, k)
         su = O.fold_scales(lay["rin"], lay["s_in"])
         sv = O.fold_scales(lay["rout"], lay["s_out"])
-        O.linear_forward_columns(x, lay["code"], lay["bits"], su, sv, [blk])
+        O.linear_forward_columns(x, lay["code"], lay["bits"], su, sv, [blk],
+                                 rounding=spec["rounding"])
         done_bytes += WL.layer_bytes(m, k, 128, lay["bits"])
         blocks += 1
         if time.perf_counter() - t0 >= seconds:
@@ -215,7 +226,7 @@ def run_reference(args, spec, rank):
     budget = 150.0 / max(1, args.steps + args.warmup)   # seconds per step
     probe = mats[0]
     t0 = time.perf_counter()
-    O.decode_columns(probe["code"][:8], probe["bits"], np.arange(128))
+    O.decode_columns(probe["code"][:8], probe["bits"], np.arange(128), rounding=spec["rounding"])
     per_ktile = max(1e-6, (time.perf_counter() - t0) / 8)
     ktiles = max(8, int(budget / per_ktile) // 8 * 8)
 
@@ -226,7 +237,8 @@ def run_reference(args, spec, rank):
         blk = int(rng.integers(n // 128))
         kk = kt * 16
         x = S.make_activations(rng, args.m, kk)
-        w = O.decode_columns(lay["code"][:kt], b, np.arange(blk * 128, blk * 128 + 128))
+        w = O.decode_columns(lay["code"][:kt], b, np.arange(blk * 128, blk * 128 + 128),
+                             rounding=spec["rounding"])
         su = O.fold_scales(lay["rin"][:kk], lay["s_in"][:kk])
         y_pre = O.had_blockwise(x * su) @ w.astype(np.float64)
         _ = O.had_blockwise(y_pre) * O.fold_scales(lay["rout"], lay["s_out"])[blk * 128:blk * 128 + 128]
@@ -291,6 +303,7 @@ def run_moe(args, spec, rank, world, local):
                     [c[2] for c in codes], mspec["bits"], t["rin_hidden"], t["s_in_hidden"],
                     t["rout_gate"], t["s_out_gate"], t["rout_up"], t["s_out_up"], t["rin_down"],
                     t["s_in_down"], t["rout_hidden"], t["s_out_hidden"])
+    moe.set_rounding(spec["rounding"])
     rng = np.random.default_rng(spec["seed"] + 29)
     R = 64
     routes = [S.make_routing(rng, m, E, 8) for _ in range(R)]
@@ -439,6 +452,7 @@ def run_prefill(args, spec, rank, world, local):
     for r in range(n_inst):
         lins.append(escha.Linear.from_arrays(S.make_linear(np.random.default_rng(
             spec["seed"] + 7919 * r + 1000003 * rank), k, n, b)))
+        lins[-1].set_rounding(spec["rounding"])
     rng = np.random.default_rng(spec["seed"] + 17)
     x_host = torch.from_numpy(S.make_activations(rng, m, k)).pin_memory()
     x = x_host.to(dev)
@@ -531,8 +545,11 @@ def make_handles(spec, inst):
         g = escha.Linear.from_arrays(inst["gate"])
         u = escha.Linear.from_arrays(inst["up"])
         d = escha.Linear.from_arrays(inst["down"])
+        for h in (g, u, d):
+            h.set_rounding(spec["rounding"])
         return escha.MLP(g, u, d), (g, u, d)
     lin = escha.Linear.from_arrays(inst["layer"])
+    lin.set_rounding(spec["rounding"])
     return lin, (lin,)
 
 

@@ -233,8 +233,22 @@ escha_status_t escha_linear_shape(escha_linear_t h, int* in_features, int* out_f
 escha_status_t escha_linear_decode(escha_linear_t h, uint16_t* w_inner, void* stream) {
   if (!h || !w_inner) return ESCHA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(w_inner) & 1u) != 0) return ESCHA_ERR_INVALID_ARG;
-  return from_cuda(launch_decode(h->code, h->bits, h->K, h->N, w_inner,
-                                 static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_decode(h->code, h->bits, h->rounding == ESCHA_ROUND_E4M3, h->K, h->N,
+                                 w_inner, static_cast<cudaStream_t>(stream)));
+}
+
+escha_status_t escha_linear_set_rounding(escha_linear_t h, int rounding) {
+  if (!h) return ESCHA_ERR_INVALID_ARG;
+  if (rounding != ESCHA_ROUND_FP16 && rounding != ESCHA_ROUND_E4M3) return ESCHA_ERR_INVALID_ARG;
+  return linear_set_rounding(h, rounding);
+}
+
+escha_status_t escha_moe_set_rounding(escha_moe_t m, int rounding) {
+  if (!m) return ESCHA_ERR_INVALID_ARG;
+  if (rounding != ESCHA_ROUND_FP16 && rounding != ESCHA_ROUND_E4M3) return ESCHA_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ESCHA_ERR_CUDA;  // no call in flight
+  m->rounding = rounding;  // read by the routing plan of every call
+  return ESCHA_OK;
 }
 
 static bool gemv_args_ok(const void* h, const void* x, const void* y, int M) {

@@ -34,6 +34,7 @@ escha_status_t dev_alloc(T** p, size_t count);
 
 struct escha_linear_s {
   int device = 0;
+  int rounding = 0;           // ESCHA_ROUND_FP16 or ESCHA_ROUND_E4M3
   int num_sms = 0;
   int K = 0, N = 0, bits = 0;
   const int16_t* code = nullptr;
@@ -66,6 +67,7 @@ struct escha_mlp_s {
 
 struct escha_moe_s {
   int device = 0;
+  int rounding = 0;           // ESCHA_ROUND_FP16 or ESCHA_ROUND_E4M3
   int num_sms = 0;
   int E = 0, hidden = 0, inter = 0;
   const uint8_t** gate_code = nullptr;  // device [E] tables of borrowed code pointers
@@ -111,6 +113,7 @@ escha_status_t linear_init(escha_linear_s* h, const int16_t* code, int bits, int
                            const uint16_t* rin, const uint16_t* rout, const float* s_in,
                            const float* s_out, cudaStream_t st);
 void linear_free(escha_linear_s* h);
+escha_status_t linear_set_rounding(escha_linear_s* h, int rounding);
 escha_status_t linear_gemv_stage(escha_linear_s* h, int stage, const uint16_t* x, uint16_t* y,
                                  int M, cudaStream_t st);
 escha_status_t linear_gemv(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,

@@ -269,7 +269,7 @@ struct SegIter {
 
 // ---------------------------------------------------------------- kernel
 
-template <int BITS>
+template <int BITS, bool E4M3>
 __global__ void __launch_bounds__(kThreadsG, 1)
     trellis_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           const int nt = nt_base + i;
           const uint32_t* tw = reinterpret_cast<const uint32_t*>(codes + (kt_local * 8 + nt) * T);
           uint32_t h[8];
-          decode8<BITS>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
+          decode8<BITS, E4M3>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const int rh = p & 1, nh = p >> 1;
@@ -606,16 +606,16 @@ __global__ void gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
     yr[32 * q] = float_to_half_bits(v[q] * kHadScale * f.sv[n0 + lane + 32 * q]);
 }
 
-template <int BITS>
+template <int BITS, bool E4M3>
 cudaError_t launch_gemm_bits(const CUtensorMap& map, const GemmArgs& a, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(trellis_gemm_kernel<BITS>,
+    cudaError_t e = cudaFuncSetAttribute(trellis_gemm_kernel<BITS, E4M3>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  trellis_gemm_kernel<BITS><<<a.grid, kThreadsG, kSmemBytes, st>>>(map, a);
+  trellis_gemm_kernel<BITS, E4M3><<<a.grid, kThreadsG, kSmemBytes, st>>>(map, a);
   return cudaGetLastError();
 }
 
@@ -625,9 +625,9 @@ size_t gemm_workspace_floats(int num_sms) { return (size_t)num_sms * 2 * kBM * k
 
 // xh: rotated activations fp16 [M, K] (16-byte aligned, K a multiple of 128);
 // ws: gemm_workspace_floats(num_sms) fp32.
-cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, int M, int K,
-                                int N, const float* sv, uint16_t* y, float* ws, int num_sms,
-                                int* err, cudaStream_t st) {
+cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, bool e4m3,
+                                int M, int K, int N, const float* sv, uint16_t* y, float* ws,
+                                int num_sms, int* err, cudaStream_t st) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -680,9 +680,9 @@ cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bit
 
   cudaError_t e;
   switch (bits) {
-    case 2: e = launch_gemm_bits<2>(map, a, st); break;
-    case 3: e = launch_gemm_bits<3>(map, a, st); break;
-    default: e = launch_gemm_bits<4>(map, a, st); break;
+    case 2: e = e4m3 ? launch_gemm_bits<2, true>(map, a, st) : launch_gemm_bits<2, false>(map, a, st); break;
+    case 3: e = e4m3 ? launch_gemm_bits<3, true>(map, a, st) : launch_gemm_bits<3, false>(map, a, st); break;
+    default: e = e4m3 ? launch_gemm_bits<4, true>(map, a, st) : launch_gemm_bits<4, false>(map, a, st); break;
   }
   if (e != cudaSuccess) return e;
   if (f.count > 0) {

@@ -98,6 +98,7 @@ struct ChunkIter {
   float* part;
   long long ub, ue;
   int bits, KT, NG, N;
+  int e4m3;
 
   __device__ __forceinline__ void load(const GemvJob* jobs) {
     const GemvJob& J = jobs[j];
@@ -110,6 +111,7 @@ struct ChunkIter {
     KT = J.KT;
     NG = J.NG;
     N = J.N;
+    e4m3 = J.e4m3;
     ue = ub + (long long)KT * NG;
   }
   __device__ __forceinline__ void init(const GemvJob* jobs, long long begin, long long end) {
@@ -167,12 +169,15 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // One unit of this warp's tile column: decode the lane's eight codebook words
 // and contract them with the unit's activation fragments.  xq[tb] points at
 // the lane's fragment of token block tb in this unit.
-template <int BITS, int TB>
+template <int BITS, int TB, bool E4M3>
 __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t* p1,
                                              const uint4* const (&xq)[TB], int sh7, uint32_t mask,
                                              uint32_t xr, float (&acc)[TB][4]) {
   uint32_t h[8];
-  decode8_pairs<BITS>(*p0, *p1, sh7, mask, xr, h);
+  if (E4M3)
+    decode8_e4m3_dup<BITS>(*p0, *p1, sh7, mask, xr, h);  // MMA forms 2*w*x
+  else
+    decode8_pairs<BITS>(*p0, *p1, sh7, mask, xr, h);
 #pragma unroll
   for (int tb = 0; tb < TB; ++tb) {
     const uint4 xf = *xq[tb];
@@ -185,7 +190,7 @@ __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t*
 // The stage holds fragments for the M real tokens only.  A lane whose token
 // (8 tb + g) is at or past M reads token M-1's fragment instead: MMA output
 // column g depends on B column g alone, and those columns are never stored.
-template <int BITS, int TB>
+template <int BITS, int TB, bool E4M3>
 __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint4* xf_s, int n,
                                               int w, int lane, int M, uint32_t mask, uint32_t xr,
                                               float (&acc)[TB][4]) {
@@ -204,15 +209,16 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint
     for (int h = 0; h < kUPS; h += 8) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        consume_unit<BITS, TB>(p0 + (h + i) * kRowWords, p1 + (h + i) * kRowWords, xq, lw.sh7,
-                               mask, xr, acc);
+        consume_unit<BITS, TB, E4M3>(p0 + (h + i) * kRowWords, p1 + (h + i) * kRowWords, xq,
+                                     lw.sh7, mask, xr, acc);
 #pragma unroll
         for (int tb = 0; tb < TB; ++tb) xq[tb] += xstride;
       }
     }
   } else {
     for (int i = 0; i < n; ++i) {
-      consume_unit<BITS, TB>(p0 + i * kRowWords, p1 + i * kRowWords, xq, lw.sh7, mask, xr, acc);
+      consume_unit<BITS, TB, E4M3>(p0 + i * kRowWords, p1 + i * kRowWords, xq, lw.sh7, mask, xr,
+                                   acc);
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb) xq[tb] += xstride;
     }
@@ -343,10 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
     }
     const uint8_t* cs = codes + stage * kCodeStageBytes;
     const uint4* xs = reinterpret_cast<const uint4*>(xfs + stage * xf_stage_bytes<TB>());
-    switch (it.bits) {
-      case 2: consume_chunk<2, TB>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 3: consume_chunk<3, TB>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      default: consume_chunk<4, TB>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+    switch (it.bits + 8 * it.e4m3) {
+      case 2: consume_chunk<2, TB, false>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 3: consume_chunk<3, TB, false>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 4: consume_chunk<4, TB, false>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 10: consume_chunk<2, TB, true>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 11: consume_chunk<3, TB, true>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      default: consume_chunk<4, TB, true>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + stage]));
@@ -359,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
       const int ps = r - cta_of_unit(gb, U, G);  // partial-sum slot
       const int n0 = 128 * ch.g + 16 * wt + (lane >> 2);
       const int t2 = 2 * (lane & 3);
+      const float f = it.e4m3 ? 0.5f : 1.0f;  // the E4M3 path's MMAs form 2*w*x
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb) {
 #pragma unroll
@@ -366,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
           const int tok = 8 * tb + t2 + i;
           if (tok < a.M) {
             float* row = it.part + ((size_t)ps * a.mpad + tok) * it.N;
-            row[n0] = acc[tb][i];
-            row[n0 + 8] = acc[tb][2 + i];
+            row[n0] = acc[tb][i] * f;
+            row[n0 + 8] = acc[tb][2 + i] * f;
           }
         }
 #pragma unroll
@@ -378,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
 }
 
 // One warp per tile: writes W_inner[16i + r][16j + c] in fp16.
-template <int BITS>
+template <int BITS, bool E4M3>
 __global__ void trellis_decode_kernel(const uint8_t* code, uint16_t* w, int KT, int NT) {
   constexpr int T = 32 * BITS;
   const long long tile = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -389,7 +399,7 @@ __global__ void trellis_decode_kernel(const uint8_t* code, uint16_t* w, int KT, 
   const LaneWindow lw = lane_window<BITS>(lane);
   const uint32_t* tw = reinterpret_cast<const uint32_t*>(code + tile * T);
   uint32_t h[8];
-  decode8<BITS>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
+  decode8<BITS, E4M3>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
   const size_t N = (size_t)NT * 16;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -528,17 +538,20 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const int16_t* code, int bits, int K, int N, uint16_t* w,
+cudaError_t launch_decode(const int16_t* code, int bits, bool e4m3, int K, int N, uint16_t* w,
                           cudaStream_t st) {
   const int KT = K / 16, NT = N / 16;
   const long long tiles = (long long)KT * NT;
   const int wpb = 8;
   const unsigned blocks = static_cast<unsigned>((tiles + wpb - 1) / wpb);
   const uint8_t* c = reinterpret_cast<const uint8_t*>(code);
-  switch (bits) {
-    case 2: trellis_decode_kernel<2><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
-    case 3: trellis_decode_kernel<3><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
-    default: trellis_decode_kernel<4><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
+  switch (bits + 8 * (e4m3 ? 1 : 0)) {
+    case 2: trellis_decode_kernel<2, false><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
+    case 3: trellis_decode_kernel<3, false><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
+    case 4: trellis_decode_kernel<4, false><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
+    case 10: trellis_decode_kernel<2, true><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
+    case 11: trellis_decode_kernel<3, true><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
+    default: trellis_decode_kernel<4, true><<<blocks, 32 * wpb, 0, st>>>(c, w, KT, NT); break;
   }
   return cudaGetLastError();
 }

@@ -33,6 +33,7 @@ struct GemvJob {
   int KT;                // in / 16
   int NG;                // out / 128
   int N;                 // out
+  int e4m3;              // codebook values rounded to FP8 E4M3 (EXLR8 variant)
 };
 
 struct GemvSchedule {
@@ -77,10 +78,10 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
 // xh is fp16 [M, K], 16-byte aligned; ws holds gemm_workspace_floats(num_sms)
 // fp32 for tiles shared between CTAs.
 size_t gemm_workspace_floats(int num_sms);
-cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, int M, int K,
-                                int N, const float* sv, uint16_t* y, float* ws, int num_sms,
-                                int* err, cudaStream_t st);
-cudaError_t launch_decode(const int16_t* code, int bits, int K, int N, uint16_t* w,
+cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, bool e4m3,
+                                int M, int K, int N, const float* sv, uint16_t* y, float* ws,
+                                int num_sms, int* err, cudaStream_t st);
+cudaError_t launch_decode(const int16_t* code, int bits, bool e4m3, int K, int N, uint16_t* w,
                           cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);
 

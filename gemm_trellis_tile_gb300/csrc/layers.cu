@@ -51,6 +51,7 @@ GemvJob make_job(const escha_linear_s* h, const uint32_t* xfrag, float* part) {
   j.KT = h->K / 16;
   j.NG = h->N / 128;
   j.N = h->N;
+  j.e4m3 = h->rounding == ESCHA_ROUND_E4M3 ? 1 : 0;
   return j;
 }
 
@@ -157,6 +158,13 @@ escha_status_t linear_gemv(escha_linear_s* h, const uint16_t* x, uint16_t* y, in
   return ESCHA_OK;
 }
 
+escha_status_t linear_set_rounding(escha_linear_s* h, int rounding) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return ESCHA_ERR_CUDA;  // no call in flight
+  h->rounding = rounding;
+  h->sched.jobs[0].e4m3 = rounding == ESCHA_ROUND_E4M3 ? 1 : 0;
+  return upload_jobs(h->sched);
+}
+
 escha_status_t linear_reserve(escha_linear_s* h, int rows) {
   if (rows <= h->xh_rows) return ESCHA_OK;
   if (h->xh) {
@@ -180,7 +188,8 @@ escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, in
   cudaError_t e = launch_rotate_in_plain(x, h->su, h->xh, M, h->K, st);
   if (e != cudaSuccess) return from_cuda(e);
   h->prof.begin(st);
-  e = launch_trellis_gemm(h->xh, h->code, h->bits, M, h->K, h->N, h->sv, y, h->gemm_ws,
+  e = launch_trellis_gemm(h->xh, h->code, h->bits, h->rounding == ESCHA_ROUND_E4M3, M, h->K,
+                          h->N, h->sv, y, h->gemm_ws,
                           h->num_sms, h->err, st);
   h->prof.end(st);
   return from_cuda(e);

@@ -58,6 +58,7 @@ struct MoePlanArgs {
   const uint8_t* const* down_code;
   const CUtensorMap* code_maps;  // [3][E]: gate, up, down
   const int* bits;
+  int e4m3;                      // codebook values rounded to E4M3
   const uint32_t* xfrag_hidden;
   uint32_t* xfrag_down;   // [kMoeMaxDistinct][inter/16][M][4][4]
   float* part1;           // [2*kMoeMaxDistinct][slots][8][inter]
@@ -72,8 +73,9 @@ struct MoePlanArgs {
 
 __device__ __forceinline__ GemvJob make_job(const uint8_t* code, const CUtensorMap* tmap,
                                             const uint32_t* xfrag, float* part, long long ub,
-                                            int bits, int KT, int NG, int N) {
+                                            int bits, int KT, int NG, int N, int e4m3) {
   GemvJob j;
+  j.e4m3 = e4m3;
   j.code = code;
   j.tmap = tmap;
   j.xfrag = reinterpret_cast<const uint4*>(xfrag);
@@ -134,13 +136,13 @@ __global__ void moe_plan_kernel(const MoePlanArgs a) {
     const int b = a.bits[e];
     a.jobs1[2 * d] = make_job(a.gate_code[e], a.code_maps + e, a.xfrag_hidden,
                               a.part1 + (2 * d) * a.part1_stride, (2 * d) * ug, b, KTg, NGg,
-                              a.inter);
+                              a.inter, a.e4m3);
     a.jobs1[2 * d + 1] = make_job(a.up_code[e], a.code_maps + a.E + e, a.xfrag_hidden,
                                   a.part1 + (2 * d + 1) * a.part1_stride, (2 * d + 1) * ug, b, KTg,
-                                  NGg, a.inter);
+                                  NGg, a.inter, a.e4m3);
     a.jobs2[d] = make_job(a.down_code[e], a.code_maps + 2 * a.E + e,
                           a.xfrag_down + d * a.xdown_stride, a.part2 + d * a.part2_stride, d * ud,
-                          b, KTd, NGd, a.hidden);
+                          b, KTd, NGd, a.hidden, a.e4m3);
   }
   if (threadIdx.x == 0) {
     r->n_distinct = nd;
@@ -380,6 +382,7 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       pa.up_code = h->up_code;
       pa.down_code = h->down_code;
       pa.code_maps = h->code_maps;
+      pa.e4m3 = h->rounding == ESCHA_ROUND_E4M3 ? 1 : 0;
       pa.bits = h->bits;
       pa.xfrag_hidden = h->xfrag_hidden;
       pa.xfrag_down = h->xfrag_down;

@@ -108,6 +108,7 @@ extern "C" escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const u
   job.code = reinterpret_cast<const uint8_t*>(code);
   job.tmap = nullptr;
   job.xfrag = nullptr;
+  job.e4m3 = 0;
   job.part = nullptr;
   job.unit_begin = 0;
   job.bits = bits;

@@ -14,6 +14,8 @@
 // Each state goes through the cb=1 MCG codebook (section "Codebook: cb=1"):
 //   v = state * 0xCBAC1FED; v = (v & 0x8FFF8FFF) ^ 0x3B603B60;
 //   w = fp16(v.lo) + fp16(v.hi)   -- one fp16 addition, round to nearest even.
+// In the EXLR8 variant (EXLR8 format page) w is then rounded to FP8 E4M3,
+// nearest even, saturating at 448.
 //
 // Placement: lane L = 4g + t, symbol j of the lane sits at tile row (input
 // channel) r = 2t + (j&1) + 8((j>>1)&1) and column (output channel)
@@ -59,6 +61,17 @@ __device__ __forceinline__ uint32_t mcg_decode_dup(uint32_t state) {
   return *reinterpret_cast<const uint32_t*>(&s);
 }
 
+// E4M3 rounding of a pair of fp16 values (nearest even, saturating to the
+// largest finite E4M3 value), returned as the two fp16 values it rounds to
+// (every E4M3 value is exact in fp16).  One hardware conversion each way.
+__device__ __forceinline__ uint32_t round_e4m3x2(uint32_t w2) {
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e) : "r"(w2));
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(e));
+  return d;
+}
+
 // The codebook word of one state before its final addition: fp16 lo in the
 // low half, fp16 hi in the high half.  A tensor-core contraction against an
 // operand that carries the same activation in both halves forms lo*x + hi*x
@@ -100,15 +113,37 @@ __device__ __forceinline__ void lane_states(uint32_t lo, uint32_t hi, uint32_t (
 }
 
 // Decode the lane's eight symbols from its word pair.  out[j] holds symbol
-// 8L+j's fp16 value in both halves.
-template <int BITS>
+// 8L+j's value in both fp16 halves (E4M3: the codebook value rounded to E4M3).
+template <int BITS, bool E4M3 = false>
 __device__ __forceinline__ void decode8(uint32_t w0, uint32_t w1, int sh7, uint32_t (&out)[8]) {
   const uint32_t lo = __funnelshift_r(w1, w0, sh7);
   const uint32_t hi = w0 >> sh7;
   uint32_t st[8];
   lane_states<BITS>(lo, hi, st);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) out[j] = mcg_decode_dup(st[j]);
+  for (int j = 0; j < 8; ++j) {
+    out[j] = mcg_decode_dup(st[j]);
+    if (E4M3) out[j] = round_e4m3x2(out[j]);
+  }
+}
+
+// E4M3 variant for the GEMV: the rounded value in both halves, with the mask
+// and flip constants as run-time values (see mcg_pair).  Against activations
+// repeated in both halves an MMA forms 2*w*x, exactly twice the product.
+template <int BITS>
+__device__ __forceinline__ void decode8_e4m3_dup(uint32_t w0, uint32_t w1, int sh7, uint32_t mask,
+                                                 uint32_t xr, uint32_t (&out)[8]) {
+  const uint32_t lo = __funnelshift_r(w1, w0, sh7);
+  const uint32_t hi = w0 >> sh7;
+  uint32_t st[8];
+  lane_states<BITS>(lo, hi, st);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t v = mcg_pair(st[j], mask, xr);
+    const __half2 h = *reinterpret_cast<const __half2*>(&v);
+    const __half2 s = __hadd2(__low2half2(h), __high2half2(h));
+    out[j] = round_e4m3x2(*reinterpret_cast<const uint32_t*>(&s));
+  }
 }
 
 // The lane's eight codebook words as (lo, hi) fp16 pairs (see mcg_pair).

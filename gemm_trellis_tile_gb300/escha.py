@@ -33,6 +33,8 @@ _lib = None
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
+ROUNDING = {"fp16": 0, "e4m3": 1}   # ESCHA_ROUND_FP16, ESCHA_ROUND_E4M3
+
 _SIGS = {
     "escha_status_string": (ctypes.c_char_p, [_I]),
     "escha_version": (_I, []),
@@ -54,6 +56,8 @@ _SIGS = {
     "escha_moe_destroy": (_I, [_P]),
     "escha_linear_moe_gemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
     "escha_linear_moe_gemv_stage": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _P]),
+    "escha_linear_set_rounding": (_I, [_P, _I]),
+    "escha_moe_set_rounding": (_I, [_P, _I]),
     "escha_linear_check": (_I, [_P, _P]),
     "escha_moe_check": (_I, [_P, _P]),
     "escha_profile_enable": (_I, [_P, _I, _I]),
@@ -206,6 +210,11 @@ class Linear:
 
     def reserve(self, max_m):
         check(load().escha_linear_reserve(self.handle, int(max_m)), "escha_linear_reserve")
+
+    def set_rounding(self, rounding):
+        """"fp16" (default) or "e4m3" (codebook values rounded to FP8 E4M3)."""
+        check(load().escha_linear_set_rounding(self.handle, ROUNDING[rounding]),
+              "escha_linear_set_rounding")
 
     def decode(self, stream=None):
         torch = _torch()
@@ -360,6 +369,11 @@ class MoE:
 
     def check(self, stream=None):
         return load().escha_moe_check(self.handle, _stream(stream))
+
+    def set_rounding(self, rounding):
+        """"fp16" (default) or "e4m3" (codebook values rounded to FP8 E4M3)."""
+        check(load().escha_moe_set_rounding(self.handle, ROUNDING[rounding]),
+              "escha_moe_set_rounding")
 
     def profile(self, on=True):
         check(load().escha_profile_enable(self.handle, KIND_MOE, int(on)), "escha_profile_enable")

@@ -213,6 +213,21 @@ escha_status_t escha_linear_moe_gemv_stage(escha_moe_t m, int stage, const uint1
                                            uint16_t* y, int M, int topk, void* stream);
 
 /*
+ * Codebook rounding of a handle's weights.  ESCHA_ROUND_FP16 (default): each
+ * weight is the codebook's fp16 value.  ESCHA_ROUND_E4M3: the EXLR8 variant
+ * (EXLR8 format page: "Every value the codebook produces is rounded to E4M3
+ * (round-to-nearest-even, saturating)"): the fp16 value is rounded to the
+ * nearest FP8 E4M3 value, ties to even, magnitudes past 448 clamped to 448.
+ * Applies to every later decode, GEMV and GEMM of the handle (MoE: every
+ * routed expert).  Synchronises the device.  A gated MLP takes each matrix's
+ * rounding when it is created.  Other values: ESCHA_ERR_INVALID_ARG.
+ */
+#define ESCHA_ROUND_FP16 0
+#define ESCHA_ROUND_E4M3 1
+escha_status_t escha_linear_set_rounding(escha_linear_t h, int rounding);
+escha_status_t escha_moe_set_rounding(escha_moe_t m, int rounding);
+
+/*
  * Synchronise `stream` and report the handle's device error flag:
  * ESCHA_ERR_TIMEOUT if a bounded wait in one of its kernels ran out,
  * ESCHA_ERR_INVALID_ARG if routing ids were out of range, ESCHA_ERR_CUDA on an

@@ -33,15 +33,15 @@ def oracle_scales(layer):
     return O.fold_scales(layer["rin"], layer["s_in"]), O.fold_scales(layer["rout"], layer["s_out"])
 
 
-def oracle_linear(layer, x, w=None):
+def oracle_linear(layer, x, w=None, rounding="fp16"):
     if w is None:
-        w = O.decode_matrix(layer["code"], layer["bits"])
+        w = O.decode_matrix(layer["code"], layer["bits"], rounding=rounding)
     su, sv = oracle_scales(layer)
     return O.linear_forward(x, w, su, sv)
 
 
-def oracle_layer_dict(layer, w=None):
+def oracle_layer_dict(layer, w=None, rounding="fp16"):
     if w is None:
-        w = O.decode_matrix(layer["code"], layer["bits"])
+        w = O.decode_matrix(layer["code"], layer["bits"], rounding=rounding)
     su, sv = oracle_scales(layer)
     return dict(w=w, su=su, sv=sv)

@@ -38,6 +38,8 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
     assert lib.escha_linear_decode(None, None, None) == 1
     assert lib.escha_linear_destroy(None) == 1
     assert lib.escha_mlp_gemv(None, None, None, 1, None) == 1
+    assert lib.escha_linear_set_rounding(None, 1) == 1
+    assert lib.escha_moe_set_rounding(None, 0) == 1
     for s in (0, 1, 2, -1, 7):
         assert lib.escha_linear_gemv_stage(None, s, None, None, 1, None) == 1
         assert lib.escha_mlp_gemv_stage(None, s, None, None, 1, None) == 1
