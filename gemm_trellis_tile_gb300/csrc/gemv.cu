@@ -56,8 +56,12 @@ __host__ __device__ constexpr int gemv_smem_bytes() {
   return kStages * (kCodeStageBytes + xf_stage_bytes<TB>()) + 2 * kStages * 8;
 }
 
+constexpr int kInlineJobs = 2;
+
 struct GemvArgs {
-  const GemvJob* jobs;
+  const GemvJob* jobs;             // job table in device memory, unless n_inline > 0
+  GemvJob inline_jobs[kInlineJobs];  // host-scheduled launches carry their jobs here,
+  int n_inline;                      // read from parameter space (no memory round trip)
   long long units;
   int grid;                    // unit ranges (kGroups per CTA)
   const long long* dev_units;  // when set, units and grid are read from device memory
@@ -226,7 +230,9 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint
 }
 
 template <int TB>
-__global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    trellis_gemv_kernel(const __grid_constant__ GemvArgs a) {
+  const GemvJob* const jobs = a.n_inline > 0 ? a.inline_jobs : a.jobs;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* codes = smem;
   uint8_t* xfs = smem + kStages * kCodeStageBytes;
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
     const int r = static_cast<int>(blockIdx.x) + q * C;
     const bool mine = q < kGroups && r < G;
     ChunkIter it;
-    if (mine) it.init(a.jobs, cta_start(r, U, G), cta_start(r + 1, U, G));
+    if (mine) it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G));
     const uint64_t pol = policy_evict_first();
     int slot = 0;  // next stage index within the group's stages
     uint32_t phase = 0;
@@ -274,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
     const CUtensorMap* fenced = nullptr;
     for (;;) {
       Chunk ch;
-      const bool has = mine && ok && it.next(a.jobs, ch);
+      const bool has = mine && ok && it.next(jobs, ch);
       if (!__any_sync(0xFFFFFFFFu, has)) break;
       if (!has) continue;
       const int stage = q + kGroups * slot;
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
   const int r = static_cast<int>(blockIdx.x) + q * C;
   if (r >= G) return;
   ChunkIter it;
-  it.init(a.jobs, cta_start(r, U, G), cta_start(r + 1, U, G));
+  it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G));
   Chunk ch;
   float acc[TB][4];
 #pragma unroll
@@ -341,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) trellis_gemv_kernel(const GemvArg
     for (int i = 0; i < 4; ++i) acc[tb][i] = 0.f;
   int slot = 0;  // next stage index within the group's stages
   uint32_t phase = 0;
-  while (it.next(a.jobs, ch)) {
+  while (it.next(jobs, ch)) {
     const int stage = q + kGroups * slot;
     if (!mbar_wait(smem_u32(&bars[stage]), phase, a.limit_ns)) {
       set_error(a.err, kDevErrTimeout);
@@ -434,6 +440,11 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   }
   GemvArgs a;
   a.jobs = s.d_jobs;
+  a.n_inline = 0;
+  if (s.jobs.size() <= (size_t)kInlineJobs) {
+    for (size_t j = 0; j < s.jobs.size(); ++j) a.inline_jobs[j] = s.jobs[j];
+    a.n_inline = static_cast<int>(s.jobs.size());
+  }
   a.units = s.units;
   a.grid = s.grid;
   a.dev_units = nullptr;
@@ -522,6 +533,7 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
   if (e != cudaSuccess) return e;
   GemvArgs a;
   a.jobs = d_jobs;
+  a.n_inline = 0;
   a.units = 0;
   a.grid = max_grid;
   a.dev_units = d_units;
