@@ -48,19 +48,32 @@ __device__ __forceinline__ float4 load4_f32(const float* p) {
 
 // Sum a group's partial-sum slots for token m, channels 128g + 4*lane .. +3.
 // The group's KT units start at unit `ub`; slot s belongs to the s-th CTA
-// that covers them.
+// that covers them.  All slot loads (up to 16 at a time) are issued before the
+// first addition so their L2 latencies overlap; the slots are added in order.
+// kBatch: loads in flight (more registers; a caller with few slots picks less).
+template <int kBatch = 16>
 __device__ __forceinline__ void sum_slots(const float* part, long long ub, int KT, int N,
                                           long long U, int G, int mpad, int m, int g, int lane,
                                           float (&v)[4]) {
   const long long gb = ub + (long long)g * KT;
   const int ns = owner_cta(gb + KT - 1, U, G) - owner_cta(gb, U, G) + 1;
+  const float* p = part + (size_t)m * N + 128 * g + 4 * lane;
+  const size_t step = (size_t)mpad * N;
   v[0] = v[1] = v[2] = v[3] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float4 p = load4_f32(part + ((size_t)s * mpad + m) * N + 128 * g + 4 * lane);
-    v[0] += p.x;
-    v[1] += p.y;
-    v[2] += p.z;
-    v[3] += p.w;
+  for (int s0 = 0; s0 < ns; s0 += kBatch) {
+    float4 q[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (s0 + i < ns) q[i] = load4_f32(p + (size_t)(s0 + i) * step);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (s0 + i < ns) {
+        v[0] += q[i].x;
+        v[1] += q[i].y;
+        v[2] += q[i].z;
+        v[3] += q[i].w;
+      }
+    }
   }
 }
 

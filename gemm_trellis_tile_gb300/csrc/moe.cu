@@ -38,6 +38,9 @@ namespace {
 constexpr int kWarpsPerBlock = 8;
 
 // Device-side routing state written by moe_plan_kernel.
+// Partial-sum slots per group: device_grid() keeps a group within 5 CTAs.
+constexpr int kMoeSlots = 6;
+
 struct MoeRoute {
   long long units1;  // gate+up GEMV
   long long units2;  // down GEMV
@@ -185,10 +188,10 @@ __global__ void moe_mid_kernel(const MoeMidArgs a) {
     const GemvJob& jg = a.jobs1[2 * d];
     const GemvJob& ju = a.jobs1[2 * d + 1];
     float gv[4], uv[4];
-    sum_slots(jg.part, jg.unit_begin, jg.KT, jg.N, r->units1, r->grid1, kMoeMaxTokens, m, g, lane,
-              gv);
-    sum_slots(ju.part, ju.unit_begin, ju.KT, ju.N, r->units1, r->grid1, kMoeMaxTokens, m, g, lane,
-              uv);
+    sum_slots<kMoeSlots>(jg.part, jg.unit_begin, jg.KT, jg.N, r->units1, r->grid1, kMoeMaxTokens,
+                         m, g, lane, gv);
+    sum_slots<kMoeSlots>(ju.part, ju.unit_begin, ju.KT, ju.N, r->units1, r->grid1, kMoeMaxTokens,
+                         m, g, lane, uv);
     fwht128_warp(gv, lane);
     fwht128_warp(uv, lane);
     const size_t off = (size_t)e * a.inter + n0;
@@ -236,7 +239,8 @@ __global__ void moe_out_kernel(const MoeOutArgs a) {
     const float w = a.expert_w[m * a.topk + k];
     const GemvJob& j = a.jobs2[d];
     float p[4];
-    sum_slots(j.part, j.unit_begin, j.KT, j.N, r->units2, r->grid2, kMoeMaxTokens, m, g, lane, p);
+    sum_slots<kMoeSlots>(j.part, j.unit_begin, j.KT, j.N, r->units2, r->grid2, kMoeMaxTokens, m, g,
+                         lane, p);
 #pragma unroll
     for (int q = 0; q < 4; ++q) v[q] += w * p[q];
   }
@@ -254,8 +258,6 @@ unsigned blocks_for(long long warps) {
   return static_cast<unsigned>((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
 }
 
-// Partial-sum slots per group: device_grid() keeps a group within 5 CTAs.
-constexpr int kMoeSlots = 6;
 
 template <typename T>
 escha_status_t upload(T** dst, const T* host, size_t n) {
