@@ -77,6 +77,47 @@ __device__ __forceinline__ void sum_slots(const float* part, long long ub, int K
   }
 }
 
+// Two groups' sums at once (the gate and up matrices of a gated MLP): both
+// sets of slot loads are in flight together.
+template <int kBatch = 8>
+__device__ __forceinline__ void sum_slots_pair(const float* part_a, long long ub_a, const float* part_b,
+                                               long long ub_b, int KT, int N, long long U, int G,
+                                               int mpad, int m, int g, int lane, float (&va)[4],
+                                               float (&vb)[4]) {
+  const long long ga = ub_a + (long long)g * KT, gbb = ub_b + (long long)g * KT;
+  const int na = owner_cta(ga + KT - 1, U, G) - owner_cta(ga, U, G) + 1;
+  const int nb = owner_cta(gbb + KT - 1, U, G) - owner_cta(gbb, U, G) + 1;
+  const float* pa = part_a + (size_t)m * N + 128 * g + 4 * lane;
+  const float* pb = part_b + (size_t)m * N + 128 * g + 4 * lane;
+  const size_t step = (size_t)mpad * N;
+  va[0] = va[1] = va[2] = va[3] = 0.f;
+  vb[0] = vb[1] = vb[2] = vb[3] = 0.f;
+  const int n = na > nb ? na : nb;
+  for (int s0 = 0; s0 < n; s0 += kBatch) {
+    float4 qa[kBatch], qb[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (s0 + i < na) qa[i] = load4_f32(pa + (size_t)(s0 + i) * step);
+      if (s0 + i < nb) qb[i] = load4_f32(pb + (size_t)(s0 + i) * step);
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (s0 + i < na) {
+        va[0] += qa[i].x;
+        va[1] += qa[i].y;
+        va[2] += qa[i].z;
+        va[3] += qa[i].w;
+      }
+      if (s0 + i < nb) {
+        vb[0] += qb[i].x;
+        vb[1] += qb[i].y;
+        vb[2] += qb[i].z;
+        vb[3] += qb[i].w;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 }  // namespace escha

@@ -92,18 +92,20 @@ __global__ void rotate_in_plain_kernel(const uint16_t* x, const float* su, uint1
 // y = fp16(had128(sum of partial slots) * sv).
 __global__ void rotate_out_kernel(const PartRef pr, long long U, int G, const float* sv,
                                   uint16_t* y, int M, int mpad) {
-  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int NG = pr.N / kHad;
-  if (wid >= (long long)M * NG) return;
   const int m = static_cast<int>(wid / NG);
   const int g = static_cast<int>(wid - (long long)m * NG);
+  const int n0 = g * kHad + 4 * lane;
+  const bool active = wid < (long long)M * NG;
+  // The scales were written at creation: load them while the GEMV finishes.
+  const float4 s = active ? *reinterpret_cast<const float4*>(sv + n0) : make_float4(0.f, 0.f, 0.f, 0.f);
+  pdl_wait();
+  if (!active) return;
   float v[4];
   sum_part_slots(pr, U, G, mpad, m, g, lane, v);
   fwht128_warp(v, lane);
-  const int n0 = g * kHad + 4 * lane;
-  const float4 s = *reinterpret_cast<const float4*>(sv + n0);
   v[0] *= kHadScale * s.x;
   v[1] *= kHadScale * s.y;
   v[2] *= kHadScale * s.z;
@@ -116,25 +118,30 @@ __global__ void rotate_out_kernel(const PartRef pr, long long U, int G, const fl
 __global__ void mlp_mid_kernel(const PartRef gate, const PartRef up, long long U, int G,
                                const float* sv_gate, const float* sv_up, const float* su_down,
                                uint32_t* xfrag_down, int M) {
-  pdl_wait();
-  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int NG = gate.N / kHad;
-  if (wid >= (long long)M * NG) return;
   const int m = static_cast<int>(wid / NG);
   const int g = static_cast<int>(wid - (long long)m * NG);
   const int n0 = g * kHad + 4 * lane;
+  const bool active = wid < (long long)M * NG;
+  // The scales were written at creation: load them while the GEMV finishes.
+  float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), su = sg, sd = sg;
+  if (active) {
+    sg = *reinterpret_cast<const float4*>(sv_gate + n0);
+    su = *reinterpret_cast<const float4*>(sv_up + n0);
+    sd = *reinterpret_cast<const float4*>(su_down + n0);
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (!active) return;
   float h[4];
   {
     float gv[4], uv[4];
-    sum_part_slots(gate, U, G, kGemvMaxTokens, m, g, lane, gv);
-    sum_part_slots(up, U, G, kGemvMaxTokens, m, g, lane, uv);
+    sum_slots_pair(gate.part, gate.unit_begin, up.part, up.unit_begin, gate.KT, gate.N, U, G,
+                   kGemvMaxTokens, m, g, lane, gv, uv);
     fwht128_warp(gv, lane);
     fwht128_warp(uv, lane);
-    const float4 sg = *reinterpret_cast<const float4*>(sv_gate + n0);
-    const float4 su = *reinterpret_cast<const float4*>(sv_up + n0);
-    const float4 sd = *reinterpret_cast<const float4*>(su_down + n0);
     const float sgv[4] = {sg.x, sg.y, sg.z, sg.w};
     const float suv[4] = {su.x, su.y, su.z, su.w};
     const float sdv[4] = {sd.x, sd.y, sd.z, sd.w};
