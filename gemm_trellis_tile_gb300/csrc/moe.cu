@@ -185,19 +185,17 @@ __global__ void moe_mid_kernel(const MoeMidArgs a) {
   const int n0 = g * kHad + 4 * lane;
   float h[4] = {0.f, 0.f, 0.f, 0.f};
   if (routed) {
-    const GemvJob& jg = a.jobs1[2 * d];
-    const GemvJob& ju = a.jobs1[2 * d + 1];
-    float gv[4], uv[4];
-    sum_slots<kMoeSlots>(jg.part, jg.unit_begin, jg.KT, jg.N, r->units1, r->grid1, kMoeMaxTokens,
-                         m, g, lane, gv);
-    sum_slots<kMoeSlots>(ju.part, ju.unit_begin, ju.KT, ju.N, r->units1, r->grid1, kMoeMaxTokens,
-                         m, g, lane, uv);
-    fwht128_warp(gv, lane);
-    fwht128_warp(uv, lane);
     const size_t off = (size_t)e * a.inter + n0;
     const float4 sg = load4_f32(a.sv_gate + off);
     const float4 su = load4_f32(a.sv_up + off);
     const float4 sd = load4_f32(a.su_down + off);
+    const GemvJob& jg = a.jobs1[2 * d];
+    const GemvJob& ju = a.jobs1[2 * d + 1];
+    float gv[4], uv[4];
+    sum_slots_pair<kMoeSlots>(jg.part, jg.unit_begin, ju.part, ju.unit_begin, jg.KT, jg.N,
+                              r->units1, r->grid1, kMoeMaxTokens, m, g, lane, gv, uv);
+    fwht128_warp(gv, lane);
+    fwht128_warp(uv, lane);
     const float sgv[4] = {sg.x, sg.y, sg.z, sg.w};
     const float suv[4] = {su.x, su.y, su.z, su.w};
     const float sdv[4] = {sd.x, sd.y, sd.z, sd.w};
@@ -232,21 +230,43 @@ __global__ void moe_out_kernel(const MoeOutArgs a) {
   const int m = static_cast<int>(wid / NG);
   const int g = static_cast<int>(wid - (long long)m * NG);
   const MoeRoute* r = a.route;
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int k = 0; k < a.topk; ++k) {
-    const int d = r->route[m * a.topk + k];
-    if (d < 0) continue;
-    const float w = a.expert_w[m * a.topk + k];
-    const GemvJob& j = a.jobs2[d];
-    float p[4];
-    sum_slots<kMoeSlots>(j.part, j.unit_begin, j.KT, j.N, r->units2, r->grid2, kMoeMaxTokens, m, g,
-                         lane, p);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) v[q] += w * p[q];
-  }
-  fwht128_warp(v, lane);
   const int n0 = g * kHad + 4 * lane;
   const float4 s = load4_f32(a.sv_hidden + n0);
+  // Routes, weights and job fields of all routed experts first (independent
+  // loads), then their partial sums two experts at a time; the experts are
+  // still added in routing order.
+  int dk[kMoeMaxTopk];
+  float wk[kMoeMaxTopk];
+#pragma unroll
+  for (int k = 0; k < kMoeMaxTopk; ++k) {
+    dk[k] = k < a.topk ? r->route[m * a.topk + k] : -1;
+    wk[k] = k < a.topk ? a.expert_w[m * a.topk + k] : 0.f;
+  }
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < kMoeMaxTopk; k += 2) {
+    const int d0 = dk[k], d1 = dk[k + 1];
+    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (d0 >= 0 && d1 >= 0) {
+      const GemvJob& j0 = a.jobs2[d0];
+      const GemvJob& j1 = a.jobs2[d1];
+      sum_slots_pair<kMoeSlots>(j0.part, j0.unit_begin, j1.part, j1.unit_begin, j0.KT, j0.N,
+                                r->units2, r->grid2, kMoeMaxTokens, m, g, lane, p0, p1);
+    } else if (d0 >= 0 || d1 >= 0) {
+      const GemvJob& j = a.jobs2[d0 >= 0 ? d0 : d1];
+      sum_slots<kMoeSlots>(j.part, j.unit_begin, j.KT, j.N, r->units2, r->grid2, kMoeMaxTokens, m,
+                           g, lane, d0 >= 0 ? p0 : p1);
+    }
+    if (d0 >= 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] += wk[k] * p0[q];
+    }
+    if (d1 >= 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] += wk[k + 1] * p1[q];
+    }
+  }
+  fwht128_warp(v, lane);
   v[0] *= kHadScale * s.x;
   v[1] *= kHadScale * s.y;
   v[2] *= kHadScale * s.z;
