@@ -243,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long U = a.units;
   int G = a.grid;
   if (a.dev_units != nullptr) {
+    // The schedule is written by the previous kernel (the routing plan).
+    pdl_wait();
     U = *a.dev_units;
     G = *a.dev_grid;
   }
@@ -545,9 +547,8 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
   a.limit_ns = kWaitLimitNs;
   a.cb_mask = kMcgMask;
   a.cb_xor = kMcgXor;
-  trellis_gemv_kernel<1><<<(max_grid + kGroups - 1) / kGroups, kThreads, gemv_smem_bytes<1>(),
-                           st>>>(a);
-  return cudaGetLastError();
+  PdlLaunch pl((max_grid + kGroups - 1) / kGroups, kThreads, gemv_smem_bytes<1>(), st);
+  return cudaLaunchKernelEx(&pl.cfg, trellis_gemv_kernel<1>, a);
 }
 
 cudaError_t launch_decode(const int16_t* code, int bits, bool e4m3, int K, int N, uint16_t* w,

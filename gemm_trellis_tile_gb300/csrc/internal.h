@@ -85,6 +85,24 @@ cudaError_t launch_decode(const int16_t* code, int bits, bool e4m3, int K, int N
                           cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);
 
+// Launch configuration with programmatic stream serialisation: the kernel
+// may start before its predecessor in the stream finishes and must call
+// griddepcontrol.wait (pdl_wait) before it touches the predecessor's output.
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  PdlLaunch(unsigned blocks, unsigned threads, size_t smem, cudaStream_t st) {
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
 // ---------------------------------------------------------------- rotations
 
 struct RotInJob {

@@ -103,6 +103,7 @@ __device__ __forceinline__ int device_grid(long long units, int KT, int grid_max
 __global__ void moe_plan_kernel(const MoePlanArgs a) {
   extern __shared__ int first_slot[];  // [E]: distinct slot of each expert, -1 if none yet
   __shared__ int s_nd;
+  pdl_trigger();  // the GEMV may launch; it waits for this kernel before reading the plan
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) first_slot[e] = -1;
   __syncthreads();
   MoeRoute* r = a.route;
@@ -154,6 +155,9 @@ __global__ void moe_plan_kernel(const MoePlanArgs a) {
     r->grid1 = device_grid(r->units1, KTg, a.grid1_max);
     r->grid2 = device_grid(r->units2, KTd, a.grid2_max);
   }
+  // Finish only after the input rotation (launched before this kernel, which
+  // does not read it) so that completing this kernel implies both.
+  pdl_wait();
 }
 
 struct MoeMidArgs {
@@ -169,6 +173,8 @@ struct MoeMidArgs {
 
 // One warp per (distinct slot d, token slot m in 0..7, 128-channel group g).
 __global__ void moe_mid_kernel(const MoeMidArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int NG = a.inter / kHad;
@@ -223,6 +229,7 @@ struct MoeOutArgs {
 
 // One warp per (token m, 128-channel group g of the hidden side).
 __global__ void moe_out_kernel(const MoeOutArgs a) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int NG = a.hidden / kHad;
@@ -419,8 +426,8 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       pa.grid1_max = h->grid_max;
       pa.grid2_max = h->grid_max;
       pa.err = h->err;
-      moe_plan_kernel<<<1, 128, h->E * sizeof(int), st>>>(pa);
-      e = cudaGetLastError();
+      PdlLaunch pl(1, 128, h->E * sizeof(int), st);
+      e = cudaLaunchKernelEx(&pl.cfg, moe_plan_kernel, pa);
       break;
     }
     case 2:
@@ -441,8 +448,8 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       ma.M = M;
       ma.inter = h->inter;
       const long long mid_warps = (long long)kMoeMaxDistinct * 8 * (h->inter / kHad);
-      moe_mid_kernel<<<blocks_for(mid_warps), 32 * kWarpsPerBlock, 0, st>>>(ma);
-      e = cudaGetLastError();
+      PdlLaunch pl(blocks_for(mid_warps), 32 * kWarpsPerBlock, 0, st);
+      e = cudaLaunchKernelEx(&pl.cfg, moe_mid_kernel, ma);
       break;
     }
     case 4:
@@ -462,8 +469,8 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       oa.topk = topk;
       oa.hidden = h->hidden;
       const long long out_warps = (long long)M * (h->hidden / kHad);
-      moe_out_kernel<<<blocks_for(out_warps), 32 * kWarpsPerBlock, 0, st>>>(oa);
-      e = cudaGetLastError();
+      PdlLaunch pl(blocks_for(out_warps), 32 * kWarpsPerBlock, 0, st);
+      e = cudaLaunchKernelEx(&pl.cfg, moe_out_kernel, oa);
       break;
     }
     default:

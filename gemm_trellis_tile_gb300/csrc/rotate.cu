@@ -162,23 +162,6 @@ unsigned blocks_for(long long warps) {
   return static_cast<unsigned>((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
 }
 
-// Launch configuration allowing this kernel to start before its predecessor
-// finishes (it calls pdl_wait() before touching the predecessor's output).
-struct DependentLaunch {
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  DependentLaunch(unsigned blocks, unsigned threads, cudaStream_t st) {
-    cfg.gridDim = dim3(blocks);
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
-};
-
 }  // namespace
 
 cudaError_t launch_fold_scales(const uint16_t* r, const float* s, float* out, int n,
@@ -210,7 +193,7 @@ cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t*
 cudaError_t launch_rotate_out(const PartRef& pr, long long units, int grid, const float* sv,
                               uint16_t* y, int M, int mpad, cudaStream_t st) {
   const long long warps = (long long)M * (pr.N / kHad);
-  DependentLaunch dl(blocks_for(warps), 32 * kWarpsPerBlock, st);
+  PdlLaunch dl(blocks_for(warps), 32 * kWarpsPerBlock, 0, st);
   return cudaLaunchKernelEx(&dl.cfg, rotate_out_kernel, pr, units, grid, sv, y, M, mpad);
 }
 
@@ -218,7 +201,7 @@ cudaError_t launch_mlp_mid(const PartRef& gate, const PartRef& up, long long uni
                            const float* sv_gate, const float* sv_up, const float* su_down,
                            uint32_t* xfrag_down, int M, cudaStream_t st) {
   const long long warps = (long long)M * (gate.N / kHad);
-  DependentLaunch dl(blocks_for(warps), 32 * kWarpsPerBlock, st);
+  PdlLaunch dl(blocks_for(warps), 32 * kWarpsPerBlock, 0, st);
   return cudaLaunchKernelEx(&dl.cfg, mlp_mid_kernel, gate, up, units, grid, sv_gate, sv_up,
                             su_down, xfrag_down, M);
 }
