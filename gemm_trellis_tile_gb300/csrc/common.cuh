@@ -100,14 +100,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Gives up after
-// limit_ns of wall time (or 2^30 polls), returning false; never spins forever.
+// Same, but the thread may stay suspended inside the instruction for up to
+// `hint_ns` until the phase completes (fewer polling instructions while a
+// stage is in flight).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait_hint(bar, parity, 100000u)) return true;
+    if ((it & 7u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
   return false;
 }
