@@ -34,6 +34,16 @@ design notes):
     placement ("tile[perm] = values", [FMT]) is the inverse of that.
   * Hadamard.  Natural (Sylvester) order, normalised by 1/sqrt(128), applied to
     each consecutive block of 128 channels.
+  * Trellis encoder.  [EXLR8] and [MLX] say the encoder picks, per tile, the
+    bitstream whose decoded tile has the least squared error, by Viterbi
+    search over the 16-bit-state trellis; they do not say how the circular
+    (tail-biting) constraint is met.  Reading taken: two Viterbi passes.  Pass
+    1 runs with every start state allowed; pass 2 fixes the 16-K bits that the
+    last window shares with the first (from pass 1's best end state) and
+    allows only start and end states that agree with them, which makes the
+    path circular.  The search decides integer codes, so it runs in fp32 with
+    each step's error (v - c)^2 and sum rounded separately, ties to the lowest
+    index: the precision and order the CUDA encoder uses.
   * E4M3 variant.  [EXLR8] rounds "every value the codebook produces" to FP8
     E4M3; the value rounded is the codebook's fp16 value (after its one fp16
     addition), to the nearest E4M3 value, ties to even mantissa, magnitudes
@@ -206,6 +216,80 @@ def codebook(states, rounding="fp16"):
     if rounding == "e4m3":
         return codebook_value_e4m3(states)
     raise ValueError(rounding)
+
+
+# ----------------------------------------------------------------------------
+# Trellis encoder: Viterbi search  ([EXLR8] "The Viterbi search picks the path
+# minimizing the tile's squared error"; [MLX] tail-biting windows)
+# ----------------------------------------------------------------------------
+
+def _viterbi_pass(values, bits, cvals, start_ok=None, end_ok=None):
+    """One Viterbi pass over the 256 symbols of a tile.
+
+    State s of symbol i is its 16-bit window; the next state is
+    ((s << bits) | new bits) & 0xFFFF, so the predecessors of s are
+    (s >> bits) | (t << (16 - bits)) for t < 2^bits.  Costs are fp32: each
+    step adds (v_i - c(s))^2, the difference, square and sum each rounded.
+    Returns (states [256] uint32, total cost).
+    """
+    nu = 1 << (16 - bits)                                    # predecessor groups
+    inf = np.float32(np.inf)
+    v = np.asarray(values, dtype=np.float32)
+    d = v[0] - cvals
+    cost = (d * d).astype(np.float32)
+    if start_ok is not None:
+        cost = np.where(start_ok, cost, inf).astype(np.float32)
+    back = np.empty((SYMBOLS_PER_TILE, nu), dtype=np.uint8)
+    succ_group = (np.arange(1 << 16, dtype=np.int64) >> bits)  # u of each state's predecessors
+    for i in range(1, SYMBOLS_PER_TILE):
+        grid = cost.reshape(1 << bits, nu)                   # [t][u]: state = u + t * nu
+        t_best = np.argmin(grid, axis=0)                     # first (lowest t) on ties
+        m = grid[t_best, np.arange(nu)]
+        back[i] = t_best
+        d = v[i] - cvals
+        cost = ((d * d).astype(np.float32) + m[succ_group]).astype(np.float32)
+    if end_ok is not None:
+        cost = np.where(end_ok, cost, inf).astype(np.float32)
+    s = int(np.argmin(cost))                                 # lowest state on ties
+    total = float(cost[s])
+    states = np.empty(SYMBOLS_PER_TILE, dtype=np.uint32)
+    states[-1] = s
+    for i in range(SYMBOLS_PER_TILE - 1, 0, -1):
+        u = s >> bits
+        s = u | (int(back[i][u]) << (16 - bits))
+        states[i - 1] = s
+    return states, total
+
+
+def viterbi_encode_tile(values, bits, rounding="fp16"):
+    """Encode one tile's 256 symbol values (symbol order): tail-biting path.
+
+    Returns (tile code int16 [16*bits], states uint32 [256], squared error).
+    """
+    cvals = codebook(np.arange(1 << 16, dtype=np.uint32), rounding).astype(np.float32)
+    st1, _ = _viterbi_pass(values, bits, cvals)
+    mask = (1 << (16 - bits)) - 1
+    o = int(st1[-1]) & mask                                  # bits shared by last and first window
+    s = np.arange(1 << 16, dtype=np.int64)
+    states, total = _viterbi_pass(values, bits, cvals, start_ok=(s >> bits) == o,
+                                  end_ok=(s & mask) == o)
+    # stream bits K*i .. K*i+K-1 are the low `bits` bits of state i, MSB first
+    shift = np.arange(bits - 1, -1, -1, dtype=np.uint32)
+    stream = ((states[:, None] >> shift[None, :]) & 1).reshape(-1).astype(np.uint8)
+    return pack_stream_bits(stream), states, total
+
+
+def encode_matrix(w, bits, rounding="fp16"):
+    """Code tensor int16 [in/16, out/16, 16*bits] of W_inner [in, out] (tile by tile)."""
+    w = np.asarray(w, dtype=np.float32)
+    k, n = w.shape
+    perm = perm_forward()
+    code = np.empty((k // TILE, n // TILE, words_per_tile(bits)), dtype=np.int16)
+    for i in range(k // TILE):
+        for j in range(n // TILE):
+            tile = w[TILE * i:TILE * (i + 1), TILE * j:TILE * (j + 1)].reshape(-1)
+            code[i, j], _, _ = viterbi_encode_tile(tile[perm], bits, rounding)
+    return code
 
 
 # ----------------------------------------------------------------------------
