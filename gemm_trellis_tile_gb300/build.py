@@ -15,7 +15,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libescha.so")
 
-SOURCES = ["api.cu", "layers.cu", "gemv.cu", "rotate.cu", "moe.cu", "gemm_tc.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "layers.cu", "gemv.cu", "rotate.cu", "moe.cu", "gemm_tc.cu", "noalloc.cu", "encode.cu"]
 HEADERS = ["common.cuh", "trellis_decode.cuh", "internal.h", "api_internal.h", "act_layout.cuh",
            "tensor_map.h"]
 

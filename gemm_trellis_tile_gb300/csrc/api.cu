@@ -324,6 +324,29 @@ escha_status_t escha_profile_collect(void* handle, int kind, double* ms_total, i
   return p->collect(ms_total, launches);
 }
 
+escha_status_t escha_trellis_encode(const float* w, int in_features, int out_features, int bits,
+                                    int rounding, int16_t* code, float* sq_err, void* stream) {
+  if (!w || !code) return ESCHA_ERR_INVALID_ARG;
+  if (in_features <= 0 || out_features <= 0) return ESCHA_ERR_INVALID_ARG;
+  if (in_features % 16 != 0 || out_features % 16 != 0) return ESCHA_ERR_UNSUPPORTED;
+  if (bits < 2 || bits > 4) return ESCHA_ERR_UNSUPPORTED;
+  if (rounding != ESCHA_ROUND_FP16 && rounding != ESCHA_ROUND_E4M3) return ESCHA_ERR_INVALID_ARG;
+  int dev, sms;
+  escha_status_t s = device_info(&dev, &sms);
+  if (s != ESCHA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long tiles = (long long)(in_features / 16) * (out_features / 16);
+  const int ctas = static_cast<int>(tiles < sms ? tiles : sms);
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, encode_scratch_bytes(bits, ctas), st);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_trellis_encode(w, in_features, out_features, bits, rounding == ESCHA_ROUND_E4M3,
+                            code, sq_err, static_cast<uint8_t*>(scratch), ctas, st);
+  const cudaError_t ef = cudaFreeAsync(scratch, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(ef);
+}
+
 escha_status_t escha_selftest_wait_timeout(int limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return ESCHA_ERR_INVALID_ARG;
   int dev, sms;

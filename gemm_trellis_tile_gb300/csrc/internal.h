@@ -85,6 +85,14 @@ cudaError_t launch_decode(const int16_t* code, int bits, bool e4m3, int K, int N
                           cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);
 
+// Viterbi trellis encoder: code [in/16][out/16][16*bits] (int16) of W_inner
+// w [in, out] (fp32, row-major); sq_err [in/16 * out/16] (may be null) gets
+// each tile's squared error.  scratch: encode_scratch_bytes(bits, ctas).
+size_t encode_scratch_bytes(int bits, int ctas);
+cudaError_t launch_trellis_encode(const float* w, int in_features, int out_features, int bits,
+                                  bool e4m3, int16_t* code, float* sq_err, uint8_t* scratch,
+                                  int ctas, cudaStream_t st);
+
 // Launch configuration with programmatic stream serialisation: the kernel
 // may start before its predecessor in the stream finishes and must call
 // griddepcontrol.wait (pdl_wait) before it touches the predecessor's output.

@@ -63,6 +63,7 @@ _SIGS = {
     "escha_profile_enable": (_I, [_P, _I, _I]),
     "escha_profile_collect": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "escha_selftest_wait_timeout": (_I, [_I, _P]),
+    "escha_trellis_encode": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "escha_linear_gemv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P]),
 }
 
@@ -396,3 +397,20 @@ class MoE:
 def selftest_wait_timeout(limit_us=10000, stream=None):
     """Run the bounded-wait self test; returns the status code (5 = timed out as designed)."""
     return load().escha_selftest_wait_timeout(int(limit_us), _stream(stream))
+
+
+def trellis_encode(w, bits, rounding="fp16", sq_err=False, stream=None):
+    """Code int16 [in/16, out/16, 16*bits] of W_inner w (fp32 [in, out], CUDA).
+
+    Viterbi search per 16x16 tile with a tail-biting path (escha_trellis_encode).
+    With sq_err=True also returns each tile's squared error, fp32 [in/16, out/16].
+    """
+    torch = _torch()
+    _dev(w, torch.float32)
+    k, n = w.shape
+    code = torch.empty((k // 16, n // 16, 16 * bits), dtype=torch.int16, device=w.device)
+    err = torch.empty((k // 16, n // 16), dtype=torch.float32, device=w.device) if sq_err else None
+    check(load().escha_trellis_encode(_ptr(w), int(k), int(n), int(bits), ROUNDING[rounding],
+                                      _ptr(code), _ptr(err), _stream(stream)),
+          "escha_trellis_encode")
+    return (code, err) if sq_err else code

@@ -282,6 +282,31 @@ escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const uint16_t* ri
                                          void* stream);
 
 /*
+ * Trellis encoder: the code of W_inner [in, out] (fp32, device), written to
+ * code int16 [in/16, out/16, 16*bits] in the layout escha_linear_create takes.
+ * Each 16x16 tile is encoded on its own by a Viterbi search over the 2^16
+ * trellis states that minimises the tile's squared error between W_inner and
+ * the decoded weights (EXLR8 format page, "Viterbi search"; with rounding ==
+ * ESCHA_ROUND_E4M3 the search uses the E4M3-rounded codebook values).  The
+ * stream is circular, so the path must be tail-biting (the first window
+ * continues the last; Metal page, windows at offset i*K): a first pass searches
+ * with a free start, a second pass fixes the 16-bits bits that the last window
+ * shares with the first (taken from the first pass's best end state) and
+ * returns the best path that agrees with them.  Costs are fp32 with every
+ * difference, square and sum rounded on its own; ties go to the lowest state.
+ *   w       fp32 [in, out] row-major, device.
+ *   code    int16 [in/16, out/16, 16*bits], device, written.
+ *   sq_err  fp32 [in/16 * out/16], device, may be NULL: each tile's squared
+ *           error (the path cost) in tile order.
+ * in_features, out_features: positive multiples of 16; bits in {2,3,4};
+ * rounding ESCHA_ROUND_FP16 or ESCHA_ROUND_E4M3.  The call allocates its
+ * scratch (256 * 2^(16-bits) bytes per SM used) stream-ordered on `stream` and
+ * frees it there; it is asynchronous like every compute call.
+ */
+escha_status_t escha_trellis_encode(const float* w, int in_features, int out_features, int bits,
+                                    int rounding, int16_t* code, float* sq_err, void* stream);
+
+/*
  * Self-test of the bounded device wait: launches one block that waits on an
  * mbarrier no one arrives at, with a limit of `limit_us` microseconds (1..1e6).
  * Returns ESCHA_ERR_TIMEOUT when the kernel gave up and reported it (the expected

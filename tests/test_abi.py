@@ -49,6 +49,13 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
     assert lib.escha_profile_enable(None, 0, 1) == 1
     assert lib.escha_selftest_wait_timeout(0, None) == 1
     assert lib.escha_selftest_wait_timeout(2000000, None) == 1
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.escha_trellis_encode(None, 16, 16, 2, 0, fake, None, None) == 1
+    assert lib.escha_trellis_encode(fake, 16, 16, 2, 0, None, None, None) == 1
+    assert lib.escha_trellis_encode(fake, 0, 16, 2, 0, fake, None, None) == 1
+    assert lib.escha_trellis_encode(fake, 24, 16, 2, 0, fake, None, None) == 2   # not whole tiles
+    assert lib.escha_trellis_encode(fake, 16, 16, 5, 0, fake, None, None) == 2   # bits
+    assert lib.escha_trellis_encode(fake, 16, 16, 2, 3, fake, None, None) == 1   # rounding
 
 
 def test_bad_config_rejected_on_host(lib):
@@ -87,6 +94,7 @@ def test_valid_config_without_gpu_fails_as_cuda_error(lib):
     assert lib.escha_linear_create(ctypes.byref(h), fake, fake, fake, None, None,
                                    ctypes.cast(arr, ctypes.c_void_p), 6, None) == 3
     assert lib.escha_selftest_wait_timeout(1000, None) == 3
+    assert lib.escha_trellis_encode(fake, 16, 16, 2, 0, fake, None, None) == 3
 
 
 def test_byte_accounting_matches_printed_layer_sizes():
