@@ -95,6 +95,39 @@ def make_moe_expert_codes(spec, e):
     return gate, up, down
 
 
+
+def make_moe_half_spec(seed, num_experts, hidden, inter, bits_choices=(2, 3, 4)):
+    """Routed-expert stack stored by halves of 128 intermediate channels: the
+    side vectors of make_moe_spec, a width per half for gate and for up
+    (gate_bits, up_bits [E, inter/128]) and one width per expert for down
+    (down_bits [E]), each drawn uniformly from bits_choices."""
+    spec = make_moe_spec(seed, num_experts, hidden, inter, bits_choices)
+    rng = np.random.default_rng([seed, 2])
+    H = inter // 128
+    choices = np.asarray(bits_choices, dtype=np.int32)
+    spec["gate_bits"] = rng.choice(choices, size=(num_experts, H)).astype(np.int32)
+    spec["up_bits"] = rng.choice(choices, size=(num_experts, H)).astype(np.int32)
+    spec["down_bits"] = spec.pop("bits")
+    spec["halves"] = H
+    return spec
+
+
+def make_moe_expert_half_codes(spec, e):
+    """Code words of expert e by halves: lists of H int16 tensors for gate and
+    up ([hidden/16, 8, 16*b], output channels 128h..128h+127) and for down
+    ([8, hidden/16, 16*b], input channels 128h..128h+127)."""
+    rng = np.random.default_rng([spec["seed"], 3, int(e)])
+    hid, H = spec["hidden"], spec["halves"]
+    bd = int(spec["down_bits"][e])
+
+    def draw(shape):
+        return rng.integers(-32768, 32768, size=shape, dtype=np.int16)
+    gate = [draw((hid // 16, 8, 16 * int(spec["gate_bits"][e, h]))) for h in range(H)]
+    up = [draw((hid // 16, 8, 16 * int(spec["up_bits"][e, h]))) for h in range(H)]
+    down = [draw((8, hid // 16, 16 * bd)) for _ in range(H)]
+    return gate, up, down
+
+
 def make_routing(rng, m, num_experts, topk=8):
     """topk distinct experts per token, uniform; weights = softmax of N(0,1) logits."""
     ids = np.stack([rng.choice(num_experts, size=topk, replace=False) for _ in range(m)]).astype(np.int32)

@@ -48,6 +48,12 @@ design notes):
     E4M3; the value rounded is the codebook's fp16 value (after its one fp16
     addition), to the nearest E4M3 value, ties to even mantissa, magnitudes
     above 448 clamped to 448 (saturating; E4M3 has no infinities).
+  * Halves.  [EXLR8] stores each expert matrix as 16 "halves" of 128
+    intermediate channels (output channels of gate and up, input channels of
+    down) with a width per half for gate/up and per expert for down, but does
+    not print a half's code layout.  Reading taken: a half is a code tensor of
+    its own in the [FMT] "Tensor mapping" layout, i.e. the whole matrix's tile
+    columns 8h..8h+7 (gate, up) or tile rows 8h..8h+7 (down).
 
 The fp16 <-> float conversions use numpy's IEEE half type.
 """
@@ -357,6 +363,32 @@ def decode_columns(code, bits, cols, rounding="fp16"):
         sel = np.nonzero(cols // TILE == jt)[0]
         out[:, sel] = strip[:, cols[sel] % TILE]
     return out
+
+
+
+def decode_column_halves(halves, bits):
+    """W_inner [in, 128*H] of a matrix stored by halves along its output side.
+
+    [EXLR8] manifest paragraph: an expert's gate and up matrices are split into
+    "halves" of 128 intermediate channels each -- their output channels -- and
+    each half is coded at its own width.  halves[h] is the code int16
+    [in/16, 8, 16*bits[h]] of output channels 128h .. 128h+127 (a code tensor in
+    the [FMT] "Tensor mapping" layout of its own); the matrix is the halves'
+    decoded columns side by side.
+    """
+    return np.concatenate([decode_matrix(c, int(b)) for c, b in zip(halves, bits)], axis=1)
+
+
+def decode_row_halves(halves, bits):
+    """W_inner [128*H, out] of a matrix stored by halves along its input side.
+
+    [EXLR8] manifest paragraph: down's halves are 128 of its input (intermediate)
+    channels, and down has one width per expert ("its width must be uniform
+    across the expert").  halves[h] is the code int16 [8, out/16, 16*bits] of
+    input channels 128h .. 128h+127; the matrix is the halves' decoded rows
+    stacked in order.
+    """
+    return np.concatenate([decode_matrix(c, int(bits)) for c in halves], axis=0)
 
 
 # ----------------------------------------------------------------------------

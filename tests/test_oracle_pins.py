@@ -396,6 +396,64 @@ def test_moe_forward_reduces_to_mlp():
     assert np.allclose(y[1], ref1)
 
 
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_halves_reassemble_the_whole_matrix(bits):
+    """EXLR8 halves: gate/up are cut along their output channels, down along its
+    input channels, 128 channels (8 tiles) per half.  Cutting one whole code
+    tensor at every 8th tile column (row) and decoding the halves one by one
+    must give the whole matrix's decode -- a half cut along the wrong axis, or
+    halves put back in the wrong order, fails."""
+    rng = np.random.default_rng(21 + bits)
+    code = rng.integers(-32768, 32768, size=(8, 32, 16 * bits), dtype=np.int16)   # 128 x 512
+    whole = O.decode_matrix(code, bits).view(np.uint16)
+    cols = [code[:, 8 * h:8 * h + 8] for h in range(4)]
+    assert np.array_equal(O.decode_column_halves(cols, [bits] * 4).view(np.uint16), whole)
+    assert not np.array_equal(O.decode_column_halves(cols[::-1], [bits] * 4).view(np.uint16), whole)
+    code_t = rng.integers(-32768, 32768, size=(32, 8, 16 * bits), dtype=np.int16)  # 512 x 128
+    whole_t = O.decode_matrix(code_t, bits).view(np.uint16)
+    rows = [code_t[8 * h:8 * h + 8] for h in range(4)]
+    assert np.array_equal(O.decode_row_halves(rows, bits).view(np.uint16), whole_t)
+
+
+def test_mixed_width_halves_place_each_half_by_its_own_width():
+    """A half's width changes only its own 128 columns: recoding one half at
+    another width leaves every other column of the matrix bit-identical, and a
+    single-symbol brute force lands the changed weight in that half's block."""
+    rng = np.random.default_rng(25)
+    widths = [2, 4, 3]
+    halves = [rng.integers(-32768, 32768, size=(4, 8, 16 * b), dtype=np.int16) for b in widths]
+    w = O.decode_column_halves(halves, widths).view(np.uint16)
+    assert w.shape == (64, 384)
+    alt = list(halves)
+    alt[1] = rng.integers(-32768, 32768, size=(4, 8, 16 * 2), dtype=np.int16)
+    w2 = O.decode_column_halves(alt, [2, 2, 3]).view(np.uint16)
+    assert np.array_equal(w2[:, :128], w[:, :128]) and np.array_equal(w2[:, 256:], w[:, 256:])
+    # flip one code bit of tile (2, 5) of half 2: only that tile's weights move
+    flip = [h.copy() for h in halves]
+    flip[2][2, 5, 0] ^= np.int16(1)
+    diff = np.nonzero(O.decode_column_halves(flip, widths).view(np.uint16) != w)
+    assert diff[0].size > 0
+    assert set(diff[0] // 16) == {2} and set(diff[1] // 16) == {2 * 8 + 5}
+
+
+def test_half_shape_and_byte_accounting_match_the_pages():
+    """A half is 128 inner channels x 6144 (about 786k weights), 16 per matrix,
+    three matrices per expert (37,748,736 weights); two halves make a
+    256-channel fragment whose size at K = 2, 3, 4 is a multiple of 64 KiB
+    (32*K bytes per 256-weight tile)."""
+    half = golden("half")
+    pair = golden("half_pair_alignment")
+    hidden, inter = half["hidden"], 2048
+    assert inter // half["inner_channels"] == half["halves_per_matrix"]
+    weights = half["inner_channels"] * hidden
+    assert abs(weights - half["weights_about"]) / half["weights_about"] < 0.01
+    assert 3 * half["halves_per_matrix"] * weights == golden("expert_weights")
+    for k in (2, 3, 4):
+        pair_bytes = (pair["pair_channels"] * hidden // 256) * 32 * k
+        assert pair_bytes % pair["align_bytes"] == 0
+
+
 def test_silu_closed_form():
     z = np.array([0.0, 1.0, -1.0, 20.0])
     assert np.allclose(O.silu(z), [0.0, 1 / (1 + np.exp(-1)), -1 / (1 + np.e), 20.0], atol=1e-7)
