@@ -49,10 +49,14 @@ def parse_args():
     p.add_argument("--steps", type=int, default=4000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="escha", choices=["escha", "reference"])
-    p.add_argument("--workload", default="mlp", choices=["mlp", "linear512", "sweep", "prefill", "moe"])
+    p.add_argument("--workload", default="mlp",
+                   choices=["mlp", "linear512", "sweep", "prefill", "moe", "encode"])
     p.add_argument("--m", type=int, default=1, help="tokens per step")
     p.add_argument("--shape", default=None, help="in x out (sweep: default 5120x10240; "
                    "prefill: default 5120x17408)")
+    p.add_argument("--halves", action="store_true",
+                   help="moe: experts stored by halves of 128 intermediate channels, a width "
+                        "per half for gate/up and per expert for down, pointer tables")
     p.add_argument("--rounding", default="fp16", choices=["fp16", "e4m3"],
                    help="codebook rounding: fp16 values, or the EXLR8 E4M3 variant")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -152,10 +156,21 @@ def _workload_spec(args):
     if args.workload == "linear512":
         return dict(kind="linear", layers=[(512, 512, 2)], seed=S.seed_for(0),
                     name="single linear 512x512 2-bit, M=%d" % args.m)
+    if args.workload == "moe" and args.halves:
+        return dict(kind="moe", halves=True, layers=WL.mlp_layers(6144, 2048, (3, 3, 3)),
+                    seed=S.seed_for(3, 2),
+                    name="routed MoE 256 experts 6144->2048->6144 stored by halves, gate/up "
+                         "2/3/4-bit per half, down 2/3/4-bit per expert, top-8, M=%d" % args.m)
     if args.workload == "moe":
         return dict(kind="moe", layers=WL.mlp_layers(6144, 2048, (3, 3, 3)), seed=S.seed_for(3),
                     name="routed MoE 256 experts 6144->2048->6144, 2/3/4-bit per expert, top-8, "
                          "M=%d" % args.m)
+    if args.workload == "encode":
+        k, n = (int(v) for v in (args.shape or "2048x2048").split("x"))
+        bits = 2
+        return dict(kind="encode", layers=[(k, n, bits)], seed=S.seed_for(5, k),
+                    name="trellis encode (Viterbi, tail-biting) of a %dx%d fp32 W_inner "
+                         "~N(0, 1.244^2) at %d bits" % (k, n, bits))
     if args.workload == "prefill":
         k, n = (int(v) for v in (args.shape or "5120x17408").split("x"))
         return dict(kind="prefill", layers=[(k, n, 3)], seed=S.seed_for(4, k),
@@ -216,10 +231,45 @@ def oracle_sample_rate(spec, m, seconds, seed=7):
             "%.1f s" % (blocks, wall))
 
 
+def run_reference_encode(args, spec):
+    """--impl reference for the encoder: the oracle's Viterbi search, a bounded
+    number of tiles of the same matrix per step."""
+    k, n, bits = spec["layers"][0]
+    rng = np.random.default_rng(spec["seed"])
+    w = (rng.standard_normal((k, n)) * S.CODEBOOK_STD).astype(np.float32)
+    steps = args.steps if args.steps != 4000 else 5
+    warm = args.warmup if args.warmup != 50 else 3
+    budget = 120.0 / max(1, steps + warm)
+    for _ in range(warm):
+        encode_oracle_rate(w, bits, min(budget, 2.0))
+    t0 = time.perf_counter()
+    c0 = time.process_time()
+    done = 0.0
+    for _ in range(steps):
+        done += encode_oracle_rate(w, bits, budget)[3]
+    wall = time.perf_counter() - t0
+    cores = round((time.process_time() - c0) / wall, 2)
+    value = done / wall
+    line = {"impl": "reference", "metric": "trellis encode weights/s (Viterbi search, whole tiles)",
+            "value": value, "unit": "weights/s", "n_gpus": args.gpus, "steps": steps,
+            "warmup": warm, "ms_per_step": 1e3 * wall / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": spec["name"]},
+            "cpu_baseline": {"value": value, "unit": "weights/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": "per step: as many whole tiles as %.0f s allow" % budget},
+            "e2e": {"value": value, "unit": "weights/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, spec, rank):
     """--impl reference: the CPU oracle, as it stands, on a bounded sample per step."""
     if rank != 0:
         return 0
+    if spec["kind"] == "encode":
+        return run_reference_encode(args, spec)
     from oracle import escha_oracle as O
     mats = instance_matrices(spec, make_instance(spec, spec["seed"]))
     rng = np.random.default_rng(11)
@@ -287,22 +337,42 @@ def run_moe(args, spec, rank, world, local):
     escha.load()
     dev = torch.device("cuda", torch.cuda.current_device())
     E, hidden, inter, m = 256, 6144, 2048, args.m
-    mspec = S.make_moe_spec(spec["seed"] + 1000003 * rank, E, hidden, inter)
+    halves = spec.get("halves", False)
+    H = inter // 128
+    seed = spec["seed"] + 1000003 * rank
+    mspec = (S.make_moe_half_spec if halves else S.make_moe_spec)(seed, E, hidden, inter)
     gen = torch.Generator(device=dev)
-    gen.manual_seed(spec["seed"] + 1000003 * rank)
-    codes = []
-    for e in range(E):
-        b = int(mspec["bits"][e])
-        shapes = [(hidden // 16, inter // 16, 16 * b)] * 2 + [(inter // 16, hidden // 16, 16 * b)]
-        codes.append(tuple(torch.randint(-32768, 32768, sh, dtype=torch.int16, device=dev,
-                                         generator=gen) for sh in shapes))
+    gen.manual_seed(seed)
+
+    def draw(shape):
+        return torch.randint(-32768, 32768, shape, dtype=torch.int16, device=dev, generator=gen)
     t = {k: torch.from_numpy(mspec[k]).to(dev) for k in (
         "rin_hidden", "s_in_hidden", "rout_gate", "s_out_gate", "rout_up", "s_out_up",
         "rin_down", "s_in_down", "rout_hidden", "s_out_hidden")}
-    moe = escha.MoE(hidden, inter, [c[0] for c in codes], [c[1] for c in codes],
-                    [c[2] for c in codes], mspec["bits"], t["rin_hidden"], t["s_in_hidden"],
-                    t["rout_gate"], t["s_out_gate"], t["rout_up"], t["s_out_up"], t["rin_down"],
-                    t["s_in_down"], t["rout_hidden"], t["s_out_hidden"])
+    sidevec = (t["rin_hidden"], t["s_in_hidden"], t["rout_gate"], t["s_out_gate"], t["rout_up"],
+            t["s_out_up"], t["rin_down"], t["s_in_down"], t["rout_hidden"], t["s_out_hidden"])
+    if halves:
+        # one allocation per half, as a loader that fetches halves one by one would hold them
+        codes = []
+        for e in range(E):
+            bd = int(mspec["down_bits"][e])
+            codes.append((
+                [draw((hidden // 16, 8, 16 * int(mspec["gate_bits"][e, h]))) for h in range(H)],
+                [draw((hidden // 16, 8, 16 * int(mspec["up_bits"][e, h]))) for h in range(H)],
+                [draw((8, hidden // 16, 16 * bd)) for _ in range(H)]))
+        tabs = [torch.tensor([[c[part][h].data_ptr() for h in range(H)] for c in codes],
+                             dtype=torch.int64, device=dev) for part in range(3)]
+        bits_t = [torch.from_numpy(np.ascontiguousarray(mspec[k])).to(dev)
+                  for k in ("gate_bits", "up_bits", "down_bits")]
+        moe = escha.MoEHalves(hidden, inter, *tabs, *bits_t, *sidevec)
+    else:
+        codes = []
+        for e in range(E):
+            b = int(mspec["bits"][e])
+            shapes = [(hidden // 16, inter // 16, 16 * b)] * 2 + [(inter // 16, hidden // 16, 16 * b)]
+            codes.append(tuple(draw(sh) for sh in shapes))
+        moe = escha.MoE(hidden, inter, [c[0] for c in codes], [c[1] for c in codes],
+                        [c[2] for c in codes], mspec["bits"], *sidevec)
     moe.set_rounding(spec["rounding"])
     rng = np.random.default_rng(spec["seed"] + 29)
     R = 64
@@ -313,8 +383,14 @@ def run_moe(args, spec, rank, world, local):
     def route_bytes(ids):
         tot = WL.side_bytes(hidden, 0) + WL.side_bytes(0, hidden) + 2 * m * 2 * hidden
         for e in sorted(set(ids.reshape(-1).tolist())):
-            b = int(mspec["bits"][e])
-            tot += 2 * WL.code_bytes(hidden, inter, b) + WL.code_bytes(inter, hidden, b)
+            if halves:
+                for h in range(H):
+                    tot += WL.code_bytes(hidden, 128, int(mspec["gate_bits"][e, h]))
+                    tot += WL.code_bytes(hidden, 128, int(mspec["up_bits"][e, h]))
+                tot += WL.code_bytes(inter, hidden, int(mspec["down_bits"][e]))
+            else:
+                b = int(mspec["bits"][e])
+                tot += 2 * WL.code_bytes(hidden, inter, b) + WL.code_bytes(inter, hidden, b)
             tot += 3 * 6 * inter
         return tot
     rbytes = [route_bytes(r[0]) for r in routes]
@@ -414,7 +490,8 @@ def run_moe(args, spec, rank, world, local):
         "words, 64 cycled uniform top-8 routings)",
         "config": {"workload": spec["name"], "tokens": m, "bytes_per_step": per_pass / R,
                    "l2": "256 experts, %.1f GB of code words; 64 routings cycled"
-                         % (sum(c.numel() * 2 for cc in codes for c in cc) / 1e9),
+                         % (sum(c.numel() * 2 for cc in codes for part in cc
+                                for c in (part if isinstance(part, list) else [part])) / 1e9),
                    "timing": "CUDA graph of 64 public API calls, CUDA events"},
         "roofline": {"bound": "hbm", "kernel": "trellis_gemv (MoE jobs)",
                      "launch_us": 1e3 * k_ms / k_n, "achieved": achieved,
@@ -539,6 +616,138 @@ def run_prefill(args, spec, rank, world, local):
     return 0
 
 
+# Trellis edges the encoder evaluates per tile: two passes (free start, then
+# the tail-biting constraint) x 256 steps x 2^16 states.  Each edge needs at
+# least three rounded fp32 operations (difference, square, path sum).
+ENCODE_EDGES_PER_TILE = 2 * 256 * 65536
+ENCODE_FP32_OPS_PER_EDGE = 3
+
+
+def encode_oracle_rate(w, bits, seconds):
+    """The CPU oracle's encoder on tiles of w until `seconds`:
+    (weights/s, cores, sample, weights encoded)."""
+    from oracle import escha_oracle as O
+    perm = O.perm_forward()
+    kt, nt = w.shape[0] // 16, w.shape[1] // 16
+    t0 = time.perf_counter()
+    c0 = time.process_time()
+    n = 0
+    while True:
+        i, j = divmod(n % (kt * nt), nt)
+        vals = w[16 * i:16 * i + 16, 16 * j:16 * j + 16].reshape(-1)[perm]
+        O.viterbi_encode_tile(vals, bits)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    wall = time.perf_counter() - t0
+    return (256 * n / wall, round((time.process_time() - c0) / wall, 2),
+            "%d tiles of the same matrix, %.1f s" % (n, wall), 256 * n)
+
+
+def run_encode(args, spec, rank, world, local):
+    """Viterbi trellis encoder: weights encoded per second (whole tiles)."""
+    import torch
+    from gemm_trellis_tile_gb300 import build, escha
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    build.build()
+    escha.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    k, n, bits = spec["layers"][0]
+    rng = np.random.default_rng(spec["seed"] + 1000003 * rank)
+    w_host_np = (rng.standard_normal((k, n)) * S.CODEBOOK_STD).astype(np.float32)
+    w_host = torch.from_numpy(w_host_np).pin_memory()
+    w = w_host.to(dev)
+    code = torch.empty((k // 16, n // 16, 16 * bits), dtype=torch.int16, device=dev)
+    lib = escha.load()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        escha.check(lib.escha_trellis_encode(escha._ptr(w), k, n, bits, 0, escha._ptr(code),
+                                             None, escha._stream(stream)), "escha_trellis_encode")
+
+    steps = args.steps if args.steps != 4000 else 5
+    warm = max(3, args.warmup if args.warmup != 50 else 3)
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1)
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tiles = (k // 16) * (n // 16)
+    weights = k * n
+    # e2e: host matrix in, host code out, through the C ABI
+    code_host = torch.empty(code.shape, dtype=torch.int16).pin_memory()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e_steps = min(steps, 3)
+    e0.record()
+    for _ in range(e_steps):
+        w.copy_(w_host, non_blocking=True)
+        step()
+        code_host.copy_(code, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    peaks, _ = measured_peaks()
+    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    # FP32 pipes: 128 lanes per SM per clock
+    peak_edges = sms * 128 * sm_mhz * 1e6 / ENCODE_FP32_OPS_PER_EDGE
+    achieved_edges = steps * tiles * ENCODE_EDGES_PER_TILE / (ms / 1e3)
+    line = {
+        "metric": "trellis encode weights/s (Viterbi search, whole tiles)",
+        "value": world * steps * weights / (ms / 1e3), "unit": "weights/s", "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded "
+        "N(0, 1.244^2) fp32 matrix)",
+        "config": {"workload": spec["name"], "tiles": tiles,
+                   "l2": "input %.0f MB, read once per tile; the search runs in shared memory"
+                         % (weights * 4 / 1e6),
+                   "timing": "CUDA events around back-to-back public API calls"},
+        "roofline": {"bound": "alu", "kernel": "trellis_encode", "achieved": achieved_edges / 1e12,
+                     "peak": peak_edges / 1e12, "unit": "T trellis edges/s",
+                     "frac": achieved_edges / peak_edges, "traffic": None,
+                     "peak_source": "derived: %d SMs x 128 fp32 lanes x %.0f MHz / %d rounded "
+                                    "fp32 operations per edge" % (sms, sm_mhz,
+                                                                  ENCODE_FP32_OPS_PER_EDGE)},
+        "e2e": {"value": e_steps * weights / (e_ms / 1e3), "unit": "weights/s",
+                "h2d_bytes_per_step": int(w_host.numel() * 4),
+                "d2h_bytes_per_step": int(code_host.numel() * 2)},
+        "gpu_launches": steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample, _ = encode_oracle_rate(w_host_np, bits, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "weights/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def make_handles(spec, inst):
     from gemm_trellis_tile_gb300 import escha
     if spec["kind"] == "mlp":
@@ -565,6 +774,8 @@ def main():
         return run_prefill(args, spec, rank, world, local)
     if spec["kind"] == "moe":
         return run_moe(args, spec, rank, world, local)
+    if spec["kind"] == "encode":
+        return run_encode(args, spec, rank, world, local)
 
     import torch
     from gemm_trellis_tile_gb300 import build, escha

@@ -159,7 +159,7 @@ escha_status_t read_and_clear_error(int* d_err, cudaStream_t st) {
     return ESCHA_ERR_CUDA;
   if (v != 0 && cudaMemset(d_err, 0, sizeof(int)) != cudaSuccess) return ESCHA_ERR_CUDA;
   if (v == kDevErrTimeout) return ESCHA_ERR_TIMEOUT;
-  if (v == kDevErrBadRoute) return ESCHA_ERR_INVALID_ARG;
+  if (v == kDevErrBadRoute || v == kDevErrBadTable) return ESCHA_ERR_INVALID_ARG;
   return v == 0 ? ESCHA_OK : ESCHA_ERR_CUDA;
 }
 
@@ -411,6 +411,45 @@ escha_status_t escha_moe_create(escha_moe_t* out, int num_experts, int hidden, i
                               rin_hidden, s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up,
                               rin_down, s_in_down, rout_hidden, s_out_hidden,
                               static_cast<cudaStream_t>(stream));
+  if (s != ESCHA_OK) {
+    moe_free(h);
+    delete h;
+    return s;
+  }
+  *out = h;
+  return ESCHA_OK;
+}
+
+escha_status_t escha_moe_create_halves(escha_moe_t* out, int num_experts, int hidden, int inter,
+                                       const int16_t* const* gate_half,
+                                       const int16_t* const* up_half,
+                                       const int16_t* const* down_half, const int32_t* gate_bits,
+                                       const int32_t* up_bits, const int32_t* down_bits,
+                                       const uint16_t* rin_hidden, const float* s_in_hidden,
+                                       const uint16_t* rout_gate, const float* s_out_gate,
+                                       const uint16_t* rout_up, const float* s_out_up,
+                                       const uint16_t* rin_down, const float* s_in_down,
+                                       const uint16_t* rout_hidden, const float* s_out_hidden,
+                                       void* stream) {
+  if (!out) return ESCHA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (num_experts < 1 || hidden <= 0 || inter <= 0) return ESCHA_ERR_INVALID_ARG;
+  if (num_experts > kMoeMaxExperts) return ESCHA_ERR_UNSUPPORTED;
+  if (hidden % 128 != 0 || inter % 128 != 0) return ESCHA_ERR_UNSUPPORTED;
+  if (!gate_half || !up_half || !down_half || !gate_bits || !up_bits || !down_bits ||
+      !rin_hidden || !rout_gate || !rout_up || !rin_down || !rout_hidden)
+    return ESCHA_ERR_INVALID_ARG;
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(gate_half) | reinterpret_cast<uintptr_t>(up_half) |
+                       reinterpret_cast<uintptr_t>(down_half);
+  const uintptr_t ba = reinterpret_cast<uintptr_t>(gate_bits) | reinterpret_cast<uintptr_t>(up_bits) |
+                       reinterpret_cast<uintptr_t>(down_bits);
+  if ((pa & 7u) != 0 || (ba & 3u) != 0) return ESCHA_ERR_INVALID_ARG;
+  escha_moe_s* h = new (std::nothrow) escha_moe_s();
+  if (!h) return ESCHA_ERR_OOM;
+  escha_status_t s = moe_init_halves(h, num_experts, hidden, inter, gate_half, up_half, down_half,
+                                     gate_bits, up_bits, down_bits, rin_hidden, s_in_hidden,
+                                     rout_gate, s_out_gate, rout_up, s_out_up, rin_down, s_in_down,
+                                     rout_hidden, s_out_hidden, static_cast<cudaStream_t>(stream));
   if (s != ESCHA_OK) {
     moe_free(h);
     delete h;

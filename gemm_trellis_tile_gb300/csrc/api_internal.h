@@ -86,6 +86,19 @@ struct escha_moe_s {
   float* part2 = nullptr;               // down partial sums per distinct expert
   escha::GemvJob* jobs1 = nullptr;      // written on the device each call
   escha::GemvJob* jobs2 = nullptr;
+  // Stored by halves (escha_moe_create_halves): H = inter / 128 halves per
+  // matrix; the caller's device tables are borrowed and re-read every call.
+  int halves = 0;
+  int H = 0;
+  const uint8_t* const* gate_half = nullptr;  // [E][H] code of each gate half
+  const uint8_t* const* up_half = nullptr;    // [E][H]
+  const uint8_t* const* down_half = nullptr;  // [E][H] (halves along down's input)
+  const int* gate_bits = nullptr;             // [E][H]
+  const int* up_bits = nullptr;               // [E][H]
+  const int* down_bits = nullptr;             // [E]
+  CUtensorMap* half_maps = nullptr;     // [kMoeMaxDistinct][H] down-half maps, written per call
+  CUtensorMap* half_map_tmpl = nullptr; // [3] down-half map templates for 2/3/4 bits
+  uint8_t* stand_in = nullptr;          // zero code replacing table entries that fail checks
   unsigned char* route = nullptr;       // device routing state
   int* err = nullptr;
   size_t xdown_stride = 0, part1_stride = 0, part2_stride = 0;
@@ -103,6 +116,16 @@ escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
                         const uint16_t* rout_up, const float* s_out_up,
                         const uint16_t* rin_down, const float* s_in_down,
                         const uint16_t* rout_hidden, const float* s_out_hidden, cudaStream_t st);
+escha_status_t moe_init_halves(escha_moe_s* h, int E, int hidden, int inter,
+                               const int16_t* const* gate_half, const int16_t* const* up_half,
+                               const int16_t* const* down_half, const int32_t* gate_bits,
+                               const int32_t* up_bits, const int32_t* down_bits,
+                               const uint16_t* rin_hidden, const float* s_in_hidden,
+                               const uint16_t* rout_gate, const float* s_out_gate,
+                               const uint16_t* rout_up, const float* s_out_up,
+                               const uint16_t* rin_down, const float* s_in_down,
+                               const uint16_t* rout_hidden, const float* s_out_hidden,
+                               cudaStream_t st);
 void moe_free(escha_moe_s* h);
 escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, const int32_t* ids,
                               const float* w, uint16_t* y, int M, int topk, cudaStream_t st);

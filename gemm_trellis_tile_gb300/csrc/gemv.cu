@@ -63,6 +63,7 @@ struct GemvArgs {
   GemvJob inline_jobs[kInlineJobs];  // host-scheduled launches carry their jobs here,
   int n_inline;                      // read from parameter space (no memory round trip)
   long long units;
+  long long job_units;         // > 0: every job has this many units (direct job lookup)
   int grid;                    // unit ranges (kGroups per CTA)
   const long long* dev_units;  // when set, units and grid are read from device memory
   const int* dev_grid;         // (a schedule built on the device, e.g. by MoE routing)
@@ -103,6 +104,7 @@ struct ChunkIter {
   long long ub, ue;
   int bits, KT, NG, N;
   int e4m3;
+  const CUtensorMap* row_maps;
 
   __device__ __forceinline__ void load(const GemvJob* jobs) {
     const GemvJob& J = jobs[j];
@@ -116,12 +118,16 @@ struct ChunkIter {
     NG = J.NG;
     N = J.N;
     e4m3 = J.e4m3;
+    row_maps = J.row_maps;
     ue = ub + (long long)KT * NG;
   }
-  __device__ __forceinline__ void init(const GemvJob* jobs, long long begin, long long end) {
+  __device__ __forceinline__ void init(const GemvJob* jobs, long long begin, long long end,
+                                       long long job_units) {
     u = begin;
     u1 = end;
-    j = 0;
+    // Launches with many equal jobs (routed experts by halves: thousands)
+    // find the first job by division; the scan below then does not move.
+    j = (job_units > 0 && u < u1) ? static_cast<int>(u / job_units) : 0;
     load(jobs);
     if (u >= u1) {  // empty range: nothing to walk
       g = kt = 0;
@@ -135,7 +141,8 @@ struct ChunkIter {
     g = static_cast<int>(rel / KT);
     kt = static_cast<int>(rel - (long long)g * KT);
   }
-  __device__ __forceinline__ bool next(const GemvJob* jobs, Chunk& ch) {
+  // rpu: the launch's k-tile rows per unit (1 or 8).
+  __device__ __forceinline__ bool next(const GemvJob* jobs, Chunk& ch, int rpu) {
     if (u >= u1) return false;
     while (u >= ue) {  // entered the next job: it starts at its group 0, k-tile 0
       ++j;
@@ -144,8 +151,11 @@ struct ChunkIter {
       kt = 0;
     }
     const long long left = u1 - u;
+    // A unit of a matrix stored by input halves is 8 k-tile rows (rpu = 8):
+    // two of them fill a stage.
+    const int cap = rpu > 1 ? kUPS / 8 : kUPS;
     int n = KT - kt;
-    if (n > kUPS) n = kUPS;
+    if (n > cap) n = cap;
     if ((long long)n > left) n = static_cast<int>(left);
     ch.g = g;
     ch.kt = kt;
@@ -229,9 +239,20 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint
   }
 }
 
-template <int TB>
+// Launch modes, fixed at compile time so that the dense path's code is not
+// shaped by the other two: kModeWhole, matrices stored whole (2-D tensor-map
+// stage copies); kModeColHalves, every job is one 128-channel column half
+// whose stage rows are contiguous (one 1-D bulk copy); kModeRowHalves, every
+// job is stored by input halves (one unit = 8 k-tile rows, one 2-D copy per
+// unit through the half's tensor map).
+constexpr int kModeWhole = kGemvWhole;
+constexpr int kModeColHalves = kGemvColHalves;
+constexpr int kModeRowHalves = kGemvRowHalves;
+
+template <int TB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     trellis_gemv_kernel(const __grid_constant__ GemvArgs a) {
+  constexpr int RPU = MODE == kModeRowHalves ? 8 : 1;  // k-tile rows per unit
   const GemvJob* const jobs = a.n_inline > 0 ? a.inline_jobs : a.jobs;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* codes = smem;
@@ -271,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = static_cast<int>(blockIdx.x) + q * C;
     const bool mine = q < kGroups && r < G;
     ChunkIter it;
-    if (mine) it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G));
+    if (mine) it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G), a.job_units);
     const uint64_t pol = policy_evict_first();
     int slot = 0;  // next stage index within the group's stages
     uint32_t phase = 0;
@@ -282,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const CUtensorMap* fenced = nullptr;
     for (;;) {
       Chunk ch;
-      const bool has = mine && ok && it.next(jobs, ch);
+      const bool has = mine && ok && it.next(jobs, ch, RPU);
       if (!__any_sync(0xFFFFFFFFu, has)) break;
       if (!has) continue;
       const int stage = q + kGroups * slot;
@@ -295,9 +316,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int T = 32 * it.bits;
       const int rowb = kCW * T;
       const uint32_t cdst = smem_u32(codes + stage * kCodeStageBytes);
-      const uint32_t xbytes = ch.n * a.M * 64;
-      mbar_arrive_expect_tx(full, ch.n * rowb + xbytes);
-      if (ch.n == kUPS) {
+      const int rows = ch.n * RPU;  // k-tile rows of the stage
+      const uint32_t xbytes = rows * a.M * 64;
+      mbar_arrive_expect_tx(full, rows * rowb + xbytes);
+      if (MODE == kModeRowHalves) {
+        // stored by input halves: each unit is one half's 8 rows of group g,
+        // one 2-D copy through that half's tensor map (written on the device)
+        for (int i = 0; i < ch.n; ++i) {
+          const CUtensorMap* hm = it.row_maps + ch.kt + i;
+          tensormap_acquire(hm);
+          tma_load_2d_hint(cdst + i * 8 * rowb, hm, ch.g * rowb / 4, 0, full, pol);
+        }
+      } else if (MODE == kModeColHalves) {
+        // a single 128-channel group (a column half): the stage's rows are
+        // contiguous, one bulk copy
+        bulk_g2s_evict_first(cdst, it.code + (size_t)ch.kt * rowb, rows * rowb, full, pol);
+      } else if (ch.n == kUPS) {
         if (a.maps_from_device && it.tmap != fenced) {
           tensormap_acquire(it.tmap);
           fenced = it.tmap;
@@ -316,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         waited = true;
       }
-      bulk_g2s(smem_u32(xfs + stage * xf_stage_bytes<TB>()), it.xfrag + (size_t)ch.kt * a.M * 4,
-               xbytes, full);
+      bulk_g2s(smem_u32(xfs + stage * xf_stage_bytes<TB>()),
+               it.xfrag + (size_t)ch.kt * RPU * a.M * 4, xbytes, full);
       armed[slot] = static_cast<int>(phase);
       if (++slot == kStages / kGroups) {
         slot = 0;
@@ -340,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = static_cast<int>(blockIdx.x) + q * C;
   if (r >= G) return;
   ChunkIter it;
-  it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G));
+  it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G), a.job_units);
   Chunk ch;
   float acc[TB][4];
 #pragma unroll
@@ -349,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 4; ++i) acc[tb][i] = 0.f;
   int slot = 0;  // next stage index within the group's stages
   uint32_t phase = 0;
-  while (it.next(jobs, ch)) {
+  while (it.next(jobs, ch, RPU)) {
     const int stage = q + kGroups * slot;
     if (!mbar_wait(smem_u32(&bars[stage]), phase, a.limit_ns)) {
       set_error(a.err, kDevErrTimeout);
@@ -357,13 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint8_t* cs = codes + stage * kCodeStageBytes;
     const uint4* xs = reinterpret_cast<const uint4*>(xfs + stage * xf_stage_bytes<TB>());
+    const int rows = ch.n * RPU;  // k-tile rows of the stage
     switch (it.bits + 8 * it.e4m3) {
-      case 2: consume_chunk<2, TB, false>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 3: consume_chunk<3, TB, false>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 4: consume_chunk<4, TB, false>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 10: consume_chunk<2, TB, true>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 11: consume_chunk<3, TB, true>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      default: consume_chunk<4, TB, true>(cs, xs, ch.n, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 2: consume_chunk<2, TB, false>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 3: consume_chunk<3, TB, false>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 4: consume_chunk<4, TB, false>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 10: consume_chunk<2, TB, true>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      case 11: consume_chunk<3, TB, true>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
+      default: consume_chunk<4, TB, true>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + stage]));
@@ -434,7 +469,7 @@ template <int TB>
 cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(trellis_gemv_kernel<TB>,
+    cudaError_t e = cudaFuncSetAttribute(trellis_gemv_kernel<TB, kModeWhole>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          gemv_smem_bytes<TB>());
     if (e != cudaSuccess) return e;
@@ -448,6 +483,7 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
     a.n_inline = static_cast<int>(s.jobs.size());
   }
   a.units = s.units;
+  a.job_units = 0;
   a.grid = s.grid;
   a.dev_units = nullptr;
   a.dev_grid = nullptr;
@@ -468,7 +504,7 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, trellis_gemv_kernel<TB>, a);
+  return cudaLaunchKernelEx(&cfg, trellis_gemv_kernel<TB, kModeWhole>, a);
 }
 
 }  // namespace
@@ -486,12 +522,27 @@ bool encode_gemv_code_map(CUtensorMap* map, const void* code, int bits, int KT, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_gemv_half_map(CUtensorMap* map, const void* code, int bits, int NT) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  const cuuint64_t row_words = (cuuint64_t)NT * 8 * bits;
+  const cuuint64_t dims[2] = {row_words, 8};
+  const cuuint64_t strides[1] = {row_words * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)(kCW * 8 * bits), 8};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(code), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int gemv_ranges_per_sm() {
   int n = 0;
-  if (cudaFuncSetAttribute(trellis_gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(trellis_gemv_kernel<2, kModeWhole>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            gemv_smem_bytes<2>()) != cudaSuccess)
     return kGroups;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, trellis_gemv_kernel<2>, kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, trellis_gemv_kernel<2, kModeWhole>,
+                                                    kThreads,
                                                     gemv_smem_bytes<2>()) != cudaSuccess)
     return kGroups;
   return kGroups * std::max(1, n);
@@ -528,27 +579,31 @@ cudaError_t launch_gemv(const GemvSchedule& s, int M, int* err, cudaStream_t st)
 
 cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* d_units,
                                         const int* d_grid, int max_grid, int M, int mpad,
-                                        int* err, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(trellis_gemv_kernel<1>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        int* err, cudaStream_t st, long long job_units,
+                                        bool maps_from_device, int layout) {
+  auto kern = layout == kGemvColHalves   ? trellis_gemv_kernel<1, kModeColHalves>
+              : layout == kGemvRowHalves ? trellis_gemv_kernel<1, kModeRowHalves>
+                                         : trellis_gemv_kernel<1, kModeWhole>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        gemv_smem_bytes<1>());
   if (e != cudaSuccess) return e;
   GemvArgs a;
   a.jobs = d_jobs;
   a.n_inline = 0;
   a.units = 0;
+  a.job_units = job_units;
   a.grid = max_grid;
   a.dev_units = d_units;
   a.dev_grid = d_grid;
   a.M = M;
   a.mpad = mpad;
   a.err = err;
-  a.maps_from_device = 0;  // copied from the host at creation
+  a.maps_from_device = maps_from_device ? 1 : 0;
   a.limit_ns = kWaitLimitNs;
   a.cb_mask = kMcgMask;
   a.cb_xor = kMcgXor;
   PdlLaunch pl((max_grid + kGroups - 1) / kGroups, kThreads, gemv_smem_bytes<1>(), st);
-  return cudaLaunchKernelEx(&pl.cfg, trellis_gemv_kernel<1>, a);
+  return cudaLaunchKernelEx(&pl.cfg, kern, a);
 }
 
 cudaError_t launch_decode(const int16_t* code, int bits, bool e4m3, int K, int N, uint16_t* w,

@@ -12,6 +12,7 @@ namespace escha {
 // Device error codes written to a handle's error word.
 constexpr int kDevErrTimeout = 1;
 constexpr int kDevErrBadRoute = 2;
+constexpr int kDevErrBadTable = 3;  // a code pointer or width in a caller's device table
 
 // ---------------------------------------------------------------- GEMV schedule
 //
@@ -34,6 +35,13 @@ struct GemvJob {
   int NG;                // out / 128
   int N;                 // out
   int e4m3;              // codebook values rounded to FP8 E4M3 (EXLR8 variant)
+  // Matrices stored by halves along the input side (an expert's down matrix):
+  // half h is loaded through row_maps[h] (tensor maps written on the device,
+  // one 8-row box per copy); such launches count one unit per half (8 k-tile
+  // rows) of one group, and KT counts halves.  Null otherwise.  (A matrix
+  // stored by halves along the output side is one job per half, with `part`
+  // pointing at the half's first output channel.)
+  const CUtensorMap* row_maps = nullptr;
 };
 
 struct GemvSchedule {
@@ -67,13 +75,28 @@ cudaError_t launch_gemv(const GemvSchedule& s, int M, int* err, cudaStream_t st)
 // words, one box = 8 tile columns x 16 k-tile rows.  Host only; false if the
 // driver cannot encode it.
 bool encode_gemv_code_map(CUtensorMap* map, const void* code, int bits, int KT, int NT);
+// Map of one half of a matrix stored by input halves: `code` [8][NT][32*bits
+// bytes] as uint32 rows of NT*8*bits words, one box = 8 tile columns x the
+// half's 8 k-tile rows.  Host only.
+bool encode_gemv_half_map(CUtensorMap* map, const void* code, int bits, int NT);
 
 // Up to 8 tokens, with the job table, unit count and grid size written on the
 // device (max_grid ranges are launched for; CTAs whose ranges start past the
 // device grid exit).
+// job_units > 0: every job of the launch has that many units (the kernel finds
+// a range's first job by division instead of a scan).  maps_from_device: the
+// jobs' tensor maps were written by a kernel.  layout: how every job of the
+// launch is stored -- kGemvWhole (whole matrices, tensor maps in `tmap`),
+// kGemvColHalves (each job one 128-channel column half: NG = 1, contiguous
+// rows, no tensor map), kGemvRowHalves (input halves through row_maps; one
+// unit = 8 k-tile rows).
+constexpr int kGemvWhole = 0;
+constexpr int kGemvColHalves = 1;
+constexpr int kGemvRowHalves = 2;
 cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* d_units,
                                         const int* d_grid, int max_grid, int M, int mpad,
-                                        int* err, cudaStream_t st);
+                                        int* err, cudaStream_t st, long long job_units = 0,
+                                        bool maps_from_device = false, int layout = kGemvWhole);
 // Prefill GEMM on tcgen05: y = fp16(had128(xh @ W_inner) * sv) for any M >= 1;
 // xh is fp16 [M, K], 16-byte aligned; ws holds gemm_workspace_floats(num_sms)
 // fp32 for tiles shared between CTAs.

@@ -100,37 +100,63 @@ __device__ __forceinline__ int device_grid(long long units, int KT, int grid_max
   return static_cast<int>(g);
 }
 
-__global__ void moe_plan_kernel(const MoePlanArgs a) {
-  extern __shared__ int first_slot[];  // [E]: distinct slot of each expert, -1 if none yet
+// The routing part of a plan (all threads of the block call it): distinct
+// experts in order of first appearance, the tokens of each, the slot of each
+// (token, k).  first_slot: shared [E].  Returns the number of distinct experts.
+//
+// The routing is worked out in shared memory while the previous kernel in the
+// stream may still run (it reads only the ids, which no kernel of the call
+// writes); then the block waits for that kernel to finish before it writes
+// any state the previous call's kernels read (the route, job tables and maps).
+// Without the wait, a plan launched right behind a contraction (a caller that
+// runs only some stages) could rewrite its job table under it.
+__device__ int plan_routing(const int32_t* ids, int M, int topk, int E, int* first_slot,
+                            MoeRoute* r, int* err) {
   __shared__ int s_nd;
-  pdl_trigger();  // the GEMV may launch; it waits for this kernel before reading the plan
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) first_slot[e] = -1;
+  __shared__ int s_expert[kMoeMaxDistinct];
+  __shared__ unsigned s_mask[kMoeMaxDistinct];
+  __shared__ int s_route[kMoeMaxTokens * kMoeMaxTopk];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) first_slot[e] = -1;
   __syncthreads();
-  MoeRoute* r = a.route;
   if (threadIdx.x == 0) {
     // Sequential on purpose: slots are numbered in order of first appearance.
     int nd = 0;
-    for (int i = 0; i < a.M * a.topk; ++i) {
-      const int e = a.ids[i];
+    for (int i = 0; i < M * topk; ++i) {
+      const int e = ids[i];
       int d = -1;
-      if (e >= 0 && e < a.E) {
+      if (e >= 0 && e < E) {
         d = first_slot[e];
         if (d < 0) {
           d = nd++;
           first_slot[e] = d;
-          r->expert[d] = e;
-          r->mask[d] = 0u;
+          s_expert[d] = e;
+          s_mask[d] = 0u;
         }
-        r->mask[d] |= 1u << (i / a.topk);
+        s_mask[d] |= 1u << (i / topk);
       } else {
-        set_error(a.err, kDevErrBadRoute);
+        set_error(err, kDevErrBadRoute);
       }
-      r->route[i] = d;
+      s_route[i] = d;
     }
     s_nd = nd;
   }
   __syncthreads();
+  pdl_wait();
   const int nd = s_nd;
+  for (int d = threadIdx.x; d < nd; d += blockDim.x) {
+    r->expert[d] = s_expert[d];
+    r->mask[d] = s_mask[d];
+  }
+  for (int i = threadIdx.x; i < M * topk; i += blockDim.x) r->route[i] = s_route[i];
+  __syncthreads();
+  return nd;
+}
+
+__global__ void moe_plan_kernel(const MoePlanArgs a) {
+  extern __shared__ int first_slot[];  // [E]: distinct slot of each expert, -1 if none yet
+  pdl_trigger();  // the GEMV may launch; it waits for this kernel before reading the plan
+  MoeRoute* r = a.route;
+  const int nd = plan_routing(a.ids, a.M, a.topk, a.E, first_slot, r, a.err);
   const int KTg = a.hidden / 16, NGg = a.inter / 128;
   const int KTd = a.inter / 16, NGd = a.hidden / 128;
   const long long ug = (long long)KTg * NGg, ud = (long long)KTd * NGd;
@@ -155,14 +181,121 @@ __global__ void moe_plan_kernel(const MoePlanArgs a) {
     r->grid1 = device_grid(r->units1, KTg, a.grid1_max);
     r->grid2 = device_grid(r->units2, KTd, a.grid2_max);
   }
-  // Finish only after the input rotation (launched before this kernel, which
-  // does not read it) so that completing this kernel implies both.
-  pdl_wait();
+}
+
+// ---------------------------------------------------------------- by halves
+//
+// EXLR8 page, manifest paragraph: each expert matrix is stored as halves of
+// 128 intermediate channels, with a width per half for gate and up and one
+// width per expert for down, and kernels take a pointer table ptr[e][h] that
+// is re-read at every launch.  Gate and up halves are 128 output channels
+// each: every (distinct expert, matrix, half) is one GEMV job of one
+// 128-channel group whose code rows are contiguous.  Down halves are 128
+// input channels (8 k-tile rows) each: a down job's unit is one half of one
+// output group, loaded through that half's tensor map, which this kernel
+// writes from a per-width template with the half's address.
+
+struct MoeHalvesPlanArgs {
+  const int32_t* ids;
+  int M, topk, E, H;
+  int hidden, inter;
+  const uint8_t* const* gate_half;  // caller's tables [E][H]
+  const uint8_t* const* up_half;
+  const uint8_t* const* down_half;
+  const int* gate_bits;             // [E][H]
+  const int* up_bits;               // [E][H]
+  const int* down_bits;             // [E]
+  const CUtensorMap* tmpl;          // [3]: down-half maps for 2, 3, 4 bits
+  CUtensorMap* half_maps;           // [kMoeMaxDistinct][H]
+  const uint8_t* stand_in;          // zero code used in place of a failing entry
+  int e4m3;
+  const uint32_t* xfrag_hidden;
+  uint32_t* xfrag_down;
+  float* part1;
+  float* part2;
+  size_t part1_stride, part2_stride, xdown_stride;
+  GemvJob* jobs1;                   // [2*kMoeMaxDistinct*H]: (slot, gate|up, half)
+  GemvJob* jobs2;                   // [kMoeMaxDistinct]
+  MoeRoute* route;
+  int grid1_max, grid2_max;
+  int* err;
+};
+
+// A table entry is used only if its pointer is non-null and 16-byte aligned
+// (the copy engine's rule) and its width is 2, 3 or 4; otherwise the handle's
+// error flag is set and a zero code of the largest half takes its place.
+__device__ __forceinline__ const uint8_t* checked_half(const uint8_t* p, const uint8_t* stand_in,
+                                                       int* err) {
+  if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) {
+    set_error(err, kDevErrBadTable);
+    return stand_in;
+  }
+  return p;
+}
+__device__ __forceinline__ int checked_bits(int b, int* err) {
+  if (b < 2 || b > 4) {
+    set_error(err, kDevErrBadTable);
+    return 2;
+  }
+  return b;
+}
+
+__global__ void moe_plan_halves_kernel(const MoeHalvesPlanArgs a) {
+  extern __shared__ int first_slot[];  // [E]
+  pdl_trigger();
+  MoeRoute* r = a.route;
+  const int nd = plan_routing(a.ids, a.M, a.topk, a.E, first_slot, r, a.err);
+  const int H = a.H;
+  const int KTg = a.hidden / 16;     // gate/up: units per half job
+  const int NGd = a.hidden / 128;    // down: output groups, H units (halves) each
+  const long long ud = (long long)H * NGd;
+  // gate and up: job q = (2d + matrix) * H + half
+  for (int q = threadIdx.x; q < 2 * nd * H; q += blockDim.x) {
+    const int h = q % H, dm = q / H;
+    const int e = r->expert[dm >> 1];
+    const bool up = (dm & 1) != 0;
+    const uint8_t* p = checked_half((up ? a.up_half : a.gate_half)[(size_t)e * H + h], a.stand_in,
+                                    a.err);
+    const int b = checked_bits((up ? a.up_bits : a.gate_bits)[(size_t)e * H + h], a.err);
+    // the half's partial sums start at its first output channel
+    a.jobs1[q] = make_job(p, nullptr, a.xfrag_hidden, a.part1 + dm * a.part1_stride + 128 * h,
+                          (long long)q * KTg, b, KTg, 1, a.inter, a.e4m3);
+  }
+  // down: the tensor map of every half of every distinct expert
+  for (int q = threadIdx.x; q < nd * H; q += blockDim.x) {
+    const int d = q / H, h = q - d * H;
+    const int e = r->expert[d];
+    const int b = checked_bits(a.down_bits[e], a.err);
+    const uint8_t* p = checked_half(a.down_half[(size_t)e * H + h], a.stand_in, a.err);
+    const uint4* src = reinterpret_cast<const uint4*>(a.tmpl + (b - 2));
+    uint4* dst = reinterpret_cast<uint4*>(a.half_maps + q);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = src[i];
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst),
+                 "l"(reinterpret_cast<uint64_t>(p))
+                 : "memory");
+    tensormap_release();
+  }
+  for (int d = threadIdx.x; d < nd; d += blockDim.x) {
+    const int b = checked_bits(a.down_bits[r->expert[d]], a.err);
+    GemvJob j = make_job(nullptr, nullptr, a.xfrag_down + d * a.xdown_stride,
+                         a.part2 + d * a.part2_stride, d * ud, b, H, NGd, a.hidden, a.e4m3);
+    j.row_maps = a.half_maps + (size_t)d * H;
+    a.jobs2[d] = j;
+  }
+  if (threadIdx.x == 0) {
+    r->n_distinct = nd;
+    r->units1 = 2LL * nd * H * KTg;
+    r->units2 = (long long)nd * ud;
+    r->grid1 = device_grid(r->units1, KTg, a.grid1_max);
+    r->grid2 = device_grid(r->units2, H, a.grid2_max);
+  }
 }
 
 struct MoeMidArgs {
   const MoeRoute* route;
   const GemvJob* jobs1;
+  int jobs_per_matrix;   // 1, or H when stored by halves (job of half 0 describes the matrix)
   const float* sv_gate;  // [E][inter]
   const float* sv_up;
   const float* su_down;
@@ -195,8 +328,8 @@ __global__ void moe_mid_kernel(const MoeMidArgs a) {
     const float4 sg = load4_f32(a.sv_gate + off);
     const float4 su = load4_f32(a.sv_up + off);
     const float4 sd = load4_f32(a.su_down + off);
-    const GemvJob& jg = a.jobs1[2 * d];
-    const GemvJob& ju = a.jobs1[2 * d + 1];
+    const GemvJob& jg = a.jobs1[(2 * d) * a.jobs_per_matrix];
+    const GemvJob& ju = a.jobs1[(2 * d + 1) * a.jobs_per_matrix];
     float gv[4], uv[4];
     sum_slots_pair<kMoeSlots>(jg.part, jg.unit_begin, ju.part, ju.unit_begin, jg.KT, jg.N,
                               r->units1, r->grid1, kMoeMaxTokens, m, g, lane, gv, uv);
@@ -297,6 +430,50 @@ escha_status_t upload(T** dst, const T* host, size_t n) {
 
 }  // namespace
 
+// Folded side vectors and the per-call scratch, shared by both ways of
+// storing the experts.  jobs1_count: gate/up jobs of the largest call.
+static escha_status_t moe_init_common(escha_moe_s* h, const uint16_t* rin_hidden,
+                               const float* s_in_hidden, const uint16_t* rout_gate,
+                               const float* s_out_gate, const uint16_t* rout_up,
+                               const float* s_out_up, const uint16_t* rin_down,
+                               const float* s_in_down, const uint16_t* rout_hidden,
+                               const float* s_out_hidden, size_t jobs1_count, cudaStream_t st) {
+  escha_status_t s = ESCHA_OK;
+  const int E = h->E, hidden = h->hidden, inter = h->inter;
+  const size_t ei = (size_t)E * inter;
+  if ((s = dev_alloc(&h->su_hidden, hidden)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->sv_hidden, hidden)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->sv_gate, ei)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->sv_up, ei)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->su_down, ei)) != ESCHA_OK) return s;
+  if (launch_fold_scales(rin_hidden, s_in_hidden, h->su_hidden, hidden, st) != cudaSuccess ||
+      launch_fold_scales(rout_hidden, s_out_hidden, h->sv_hidden, hidden, st) != cudaSuccess ||
+      launch_fold_scales(rout_gate, s_out_gate, h->sv_gate, static_cast<int>(ei), st) != cudaSuccess ||
+      launch_fold_scales(rout_up, s_out_up, h->sv_up, static_cast<int>(ei), st) != cudaSuccess ||
+      launch_fold_scales(rin_down, s_in_down, h->su_down, static_cast<int>(ei), st) != cudaSuccess)
+    return ESCHA_ERR_CUDA;
+
+  h->xdown_stride = (size_t)(inter / 16) * kMoeMaxTokens * 16;  // words per distinct slot
+  h->part1_stride = (size_t)kMoeSlots * kMoeMaxTokens * inter;
+  h->part2_stride = (size_t)kMoeSlots * kMoeMaxTokens * hidden;
+  if ((s = dev_alloc(&h->xfrag_hidden, (size_t)(hidden / 16) * kMoeMaxTokens * 16)) != ESCHA_OK)
+    return s;
+  if ((s = dev_alloc(&h->xfrag_down, h->xdown_stride * kMoeMaxDistinct)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->part1, h->part1_stride * 2 * kMoeMaxDistinct)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->part2, h->part2_stride * kMoeMaxDistinct)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->jobs1, jobs1_count)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->jobs2, kMoeMaxDistinct)) != ESCHA_OK) return s;
+  unsigned char* rt = nullptr;
+  if ((s = dev_alloc(&rt, sizeof(MoeRoute))) != ESCHA_OK) return s;
+  h->route = rt;
+  if ((s = dev_alloc(&h->err, 1)) != ESCHA_OK) return s;
+  if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return ESCHA_ERR_CUDA;
+  if (cudaMemset(h->route, 0, sizeof(MoeRoute)) != cudaSuccess) return ESCHA_ERR_CUDA;
+  h->grid_max = h->num_sms * gemv_ranges_per_sm();
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ESCHA_ERR_CUDA;
+  return ESCHA_OK;
+}
+
 escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
                         const int16_t* const* gate_code, const int16_t* const* up_code,
                         const int16_t* const* down_code, const int32_t* bits,
@@ -334,41 +511,54 @@ escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
     if ((s = upload(&h->code_maps, maps.data(), maps.size())) != ESCHA_OK) return s;
   }
 
-  const size_t ei = (size_t)E * inter;
-  if ((s = dev_alloc(&h->su_hidden, hidden)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->sv_hidden, hidden)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->sv_gate, ei)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->sv_up, ei)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->su_down, ei)) != ESCHA_OK) return s;
-  if (launch_fold_scales(rin_hidden, s_in_hidden, h->su_hidden, hidden, st) != cudaSuccess ||
-      launch_fold_scales(rout_hidden, s_out_hidden, h->sv_hidden, hidden, st) != cudaSuccess ||
-      launch_fold_scales(rout_gate, s_out_gate, h->sv_gate, static_cast<int>(ei), st) != cudaSuccess ||
-      launch_fold_scales(rout_up, s_out_up, h->sv_up, static_cast<int>(ei), st) != cudaSuccess ||
-      launch_fold_scales(rin_down, s_in_down, h->su_down, static_cast<int>(ei), st) != cudaSuccess)
-    return ESCHA_ERR_CUDA;
+  return moe_init_common(h, rin_hidden, s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up,
+                         rin_down, s_in_down, rout_hidden, s_out_hidden, 2 * kMoeMaxDistinct, st);
+}
 
-  h->xdown_stride = (size_t)(inter / 16) * kMoeMaxTokens * 16;  // words per distinct slot
-  h->part1_stride = (size_t)kMoeSlots * kMoeMaxTokens * inter;
-  h->part2_stride = (size_t)kMoeSlots * kMoeMaxTokens * hidden;
-  if ((s = dev_alloc(&h->xfrag_hidden, (size_t)(hidden / 16) * kMoeMaxTokens * 16)) != ESCHA_OK)
-    return s;
-  if ((s = dev_alloc(&h->xfrag_down, h->xdown_stride * kMoeMaxDistinct)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->part1, h->part1_stride * 2 * kMoeMaxDistinct)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->part2, h->part2_stride * kMoeMaxDistinct)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->jobs1, 2 * kMoeMaxDistinct)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->jobs2, kMoeMaxDistinct)) != ESCHA_OK) return s;
-  unsigned char* rt = nullptr;
-  if ((s = dev_alloc(&rt, sizeof(MoeRoute))) != ESCHA_OK) return s;
-  h->route = rt;
-  if ((s = dev_alloc(&h->err, 1)) != ESCHA_OK) return s;
-  if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) return ESCHA_ERR_CUDA;
-  if (cudaMemset(h->route, 0, sizeof(MoeRoute)) != cudaSuccess) return ESCHA_ERR_CUDA;
-  h->grid_max = h->num_sms * gemv_ranges_per_sm();
-  if (cudaStreamSynchronize(st) != cudaSuccess) return ESCHA_ERR_CUDA;
-  return ESCHA_OK;
+escha_status_t moe_init_halves(escha_moe_s* h, int E, int hidden, int inter,
+                               const int16_t* const* gate_half, const int16_t* const* up_half,
+                               const int16_t* const* down_half, const int32_t* gate_bits,
+                               const int32_t* up_bits, const int32_t* down_bits,
+                               const uint16_t* rin_hidden, const float* s_in_hidden,
+                               const uint16_t* rout_gate, const float* s_out_gate,
+                               const uint16_t* rout_up, const float* s_out_up,
+                               const uint16_t* rin_down, const float* s_in_down,
+                               const uint16_t* rout_hidden, const float* s_out_hidden,
+                               cudaStream_t st) {
+  escha_status_t s = device_info(&h->device, &h->num_sms);
+  if (s != ESCHA_OK) return s;
+  h->E = E;
+  h->hidden = hidden;
+  h->inter = inter;
+  h->halves = 1;
+  h->H = inter / 128;
+  h->gate_half = reinterpret_cast<const uint8_t* const*>(gate_half);
+  h->up_half = reinterpret_cast<const uint8_t* const*>(up_half);
+  h->down_half = reinterpret_cast<const uint8_t* const*>(down_half);
+  h->gate_bits = gate_bits;
+  h->up_bits = up_bits;
+  h->down_bits = down_bits;
+  // Zero code as large as the largest half (4 bits), standing in for table
+  // entries that fail the device-side checks.
+  const size_t stand_bytes = (size_t)(hidden / 16) * 8 * 128;
+  if ((s = dev_alloc(&h->stand_in, stand_bytes)) != ESCHA_OK) return s;
+  if (cudaMemset(h->stand_in, 0, stand_bytes) != cudaSuccess) return ESCHA_ERR_CUDA;
+  {
+    CUtensorMap tm[3];
+    for (int b = 2; b <= 4; ++b)
+      if (!encode_gemv_half_map(&tm[b - 2], h->stand_in, b, hidden / 16)) return ESCHA_ERR_CUDA;
+    if ((s = upload(&h->half_map_tmpl, tm, 3)) != ESCHA_OK) return s;
+  }
+  if ((s = dev_alloc(&h->half_maps, (size_t)kMoeMaxDistinct * h->H)) != ESCHA_OK) return s;
+  return moe_init_common(h, rin_hidden, s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up,
+                         rin_down, s_in_down, rout_hidden, s_out_hidden,
+                         (size_t)2 * kMoeMaxDistinct * h->H, st);
 }
 
 void moe_free(escha_moe_s* h) {
+  cudaFree(h->half_maps);
+  cudaFree(h->half_map_tmpl);
+  cudaFree(h->stand_in);
   cudaFree(h->code_maps);
   cudaFree(h->gate_code);
   cudaFree(h->up_code);
@@ -400,6 +590,42 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       break;
     }
     case 1: {
+      if (h->halves) {
+        MoeHalvesPlanArgs pa;
+        pa.ids = ids;
+        pa.M = M;
+        pa.topk = topk;
+        pa.E = h->E;
+        pa.H = h->H;
+        pa.hidden = h->hidden;
+        pa.inter = h->inter;
+        pa.gate_half = h->gate_half;
+        pa.up_half = h->up_half;
+        pa.down_half = h->down_half;
+        pa.gate_bits = h->gate_bits;
+        pa.up_bits = h->up_bits;
+        pa.down_bits = h->down_bits;
+        pa.tmpl = h->half_map_tmpl;
+        pa.half_maps = h->half_maps;
+        pa.stand_in = h->stand_in;
+        pa.e4m3 = h->rounding == ESCHA_ROUND_E4M3 ? 1 : 0;
+        pa.xfrag_hidden = h->xfrag_hidden;
+        pa.xfrag_down = h->xfrag_down;
+        pa.part1 = h->part1;
+        pa.part2 = h->part2;
+        pa.part1_stride = h->part1_stride;
+        pa.part2_stride = h->part2_stride;
+        pa.xdown_stride = h->xdown_stride;
+        pa.jobs1 = h->jobs1;
+        pa.jobs2 = h->jobs2;
+        pa.route = route;
+        pa.grid1_max = h->grid_max;
+        pa.grid2_max = h->grid_max;
+        pa.err = h->err;
+        PdlLaunch pl(1, 1024, h->E * sizeof(int), st);
+        e = cudaLaunchKernelEx(&pl.cfg, moe_plan_halves_kernel, pa);
+        break;
+      }
       MoePlanArgs pa;
       pa.ids = ids;
       pa.M = M;
@@ -432,14 +658,19 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
     }
     case 2:
       h->prof.begin(st);
+      // every job has the same number of units: one matrix, or one half of one
       e = launch_gemv_device_schedule(h->jobs1, &route->units1, &route->grid1, h->grid_max, M,
-                                      kMoeMaxTokens, h->err, st);
+                                      kMoeMaxTokens, h->err, st,
+                                      h->halves ? (long long)(h->hidden / 16)
+                                                : (long long)(h->hidden / 16) * (h->inter / 128),
+                                      false, h->halves ? kGemvColHalves : kGemvWhole);
       h->prof.end(st);
       break;
     case 3: {
       MoeMidArgs ma;
       ma.route = route;
       ma.jobs1 = h->jobs1;
+      ma.jobs_per_matrix = h->halves ? h->H : 1;
       ma.sv_gate = h->sv_gate;
       ma.sv_up = h->sv_up;
       ma.su_down = h->su_down;
@@ -455,7 +686,10 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
     case 4:
       h->prof.begin(st);
       e = launch_gemv_device_schedule(h->jobs2, &route->units2, &route->grid2, h->grid_max, M,
-                                      kMoeMaxTokens, h->err, st);
+                                      kMoeMaxTokens, h->err, st,
+                                      h->halves ? (long long)h->H * (h->hidden / 128)
+                                                : (long long)(h->inter / 16) * (h->hidden / 128),
+                                      h->halves != 0, h->halves ? kGemvRowHalves : kGemvWhole);
       h->prof.end(st);
       break;
     case 5: {

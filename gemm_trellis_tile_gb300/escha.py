@@ -13,6 +13,8 @@ import ctypes
 import os
 import re
 
+import numpy as np
+
 from . import build as _build
 
 ESCHA_OK = 0
@@ -53,6 +55,8 @@ _SIGS = {
     "escha_mlp_gemv_stage": (_I, [_P, _I, _P, _P, _I, _P]),
     "escha_moe_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _P, _P, _P, _P,
                               _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "escha_moe_create_halves": (_I, [ctypes.POINTER(_P), _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                     _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "escha_moe_destroy": (_I, [_P]),
     "escha_linear_moe_gemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
     "escha_linear_moe_gemv_stage": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _P]),
@@ -392,6 +396,73 @@ class MoE:
             self.close()
         except Exception:
             pass
+
+
+class MoEHalves(MoE):
+    """Routed-expert layer stored by halves of 128 intermediate channels, with
+    per-half widths for gate/up and per-expert widths for down
+    (escha_moe_create_halves).
+
+    gate_half, up_half, down_half: int64 CUDA tensors [E, H] of device
+    pointers (H = inter / 128); gate_bits, up_bits: int32 CUDA tensors [E, H];
+    down_bits: int32 CUDA tensor [E].  The tables are borrowed and re-read by
+    every call, so writing new pointers or widths into them (between calls)
+    changes the layer.  Side vectors as for MoE.
+    """
+
+    def __init__(self, hidden, inter, gate_half, up_half, down_half, gate_bits, up_bits,
+                 down_bits, rin_hidden, s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up,
+                 rin_down, s_in_down, rout_hidden, s_out_hidden, stream=None):
+        torch = _torch()
+        E = gate_bits.shape[0]
+        H = inter // 128
+        for t in (gate_half, up_half, down_half):
+            _dev(t, torch.int64, (E, H))
+        _dev(gate_bits, torch.int32, (E, H))
+        _dev(up_bits, torch.int32, (E, H))
+        _dev(down_bits, torch.int32, (E,))
+        self._keep = (gate_half, up_half, down_half, gate_bits, up_bits, down_bits, rin_hidden,
+                      s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up, rin_down, s_in_down,
+                      rout_hidden, s_out_hidden)
+        h = ctypes.c_void_p()
+        check(load().escha_moe_create_halves(
+            ctypes.byref(h), E, hidden, inter, _ptr(gate_half), _ptr(up_half), _ptr(down_half),
+            _ptr(gate_bits), _ptr(up_bits), _ptr(down_bits), _ptr(rin_hidden), _ptr(s_in_hidden),
+            _ptr(rout_gate), _ptr(s_out_gate), _ptr(rout_up), _ptr(s_out_up), _ptr(rin_down),
+            _ptr(s_in_down), _ptr(rout_hidden), _ptr(s_out_hidden), _stream(stream)),
+            "escha_moe_create_halves")
+        self.handle = h
+        self.hidden = hidden
+        self.tables = dict(gate_half=gate_half, up_half=up_half, down_half=down_half,
+                           gate_bits=gate_bits, up_bits=up_bits, down_bits=down_bits)
+
+    @classmethod
+    def from_arrays(cls, spec, expert_codes, device="cuda"):
+        """Build from host arrays: spec from synthetic.make_moe_half_spec;
+        expert_codes maps expert id -> (gate halves, up halves, down halves),
+        lists of int16 arrays.  Entries of experts without codes point at one
+        zero-filled stand-in half (never read unless routed to)."""
+        torch = _torch()
+        E, hidden, inter, H = spec["num_experts"], spec["hidden"], spec["inter"], spec["halves"]
+        dev = {e: tuple([torch.from_numpy(c).to(device) for c in part] for part in codes)
+               for e, codes in expert_codes.items()}
+        stand_in = torch.zeros(hidden * 64, dtype=torch.int16, device=device)
+        tabs = []
+        for part in range(3):
+            ptrs = [[(dev[e][part][h] if e in dev else stand_in).data_ptr() for h in range(H)]
+                    for e in range(E)]
+            tabs.append(torch.tensor(ptrs, dtype=torch.int64, device=device))
+        bits = [torch.from_numpy(np.ascontiguousarray(spec[k])).to(device)
+                for k in ("gate_bits", "up_bits", "down_bits")]
+        t = {k: torch.from_numpy(spec[k]).to(device) for k in (
+            "rin_hidden", "s_in_hidden", "rout_gate", "s_out_gate", "rout_up", "s_out_up",
+            "rin_down", "s_in_down", "rout_hidden", "s_out_hidden")}
+        obj = cls(hidden, inter, tabs[0], tabs[1], tabs[2], bits[0], bits[1], bits[2],
+                  t["rin_hidden"], t["s_in_hidden"], t["rout_gate"], t["s_out_gate"], t["rout_up"],
+                  t["s_out_up"], t["rin_down"], t["s_in_down"], t["rout_hidden"],
+                  t["s_out_hidden"])
+        obj._keep_dev = (dev, stand_in, t)
+        return obj
 
 
 def selftest_wait_timeout(limit_us=10000, stream=None):

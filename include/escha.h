@@ -166,6 +166,46 @@ escha_status_t escha_moe_create(escha_moe_t* out, int num_experts, int hidden, i
                                 const uint16_t* rin_down, const float* s_in_down,
                                 const uint16_t* rout_hidden, const float* s_out_hidden,
                                 void* stream);
+
+/*
+ * Routed-expert layer stored by halves (EXLR8 page, manifest paragraph): each
+ * expert matrix is split into H = inter/128 halves of 128 intermediate
+ * channels.  Gate and up are split along their output channels and each half
+ * has its own width; down is split along its input channels and has one width
+ * per expert.  Kernels get a pointer table ptr[e][h] instead of one pointer per
+ * matrix, and the table is re-read at every launch.  Everything else (shared
+ * hidden-side rotation, side vectors, the call escha_linear_moe_gemv and its
+ * stages, rounding, check) is as for escha_moe_create.
+ *   gate_half, up_half  DEVICE arrays [E * H] of device pointers: entry
+ *       e*H + h is the code of output channels 128h .. 128h+127 of expert e's
+ *       gate (up) matrix, int16 [hidden/16, 8, 16*b] with b = gate_bits[e*H + h]
+ *       (up_bits[e*H + h]) -- the tiles of those 128 columns in the layout of
+ *       escha_moe_create's code tensors.
+ *   down_half  DEVICE array [E * H] of device pointers: entry e*H + h is the
+ *       code of input channels 128h .. 128h+127 of expert e's down matrix,
+ *       int16 [8, hidden/16, 16*b] with b = down_bits[e].
+ *   gate_bits, up_bits  DEVICE int32 [E * H]; down_bits DEVICE int32 [E].
+ *   Side vectors: as for escha_moe_create.
+ * The six tables are borrowed, not copied: each call's routing kernel reads
+ * the entries of the experts it routes to, so the caller may point halves at
+ * other code or change widths between calls (not while a call that uses them
+ * is in flight on the GPU) without creating a new handle.  The tables must be
+ * 8-byte (pointers) and 4-byte (widths) aligned.  An entry that is null, not
+ * 16-byte aligned, or a width outside {2,3,4} is replaced by a zero code of
+ * width 2 and sets the handle's error flag: escha_moe_check then reports
+ * ESCHA_ERR_INVALID_ARG and that call's output is not meaningful.
+ */
+escha_status_t escha_moe_create_halves(escha_moe_t* out, int num_experts, int hidden, int inter,
+                                       const int16_t* const* gate_half,
+                                       const int16_t* const* up_half,
+                                       const int16_t* const* down_half, const int32_t* gate_bits,
+                                       const int32_t* up_bits, const int32_t* down_bits,
+                                       const uint16_t* rin_hidden, const float* s_in_hidden,
+                                       const uint16_t* rout_gate, const float* s_out_gate,
+                                       const uint16_t* rout_up, const float* s_out_up,
+                                       const uint16_t* rin_down, const float* s_in_down,
+                                       const uint16_t* rout_hidden, const float* s_out_hidden,
+                                       void* stream);
 escha_status_t escha_moe_destroy(escha_moe_t m);
 
 /*

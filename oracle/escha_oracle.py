@@ -366,7 +366,7 @@ def decode_columns(code, bits, cols, rounding="fp16"):
 
 
 
-def decode_column_halves(halves, bits):
+def decode_column_halves(halves, bits, rounding="fp16"):
     """W_inner [in, 128*H] of a matrix stored by halves along its output side.
 
     [EXLR8] manifest paragraph: an expert's gate and up matrices are split into
@@ -376,10 +376,11 @@ def decode_column_halves(halves, bits):
     the [FMT] "Tensor mapping" layout of its own); the matrix is the halves'
     decoded columns side by side.
     """
-    return np.concatenate([decode_matrix(c, int(b)) for c, b in zip(halves, bits)], axis=1)
+    return np.concatenate([decode_matrix(c, int(b), rounding=rounding)
+                           for c, b in zip(halves, bits)], axis=1)
 
 
-def decode_row_halves(halves, bits):
+def decode_row_halves(halves, bits, rounding="fp16"):
     """W_inner [128*H, out] of a matrix stored by halves along its input side.
 
     [EXLR8] manifest paragraph: down's halves are 128 of its input (intermediate)
@@ -388,7 +389,8 @@ def decode_row_halves(halves, bits):
     input channels 128h .. 128h+127; the matrix is the halves' decoded rows
     stacked in order.
     """
-    return np.concatenate([decode_matrix(c, int(bits)) for c in halves], axis=0)
+    return np.concatenate([decode_matrix(c, int(bits), rounding=rounding) for c in halves],
+                          axis=0)
 
 
 # ----------------------------------------------------------------------------

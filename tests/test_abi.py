@@ -83,6 +83,29 @@ def test_bad_config_rejected_on_host(lib):
                                    ctypes.cast(arr, ctypes.c_void_p), 6, None) == 1
 
 
+def test_moe_halves_create_rejects_bad_arguments_on_host(lib):
+    """escha_moe_create_halves: sizes, null tables and misaligned tables are
+    rejected before any CUDA call (table entries live on the device and are
+    checked there)."""
+    h = ctypes.c_void_p()
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+
+    def create(E=4, hidden=256, inter=256, tabs=(fake, fake, fake), bits=(fake, fake, fake)):
+        return lib.escha_moe_create_halves(ctypes.byref(h), E, hidden, inter, *tabs, *bits,
+                                           fake, None, fake, None, fake, None, fake, None,
+                                           fake, None, None)
+    assert lib.escha_moe_create_halves(None, 4, 256, 256, *([fake] * 6), *([fake] * 10), None) == 1
+    assert create(E=0) == 1
+    assert create(E=5000) == 2
+    assert create(inter=200) == 2
+    assert create(hidden=320) == 2
+    assert create(tabs=(fake, None, fake)) == 1
+    assert create(bits=(fake, fake, None)) == 1
+    assert create(tabs=(fake, odd, fake)) == 1        # pointer table not 8-byte aligned
+    assert create(bits=(fake, ctypes.c_void_p(0x10002), fake)) == 1
+
+
 def test_valid_config_without_gpu_fails_as_cuda_error(lib):
     """No GPU here: a well-formed create reaches the device query and reports a CUDA error."""
     import torch
