@@ -272,6 +272,11 @@ escha_status_t escha_linear_check(escha_linear_t h, void* stream) {
   return read_and_clear_error(h->err, static_cast<cudaStream_t>(stream));
 }
 
+escha_status_t escha_mlp_check(escha_mlp_t m, void* stream) {
+  if (!m) return ESCHA_ERR_INVALID_ARG;
+  return read_and_clear_error(m->err, static_cast<cudaStream_t>(stream));
+}
+
 escha_status_t escha_mlp_create(escha_mlp_t* out, escha_linear_t gate, escha_linear_t up,
                                 escha_linear_t down) {
   if (!out) return ESCHA_ERR_INVALID_ARG;

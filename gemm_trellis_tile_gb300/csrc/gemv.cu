@@ -204,10 +204,13 @@ __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t*
 // The stage holds fragments for the M real tokens only.  A lane whose token
 // (8 tb + g) is at or past M reads token M-1's fragment instead: MMA output
 // column g depends on B column g alone, and those columns are never stored.
-template <int BITS, int TB, bool E4M3>
+// MC > 0: the token count M is the compile-time MC (activation fragment
+// addresses become immediate offsets); MC = 0: M at run time.
+template <int BITS, int TB, bool E4M3, int MC = 0>
 __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint4* xf_s, int n,
-                                              int w, int lane, int M, uint32_t mask, uint32_t xr,
-                                              float (&acc)[TB][4]) {
+                                              int w, int lane, int M_rt, uint32_t mask,
+                                              uint32_t xr, float (&acc)[TB][4]) {
+  const int M = MC > 0 ? MC : M_rt;
   constexpr int T = 32 * BITS;
   constexpr int kRowWords = kCW * T / 4;  // uint32 words per unit in the stage
   const LaneWindow lw = lane_window<BITS>(lane);
@@ -236,6 +239,21 @@ __device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb) xq[tb] += xstride;
     }
+  }
+}
+
+// The chunk's decode at its width and rounding (key = bits + 8 * e4m3).
+template <int TB, int MC>
+__device__ __forceinline__ void consume_dispatch(int key, const uint8_t* cs, const uint4* xs,
+                                                 int rows, int wt, int lane, int M, uint32_t mask,
+                                                 uint32_t xr, float (&acc)[TB][4]) {
+  switch (key) {
+    case 2: consume_chunk<2, TB, false, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
+    case 3: consume_chunk<3, TB, false, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
+    case 4: consume_chunk<4, TB, false, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
+    case 10: consume_chunk<2, TB, true, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
+    case 11: consume_chunk<3, TB, true, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
+    default: consume_chunk<4, TB, true, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
   }
 }
 
@@ -392,14 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t* cs = codes + stage * kCodeStageBytes;
     const uint4* xs = reinterpret_cast<const uint4*>(xfs + stage * xf_stage_bytes<TB>());
     const int rows = ch.n * RPU;  // k-tile rows of the stage
-    switch (it.bits + 8 * it.e4m3) {
-      case 2: consume_chunk<2, TB, false>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 3: consume_chunk<3, TB, false>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 4: consume_chunk<4, TB, false>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 10: consume_chunk<2, TB, true>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      case 11: consume_chunk<3, TB, true>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-      default: consume_chunk<4, TB, true>(cs, xs, rows, wt, lane, a.M, a.cb_mask, a.cb_xor, acc); break;
-    }
+    if (TB == 1 && a.M == 1)  // one token: the common decode case, specialised
+      consume_dispatch<TB, 1>(it.bits + 8 * it.e4m3, cs, xs, rows, wt, lane, 1, a.cb_mask,
+                              a.cb_xor, acc);
+    else
+      consume_dispatch<TB, 0>(it.bits + 8 * it.e4m3, cs, xs, rows, wt, lane, a.M, a.cb_mask,
+                              a.cb_xor, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + stage]));
     if (++slot == kStages / kGroups) {

@@ -64,6 +64,7 @@ _SIGS = {
     "escha_moe_set_rounding": (_I, [_P, _I]),
     "escha_linear_check": (_I, [_P, _P]),
     "escha_moe_check": (_I, [_P, _P]),
+    "escha_mlp_check": (_I, [_P, _P]),
     "escha_profile_enable": (_I, [_P, _I, _I]),
     "escha_profile_collect": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "escha_selftest_wait_timeout": (_I, [_I, _P]),
@@ -276,7 +277,9 @@ class MLP:
         return y
 
     def check(self, stream=None):
-        return max(layer.check(stream) for layer in self._layers)
+        """The MLP's own device error flag (its launches), then the layers'."""
+        st = load().escha_mlp_check(self.handle, _stream(stream))
+        return st if st != 0 else max(layer.check(stream) for layer in self._layers)
 
     def profile(self, on=True):
         check(load().escha_profile_enable(self.handle, KIND_MLP, int(on)), "escha_profile_enable")

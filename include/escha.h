@@ -272,8 +272,11 @@ escha_status_t escha_moe_set_rounding(escha_moe_t m, int rounding);
  * ESCHA_ERR_TIMEOUT if a bounded wait in one of its kernels ran out,
  * ESCHA_ERR_INVALID_ARG if routing ids were out of range, ESCHA_ERR_CUDA on an
  * asynchronous CUDA error, else ESCHA_OK.  The flag is cleared by the read.
+ * A gated MLP has a flag of its own for its launches; its three layers keep
+ * theirs (read them with escha_linear_check).
  */
 escha_status_t escha_linear_check(escha_linear_t h, void* stream);
+escha_status_t escha_mlp_check(escha_mlp_t m, void* stream);
 escha_status_t escha_moe_check(escha_moe_t m, void* stream);
 
 /*
