@@ -40,33 +40,66 @@ namespace {
 constexpr int kEncThreads = 1024;
 #define ENC_INF __int_as_float(0x7f800000)
 
-// Codebook value of a state as fp32 (exact: the fp16 value, or its E4M3 rounding).
+// Codebook value of a state as fp16 (the fp16 value, or its E4M3 rounding;
+// both are exact in fp16).
 template <bool E4M3>
-__device__ __forceinline__ float codebook_f32(uint32_t s) {
+__device__ __forceinline__ __half codebook_h(uint32_t s) {
   uint32_t d = mcg_decode_dup(s);
   if (E4M3) d = round_e4m3x2(d);
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(d & 0xFFFFu)));
+  return __ushort_as_half(static_cast<unsigned short>(d & 0xFFFFu));
+}
+
+// A thread's states: groups u = tid + k * kEncThreads (k < KPT) of the states
+// u | t << (16 - K) (t < 2^K) -- 64 states, the same at every step.  Their
+// codebook values stay in registers for the whole search, value k * 2^K + t
+// in half (k * 2^K + t) & 1 of cb[(k * 2^K + t) / 2].
+constexpr int kCbPairs = (1 << 16) / kEncThreads / 2;
+
+template <int K, bool E4M3>
+__device__ __forceinline__ void load_codebook(__half2 (&cb)[kCbPairs]) {
+  constexpr int TT = 1 << K;
+  const uint32_t tid = threadIdx.x;
+#pragma unroll
+  for (int q = 0; q < kCbPairs; ++q) {
+    const int i0 = 2 * q, i1 = 2 * q + 1;
+    const uint32_t s0 = (tid + (i0 / TT) * kEncThreads) | (uint32_t(i0 % TT) << (16 - K));
+    const uint32_t s1 = (tid + (i1 / TT) * kEncThreads) | (uint32_t(i1 % TT) << (16 - K));
+    cb[q] = __halves2half2(codebook_h<E4M3>(s0), codebook_h<E4M3>(s1));
+  }
+}
+
+__device__ __forceinline__ float cb_value(const __half2 (&cb)[kCbPairs], int idx) {
+  return (idx & 1) ? __high2float(cb[idx >> 1]) : __low2float(cb[idx >> 1]);
 }
 
 // One forward pass.  Pass 1 (o < 0): any start state.  Pass 2: start states
 // with (s >> K) == o, end states with (s & mask) == o.  Leaves the choices of t
 // in `back` ([256][nu] bytes) and returns the best end state (all threads).
+// The predecessor (u | t << (16-K)) >> K of group u = tid + k * kEncThreads is
+// (tid >> K) + k * (kEncThreads >> K) + t * 2^(16-2K): a fixed offset from
+// the thread's base for every (k, t).
 template <int K, bool E4M3>
-__device__ int viterbi_pass(const float* vals, float* m0, float* m1, uint8_t* back, int o,
-                            float* red_v, int* red_s, float* total) {
+__device__ int viterbi_pass(const __half2 (&cb)[kCbPairs], const float* vals, float* m0,
+                            float* m1, uint8_t* back, int o, float* red_v, int* red_s,
+                            float* total) {
   constexpr int kNu = 1 << (16 - K);
   constexpr uint32_t kMask = kNu - 1;
+  constexpr int KPT = kNu / kEncThreads;  // groups per thread
+  constexpr int TT = 1 << K;
   const int tid = threadIdx.x;
+  const int pbase = tid >> K;
   // step 0: group minima of the first symbol's costs
   {
     const float v = vals[0];
-    for (int u = tid; u < kNu; u += kEncThreads) {
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+      const uint32_t u = static_cast<uint32_t>(tid + k * kEncThreads);
       float best = ENC_INF;
       int bt = 0;
 #pragma unroll
-      for (int t = 0; t < (1 << K); ++t) {
-        const uint32_t s = static_cast<uint32_t>(u) | (static_cast<uint32_t>(t) << (16 - K));
-        const float d = __fsub_rn(v, codebook_f32<E4M3>(s));
+      for (int t = 0; t < TT; ++t) {
+        const uint32_t s = u | (static_cast<uint32_t>(t) << (16 - K));
+        const float d = __fsub_rn(v, cb_value(cb, k * TT + t));
         float cost = __fmul_rn(d, d);
         if (o >= 0 && static_cast<int>(s >> K) != o) cost = ENC_INF;
         if (t == 0 || cost < best) {
@@ -83,21 +116,25 @@ __device__ int viterbi_pass(const float* vals, float* m0, float* m1, uint8_t* ba
   float* mc = m1;
   for (int i = 1; i < 255; ++i) {
     const float v = vals[i];
-    for (int u = tid; u < kNu; u += kEncThreads) {
+    const float* mpb = mp + pbase;
+    uint8_t* bk = back + (size_t)(i + 1) * kNu;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+      const int u = tid + k * kEncThreads;
       float best = ENC_INF;
       int bt = 0;
 #pragma unroll
-      for (int t = 0; t < (1 << K); ++t) {
-        const uint32_t s = static_cast<uint32_t>(u) | (static_cast<uint32_t>(t) << (16 - K));
-        const float d = __fsub_rn(v, codebook_f32<E4M3>(s));
-        const float cost = __fadd_rn(__fmul_rn(d, d), mp[s >> K]);
+      for (int t = 0; t < TT; ++t) {
+        const float d = __fsub_rn(v, cb_value(cb, k * TT + t));
+        const float cost =
+            __fadd_rn(__fmul_rn(d, d), mpb[k * (kEncThreads >> K) + t * (1 << (16 - 2 * K))]);
         if (t == 0 || cost < best) {
           best = cost;
           bt = t;
         }
       }
       mc[u] = best;
-      back[(i + 1) * kNu + u] = static_cast<uint8_t>(bt);
+      bk[u] = static_cast<uint8_t>(bt);
     }
     __syncthreads();
     float* tmp = mp;
@@ -109,13 +146,20 @@ __device__ int viterbi_pass(const float* vals, float* m0, float* m1, uint8_t* ba
   int bs = 0x7fffffff;
   {
     const float v = vals[255];
-    for (int s = tid; s < (1 << 16); s += kEncThreads) {
-      if (o >= 0 && static_cast<int>(static_cast<uint32_t>(s) & kMask) != o) continue;
-      const float d = __fsub_rn(v, codebook_f32<E4M3>(static_cast<uint32_t>(s)));
-      const float cost = __fadd_rn(__fmul_rn(d, d), mp[s >> K]);
-      if (cost < best || (cost == best && s < bs)) {
-        best = cost;
-        bs = s;
+    const float* mpb = mp + pbase;
+#pragma unroll
+    for (int k = 0; k < KPT; ++k) {
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const int s = (tid + k * kEncThreads) | (t << (16 - K));
+        if (o >= 0 && static_cast<int>(static_cast<uint32_t>(s) & kMask) != o) continue;
+        const float d = __fsub_rn(v, cb_value(cb, k * TT + t));
+        const float cost =
+            __fadd_rn(__fmul_rn(d, d), mpb[k * (kEncThreads >> K) + t * (1 << (16 - 2 * K))]);
+        if (cost < best || (cost == best && s < bs)) {
+          best = cost;
+          bs = s;
+        }
       }
     }
   }
@@ -176,6 +220,8 @@ __global__ void __launch_bounds__(kEncThreads, 1)
   const int tid = threadIdx.x;
   const int KT = in_features / 16, NT = out_features / 16;
   const long long tiles = (long long)KT * NT;
+  __half2 cb[kCbPairs];
+  load_codebook<K, E4M3>(cb);
   for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int ti = static_cast<int>(tile / NT);
     const int tj = static_cast<int>(tile - (long long)ti * NT);
@@ -186,9 +232,9 @@ __global__ void __launch_bounds__(kEncThreads, 1)
       vals[tid] = w[(size_t)(16 * ti + r) * out_features + 16 * tj + c];
     }
     __syncthreads();
-    const int end1 = viterbi_pass<K, E4M3>(vals, m0, m1, back, -1, red_v, red_s, total);
+    const int end1 = viterbi_pass<K, E4M3>(cb, vals, m0, m1, back, -1, red_v, red_s, total);
     const int o = end1 & (kNu - 1);
-    const int end2 = viterbi_pass<K, E4M3>(vals, m0, m1, back, o, red_v, red_s, total);
+    const int end2 = viterbi_pass<K, E4M3>(cb, vals, m0, m1, back, o, red_v, red_s, total);
     if (tid == 0) {
       // trace the path back from the end state
       uint32_t s = static_cast<uint32_t>(end2) & 0xFFFFu;
