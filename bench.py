@@ -447,16 +447,16 @@ def run_moe(args, spec, rank, world, local):
     ms, clocks = timed(g_main, reps, ClockSampler(dev.index if dev.index is not None else 0))
 
     # Dominant kernel: the two trellis contraction launches of each call
-    # (stages 2 and 4), timed as (routing plan + contractions) minus (routing
-    # plan alone) over the same cycled routings, CUDA events on the launching
-    # stream around whole graph replays.
+    # (stages 1 and 3), timed as (routing plan and rotation + contractions)
+    # minus (routing plan and rotation alone) over the same cycled routings,
+    # CUDA events on the launching stream around whole graph replays.
     def stages(ss):
         def fn(i):
             for s in ss:
                 moe.gemv(x, ids_d[i % R], w_d[i % R], y, stage=s)
         return fn
-    g_k = capture(stages((1, 2, 4)))
-    g_p = capture(stages((1,)))
+    g_k = capture(stages((0, 1, 3)))
+    g_p = capture(stages((0,)))
     kp_ms, _ = timed(g_k, reps)
     p_ms, _ = timed(g_p, reps)
     k_ms = kp_ms - p_ms
@@ -500,7 +500,7 @@ def run_moe(args, spec, rank, world, local):
         "e2e": {"value": e_steps * (per_pass / R) / (e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(y_host.numel() * 2)},
-        "gpu_launches": 6 * steps,
+        "gpu_launches": 5 * steps,
         "clocks": clocks,
     }
     if rank == 0:

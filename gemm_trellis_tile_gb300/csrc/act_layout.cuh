@@ -120,4 +120,22 @@ __device__ __forceinline__ void sum_slots_pair(const float* part_a, long long ub
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// One warp's share of an input rotation: token m, 128-channel block kb of
+// xh = fp16(had128(x * su)), stored in the GEMV's fragment layout (M tokens).
+__device__ __forceinline__ void rotate_in_block(const uint16_t* x, const float* su,
+                                               uint32_t* xfrag, int K, int M, int m, int kb,
+                                               int lane) {
+  const int k0 = kb * kHad + 4 * lane;
+  float v[4];
+  load4_half(x + (size_t)m * K + k0, v);
+  const float4 s = *reinterpret_cast<const float4*>(su + k0);
+  v[0] *= s.x;
+  v[1] *= s.y;
+  v[2] *= s.z;
+  v[3] *= s.w;
+  fwht128_warp(v, lane);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) xfrag_store(xfrag, M, m, k0 + r, float_to_half_bits(v[r] * kHadScale));
+}
+
 }  // namespace escha

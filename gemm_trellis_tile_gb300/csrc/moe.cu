@@ -6,17 +6,18 @@
 // one shared output rotation had(.) * sv_hidden (exact by linearity).  The
 // intermediate side is per expert.
 //
-// One call, six launches on the caller's stream, no host synchronisation:
-//   1. rotate_in        xfrag_hidden = fp16(had128(x * su_hidden))
-//   2. moe_plan         reads the routing on the device: distinct experts in
-//                       order of first appearance, tokens per expert, and the
-//                       job tables / unit counts / grid sizes of launches 3, 5
-//   3. trellis GEMV     gate and up of every distinct expert (mixed widths)
-//   4. moe_mid          per (expert, token): had(gate)*sv_g, had(up)*sv_u,
+// One call, five launches on the caller's stream, no host synchronisation:
+//   1. moe_plan         block 0 reads the routing on the device: distinct
+//                       experts in order of first appearance, tokens per
+//                       expert, and the job tables / unit counts / grid sizes
+//                       of launches 2 and 4; the other blocks rotate the
+//                       token(s): xfrag_hidden = fp16(had128(x * su_hidden))
+//   2. trellis GEMV     gate and up of every distinct expert (mixed widths)
+//   3. moe_mid          per (expert, token): had(gate)*sv_g, had(up)*sv_u,
 //                       silu(g)*u, then had(h * su_down) into that expert's
 //                       down fragments (zeros for tokens not routed to it)
-//   5. trellis GEMV     down of every distinct expert
-//   6. moe_out          y = fp16(had(sum_k w_k * down partials) * sv_hidden)
+//   4. trellis GEMV     down of every distinct expert
+//   5. moe_out          y = fp16(had(sum_k w_k * down partials) * sv_hidden)
 // Distinct experts decode once however many tokens route to them: the GEMV's
 // B operand carries all 8 token slots, so every token of an expert shares one
 // decode of its tiles.
@@ -91,6 +92,37 @@ __device__ __forceinline__ GemvJob make_job(const uint8_t* code, const CUtensorM
   return j;
 }
 
+// The input rotation done by the plan launch's blocks 1..: xfrag_hidden =
+// fp16(had128(x * su_hidden)), one warp per (token, 128-channel block).
+struct MoeRotIn {
+  const uint16_t* x;
+  const float* su;
+  uint32_t* xfrag;
+  int K, M;
+};
+constexpr int kPlanThreads = 256;
+
+// Blocks past the first: wait for the previous kernel (the previous call may
+// still read xfrag), then rotate.  Returns true for block 0 (the plan).
+__device__ __forceinline__ bool plan_block_or_rotate(const MoeRotIn& rot) {
+  if (blockIdx.x == 0) return true;
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int nb = rot.K / kHad;
+  const long long task = (long long)(blockIdx.x - 1) * (kPlanThreads / 32) + (threadIdx.x >> 5);
+  if (task < (long long)rot.M * nb) {
+    const int m = static_cast<int>(task / nb);
+    rotate_in_block(rot.x, rot.su, rot.xfrag, rot.K, rot.M, m, static_cast<int>(task - (long long)m * nb),
+                    lane);
+  }
+  return false;
+}
+
+unsigned plan_blocks(int M, int K) {
+  const long long tasks = (long long)M * (K / kHad);
+  return static_cast<unsigned>(1 + (tasks + kPlanThreads / 32 - 1) / (kPlanThreads / 32));
+}
+
 // Grid size that gives every CTA at least a quarter of a group's k-tiles, so
 // a group's units span at most five CTAs (five partial-sum slots).
 __device__ __forceinline__ int device_grid(long long units, int KT, int grid_max) {
@@ -152,9 +184,10 @@ __device__ int plan_routing(const int32_t* ids, int M, int topk, int E, int* fir
   return nd;
 }
 
-__global__ void moe_plan_kernel(const MoePlanArgs a) {
+__global__ void moe_plan_kernel(const MoePlanArgs a, const MoeRotIn rot) {
   extern __shared__ int first_slot[];  // [E]: distinct slot of each expert, -1 if none yet
   pdl_trigger();  // the GEMV may launch; it waits for this kernel before reading the plan
+  if (!plan_block_or_rotate(rot)) return;
   MoeRoute* r = a.route;
   const int nd = plan_routing(a.ids, a.M, a.topk, a.E, first_slot, r, a.err);
   const int KTg = a.hidden / 16, NGg = a.inter / 128;
@@ -240,9 +273,10 @@ __device__ __forceinline__ int checked_bits(int b, int* err) {
   return b;
 }
 
-__global__ void moe_plan_halves_kernel(const MoeHalvesPlanArgs a) {
+__global__ void moe_plan_halves_kernel(const MoeHalvesPlanArgs a, const MoeRotIn rot) {
   extern __shared__ int first_slot[];  // [E]
   pdl_trigger();
+  if (!plan_block_or_rotate(rot)) return;
   MoeRoute* r = a.route;
   const int nd = plan_routing(a.ids, a.M, a.topk, a.E, first_slot, r, a.err);
   const int H = a.H;
@@ -304,15 +338,17 @@ struct MoeMidArgs {
   int M, inter;
 };
 
-// One warp per (distinct slot d, token slot m in 0..7, 128-channel group g).
+// One warp per (distinct slot d, token m < M, 128-channel group g); the grid
+// covers the most distinct experts the call can route to (M * topk, at most
+// kMoeMaxDistinct).
 __global__ void moe_mid_kernel(const MoeMidArgs a) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int NG = a.inter / kHad;
-  const int d = static_cast<int>(wid / (8 * NG));
-  const int rem = static_cast<int>(wid - (long long)d * 8 * NG);
+  const int d = static_cast<int>(wid / (a.M * NG));
+  const int rem = static_cast<int>(wid - (long long)d * a.M * NG);
   const int m = rem / NG;
   const int g = rem - m * NG;
   if (d >= kMoeMaxDistinct) return;
@@ -585,11 +621,9 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
   cudaError_t e = cudaSuccess;
   switch (stage) {
     case 0: {
-      RotInJob rj{x, h->su_hidden, h->xfrag_hidden, h->hidden};
-      e = launch_rotate_in_xfrag(&rj, 1, M, st);
-      break;
-    }
-    case 1: {
+      // routing plan (block 0) and the shared input rotation (the other blocks)
+      const MoeRotIn rot{x, h->su_hidden, h->xfrag_hidden, h->hidden, M};
+      const unsigned nblk = plan_blocks(M, h->hidden);
       if (h->halves) {
         MoeHalvesPlanArgs pa;
         pa.ids = ids;
@@ -622,8 +656,8 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
         pa.grid1_max = h->grid_max;
         pa.grid2_max = h->grid_max;
         pa.err = h->err;
-        PdlLaunch pl(1, 1024, h->E * sizeof(int), st);
-        e = cudaLaunchKernelEx(&pl.cfg, moe_plan_halves_kernel, pa);
+        PdlLaunch pl(nblk, kPlanThreads, h->E * sizeof(int), st);
+        e = cudaLaunchKernelEx(&pl.cfg, moe_plan_halves_kernel, pa, rot);
         break;
       }
       MoePlanArgs pa;
@@ -652,11 +686,11 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       pa.grid1_max = h->grid_max;
       pa.grid2_max = h->grid_max;
       pa.err = h->err;
-      PdlLaunch pl(1, 128, h->E * sizeof(int), st);
-      e = cudaLaunchKernelEx(&pl.cfg, moe_plan_kernel, pa);
+      PdlLaunch pl(nblk, kPlanThreads, h->E * sizeof(int), st);
+      e = cudaLaunchKernelEx(&pl.cfg, moe_plan_kernel, pa, rot);
       break;
     }
-    case 2:
+    case 1:
       h->prof.begin(st);
       // every job has the same number of units: one matrix, or one half of one
       e = launch_gemv_device_schedule(h->jobs1, &route->units1, &route->grid1, h->grid_max, M,
@@ -666,7 +700,7 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
                                       false, h->halves ? kGemvColHalves : kGemvWhole);
       h->prof.end(st);
       break;
-    case 3: {
+    case 2: {
       MoeMidArgs ma;
       ma.route = route;
       ma.jobs1 = h->jobs1;
@@ -678,12 +712,13 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       ma.xdown_stride = h->xdown_stride;
       ma.M = M;
       ma.inter = h->inter;
-      const long long mid_warps = (long long)kMoeMaxDistinct * 8 * (h->inter / kHad);
+      const long long mid_warps =
+          (long long)std::min(kMoeMaxDistinct, M * topk) * M * (h->inter / kHad);
       PdlLaunch pl(blocks_for(mid_warps), 32 * kWarpsPerBlock, 0, st);
       e = cudaLaunchKernelEx(&pl.cfg, moe_mid_kernel, ma);
       break;
     }
-    case 4:
+    case 3:
       h->prof.begin(st);
       e = launch_gemv_device_schedule(h->jobs2, &route->units2, &route->grid2, h->grid_max, M,
                                       kMoeMaxTokens, h->err, st,
@@ -692,7 +727,7 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
                                       h->halves != 0, h->halves ? kGemvRowHalves : kGemvWhole);
       h->prof.end(st);
       break;
-    case 5: {
+    case 4: {
       MoeOutArgs oa;
       oa.route = route;
       oa.jobs2 = h->jobs2;

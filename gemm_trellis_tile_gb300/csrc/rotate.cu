@@ -52,18 +52,7 @@ __global__ void rotate_in_xfrag_kernel(const RotInArgs a) {
   const int nb = J.K / kHad;
   const int m = static_cast<int>(wid / nb);
   const int kb = static_cast<int>(wid - (long long)m * nb);
-  const int k0 = kb * kHad + 4 * lane;
-  float v[4];
-  load4_half(J.x + (size_t)m * J.K + k0, v);
-  const float4 su = *reinterpret_cast<const float4*>(J.su + k0);
-  v[0] *= su.x;
-  v[1] *= su.y;
-  v[2] *= su.z;
-  v[3] *= su.w;
-  fwht128_warp(v, lane);
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-    xfrag_store(J.xfrag, a.M, m, k0 + r, float_to_half_bits(v[r] * kHadScale));
+  rotate_in_block(J.x, J.su, J.xfrag, J.K, a.M, m, kb, lane);
 }
 
 // xh[m, k] = fp16(had128(x * su)), plain row-major (the GEMM's A operand).

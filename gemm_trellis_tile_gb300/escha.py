@@ -354,7 +354,7 @@ class MoE:
         obj._keep_dev = (dev, stand_in, t)
         return obj
 
-    STAGES = 6
+    STAGES = 5
 
     def gemv(self, x, expert_ids, expert_w, y=None, stream=None, stage=None):
         torch = _torch()

@@ -234,16 +234,17 @@ escha_status_t escha_linear_moe_gemv(escha_moe_t m, const uint16_t* x, const int
  *     1 gate and up contraction (one launch); 2 output rotations of gate and
  *     up, silu(gate) * up, input rotation of down; 3 down contraction;
  *     4 output rotation of down.
- *   moe (ESCHA_MOE_STAGES = 6): 0 input rotation (shared hidden side);
- *     1 routing plan (reads expert_ids); 2 gate and up contraction of the
- *     routed experts; 3 their output rotations, silu(gate) * up and the input
- *     rotation of down; 4 down contraction; 5 output rotation, weighted sum
- *     over the routed experts (reads expert_w).
+ *   moe (ESCHA_MOE_STAGES = 5): 0 routing plan (reads expert_ids) and, in
+ *     the same launch, the input rotation (shared hidden side); 1 gate and up
+ *     contraction of the routed experts; 2 their output rotations,
+ *     silu(gate) * up and the input rotation of down; 3 down contraction;
+ *     4 output rotation, weighted sum over the routed experts (reads
+ *     expert_w).
  * Stage numbers outside [0, N) return ESCHA_ERR_INVALID_ARG.
  */
 #define ESCHA_LINEAR_STAGES 3
 #define ESCHA_MLP_STAGES 5
-#define ESCHA_MOE_STAGES 6
+#define ESCHA_MOE_STAGES 5
 escha_status_t escha_linear_gemv_stage(escha_linear_t h, int stage, const uint16_t* x,
                                        uint16_t* y, int M, void* stream);
 escha_status_t escha_mlp_gemv_stage(escha_mlp_t m, int stage, const uint16_t* x, uint16_t* y,
