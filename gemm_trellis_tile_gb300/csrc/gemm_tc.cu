@@ -526,11 +526,14 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             for (int qq = 0; qq < 4; ++qq) {
               const float(&w)[8] = qq == 0 ? x0 : (qq == 1 ? x1 : (qq == 2 ? x2 : x3));
               const int col = n0 + c8 + 32 * qq;
+              const float4 sa = __ldg(reinterpret_cast<const float4*>(a.sv + col));
+              const float4 sb = __ldg(reinterpret_cast<const float4*>(a.sv + col + 4));
+              const float sc[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
               uint32_t pk[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float s0 = __ldg(a.sv + col + 2 * e) * kHadScale;
-                const float s1 = __ldg(a.sv + col + 2 * e + 1) * kHadScale;
+                const float s0 = sc[2 * e] * kHadScale;
+                const float s1 = sc[2 * e + 1] * kHadScale;
                 pk[e] = float_to_half_bits(w[2 * e] * s0) |
                         (uint32_t(float_to_half_bits(w[2 * e + 1] * s1)) << 16);
               }
