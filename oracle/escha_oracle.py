@@ -472,6 +472,20 @@ def reconstruct_weight(w_inner, su, sv):
     return w * np.asarray(sv)[None, :]
 
 
+def rms_norm(x, w_stored, eps, stored_minus_one=True):
+    """RMSNorm of each row of x: x / sqrt(mean(x^2) + eps) * w, fp64.
+
+    "Escha-W2 runs on Metal", model-loading paragraph: escha stores RMSNorm
+    weights centred on zero (w - 1), so the weight applied is stored + 1 --
+    except the gated norms inside the linear-attention block, which are
+    stored as they are (stored_minus_one=False).
+    """
+    x = np.asarray(x).astype(np.float64)
+    w = np.asarray(w_stored).astype(np.float64) + (1.0 if stored_minus_one else 0.0)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * w
+
+
 def silu(z):
     return z / (1.0 + np.exp(-z))
 

@@ -454,6 +454,43 @@ def test_half_shape_and_byte_accounting_match_the_pages():
         assert pair_bytes % pair["align_bytes"] == 0
 
 
+
+def test_rms_norm_weight_offset_reproduces_the_pages_table():
+    """The Metal page's table: a stored escha norm weight plus 1 gives the base
+    weight for the offset tensors (residual at bf16 rounding), and the
+    linear-attention gated norm carries no offset.  On a constant input (and
+    eps = 0) RMSNorm returns exactly the applied weight."""
+    for row in golden("rmsnorm_offset_table"):
+        x = np.full((1, 4), 2.5)
+        w = np.full(4, row["escha"])
+        y = O.rms_norm(x, w, 0.0, stored_minus_one=row["offset"])
+        assert np.allclose(y, row["base"], atol=1e-12)
+        assert abs(row["escha"] + (1.0 if row["offset"] else 0.0) - row["base"]) < 1e-9
+        other = O.rms_norm(x, w, 0.0, stored_minus_one=not row["offset"])
+        assert abs(other[0, 0] - row["base"]) > 0.99          # the trap the page describes
+
+
+def test_rms_norm_closed_forms():
+    """x = (3, 4): mean square 12.5; scale invariance; unit RMS for unit weight;
+    a zero row stays zero (eps > 0); brute-force loops on a random case."""
+    y = O.rms_norm(np.array([[3.0, 4.0]]), np.zeros(2), 0.0)
+    assert np.allclose(y, [[3.0 / np.sqrt(12.5), 4.0 / np.sqrt(12.5)]], rtol=1e-15)
+    rng = np.random.default_rng(30)
+    x = rng.normal(size=(3, 64))
+    w = rng.normal(size=64) * 0.1
+    assert np.allclose(O.rms_norm(7.0 * x, w, 0.0), O.rms_norm(x, w, 0.0), rtol=1e-12)
+    u = O.rms_norm(x, np.zeros(64), 0.0)
+    assert np.allclose(np.sqrt(np.mean(u * u, axis=1)), 1.0, rtol=1e-12)
+    assert np.array_equal(O.rms_norm(np.zeros((1, 8)), np.zeros(8), 1e-6), np.zeros((1, 8)))
+    eps = 1e-3
+    ref = np.empty_like(x)
+    for i in range(3):
+        ms = sum(v * v for v in x[i]) / 64
+        for j in range(64):
+            ref[i, j] = x[i, j] / np.sqrt(ms + eps) * (w[j] + 1.0)
+    assert np.allclose(O.rms_norm(x, w, eps), ref, rtol=1e-13)
+
+
 def test_silu_closed_form():
     z = np.array([0.0, 1.0, -1.0, 20.0])
     assert np.allclose(O.silu(z), [0.0, 1 / (1 + np.exp(-1)), -1 / (1 + np.e), 20.0], atol=1e-7)
