@@ -54,6 +54,8 @@ def parse_args():
     p.add_argument("--m", type=int, default=1, help="tokens per step")
     p.add_argument("--shape", default=None, help="in x out (sweep: default 5120x10240; "
                    "prefill: default 5120x17408)")
+    p.add_argument("--norm", action="store_true",
+                   help="mlp: input RMSNorm (weight stored as w - 1) fused into the input rotations")
     p.add_argument("--halves", action="store_true",
                    help="moe: experts stored by halves of 128 intermediate channels, a width "
                         "per half for gate/up and per expert for down, pointer tables")
@@ -145,6 +147,9 @@ def workload_spec(args):
     spec["rounding"] = args.rounding
     if args.rounding == "e4m3":
         spec["name"] += ", E4M3 codebook rounding"
+    if args.norm and spec["kind"] == "mlp":
+        spec["norm"] = True
+        spec["name"] += ", input RMSNorm"
     return spec
 
 
@@ -803,6 +808,10 @@ def main():
     for r in range(n_inst):
         inst = make_instance(spec, spec["seed"] + 7919 * r + 1000003 * rank)
         handles.append(make_handles(spec, inst))
+        if spec.get("norm"):
+            nrng = np.random.default_rng(spec["seed"] + 31 * r)
+            handles[-1][0].set_input_norm(
+                torch.from_numpy(S.make_norm_weight(nrng, spec["layers"][0][0])).to(dev))
         del inst
     rng = np.random.default_rng(spec["seed"] + 17)
     x_host = torch.from_numpy(S.make_activations(rng, m, k_in)).pin_memory()

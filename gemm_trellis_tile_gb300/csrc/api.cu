@@ -272,6 +272,14 @@ escha_status_t escha_linear_check(escha_linear_t h, void* stream) {
   return read_and_clear_error(h->err, static_cast<cudaStream_t>(stream));
 }
 
+escha_status_t escha_mlp_set_input_norm(escha_mlp_t m, const uint16_t* norm_w, float eps,
+                                        int stored_minus_one) {
+  if (!m) return ESCHA_ERR_INVALID_ARG;
+  if (norm_w && !(eps >= 0.0f && eps < 1.0f)) return ESCHA_ERR_INVALID_ARG;
+  if (norm_w && (reinterpret_cast<uintptr_t>(norm_w) & 1u)) return ESCHA_ERR_INVALID_ARG;
+  return mlp_set_input_norm(m, norm_w, eps, stored_minus_one);
+}
+
 escha_status_t escha_mlp_check(escha_mlp_t m, void* stream) {
   if (!m) return ESCHA_ERR_INVALID_ARG;
   return read_and_clear_error(m->err, static_cast<cudaStream_t>(stream));

@@ -59,6 +59,11 @@ struct escha_mlp_s {
   float* part_gate = nullptr;
   float* part_up = nullptr;
   float* part_down = nullptr;
+  // input RMSNorm (escha_mlp_set_input_norm): (w + offset) * su of gate and up
+  int norm_on = 0;
+  float norm_eps = 0.f;
+  float* norm_g_gate = nullptr;
+  float* norm_g_up = nullptr;
   int* err = nullptr;
   escha::GemvSchedule s_gate_up;  // jobs: gate, up
   escha::GemvSchedule s_down;     // job: down
@@ -147,6 +152,8 @@ escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, in
 escha_status_t mlp_init(escha_mlp_s* m, escha_linear_s* gate, escha_linear_s* up,
                         escha_linear_s* down);
 void mlp_free(escha_mlp_s* m);
+escha_status_t mlp_set_input_norm(escha_mlp_s* m, const uint16_t* w, float eps,
+                                  int stored_minus_one);
 escha_status_t mlp_gemv_stage(escha_mlp_s* m, int stage, const uint16_t* x, uint16_t* y, int M,
                               cudaStream_t st);
 escha_status_t mlp_gemv(escha_mlp_s* m, const uint16_t* x, uint16_t* y, int M, cudaStream_t st);

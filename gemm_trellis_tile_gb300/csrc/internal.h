@@ -154,6 +154,13 @@ struct PartRef {
 cudaError_t launch_fold_scales(const uint16_t* r, const float* s, float* out, int n,
                                cudaStream_t st);
 cudaError_t launch_rotate_in_xfrag(const RotInJob* jobs, int njobs, int M, cudaStream_t st);
+// Gated-MLP input rotations with the input RMSNorm: per token m,
+// n = x / sqrt(mean(x^2) + eps); xfrag_gate = had128(n * g_gate), likewise up.
+cudaError_t launch_rotate_in_norm(const uint16_t* x, const float* g_gate, const float* g_up,
+                                  uint32_t* xfrag_gate, uint32_t* xfrag_up, int K, int M, float eps,
+                                  cudaStream_t st);
+cudaError_t launch_fold_norm(const uint16_t* w, float offset, const float* su, float* g, int n,
+                             cudaStream_t st);
 cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t* xh, int M,
                                    int K, cudaStream_t st);
 cudaError_t launch_rotate_out(const PartRef& pr, long long units, int grid, const float* sv,

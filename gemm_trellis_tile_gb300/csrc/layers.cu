@@ -232,6 +232,8 @@ void mlp_free(escha_mlp_s* m) {
   cudaFree(m->part_up);
   cudaFree(m->part_down);
   cudaFree(m->err);
+  cudaFree(m->norm_g_gate);
+  cudaFree(m->norm_g_up);
   cudaFree(m->s_gate_up.d_jobs);
   cudaFree(m->s_down.d_jobs);
 }
@@ -241,6 +243,11 @@ escha_status_t mlp_gemv_stage(escha_mlp_s* m, int stage, const uint16_t* x, uint
   cudaError_t e = cudaSuccess;
   switch (stage) {
     case 0: {
+      if (m->norm_on) {
+        e = launch_rotate_in_norm(x, m->norm_g_gate, m->norm_g_up, m->xfrag_gate, m->xfrag_up,
+                                  m->gate->K, M, m->norm_eps, st);
+        break;
+      }
       RotInJob rj[2] = {{x, m->gate->su, m->xfrag_gate, m->gate->K},
                         {x, m->up->su, m->xfrag_up, m->up->K}};
       e = launch_rotate_in_xfrag(rj, 2, M, st);
@@ -269,6 +276,27 @@ escha_status_t mlp_gemv_stage(escha_mlp_s* m, int stage, const uint16_t* x, uint
       return ESCHA_ERR_INVALID_ARG;
   }
   return from_cuda(e);
+}
+
+escha_status_t mlp_set_input_norm(escha_mlp_s* m, const uint16_t* w, float eps,
+                                  int stored_minus_one) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return ESCHA_ERR_CUDA;  // no call in flight
+  if (!w) {
+    m->norm_on = 0;
+    return ESCHA_OK;
+  }
+  const int K = m->gate->K;
+  escha_status_t s;
+  if (!m->norm_g_gate && (s = dev_alloc(&m->norm_g_gate, K)) != ESCHA_OK) return s;
+  if (!m->norm_g_up && (s = dev_alloc(&m->norm_g_up, K)) != ESCHA_OK) return s;
+  const float off = stored_minus_one ? 1.0f : 0.0f;
+  if (launch_fold_norm(w, off, m->gate->su, m->norm_g_gate, K, 0) != cudaSuccess ||
+      launch_fold_norm(w, off, m->up->su, m->norm_g_up, K, 0) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return ESCHA_ERR_CUDA;
+  m->norm_eps = eps;
+  m->norm_on = 1;
+  return ESCHA_OK;
 }
 
 escha_status_t mlp_gemv(escha_mlp_s* m, const uint16_t* x, uint16_t* y, int M, cudaStream_t st) {

@@ -55,6 +55,76 @@ __global__ void rotate_in_xfrag_kernel(const RotInArgs a) {
   rotate_in_block(J.x, J.su, J.xfrag, J.K, a.M, m, kb, lane);
 }
 
+// Input RMSNorm fused into the gate/up input rotations of a gated MLP: one
+// block per token; n = x / sqrt(mean(x^2) + eps), then
+// xfrag_gate = fp16(had128(n * g_gate)), xfrag_up = fp16(had128(n * g_up)),
+// where g = (stored norm weight + offset) * su was folded when the norm was set.
+constexpr int kNormThreads = 1024;
+constexpr int kNormCached = 2;  // 128-blocks per warp kept in registers between the passes
+__global__ void __launch_bounds__(kNormThreads)
+    rotate_in_norm_kernel(const uint16_t* x, const float* g_gate, const float* g_up,
+                          uint32_t* xfrag_gate, uint32_t* xfrag_up, int K, int M, float eps) {
+  __shared__ float part[kNormThreads / 32];
+  constexpr int W = kNormThreads / 32;
+  pdl_trigger();  // the GEMV may start streaming code; it waits for this kernel's output
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int m = blockIdx.x;
+  const int nb = K / kHad;
+  const uint16_t* xr = x + (size_t)m * K;
+  float cache[kNormCached][4];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormCached; ++i) {
+    const int b = warp + i * W;
+    if (b < nb) {
+      load4_half(xr + b * kHad + 4 * lane, cache[i]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ss += cache[i][q] * cache[i][q];
+    }
+  }
+  for (int b = warp + kNormCached * W; b < nb; b += W) {
+    float v[4];
+    load4_half(xr + b * kHad + 4 * lane, v);
+    ss += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  if (lane == 0) part[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < W; ++w) tot += part[w];
+  const float r = rsqrtf(tot / static_cast<float>(K) + eps);
+  for (int i = 0, b = warp; b < nb; ++i, b += W) {
+    const int k0 = b * kHad + 4 * lane;
+    float v[4];
+    if (i < kNormCached) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = i == 0 ? cache[0][q] : cache[1][q];
+    } else {
+      load4_half(xr + k0, v);
+    }
+    const float4 sg = *reinterpret_cast<const float4*>(g_gate + k0);
+    const float4 su = *reinterpret_cast<const float4*>(g_up + k0);
+    float a[4] = {v[0] * r * sg.x, v[1] * r * sg.y, v[2] * r * sg.z, v[3] * r * sg.w};
+    float c[4] = {v[0] * r * su.x, v[1] * r * su.y, v[2] * r * su.z, v[3] * r * su.w};
+    fwht128_warp(a, lane);
+    fwht128_warp(c, lane);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      xfrag_store(xfrag_gate, M, m, k0 + q, float_to_half_bits(a[q] * kHadScale));
+      xfrag_store(xfrag_up, M, m, k0 + q, float_to_half_bits(c[q] * kHadScale));
+    }
+  }
+}
+
+// g[k] = (w[k] + offset) * su[k]: a stored norm weight folded into an input scale.
+__global__ void fold_norm_kernel(const uint16_t* w, float offset, const float* su, float* g,
+                                 int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) g[i] = (half_bits_to_float(w[i]) + offset) * su[i];
+}
+
 // xh[m, k] = fp16(had128(x * su)), plain row-major (the GEMM's A operand).
 __global__ void rotate_in_plain_kernel(const uint16_t* x, const float* su, uint16_t* xh, int M,
                                        int K) {
@@ -169,6 +239,20 @@ cudaError_t launch_rotate_in_xfrag(const RotInJob* jobs, int njobs, int M, cudaS
   a.njobs = njobs;
   a.M = M;
   rotate_in_xfrag_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_in_norm(const uint16_t* x, const float* g_gate, const float* g_up,
+                                  uint32_t* xfrag_gate, uint32_t* xfrag_up, int K, int M, float eps,
+                                  cudaStream_t st) {
+  rotate_in_norm_kernel<<<M, kNormThreads, 0, st>>>(x, g_gate, g_up, xfrag_gate, xfrag_up, K, M,
+                                                    eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold_norm(const uint16_t* w, float offset, const float* su, float* g, int n,
+                             cudaStream_t st) {
+  fold_norm_kernel<<<(n + 255) / 256, 256, 0, st>>>(w, offset, su, g, n);
   return cudaGetLastError();
 }
 

@@ -65,6 +65,7 @@ _SIGS = {
     "escha_linear_check": (_I, [_P, _P]),
     "escha_moe_check": (_I, [_P, _P]),
     "escha_mlp_check": (_I, [_P, _P]),
+    "escha_mlp_set_input_norm": (_I, [_P, _P, ctypes.c_float, _I]),
     "escha_profile_enable": (_I, [_P, _I, _I]),
     "escha_profile_collect": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "escha_selftest_wait_timeout": (_I, [_I, _P]),
@@ -275,6 +276,16 @@ class MLP:
             check(load().escha_mlp_gemv_stage(self.handle, int(stage), _ptr(x), _ptr(y), m,
                                               _stream(stream)), "escha_mlp_gemv_stage")
         return y
+
+    def set_input_norm(self, norm_w, eps=1e-6, stored_minus_one=True):
+        """Input RMSNorm (weight as stored: fp16 CUDA tensor [in], or None to remove)."""
+        torch = _torch()
+        if norm_w is not None:
+            _dev(norm_w, torch.float16, (self.hidden,))
+        check(load().escha_mlp_set_input_norm(self.handle, _ptr(norm_w), float(eps),
+                                              int(bool(stored_minus_one))),
+              "escha_mlp_set_input_norm")
+        self._norm = norm_w
 
     def check(self, stream=None):
         """The MLP's own device error flag (its launches), then the layers'."""

@@ -50,6 +50,11 @@ def make_mlp(rng, hidden, inter, bits_gate, bits_up, bits_down):
                 down=make_linear(rng, inter, hidden, bits_down, guard=True))
 
 
+def make_norm_weight(rng, n):
+    """An RMSNorm weight as escha stores it (centred on zero: w - 1), fp16."""
+    return rng.normal(0.2, 0.3, n).astype(np.float16)
+
+
 def make_moe_spec(seed, num_experts, hidden, inter, bits_choices=(2, 3, 4)):
     """Routed-expert stack: widths, shared hidden-side vectors and per-expert
     intermediate-side vectors.  Code words are drawn per expert on demand

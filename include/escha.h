@@ -141,6 +141,21 @@ escha_status_t escha_mlp_destroy(escha_mlp_t m);
 escha_status_t escha_mlp_gemv(escha_mlp_t m, const uint16_t* x, uint16_t* y, int M, void* stream);
 
 /*
+ * Input RMSNorm of a gated MLP ("Escha-W2 runs on Metal", model-loading
+ * paragraph): after this call escha_mlp_gemv computes
+ *     n = x / sqrt(mean(x^2) + eps) * w,   y = down( silu(gate(n)) * up(n) )
+ * per token, the norm fused into the input rotations (one launch per call, as
+ * before).  norm_w: DEVICE fp16 [in], the weight as stored; escha stores
+ * RMSNorm weights centred on zero, so with stored_minus_one != 0 the weight
+ * applied is norm_w + 1 (the gated norms inside a linear-attention block carry
+ * no offset: pass 0).  norm_w is read during this call only (folded with the
+ * gate and up input scales); eps in [0, 1).  norm_w = NULL removes the norm.
+ * Synchronises the device.
+ */
+escha_status_t escha_mlp_set_input_norm(escha_mlp_t m, const uint16_t* norm_w, float eps,
+                                        int stored_minus_one);
+
+/*
  * Routed-expert layer (EXLR8 page, "The sharing trick" and the GLM-5.3 expert
  * shapes): E experts, each with gate/up [hidden -> inter] and down [inter ->
  * hidden] trellis matrices at its own width bits[e] in {2,3,4}.  The hidden side
