@@ -511,3 +511,10 @@ def moe_forward(x, experts, ids, weights):
             gate, up, down = experts[int(ids[t, k])]
             y[t] += float(weights[t, k]) * mlp_forward(x[t:t + 1], gate, up, down)[0]
     return y
+
+
+def moe_forward_shared(x, experts, ids, weights, shared):
+    """Routed experts plus the shared expert, which every token uses with
+    weight 1 ([EXLR8] "The sharing trick": the hidden-side rotation is shared
+    by all routed experts and the shared expert).  shared = (gate, up, down)."""
+    return moe_forward(x, experts, ids, weights) + mlp_forward(x, *shared)

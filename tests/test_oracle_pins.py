@@ -491,6 +491,30 @@ def test_rms_norm_closed_forms():
     assert np.allclose(O.rms_norm(x, w, eps), ref, rtol=1e-13)
 
 
+
+def test_moe_shared_expert_is_an_expert_every_token_uses_with_weight_one():
+    """Adding the shared expert equals routing it to every token as a ninth
+    expert of weight 1 (and a zero shared expert changes nothing)."""
+    rng = np.random.default_rng(14)
+
+    def layer(k, n, b):
+        code, rin, rout, s_in, s_out = make_small_layer(rng, k, n, b)
+        return dict(w=O.decode_matrix(code, b), su=O.fold_scales(rin, s_in),
+                    sv=O.fold_scales(rout, s_out))
+    experts = [(layer(128, 256, 2), layer(128, 256, 3), layer(256, 128, 2)) for _ in range(4)]
+    shared = (layer(128, 256, 4), layer(128, 256, 4), layer(256, 128, 4))
+    x = rng.normal(size=(3, 128))
+    ids = np.array([[0, 2], [1, 3], [3, 0]])
+    wts = rng.random((3, 2))
+    y = O.moe_forward_shared(x, experts, ids, wts, shared)
+    ids9 = np.concatenate([ids, np.full((3, 1), 4)], axis=1)
+    w9 = np.concatenate([wts, np.ones((3, 1))], axis=1)
+    assert np.allclose(y, O.moe_forward(x, experts + [shared], ids9, w9), rtol=1e-12)
+    zero = tuple(dict(d, w=np.zeros_like(d["w"])) for d in shared)
+    assert np.allclose(O.moe_forward_shared(x, experts, ids, wts, zero),
+                       O.moe_forward(x, experts, ids, wts), rtol=1e-12, atol=1e-12)
+
+
 def test_silu_closed_form():
     z = np.array([0.0, 1.0, -1.0, 20.0])
     assert np.allclose(O.silu(z), [0.0, 1 / (1 + np.exp(-1)), -1 / (1 + np.e), 20.0], atol=1e-7)
