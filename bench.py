@@ -56,6 +56,8 @@ def parse_args():
                    "prefill: default 5120x17408)")
     p.add_argument("--norm", action="store_true",
                    help="mlp: input RMSNorm (weight stored as w - 1) fused into the input rotations")
+    p.add_argument("--shared", action="store_true",
+                   help="moe: add a shared expert (3-bit) that every token uses with weight 1")
     p.add_argument("--halves", action="store_true",
                    help="moe: experts stored by halves of 128 intermediate channels, a width "
                         "per half for gate/up and per expert for down, pointer tables")
@@ -168,8 +170,9 @@ def _workload_spec(args):
                          "2/3/4-bit per half, down 2/3/4-bit per expert, top-8, M=%d" % args.m)
     if args.workload == "moe":
         return dict(kind="moe", layers=WL.mlp_layers(6144, 2048, (3, 3, 3)), seed=S.seed_for(3),
+                    shared=args.shared,
                     name="routed MoE 256 experts 6144->2048->6144, 2/3/4-bit per expert, top-8, "
-                         "M=%d" % args.m)
+                         "M=%d" % args.m + (", plus a 3-bit shared expert" if args.shared else ""))
     if args.workload == "encode":
         k, n = (int(v) for v in (args.shape or "2048x2048").split("x"))
         bits = 2
@@ -379,6 +382,14 @@ def run_moe(args, spec, rank, world, local):
         moe = escha.MoE(hidden, inter, [c[0] for c in codes], [c[1] for c in codes],
                         [c[2] for c in codes], mspec["bits"], *sidevec)
     moe.set_rounding(spec["rounding"])
+    shared_keep = None
+    if spec.get("shared"):
+        sh = S.make_moe_shared_expert(mspec, bits=3)
+        shared_keep = {k: torch.from_numpy(v).to(dev) for k, v in sh.items() if k != "bits"}
+        t2 = shared_keep
+        moe.set_shared_expert(t2["gate"], t2["up"], t2["down"], 3, t2["rout_gate"],
+                              t2["s_out_gate"], t2["rout_up"], t2["s_out_up"], t2["rin_down"],
+                              t2["s_in_down"])
     rng = np.random.default_rng(spec["seed"] + 29)
     R = 64
     routes = [S.make_routing(rng, m, E, 8) for _ in range(R)]
@@ -397,6 +408,8 @@ def run_moe(args, spec, rank, world, local):
                 b = int(mspec["bits"][e])
                 tot += 2 * WL.code_bytes(hidden, inter, b) + WL.code_bytes(inter, hidden, b)
             tot += 3 * 6 * inter
+        if spec.get("shared"):
+            tot += 2 * WL.code_bytes(hidden, inter, 3) + WL.code_bytes(inter, hidden, 3) + 3 * 6 * inter
         return tot
     rbytes = [route_bytes(r[0]) for r in routes]
     x_host = torch.from_numpy(S.make_activations(rng, m, hidden)).pin_memory()

@@ -472,6 +472,25 @@ escha_status_t escha_moe_create_halves(escha_moe_t* out, int num_experts, int hi
   return ESCHA_OK;
 }
 
+escha_status_t escha_moe_set_shared_expert(escha_moe_t m, const int16_t* gate_code,
+                                           const int16_t* up_code, const int16_t* down_code,
+                                           int bits, const uint16_t* rout_gate,
+                                           const float* s_out_gate, const uint16_t* rout_up,
+                                           const float* s_out_up, const uint16_t* rin_down,
+                                           const float* s_in_down) {
+  if (!m) return ESCHA_ERR_INVALID_ARG;
+  if (m->halves) return ESCHA_ERR_UNSUPPORTED;
+  if (gate_code) {
+    if (!up_code || !down_code || !rout_gate || !rout_up || !rin_down)
+      return ESCHA_ERR_INVALID_ARG;
+    if (!aligned16(gate_code) || !aligned16(up_code) || !aligned16(down_code))
+      return ESCHA_ERR_INVALID_ARG;
+    if (bits < 2 || bits > 4) return ESCHA_ERR_UNSUPPORTED;
+  }
+  return moe_set_shared_expert(m, gate_code, up_code, down_code, bits, rout_gate, s_out_gate,
+                               rout_up, s_out_up, rin_down, s_in_down);
+}
+
 escha_status_t escha_moe_destroy(escha_moe_t m) {
   if (!m) return ESCHA_ERR_INVALID_ARG;
   cudaDeviceSynchronize();

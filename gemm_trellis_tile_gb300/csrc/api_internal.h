@@ -95,6 +95,7 @@ struct escha_moe_s {
   // matrix; the caller's device tables are borrowed and re-read every call.
   int halves = 0;
   int H = 0;
+  int shared_on = 0;  // a shared expert is set (entry E of the whole-matrix tables)
   const uint8_t* const* gate_half = nullptr;  // [E][H] code of each gate half
   const uint8_t* const* up_half = nullptr;    // [E][H]
   const uint8_t* const* down_half = nullptr;  // [E][H] (halves along down's input)
@@ -132,6 +133,11 @@ escha_status_t moe_init_halves(escha_moe_s* h, int E, int hidden, int inter,
                                const uint16_t* rout_hidden, const float* s_out_hidden,
                                cudaStream_t st);
 void moe_free(escha_moe_s* h);
+escha_status_t moe_set_shared_expert(escha_moe_s* h, const int16_t* gate_code,
+                                     const int16_t* up_code, const int16_t* down_code, int bits,
+                                     const uint16_t* rout_gate, const float* s_out_gate,
+                                     const uint16_t* rout_up, const float* s_out_up,
+                                     const uint16_t* rin_down, const float* s_in_down);
 escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, const int32_t* ids,
                               const float* w, uint16_t* y, int M, int topk, cudaStream_t st);
 escha_status_t moe_gemv(escha_moe_s* h, const uint16_t* x, const int32_t* ids, const float* w,

@@ -41,6 +41,8 @@ constexpr int kWarpsPerBlock = 8;
 // Device-side routing state written by moe_plan_kernel.
 // Partial-sum slots per group: device_grid() keeps a group within 5 CTAs.
 constexpr int kMoeSlots = 6;
+// Expert slots of a call: the distinct routed experts, then the shared expert.
+constexpr int kMoeMaxSlots = kMoeMaxDistinct + 1;
 
 struct MoeRoute {
   long long units1;  // gate+up GEMV
@@ -48,9 +50,10 @@ struct MoeRoute {
   int grid1, grid2;
   int n_distinct;
   int pad;
-  int expert[kMoeMaxDistinct];              // expert id of distinct slot d
-  unsigned mask[kMoeMaxDistinct];           // bit m set: token m routes to d
+  int expert[kMoeMaxSlots];                 // expert id of slot d (E: the shared expert)
+  unsigned mask[kMoeMaxSlots];              // bit m set: token m routes to d
   int route[kMoeMaxTokens * kMoeMaxTopk];   // distinct slot of (m, k), -1 if skipped
+  int shared_slot;                          // slot of the shared expert, -1 if none
 };
 
 struct MoePlanArgs {
@@ -60,7 +63,8 @@ struct MoePlanArgs {
   const uint8_t* const* gate_code;
   const uint8_t* const* up_code;
   const uint8_t* const* down_code;
-  const CUtensorMap* code_maps;  // [3][E]: gate, up, down
+  const CUtensorMap* code_maps;  // [3][E + 1]: gate, up, down (entry E: the shared expert)
+  int shared;                    // the shared expert is set: every token uses it
   const int* bits;
   int e4m3;                      // codebook values rounded to E4M3
   const uint32_t* xfrag_hidden;
@@ -189,21 +193,32 @@ __global__ void moe_plan_kernel(const MoePlanArgs a, const MoeRotIn rot) {
   pdl_trigger();  // the GEMV may launch; it waits for this kernel before reading the plan
   if (!plan_block_or_rotate(rot)) return;
   MoeRoute* r = a.route;
-  const int nd = plan_routing(a.ids, a.M, a.topk, a.E, first_slot, r, a.err);
+  const int nrouted = plan_routing(a.ids, a.M, a.topk, a.E, first_slot, r, a.err);
+  // the shared expert takes the slot after the routed ones, for every token
+  if (threadIdx.x == 0) {
+    r->shared_slot = a.shared ? nrouted : -1;
+    if (a.shared) {
+      r->expert[nrouted] = a.E;
+      r->mask[nrouted] = (a.M >= 32) ? 0xFFFFFFFFu : ((1u << a.M) - 1u);
+    }
+  }
+  __syncthreads();
+  const int nd = nrouted + (a.shared ? 1 : 0);
+  const int Es = a.E + 1;  // entries per matrix in the tables
   const int KTg = a.hidden / 16, NGg = a.inter / 128;
   const int KTd = a.inter / 16, NGd = a.hidden / 128;
   const long long ug = (long long)KTg * NGg, ud = (long long)KTd * NGd;
   // Slots past nd keep well-formed shapes (never scheduled: the unit counts stop at nd).
-  for (int d = threadIdx.x; d < kMoeMaxDistinct; d += blockDim.x) {
+  for (int d = threadIdx.x; d < kMoeMaxSlots; d += blockDim.x) {
     const int e = d < nd ? r->expert[d] : 0;
     const int b = a.bits[e];
     a.jobs1[2 * d] = make_job(a.gate_code[e], a.code_maps + e, a.xfrag_hidden,
                               a.part1 + (2 * d) * a.part1_stride, (2 * d) * ug, b, KTg, NGg,
                               a.inter, a.e4m3);
-    a.jobs1[2 * d + 1] = make_job(a.up_code[e], a.code_maps + a.E + e, a.xfrag_hidden,
+    a.jobs1[2 * d + 1] = make_job(a.up_code[e], a.code_maps + Es + e, a.xfrag_hidden,
                                   a.part1 + (2 * d + 1) * a.part1_stride, (2 * d + 1) * ug, b, KTg,
                                   NGg, a.inter, a.e4m3);
-    a.jobs2[d] = make_job(a.down_code[e], a.code_maps + 2 * a.E + e,
+    a.jobs2[d] = make_job(a.down_code[e], a.code_maps + 2 * Es + e,
                           a.xfrag_down + d * a.xdown_stride, a.part2 + d * a.part2_stride, d * ud,
                           b, KTd, NGd, a.hidden, a.e4m3);
   }
@@ -279,6 +294,7 @@ __global__ void moe_plan_halves_kernel(const MoeHalvesPlanArgs a, const MoeRotIn
   if (!plan_block_or_rotate(rot)) return;
   MoeRoute* r = a.route;
   const int nd = plan_routing(a.ids, a.M, a.topk, a.E, first_slot, r, a.err);
+  if (threadIdx.x == 0) r->shared_slot = -1;  // no shared expert for experts stored by halves
   const int H = a.H;
   const int KTg = a.hidden / 16;     // gate/up: units per half job
   const int NGd = a.hidden / 128;    // down: output groups, H units (halves) each
@@ -351,7 +367,7 @@ __global__ void moe_mid_kernel(const MoeMidArgs a) {
   const int rem = static_cast<int>(wid - (long long)d * a.M * NG);
   const int m = rem / NG;
   const int g = rem - m * NG;
-  if (d >= kMoeMaxDistinct) return;
+  if (d >= kMoeMaxSlots) return;
   const MoeRoute* r = a.route;
   if (d >= r->n_distinct) return;
   const int e = r->expert[d];
@@ -442,6 +458,14 @@ __global__ void moe_out_kernel(const MoeOutArgs a) {
       for (int q = 0; q < 4; ++q) v[q] += wk[k + 1] * p1[q];
     }
   }
+  if (r->shared_slot >= 0) {  // the shared expert, weight 1, after the routed ones
+    const GemvJob& j = a.jobs2[r->shared_slot];
+    float ps[4];
+    sum_slots<kMoeSlots>(j.part, j.unit_begin, j.KT, j.N, r->units2, r->grid2, kMoeMaxTokens, m, g,
+                         lane, ps);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] += ps[q];
+  }
   fwht128_warp(v, lane);
   v[0] *= kHadScale * s.x;
   v[1] *= kHadScale * s.y;
@@ -477,11 +501,12 @@ static escha_status_t moe_init_common(escha_moe_s* h, const uint16_t* rin_hidden
   escha_status_t s = ESCHA_OK;
   const int E = h->E, hidden = h->hidden, inter = h->inter;
   const size_t ei = (size_t)E * inter;
+  const size_t ei1 = ei + inter;  // one more row: the shared expert
   if ((s = dev_alloc(&h->su_hidden, hidden)) != ESCHA_OK) return s;
   if ((s = dev_alloc(&h->sv_hidden, hidden)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->sv_gate, ei)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->sv_up, ei)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->su_down, ei)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->sv_gate, ei1)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->sv_up, ei1)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->su_down, ei1)) != ESCHA_OK) return s;
   if (launch_fold_scales(rin_hidden, s_in_hidden, h->su_hidden, hidden, st) != cudaSuccess ||
       launch_fold_scales(rout_hidden, s_out_hidden, h->sv_hidden, hidden, st) != cudaSuccess ||
       launch_fold_scales(rout_gate, s_out_gate, h->sv_gate, static_cast<int>(ei), st) != cudaSuccess ||
@@ -494,11 +519,11 @@ static escha_status_t moe_init_common(escha_moe_s* h, const uint16_t* rin_hidden
   h->part2_stride = (size_t)kMoeSlots * kMoeMaxTokens * hidden;
   if ((s = dev_alloc(&h->xfrag_hidden, (size_t)(hidden / 16) * kMoeMaxTokens * 16)) != ESCHA_OK)
     return s;
-  if ((s = dev_alloc(&h->xfrag_down, h->xdown_stride * kMoeMaxDistinct)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->part1, h->part1_stride * 2 * kMoeMaxDistinct)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->part2, h->part2_stride * kMoeMaxDistinct)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->xfrag_down, h->xdown_stride * kMoeMaxSlots)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->part1, h->part1_stride * 2 * kMoeMaxSlots)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->part2, h->part2_stride * kMoeMaxSlots)) != ESCHA_OK) return s;
   if ((s = dev_alloc(&h->jobs1, jobs1_count)) != ESCHA_OK) return s;
-  if ((s = dev_alloc(&h->jobs2, kMoeMaxDistinct)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->jobs2, kMoeMaxSlots)) != ESCHA_OK) return s;
   unsigned char* rt = nullptr;
   if ((s = dev_alloc(&rt, sizeof(MoeRoute))) != ESCHA_OK) return s;
   h->route = rt;
@@ -523,32 +548,37 @@ escha_status_t moe_init(escha_moe_s* h, int E, int hidden, int inter,
   h->E = E;
   h->hidden = hidden;
   h->inter = inter;
-  std::vector<const uint8_t*> g(E), u(E), d(E);
-  std::vector<int> b(E);
-  for (int e = 0; e < E; ++e) {
-    g[e] = reinterpret_cast<const uint8_t*>(gate_code[e]);
-    u[e] = reinterpret_cast<const uint8_t*>(up_code[e]);
-    d[e] = reinterpret_cast<const uint8_t*>(down_code[e]);
-    b[e] = bits[e];
+  // Tables hold E + 1 entries: entry E is the shared expert
+  // (escha_moe_set_shared_expert); until one is set it repeats expert 0 and
+  // is never scheduled.
+  const int Es = E + 1;
+  std::vector<const uint8_t*> g(Es), u(Es), d(Es);
+  std::vector<int> b(Es);
+  for (int e = 0; e < Es; ++e) {
+    const int src = e < E ? e : 0;
+    g[e] = reinterpret_cast<const uint8_t*>(gate_code[src]);
+    u[e] = reinterpret_cast<const uint8_t*>(up_code[src]);
+    d[e] = reinterpret_cast<const uint8_t*>(down_code[src]);
+    b[e] = bits[src];
   }
-  if ((s = upload(&h->gate_code, g.data(), E)) != ESCHA_OK) return s;
-  if ((s = upload(&h->up_code, u.data(), E)) != ESCHA_OK) return s;
-  if ((s = upload(&h->down_code, d.data(), E)) != ESCHA_OK) return s;
-  if ((s = upload(&h->bits, b.data(), E)) != ESCHA_OK) return s;
+  if ((s = upload(&h->gate_code, g.data(), Es)) != ESCHA_OK) return s;
+  if ((s = upload(&h->up_code, u.data(), Es)) != ESCHA_OK) return s;
+  if ((s = upload(&h->down_code, d.data(), Es)) != ESCHA_OK) return s;
+  if ((s = upload(&h->bits, b.data(), Es)) != ESCHA_OK) return s;
   {
-    // Tensor maps of every expert's three code tensors, [gate | up | down][E].
-    std::vector<CUtensorMap> maps(3 * (size_t)E);
-    for (int e = 0; e < E; ++e) {
+    // Tensor maps of every expert's three code tensors, [gate | up | down][E + 1].
+    std::vector<CUtensorMap> maps(3 * (size_t)Es);
+    for (int e = 0; e < Es; ++e) {
       if (!encode_gemv_code_map(&maps[e], g[e], b[e], hidden / 16, inter / 16) ||
-          !encode_gemv_code_map(&maps[E + e], u[e], b[e], hidden / 16, inter / 16) ||
-          !encode_gemv_code_map(&maps[2 * (size_t)E + e], d[e], b[e], inter / 16, hidden / 16))
+          !encode_gemv_code_map(&maps[Es + e], u[e], b[e], hidden / 16, inter / 16) ||
+          !encode_gemv_code_map(&maps[2 * (size_t)Es + e], d[e], b[e], inter / 16, hidden / 16))
         return ESCHA_ERR_CUDA;
     }
     if ((s = upload(&h->code_maps, maps.data(), maps.size())) != ESCHA_OK) return s;
   }
 
   return moe_init_common(h, rin_hidden, s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up,
-                         rin_down, s_in_down, rout_hidden, s_out_hidden, 2 * kMoeMaxDistinct, st);
+                         rin_down, s_in_down, rout_hidden, s_out_hidden, 2 * kMoeMaxSlots, st);
 }
 
 escha_status_t moe_init_halves(escha_moe_s* h, int E, int hidden, int inter,
@@ -589,6 +619,42 @@ escha_status_t moe_init_halves(escha_moe_s* h, int E, int hidden, int inter,
   return moe_init_common(h, rin_hidden, s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up,
                          rin_down, s_in_down, rout_hidden, s_out_hidden,
                          (size_t)2 * kMoeMaxDistinct * h->H, st);
+}
+
+escha_status_t moe_set_shared_expert(escha_moe_s* h, const int16_t* gate_code,
+                                     const int16_t* up_code, const int16_t* down_code, int bits,
+                                     const uint16_t* rout_gate, const float* s_out_gate,
+                                     const uint16_t* rout_up, const float* s_out_up,
+                                     const uint16_t* rin_down, const float* s_in_down) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return ESCHA_ERR_CUDA;  // no call in flight
+  if (!gate_code) {
+    h->shared_on = 0;
+    return ESCHA_OK;
+  }
+  const int E = h->E, Es = E + 1, hidden = h->hidden, inter = h->inter;
+  const uint8_t* g = reinterpret_cast<const uint8_t*>(gate_code);
+  const uint8_t* u = reinterpret_cast<const uint8_t*>(up_code);
+  const uint8_t* d = reinterpret_cast<const uint8_t*>(down_code);
+  CUtensorMap maps[3];
+  if (!encode_gemv_code_map(&maps[0], g, bits, hidden / 16, inter / 16) ||
+      !encode_gemv_code_map(&maps[1], u, bits, hidden / 16, inter / 16) ||
+      !encode_gemv_code_map(&maps[2], d, bits, inter / 16, hidden / 16))
+    return ESCHA_ERR_CUDA;
+  bool ok = cudaMemcpy(h->gate_code + E, &g, sizeof(g), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(h->up_code + E, &u, sizeof(u), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(h->down_code + E, &d, sizeof(d), cudaMemcpyHostToDevice) == cudaSuccess &&
+            cudaMemcpy(h->bits + E, &bits, sizeof(int), cudaMemcpyHostToDevice) == cudaSuccess;
+  for (int p = 0; ok && p < 3; ++p)
+    ok = cudaMemcpy(h->code_maps + (size_t)p * Es + E, &maps[p], sizeof(CUtensorMap),
+                    cudaMemcpyHostToDevice) == cudaSuccess;
+  const size_t off = (size_t)E * inter;
+  ok = ok && launch_fold_scales(rout_gate, s_out_gate, h->sv_gate + off, inter, 0) == cudaSuccess &&
+       launch_fold_scales(rout_up, s_out_up, h->sv_up + off, inter, 0) == cudaSuccess &&
+       launch_fold_scales(rin_down, s_in_down, h->su_down + off, inter, 0) == cudaSuccess &&
+       cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) return ESCHA_ERR_CUDA;
+  h->shared_on = 1;
+  return ESCHA_OK;
 }
 
 void moe_free(escha_moe_s* h) {
@@ -671,6 +737,7 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       pa.up_code = h->up_code;
       pa.down_code = h->down_code;
       pa.code_maps = h->code_maps;
+      pa.shared = h->shared_on;
       pa.e4m3 = h->rounding == ESCHA_ROUND_E4M3 ? 1 : 0;
       pa.bits = h->bits;
       pa.xfrag_hidden = h->xfrag_hidden;
@@ -713,7 +780,8 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       ma.M = M;
       ma.inter = h->inter;
       const long long mid_warps =
-          (long long)std::min(kMoeMaxDistinct, M * topk) * M * (h->inter / kHad);
+          (long long)(std::min(kMoeMaxDistinct, M * topk) + (h->shared_on ? 1 : 0)) * M *
+          (h->inter / kHad);
       PdlLaunch pl(blocks_for(mid_warps), 32 * kWarpsPerBlock, 0, st);
       e = cudaLaunchKernelEx(&pl.cfg, moe_mid_kernel, ma);
       break;

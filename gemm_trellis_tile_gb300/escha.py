@@ -58,6 +58,7 @@ _SIGS = {
     "escha_moe_create_halves": (_I, [ctypes.POINTER(_P), _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                      _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "escha_moe_destroy": (_I, [_P]),
+    "escha_moe_set_shared_expert": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "escha_linear_moe_gemv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P]),
     "escha_linear_moe_gemv_stage": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _P]),
     "escha_linear_set_rounding": (_I, [_P, _I]),
@@ -385,6 +386,21 @@ class MoE:
                                                      topk, _stream(stream)),
                   "escha_linear_moe_gemv_stage")
         return y
+
+    def set_shared_expert(self, gate_code, up_code, down_code, bits, rout_gate, s_out_gate,
+                          rout_up, s_out_up, rin_down, s_in_down):
+        """Shared expert (CUDA tensors; codes borrowed), or gate_code=None to remove it."""
+        if gate_code is None:
+            check(load().escha_moe_set_shared_expert(self.handle, None, None, None, 0, None, None,
+                                                     None, None, None, None),
+                  "escha_moe_set_shared_expert")
+            self._shared = None
+            return
+        self._shared = (gate_code, up_code, down_code)
+        check(load().escha_moe_set_shared_expert(
+            self.handle, _ptr(gate_code), _ptr(up_code), _ptr(down_code), int(bits),
+            _ptr(rout_gate), _ptr(s_out_gate), _ptr(rout_up), _ptr(s_out_up), _ptr(rin_down),
+            _ptr(s_in_down)), "escha_moe_set_shared_expert")
 
     def check(self, stream=None):
         return load().escha_moe_check(self.handle, _stream(stream))

@@ -101,6 +101,26 @@ def make_moe_expert_codes(spec, e):
 
 
 
+def make_moe_shared_expert(spec, bits=4):
+    """The shared expert of a routed-expert stack: code words and its own
+    intermediate-side vectors, drawn like a routed expert's (rout vectors with
+    the fp16 range guard)."""
+    rng = np.random.default_rng([spec["seed"], 4])
+    h, i = spec["hidden"], spec["inter"]
+    kg = overflow_guard_shift(h)
+
+    def code(k, n):
+        return rng.integers(-32768, 32768, size=(k // 16, n // 16, 16 * bits), dtype=np.int16)
+    return dict(
+        bits=bits, gate=code(h, i), up=code(h, i), down=code(i, h),
+        rout_gate=(rng.normal(1.0, 0.1, i) * 2.0 ** (-kg)).astype(np.float16),
+        s_out_gate=rng.uniform(0.98, 1.02, i).astype(np.float32),
+        rout_up=(rng.normal(1.0, 0.1, i) * 2.0 ** (-kg)).astype(np.float16),
+        s_out_up=rng.uniform(0.98, 1.02, i).astype(np.float32),
+        rin_down=rng.normal(1.0, 0.1, i).astype(np.float16),
+        s_in_down=rng.uniform(0.98, 1.02, i).astype(np.float32))
+
+
 def make_moe_half_spec(seed, num_experts, hidden, inter, bits_choices=(2, 3, 4)):
     """Routed-expert stack stored by halves of 128 intermediate channels: the
     side vectors of make_moe_spec, a width per half for gate and for up

@@ -224,6 +224,27 @@ escha_status_t escha_moe_create_halves(escha_moe_t* out, int num_experts, int hi
 escha_status_t escha_moe_destroy(escha_moe_t m);
 
 /*
+ * Shared expert of a routed-expert layer (EXLR8 page, "The sharing trick": the
+ * hidden-side rotation is shared by all routed experts and the shared
+ * expert).  After this call escha_linear_moe_gemv adds, for every token, the
+ * shared expert's down(silu(gate(x)) * up(x)) with weight 1 to the weighted
+ * sum of its routed experts.  The shared expert has the routed experts'
+ * shapes and uses the layer's hidden-side vectors; its intermediate side is
+ * its own.  gate_code, up_code [hidden/16, inter/16, 16*bits], down_code
+ * [inter/16, hidden/16, 16*bits]: DEVICE, borrowed; rout_gate, rout_up,
+ * rin_down fp16 [inter]; s_out_gate, s_out_up, s_in_down fp32 [inter] (may be
+ * NULL = 1.0), read during this call.  gate_code = NULL removes the shared
+ * expert.  Handles from escha_moe_create only (ESCHA_ERR_UNSUPPORTED for
+ * experts stored by halves).  Synchronises the device.
+ */
+escha_status_t escha_moe_set_shared_expert(escha_moe_t m, const int16_t* gate_code,
+                                           const int16_t* up_code, const int16_t* down_code,
+                                           int bits, const uint16_t* rout_gate,
+                                           const float* s_out_gate, const uint16_t* rout_up,
+                                           const float* s_out_up, const uint16_t* rin_down,
+                                           const float* s_in_down);
+
+/*
  * y[m] = sum_k expert_w[m,k] * down_e( silu(gate_e(x[m])) * up_e(x[m]) ),
  * e = expert_ids[m,k].  1 <= M <= 8, 1 <= topk <= 8; ids in [0, E) and distinct
  * within a token (duplicates are summed, out-of-range ids are skipped and set

@@ -46,6 +46,8 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
         assert lib.escha_linear_moe_gemv_stage(None, s, None, None, None, None, 1, 8, None) == 1
     assert lib.escha_mlp_create(ctypes.byref(h), None, None, None) == 1
     assert lib.escha_mlp_set_input_norm(None, None, ctypes.c_float(1e-6), 1) == 1
+    assert lib.escha_moe_set_shared_expert(None, None, None, None, 2, None, None, None, None,
+                                           None, None) == 1
     assert lib.escha_linear_check(None, None) == 1
     assert lib.escha_profile_enable(None, 0, 1) == 1
     assert lib.escha_selftest_wait_timeout(0, None) == 1

@@ -171,3 +171,66 @@ def test_moe_stages_compose_to_the_full_call():
     with pytest.raises(escha.EschaError) as e:
         moe.gemv(x, ids, w, staged, stage=escha.MoE.STAGES)
     assert e.value.status == 1
+
+
+def _shared_layers(spec, sh):
+    su_h = O.fold_scales(spec["rin_hidden"], spec["s_in_hidden"])
+    sv_h = O.fold_scales(spec["rout_hidden"], spec["s_out_hidden"])
+    b = sh["bits"]
+    return (dict(w=O.decode_matrix(sh["gate"], b), su=su_h,
+                 sv=O.fold_scales(sh["rout_gate"], sh["s_out_gate"])),
+            dict(w=O.decode_matrix(sh["up"], b), su=su_h,
+                 sv=O.fold_scales(sh["rout_up"], sh["s_out_up"])),
+            dict(w=O.decode_matrix(sh["down"], b),
+                 su=O.fold_scales(sh["rin_down"], sh["s_in_down"]), sv=sv_h))
+
+
+def _set_shared(moe, sh):
+    t = {k: torch.from_numpy(v).cuda() for k, v in sh.items() if k != "bits"}
+    moe.set_shared_expert(t["gate"], t["up"], t["down"], sh["bits"], t["rout_gate"],
+                          t["s_out_gate"], t["rout_up"], t["s_out_up"], t["rin_down"],
+                          t["s_in_down"])
+    return t
+
+
+@pytest.mark.parametrize("m,topk", [(1, 8), (4, 8), (8, 8), (3, 2)])
+def test_moe_shared_expert_matches_oracle(m, topk):
+    """Routed experts plus the shared expert; at M = 8, top-8 with 64 distinct
+    experts the shared expert takes the 65th slot."""
+    from gemm_trellis_tile_gb300 import escha
+    E = 96 if m == 8 else 16
+    spec = S.make_moe_spec(3700 + m, E, 512, 256)
+    rng = np.random.default_rng(3710 + m * 10 + topk)
+    x = S.make_activations(rng, m, spec["hidden"])
+    if m == 8:
+        ids = rng.permutation(E)[:64].reshape(8, 8).astype(np.int32)  # 64 distinct experts
+        _, w = S.make_routing(rng, m, E, topk)
+    else:
+        ids, w = S.make_routing(rng, m, E, topk)
+    used = sorted(set(ids.reshape(-1).tolist()))
+    codes = {e: S.make_moe_expert_codes(spec, e) for e in used}
+    moe = escha.MoE.from_arrays(spec, codes)
+    sh = S.make_moe_shared_expert(spec)
+    keep = _set_shared(moe, sh)
+    y = _run(moe, x, ids, w)
+    assert moe.check() == 0
+    experts = {e: _expert_layers(spec, e, codes[e]) for e in used}
+    ref = O.moe_forward_shared(x, experts, ids, w, _shared_layers(spec, sh))
+    assert rel_l2(y, ref) <= REL_L2_TOL
+    del keep
+
+
+def test_moe_shared_expert_removed_restores_routed_only():
+    spec, moe, experts = _small(3800)
+    rng = np.random.default_rng(3801)
+    x = torch.from_numpy(S.make_activations(rng, 2, spec["hidden"])).cuda()
+    ids, w = S.make_routing(rng, 2, spec["num_experts"], 8)
+    ids, w = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+    plain = moe.gemv(x, ids, w)
+    keep = _set_shared(moe, S.make_moe_shared_expert(spec, bits=2))
+    with_shared = moe.gemv(x, ids, w)
+    moe.set_shared_expert(None, None, None, 0, None, None, None, None, None, None)
+    again = moe.gemv(x, ids, w)
+    torch.cuda.synchronize()
+    assert torch.equal(plain, again) and not torch.equal(plain, with_shared)
+    del keep
