@@ -40,11 +40,17 @@ namespace {
 constexpr int kUPS = 16;    // units per pipeline stage
 constexpr int kCW = 8;      // consumer warps per group = tiles per unit
 constexpr int kGroups = 3;  // consumer groups = unit ranges per CTA
-constexpr int kStages = 6;  // ring depth; stage s serves group s % kGroups
+// Ring depth (stage s serves group s % kGroups): three stages per group when
+// one token block's activation fragments leave room (216 KB), else two.
+template <int TB>
+__host__ __device__ constexpr int stages_for() {
+  return TB == 1 ? 9 : 6;
+}
 constexpr int kConsumers = kCW * kGroups * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kCodeStageBytes = kUPS * kCW * 128;  // sized for bits = 4
-static_assert(kStages % kGroups == 0, "a stage must always serve the same group");
+static_assert(stages_for<1>() % kGroups == 0 && stages_for<2>() % kGroups == 0,
+              "a stage must always serve the same group");
 
 // Activation fragments of a stage: kUPS units x M tokens x 64 bytes (M <= 8 TB).
 template <int TB>
@@ -53,7 +59,7 @@ __host__ __device__ constexpr int xf_stage_bytes() {
 }
 template <int TB>
 __host__ __device__ constexpr int gemv_smem_bytes() {
-  return kStages * (kCodeStageBytes + xf_stage_bytes<TB>()) + 2 * kStages * 8;
+  return stages_for<TB>() * (kCodeStageBytes + xf_stage_bytes<TB>()) + 2 * stages_for<TB>() * 8;
 }
 
 constexpr int kInlineJobs = 2;
@@ -274,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const GemvJob* const jobs = a.n_inline > 0 ? a.inline_jobs : a.jobs;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* codes = smem;
+  constexpr int kStages = stages_for<TB>();
   uint8_t* xfs = smem + kStages * kCodeStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(xfs + kStages * xf_stage_bytes<TB>());
   const int warp = threadIdx.x >> 5;
