@@ -7,25 +7,24 @@
 // "Codebook: cb=1") and fed to the tensor cores.
 //
 // Kernel layout (persistent, one CTA per SM):
-//   warp 0      producer: streams each stage's code words (16 k-tile rows x 8
-//               tile columns, one 2-D TMA copy) and the matching activation
-//               fragments into a shared-memory ring, completing on mbarriers.
-//   warps 1..24 consumers, three groups of eight.  Each group owns one of the
+//   warps 0..2  producers, one per consumer group: stream each stage's code
+//               words (16 k-tile rows x 8 tile columns, one 2-D TMA copy) and
+//               the matching activation fragments into the group's stages of
+//               a shared-memory ring, completing on mbarriers.
+//   warps 3..26 consumers, three groups of eight.  Each group owns one of the
 //               launch's contiguous unit ranges (CTA b of C: ranges b, b + C,
-//               b + 2C) and two ring
-//               stages; in a group, warp w owns output tile column w of the
-//               current 128-channel group.  Per unit it reads its tile's two
-//               words per lane, decodes eight weights per lane, and issues
-//               m16n8k16 MMAs with the weight tile as A (rows = output
-//               channels) and up to 8 tokens as B; a second token block
-//               handles 9..16 tokens.
-// The producer serves the three groups' stages in turn (lanes 0..2 of warp 0,
-// one range each), which keeps them
-// within a stage of each other.  (Separate CTAs on one SM drift apart: the
-// warp scheduler favours the oldest CTA, whose ring runs ahead while the
-// youngest one's work piles up at the end of the launch, when the SM is no
-// longer busy.)  A TMA copy costs the issuing CTA a roughly fixed time however
-// small it is, so each full stage is one 2-D copy of 8-16 KB.
+//               b + 2C) and three ring stages (two with 9..16 tokens); in a
+//               group, warp w owns output tile column w of the current
+//               128-channel group.  Per unit it reads its tile's two words per
+//               lane, decodes eight weights per lane, and issues m16n8k16 MMAs
+//               with the weight tile as A (rows = output channels) and up to 8
+//               tokens as B; a second token block handles 9..16 tokens.
+// The three groups share one CTA rather than running as three CTAs per SM:
+// separate CTAs on one SM drift apart (the warp scheduler favours the oldest
+// CTA, whose ring runs ahead while the youngest one's work piles up at the end
+// of the launch, when the SM is no longer busy).  A TMA copy costs the issuing
+// thread a roughly fixed time however small it is, so each full stage is one
+// 2-D copy of 8-16 KB.
 #include "common.cuh"
 #include "internal.h"
 #include "tensor_map.h"
@@ -47,7 +46,7 @@ __host__ __device__ constexpr int stages_for() {
   return TB == 1 ? 9 : 6;
 }
 constexpr int kConsumers = kCW * kGroups * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kThreads = kConsumers + 32 * kGroups;  // one producer warp per group
 constexpr int kCodeStageBytes = kUPS * kCW * 128;  // sized for bits = 4
 static_assert(stages_for<1>() % kGroups == 0 && stages_for<2>() % kGroups == 0,
               "a stage must always serve the same group");
@@ -307,15 +306,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Lane q < kGroups walks range blockIdx.x + q*C and fills its group's
-    // stages; the lanes advance together, so the groups are served in turn.
-    // A full stage is one tensor copy, a partial one (end of a segment or of
-    // the range) one copy per k-tile row.
-    const int q = lane;
+  if (warp < kGroups) {
+    // ------------------------------------------------------------ producers
+    // Lane 0 of warp q walks range blockIdx.x + q*C and fills group q's
+    // stages, independently of the other groups' producers.  A full stage is
+    // one tensor copy, a partial one (end of a segment or of the range) one
+    // copy per k-tile row.
+    const int q = warp;
     const int r = static_cast<int>(blockIdx.x) + q * C;
-    const bool mine = q < kGroups && r < G;
+    const bool mine = lane == 0 && r < G;
     ChunkIter it;
     if (mine) it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G), a.job_units);
     const uint64_t pol = policy_evict_first();
@@ -394,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  const int q = (warp - 1) / kCW;       // group: unit range blockIdx.x + q*C
-  const int wt = (warp - 1) - q * kCW;  // tile column within a unit
+  const int q = (warp - kGroups) / kCW;       // group: unit range blockIdx.x + q*C
+  const int wt = (warp - kGroups) - q * kCW;  // tile column within a unit
   const int r = static_cast<int>(blockIdx.x) + q * C;
   if (r >= G) return;
   ChunkIter it;
