@@ -39,16 +39,33 @@ namespace {
 constexpr int kUPS = 16;    // units per pipeline stage
 constexpr int kCW = 8;      // consumer warps per group = tiles per unit
 constexpr int kGroups = 3;  // consumer groups = unit ranges per CTA
-// Ring depth (stage s serves group s % kGroups): three stages per group when
-// one token block's activation fragments leave room (216 KB), else two.
-template <int TB>
+// Storage layouts a launch can serve, fixed at compile time (see below).
+constexpr int kModeWhole = kGemvWhole;
+constexpr int kModeColHalves = kGemvColHalves;
+constexpr int kModeRowHalves = kGemvRowHalves;
+
+// Per layout, measured: whole matrices run best with one producer warp per
+// consumer group and, with one token block, three ring stages per group
+// (216 KB); the two layouts of experts stored by halves, whose jobs change
+// every few stages, with one producer warp (a lane per group) and two stages
+// per group.  Stage s serves group s % kGroups.
+template <int MODE>
+__host__ __device__ constexpr int producer_warps() {
+  return MODE == kModeWhole ? kGroups : 1;
+}
+template <int TB, int MODE>
 __host__ __device__ constexpr int stages_for() {
-  return TB == 1 ? 9 : 6;
+  return (TB == 1 && MODE == kModeWhole) ? 9 : 6;
 }
 constexpr int kConsumers = kCW * kGroups * 32;
-constexpr int kThreads = kConsumers + 32 * kGroups;  // one producer warp per group
+template <int MODE>
+__host__ __device__ constexpr int threads_for() {
+  return kConsumers + 32 * producer_warps<MODE>();
+}
 constexpr int kCodeStageBytes = kUPS * kCW * 128;  // sized for bits = 4
-static_assert(stages_for<1>() % kGroups == 0 && stages_for<2>() % kGroups == 0,
+static_assert(stages_for<1, kModeWhole>() % kGroups == 0 &&
+                  stages_for<2, kModeWhole>() % kGroups == 0 &&
+                  stages_for<1, kModeColHalves>() % kGroups == 0,
               "a stage must always serve the same group");
 
 // Activation fragments of a stage: kUPS units x M tokens x 64 bytes (M <= 8 TB).
@@ -56,9 +73,10 @@ template <int TB>
 __host__ __device__ constexpr int xf_stage_bytes() {
   return kUPS * TB * 512;
 }
-template <int TB>
+template <int TB, int MODE>
 __host__ __device__ constexpr int gemv_smem_bytes() {
-  return stages_for<TB>() * (kCodeStageBytes + xf_stage_bytes<TB>()) + 2 * stages_for<TB>() * 8;
+  return stages_for<TB, MODE>() * (kCodeStageBytes + xf_stage_bytes<TB>()) +
+         2 * stages_for<TB, MODE>() * 8;
 }
 
 constexpr int kInlineJobs = 2;
@@ -268,18 +286,15 @@ __device__ __forceinline__ void consume_dispatch(int key, const uint8_t* cs, con
 // whose stage rows are contiguous (one 1-D bulk copy); kModeRowHalves, every
 // job is stored by input halves (one unit = 8 k-tile rows, one 2-D copy per
 // unit through the half's tensor map).
-constexpr int kModeWhole = kGemvWhole;
-constexpr int kModeColHalves = kGemvColHalves;
-constexpr int kModeRowHalves = kGemvRowHalves;
-
 template <int TB, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for<MODE>(), 1)
     trellis_gemv_kernel(const __grid_constant__ GemvArgs a) {
   constexpr int RPU = MODE == kModeRowHalves ? 8 : 1;  // k-tile rows per unit
   const GemvJob* const jobs = a.n_inline > 0 ? a.inline_jobs : a.jobs;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* codes = smem;
-  constexpr int kStages = stages_for<TB>();
+  constexpr int kStages = stages_for<TB, MODE>();
+  constexpr int PW = producer_warps<MODE>();
   uint8_t* xfs = smem + kStages * kCodeStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(xfs + kStages * xf_stage_bytes<TB>());
   const int warp = threadIdx.x >> 5;
@@ -306,15 +321,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  if (warp < kGroups) {
+  if (warp < PW) {
     // ------------------------------------------------------------ producers
     // Lane 0 of warp q walks range blockIdx.x + q*C and fills group q's
     // stages, independently of the other groups' producers.  A full stage is
     // one tensor copy, a partial one (end of a segment or of the range) one
     // copy per k-tile row.
-    const int q = warp;
+    // one warp per group (lane 0), or one warp with a lane per group
+    const int q = PW == 1 ? lane : warp;
     const int r = static_cast<int>(blockIdx.x) + q * C;
-    const bool mine = lane == 0 && r < G;
+    const bool mine = (PW == 1 ? q < kGroups : lane == 0) && r < G;
     ChunkIter it;
     if (mine) it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G), a.job_units);
     const uint64_t pol = policy_evict_first();
@@ -393,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  const int q = (warp - kGroups) / kCW;       // group: unit range blockIdx.x + q*C
-  const int wt = (warp - kGroups) - q * kCW;  // tile column within a unit
+  const int q = (warp - PW) / kCW;       // group: unit range blockIdx.x + q*C
+  const int wt = (warp - PW) - q * kCW;  // tile column within a unit
   const int r = static_cast<int>(blockIdx.x) + q * C;
   if (r >= G) return;
   ChunkIter it;
@@ -493,7 +509,7 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(trellis_gemv_kernel<TB, kModeWhole>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gemv_smem_bytes<TB>());
+                                         gemv_smem_bytes<TB, kModeWhole>());
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -518,8 +534,8 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   a.cb_xor = kMcgXor;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s.ctas);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = gemv_smem_bytes<TB>();
+  cfg.blockDim = dim3(threads_for<kModeWhole>());
+  cfg.dynamicSmemBytes = gemv_smem_bytes<TB, kModeWhole>();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -561,11 +577,11 @@ int gemv_ranges_per_sm() {
   int n = 0;
   if (cudaFuncSetAttribute(trellis_gemv_kernel<2, kModeWhole>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           gemv_smem_bytes<2>()) != cudaSuccess)
+                           gemv_smem_bytes<2, kModeWhole>()) != cudaSuccess)
     return kGroups;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, trellis_gemv_kernel<2, kModeWhole>,
-                                                    kThreads,
-                                                    gemv_smem_bytes<2>()) != cudaSuccess)
+                                                    threads_for<kModeWhole>(),
+                                                    gemv_smem_bytes<2, kModeWhole>()) != cudaSuccess)
     return kGroups;
   return kGroups * std::max(1, n);
 }
@@ -606,8 +622,11 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
   auto kern = layout == kGemvColHalves   ? trellis_gemv_kernel<1, kModeColHalves>
               : layout == kGemvRowHalves ? trellis_gemv_kernel<1, kModeRowHalves>
                                          : trellis_gemv_kernel<1, kModeWhole>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       gemv_smem_bytes<1>());
+  const int smem = layout == kGemvWhole ? gemv_smem_bytes<1, kModeWhole>()
+                                        : gemv_smem_bytes<1, kModeColHalves>();
+  const int threads = layout == kGemvWhole ? threads_for<kModeWhole>()
+                                           : threads_for<kModeColHalves>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   GemvArgs a;
   a.jobs = d_jobs;
@@ -624,7 +643,7 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
   a.limit_ns = kWaitLimitNs;
   a.cb_mask = kMcgMask;
   a.cb_xor = kMcgXor;
-  PdlLaunch pl((max_grid + kGroups - 1) / kGroups, kThreads, gemv_smem_bytes<1>(), st);
+  PdlLaunch pl((max_grid + kGroups - 1) / kGroups, threads, smem, st);
   return cudaLaunchKernelEx(&pl.cfg, kern, a);
 }
 
