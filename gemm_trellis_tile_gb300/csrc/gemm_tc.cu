@@ -611,13 +611,9 @@ __global__ void gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
 
 template <int BITS, bool E4M3>
 cudaError_t launch_gemm_bits(const CUtensorMap& map, const GemmArgs& a, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(trellis_gemm_kernel<BITS, E4M3>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(trellis_gemm_kernel<BITS, E4M3>),
+                                 kSmemBytes);
+  if (e != cudaSuccess) return e;
   trellis_gemm_kernel<BITS, E4M3><<<a.grid, kThreadsG, kSmemBytes, st>>>(map, a);
   return cudaGetLastError();
 }

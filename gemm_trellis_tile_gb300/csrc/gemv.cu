@@ -505,14 +505,9 @@ __global__ void wait_selftest_kernel(int* err, uint64_t limit_ns) {
 
 template <int TB>
 cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(trellis_gemv_kernel<TB, kModeWhole>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gemv_smem_bytes<TB, kModeWhole>());
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(trellis_gemv_kernel<TB, kModeWhole>),
+                                 gemv_smem_bytes<TB, kModeWhole>());
+  if (e != cudaSuccess) return e;
   GemvArgs a;
   a.jobs = s.d_jobs;
   a.n_inline = 0;
@@ -626,7 +621,7 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
                                         : gemv_smem_bytes<1, kModeColHalves>();
   const int threads = layout == kGemvWhole ? threads_for<kModeWhole>()
                                            : threads_for<kModeColHalves>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   GemvArgs a;
   a.jobs = d_jobs;

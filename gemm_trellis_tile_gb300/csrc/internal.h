@@ -64,6 +64,10 @@ constexpr int kMoeMaxDistinct = kMoeMaxTokens * kMoeMaxTopk;
 constexpr int kMoeMaxExperts = 4096;
 constexpr int kMinUnitsPerCta = 8;
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device, bytes); thread-safe.
+cudaError_t set_smem_limit(const void* func, int bytes);
+
 int gemv_ranges_per_sm();
 // Fill unit_begin, units, grid and max_slots for the given jobs.
 void plan_gemv(GemvSchedule& s, int num_sms, int ranges_per_sm);

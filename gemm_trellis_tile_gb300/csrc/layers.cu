@@ -12,10 +12,27 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
+#include <set>
+#include <tuple>
 
 #include "api_internal.h"
 
 namespace escha {
+
+cudaError_t set_smem_limit(const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::set<std::tuple<const void*, int, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(func, dev, bytes);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
+}
 
 template <typename T>
 escha_status_t dev_alloc(T** p, size_t count) {
