@@ -624,7 +624,7 @@ def run_prefill(args, spec, rank, world, local):
         "e2e": {"value": e_steps * flops / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(y_host.numel() * 2)},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": prefill_launches(m, k, n, props_sms(dev)) * args.steps,
         "clocks": clocks,
     }
     if rank == 0:
@@ -764,6 +764,26 @@ def run_encode(args, spec, rank, world, local):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def props_sms(dev):
+    import torch
+    return torch.cuda.get_device_properties(dev).multi_processor_count
+
+
+def prefill_launches(m, k, n, sms):
+    """Launches of one prefill call: the input rotation, the GEMM, and the
+    fix-up kernel when stream-K splits a 512 x 128 tile between CTAs (the
+    GEMM's own rule: at least 16 K-blocks per CTA, at most one CTA per SM)."""
+    kb = k // 64
+    tiles = -(-m // 512) * (n // 128)
+    units = tiles * kb
+    grid = max(1, min(sms, units // 16))
+
+    def owner(u):
+        return ((u + 1) * grid - 1) // units
+    split = any(owner(t * kb) != owner(t * kb + kb - 1) for t in range(tiles))
+    return 3 if split else 2
 
 
 def make_handles(spec, inst):
