@@ -13,8 +13,11 @@ HBM copy bandwidth; `e2e` is the same metric through the C ABI with host
 buffers and the copies inside the timed region; `cpu_baseline` is the CPU
 oracle on a bounded sample of the same workload.
 
-Other workloads (--workload linear512 | sweep) print the same line for their
-own shapes.
+Other workloads print the same line for their own shapes and metric:
+--workload linear512 | sweep (--m, --shape) | moe (--m, --halves, --shared)
+| prefill (TFLOP/s; --shape) | encode (weights/s); --norm adds the MLP's
+input RMSNorm, --rounding e4m3 the EXLR8 codebook rounding.  --impl
+reference times the CPU oracle on a bounded sample of the same workload.
 """
 
 import argparse
