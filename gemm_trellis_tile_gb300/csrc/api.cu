@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <cstdlib>
 #include <new>
 #include <utility>
 #include <vector>
@@ -151,6 +152,23 @@ escha_status_t upload_jobs(GemvSchedule& s) {
   return ESCHA_OK;
 }
 
+// ESCHA_SYNC_DEBUG=1 in the environment (read once): every compute call
+// synchronises its stream after launching and reports an asynchronous CUDA
+// error at that call instead of a later one.
+static bool sync_debug() {
+  static const bool on = [] {
+    const char* v = std::getenv("ESCHA_SYNC_DEBUG");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
+escha_status_t after_launch(escha_status_t s, cudaStream_t st) {
+  if (s != ESCHA_OK || !sync_debug()) return s;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ESCHA_ERR_CUDA;
+  return from_cuda(cudaGetLastError());
+}
+
 escha_status_t read_and_clear_error(int* d_err, cudaStream_t st) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return ESCHA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return ESCHA_ERR_CUDA;
@@ -258,13 +276,15 @@ static bool gemv_args_ok(const void* h, const void* x, const void* y, int M) {
 escha_status_t escha_linear_gemv(escha_linear_t h, const uint16_t* x, uint16_t* y, int M,
                                  void* stream) {
   if (!gemv_args_ok(h, x, y, M)) return ESCHA_ERR_INVALID_ARG;
-  return linear_gemv(h, x, y, M, static_cast<cudaStream_t>(stream));
+  return after_launch(linear_gemv(h, x, y, M, static_cast<cudaStream_t>(stream)),
+                      static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_linear_gemv_stage(escha_linear_t h, int stage, const uint16_t* x,
                                        uint16_t* y, int M, void* stream) {
   if (!gemv_args_ok(h, x, y, M)) return ESCHA_ERR_INVALID_ARG;
-  return linear_gemv_stage(h, stage, x, y, M, static_cast<cudaStream_t>(stream));
+  return after_launch(linear_gemv_stage(h, stage, x, y, M, static_cast<cudaStream_t>(stream)),
+                      static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_linear_check(escha_linear_t h, void* stream) {
@@ -315,13 +335,15 @@ escha_status_t escha_mlp_destroy(escha_mlp_t m) {
 escha_status_t escha_mlp_gemv(escha_mlp_t m, const uint16_t* x, uint16_t* y, int M,
                               void* stream) {
   if (!gemv_args_ok(m, x, y, M)) return ESCHA_ERR_INVALID_ARG;
-  return mlp_gemv(m, x, y, M, static_cast<cudaStream_t>(stream));
+  return after_launch(mlp_gemv(m, x, y, M, static_cast<cudaStream_t>(stream)),
+                      static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_mlp_gemv_stage(escha_mlp_t m, int stage, const uint16_t* x, uint16_t* y,
                                     int M, void* stream) {
   if (!gemv_args_ok(m, x, y, M)) return ESCHA_ERR_INVALID_ARG;
-  return mlp_gemv_stage(m, stage, x, y, M, static_cast<cudaStream_t>(stream));
+  return after_launch(mlp_gemv_stage(m, stage, x, y, M, static_cast<cudaStream_t>(stream)),
+                      static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_profile_enable(void* handle, int kind, int on) {
@@ -388,7 +410,8 @@ escha_status_t escha_linear_gemm(escha_linear_t h, const uint16_t* x, uint16_t* 
   if (!h || !x || !y) return ESCHA_ERR_INVALID_ARG;
   if (M < 1) return ESCHA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y)) return ESCHA_ERR_INVALID_ARG;
-  return linear_gemm(h, x, y, M, static_cast<cudaStream_t>(stream));
+  return after_launch(linear_gemm(h, x, y, M, static_cast<cudaStream_t>(stream)),
+                      static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_linear_reserve(escha_linear_t h, int max_m) {
@@ -509,7 +532,9 @@ escha_status_t escha_linear_moe_gemv(escha_moe_t m, const uint16_t* x, const int
                                      const float* expert_w, uint16_t* y, int M, int topk,
                                      void* stream) {
   if (!moe_args_ok(m, x, expert_ids, expert_w, y, M, topk)) return ESCHA_ERR_INVALID_ARG;
-  return moe_gemv(m, x, expert_ids, expert_w, y, M, topk, static_cast<cudaStream_t>(stream));
+  return after_launch(
+      moe_gemv(m, x, expert_ids, expert_w, y, M, topk, static_cast<cudaStream_t>(stream)),
+      static_cast<cudaStream_t>(stream));
 }
 
 escha_status_t escha_linear_moe_gemv_stage(escha_moe_t m, int stage, const uint16_t* x,

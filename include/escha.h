@@ -39,6 +39,9 @@
  *     tile == 16.  Anything else is ESCHA_ERR_UNSUPPORTED.
  *   - No CPU fallback exists: without a usable sm_103a device every compute call
  *     fails with ESCHA_ERR_CUDA.
+ *   - Debugging: with ESCHA_SYNC_DEBUG=1 in the environment (read at the first
+ *     call) every gemv/gemm/moe call and stage synchronises its stream after
+ *     launching and reports an asynchronous CUDA error at that call.
  */
 #ifndef ESCHA_H
 #define ESCHA_H

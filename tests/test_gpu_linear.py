@@ -240,3 +240,38 @@ def test_stages_compose_to_the_full_call():
         with pytest.raises(escha.EschaError) as e:
             lin.gemv(xt, staged[:, :1280], stage=bad)
         assert e.value.status == 1
+
+
+_SYNC_DEBUG_SCRIPT = r"""
+import hashlib, sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+from gemm_trellis_tile_gb300 import escha, synthetic as S
+escha.load()
+rng = np.random.default_rng(91)
+lin = escha.Linear.from_arrays(S.make_linear(rng, 512, 768, 3))
+x = torch.from_numpy(S.make_activations(rng, 4, 512)).cuda()
+y1 = lin.gemv(x)
+y2 = lin.gemm(torch.cat([x] * 80))
+torch.cuda.synchronize()
+assert lin.check() == 0
+h = hashlib.sha256(y1.cpu().numpy().tobytes() + y2.cpu().numpy().tobytes()).hexdigest()
+print(h)
+"""
+
+
+def test_sync_debug_mode_gives_the_same_results():
+    """ESCHA_SYNC_DEBUG=1 synchronises after every compute call; results are
+    bit-identical to a run without it."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for flag in ("0", "1"):
+        env = dict(os.environ, ESCHA_SYNC_DEBUG=flag)
+        r = subprocess.run([sys.executable, "-c", _SYNC_DEBUG_SCRIPT, root], env=env,
+                           capture_output=True, text=True, timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs.append(r.stdout.strip().splitlines()[-1])
+    assert outs[0] == outs[1]
