@@ -341,6 +341,10 @@ __global__ void __launch_bounds__(threads_for<MODE>(), 1)
     for (int s = 0; s < kStages / kGroups; ++s) armed[s] = -1;
     bool waited = false, ok = true;
     const CUtensorMap* fenced = nullptr;
+    // halves of the current job whose tensor maps this thread has acquired
+    // (each output group walks the same halves again)
+    const CUtensorMap* half_job = nullptr;
+    uint64_t half_fenced = 0;
     for (;;) {
       Chunk ch;
       const bool has = mine && ok && it.next(jobs, ch, RPU);
@@ -362,9 +366,18 @@ __global__ void __launch_bounds__(threads_for<MODE>(), 1)
       if (MODE == kModeRowHalves) {
         // stored by input halves: each unit is one half's 8 rows of group g,
         // one 2-D copy through that half's tensor map (written on the device)
+        if (it.row_maps != half_job) {
+          half_job = it.row_maps;
+          half_fenced = 0;
+        }
         for (int i = 0; i < ch.n; ++i) {
-          const CUtensorMap* hm = it.row_maps + ch.kt + i;
-          tensormap_acquire(hm);
+          const int h = ch.kt + i;
+          const CUtensorMap* hm = it.row_maps + h;
+          const uint64_t bit = h < 64 ? (1ull << h) : 0ull;
+          if (!(half_fenced & bit)) {
+            tensormap_acquire(hm);
+            half_fenced |= bit;
+          }
           tma_load_2d_hint(cdst + i * 8 * rowb, hm, ch.g * rowb / 4, 0, full, pol);
         }
       } else if (MODE == kModeColHalves) {
