@@ -44,10 +44,18 @@ design notes):
     path circular.  The search decides integer codes, so it runs in fp32 with
     each step's error (v - c)^2 and sum rounded separately, ties to the lowest
     index: the precision and order the CUDA encoder uses.
-  * E4M3 variant.  [EXLR8] rounds "every value the codebook produces" to FP8
-    E4M3; the value rounded is the codebook's fp16 value (after its one fp16
+  * E4M3 variant.  [EXLR8] rounds each codebook output to FP8 E4M3; the
+    value rounded is the codebook's fp16 value (after its one fp16
     addition), to the nearest E4M3 value, ties to even mantissa, magnitudes
     above 448 clamped to 448 (saturating; E4M3 has no infinities).
+  * FP8 prefill.  [EXLR8] says E4M3-exact weights let prefill multiply on FP8
+    tensor cores, but not how the activations become FP8.  Reading taken:
+    each token's rotated fp16 activations xh are scaled by their largest
+    magnitude onto E4M3's range: amax = max|xh|, inv = fl32(448 / amax),
+    q = E4M3(fl32(xh * inv)), d = fl32(amax / 448), and the layer computes
+    y = had(d * (q @ W_inner)) * sv.  q is an integer decision, so it is taken
+    in fp32 with IEEE rounding, the precision of the CUDA quantiser; a zero
+    row gives q = 0 and d = 0.
   * Halves.  [EXLR8] stores each expert matrix as 16 "halves" of 128
     intermediate channels (output channels of gate and up, input channels of
     down) with a width per half for gate/up and per expert for down, but does
@@ -470,6 +478,57 @@ def reconstruct_weight(w_inner, su, sv):
     w = w * np.asarray(su)[:, None]
     w = w @ blockdiag_hadamard(n)
     return w * np.asarray(sv)[None, :]
+
+
+# ----------------------------------------------------------------------------
+# FP8 prefill  ([EXLR8]: decoded weights are exact E4M3 values, so prefill can
+# multiply them on FP8 tensor cores; the activation scaling is the reading in
+# the header)
+# ----------------------------------------------------------------------------
+
+def rotate_in_fp16(x, su):
+    """xh = fp16(had128(x * su)): the rotated activations, rounded once to fp16."""
+    return had_blockwise(np.asarray(x).astype(np.float64) * su).astype(np.float16)
+
+
+def quantize_rows_e4m3(xh):
+    """Per-token E4M3 quantisation of fp16 activations: (q, d) with xh ~ q * d.
+
+    xh: [M, K] fp16.  Per row: amax = max|xh|, inv = fl32(448 / amax),
+    q = E4M3(fl32(xh * inv)) (nearest even, saturating), d = fl32(amax / 448);
+    a row of zeros gives q = 0, d = 0.  Returns q [M, K] float64 (each an E4M3
+    value, exactly) and d [M] float32.
+    """
+    xh32 = np.asarray(xh, dtype=np.float16).astype(np.float32)
+    amax = np.max(np.abs(xh32), axis=1)
+    nz = amax > 0
+    inv = np.zeros_like(amax)
+    d = np.zeros_like(amax)
+    inv[nz] = np.float32(E4M3_MAX) / amax[nz]
+    d[nz] = amax[nz] / np.float32(E4M3_MAX)
+    prod = xh32 * inv[:, None]            # fp32 products, one rounding each
+    q = e4m3_round(prod.astype(np.float64))
+    return q, d
+
+
+def linear_forward_fp8(x, w_inner, su, sv):
+    """FP8 prefill layer: y = had(d * (q @ W_inner)) * sv, (q, d) = quantised xh.
+
+    W_inner must hold E4M3 values (the EXLR8 rounding); the contraction of the
+    two E4M3 operands and everything after it is fp64.
+    """
+    q, d = quantize_rows_e4m3(rotate_in_fp16(x, su))
+    y_pre = (q @ np.asarray(w_inner).astype(np.float64)) * d.astype(np.float64)[:, None]
+    return had_blockwise(y_pre) * sv
+
+
+def linear_forward_fp8_columns(x, code, bits, su, sv, blocks):
+    """Output columns of the 128-blocks `blocks` of linear_forward_fp8 (E4M3 weights)."""
+    q, d = quantize_rows_e4m3(rotate_in_fp16(x, su))
+    cols = np.concatenate([np.arange(b * HAD_BLOCK, (b + 1) * HAD_BLOCK) for b in blocks])
+    w = decode_columns(code, bits, cols, "e4m3").astype(np.float64)
+    y_pre = (q @ w) * d.astype(np.float64)[:, None]
+    return cols, had_blockwise(y_pre) * sv[cols]
 
 
 def rms_norm(x, w_stored, eps, stored_minus_one=True):

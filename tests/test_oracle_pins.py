@@ -592,6 +592,125 @@ def test_decode_e4m3_is_rounding_of_decode_fp16():
     assert np.array_equal(w8, ref)
 
 
+# ---------------------------------------------------------------- FP8 prefill activations (EXLR8)
+
+def _e4m3_scaled_rows(rng, m, k, exps):
+    """Rows whose values are E4M3 values times 2^e (e per row), each row holding
+    +-448 * 2^e once: exactly representable in fp16 and in the quantiser."""
+    t = _e4m3_table()
+    rows = []
+    for e in exps:
+        r = rng.choice(t, size=k)
+        r[rng.integers(k)] = rng.choice([-448.0, 448.0])
+        rows.append(r * 2.0 ** e)
+    x = np.array(rows).astype(np.float16)
+    assert np.array_equal(x.astype(np.float64), np.array(rows))
+    return x, np.array(rows)
+
+
+def test_quantize_rows_is_exact_on_scaled_e4m3_rows():
+    """amax = 448 * 2^e makes the scale a power of two: q are the E4M3 values
+    and d = 2^e, exactly (a wrong axis, constant or inverse breaks this)."""
+    rng = np.random.default_rng(901)
+    exps = [-8, -5, -2, 0, -3]
+    xh, exact = _e4m3_scaled_rows(rng, len(exps), 384, exps)
+    q, d = O.quantize_rows_e4m3(xh)
+    assert d.dtype == np.float32
+    assert np.array_equal(d.astype(np.float64), 2.0 ** np.array(exps, dtype=np.float64))
+    assert np.array_equal(q * d.astype(np.float64)[:, None], exact)
+
+
+def test_quantize_rows_matches_torch_float8_cast():
+    """The rounding step against torch's float8_e4m3fn cast of the same fp32 products."""
+    rng = np.random.default_rng(902)
+    xh = (rng.standard_normal((7, 640)) * rng.choice([1e-3, 0.1, 3.0, 50.0], size=(7, 1)))
+    xh = xh.astype(np.float16)
+    q, d = O.quantize_rows_e4m3(xh)
+    x32 = torch.from_numpy(xh.astype(np.float32))
+    amax = x32.abs().amax(dim=1)
+    inv = torch.tensor(448.0, dtype=torch.float32) / amax
+    ref = (x32 * inv[:, None]).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(q, ref)
+    assert np.array_equal(d, (amax / torch.tensor(448.0, dtype=torch.float32)).numpy())
+
+
+def test_quantize_rows_range_and_error_bound():
+    """|q| <= 448 with 448 reached at each row's largest element; the
+    dequantised error is within E4M3's half spacing: 2^-4 relative above 2^-6,
+    2^-10 absolute below (times d), plus fp32 rounding of the scale."""
+    rng = np.random.default_rng(903)
+    xh = (rng.standard_normal((9, 1024)) * np.exp(rng.uniform(-6, 4, size=(9, 1)))).astype(np.float16)
+    q, d = O.quantize_rows_e4m3(xh)
+    x = xh.astype(np.float64)
+    assert np.all(np.abs(q) <= 448.0)
+    rows = np.arange(9)
+    assert np.all(np.abs(q[rows, np.argmax(np.abs(x), axis=1)]) == 448.0)
+    assert np.all(np.isin(q, _e4m3_table()))
+    dd = d.astype(np.float64)[:, None]
+    err = np.abs(q * dd - x)
+    bound = (2.0 ** -4 * np.abs(x) + 2.0 ** -10 * dd) * (1 + 2.0 ** -20)
+    assert np.all(err <= bound)
+    # the bound is not loose everywhere: rounding really happens
+    assert np.max(err / np.maximum(bound, 1e-30)) > 0.5
+
+
+def test_quantize_rows_zero_row_and_single_element():
+    xh = np.zeros((3, 128), dtype=np.float16)
+    xh[1, 5] = -0.75
+    q, d = O.quantize_rows_e4m3(xh)
+    assert d[0] == 0 and d[2] == 0 and np.all(q[0] == 0) and np.all(q[2] == 0)
+    assert q[1, 5] == -448.0 and np.count_nonzero(q[1]) == 1
+    assert d[1] == np.float32(0.75) / np.float32(448)
+
+
+def test_linear_fp8_equals_exact_layer_when_activations_are_e4m3():
+    """With rotated activations that the quantiser represents exactly, the FP8
+    layer is the plain layer definition (had(had(x su) W) sv) on E4M3 weights."""
+    rng = np.random.default_rng(904)
+    k, n = 256, 384
+    code = rng.integers(-32768, 32768, size=(k // 16, n // 16, 48), dtype=np.int16)
+    w8 = O.decode_matrix(code, 3, rounding="e4m3").astype(np.float64)
+    su = rng.uniform(0.5, 1.5, size=k)
+    sv = rng.uniform(0.5, 1.5, size=n)
+    _, xh_target = _e4m3_scaled_rows(rng, 4, k, [-6, -3, -1, -4])
+    x = O.had_blockwise(xh_target) / su               # had is its own inverse
+    assert np.array_equal(O.rotate_in_fp16(x, su).astype(np.float64), xh_target)
+    got = O.linear_forward_fp8(x, w8, su, sv)
+    ref = O.linear_forward(x, w8, su, sv)
+    assert np.max(np.abs(got - ref)) <= 1e-10 * np.max(np.abs(ref))
+
+
+def test_linear_fp8_differs_from_fp16_layer_by_the_activation_rounding():
+    """On Gaussian activations the FP8 layer stays within E4M3's relative
+    rounding (RMS at most 2^-4/sqrt(3)) of the fp16 layer, and is not equal to it."""
+    rng = np.random.default_rng(905)
+    k, n = 512, 256
+    code = rng.integers(-32768, 32768, size=(k // 16, n // 16, 32), dtype=np.int16)
+    w8 = O.decode_matrix(code, 2, rounding="e4m3").astype(np.float64)
+    su = rng.uniform(0.9, 1.1, size=k)
+    sv = np.ones(n)
+    x = rng.standard_normal((6, k))
+    got = O.linear_forward_fp8(x, w8, su, sv)
+    xh = O.rotate_in_fp16(x, su).astype(np.float64)
+    ref = O.linear_forward(O.had_blockwise(xh), w8, np.ones(k), sv)   # had(had(xh)) = xh
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert 1e-3 < rel < 2.0 ** -4 / np.sqrt(3)
+
+
+def test_linear_fp8_columns_match_full_layer():
+    rng = np.random.default_rng(906)
+    k, n = 256, 512
+    code = rng.integers(-32768, 32768, size=(k // 16, n // 16, 64), dtype=np.int16)
+    w8 = O.decode_matrix(code, 4, rounding="e4m3").astype(np.float64)
+    su = rng.uniform(0.5, 1.5, size=k)
+    sv = rng.uniform(0.5, 1.5, size=n)
+    x = rng.standard_normal((5, k))
+    full = O.linear_forward_fp8(x, w8, su, sv)
+    cols, part = O.linear_forward_fp8_columns(x, code, 4, su, sv, [1, 3])
+    assert np.array_equal(cols, np.r_[128:256, 384:512])
+    assert np.allclose(part, full[:, cols], rtol=0, atol=1e-12 * np.max(np.abs(full)))
+
+
 # ---------------------------------------------------------------- Viterbi encoder (EXLR8, MLX)
 
 def _decoded(code, bits, rounding="fp16"):
