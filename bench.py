@@ -15,9 +15,10 @@ oracle on a bounded sample of the same workload.
 
 Other workloads print the same line for their own shapes and metric:
 --workload linear512 | sweep (--m, --shape) | moe (--m, --halves, --shared)
-| prefill (TFLOP/s; --shape) | encode (weights/s); --norm adds the MLP's
-input RMSNorm, --rounding e4m3 the EXLR8 codebook rounding.  --impl
-reference times the CPU oracle on a bounded sample of the same workload.
+| prefill (TFLOP/s; --shape, --fp8) | encode (weights/s); --norm adds the
+MLP's input RMSNorm, --rounding e4m3 the EXLR8 codebook rounding, --fp8 the
+prefill on FP8 tensor cores (E4M3 weights, per-token E4M3 activations).
+--impl reference times the CPU oracle on a bounded sample of the same workload.
 """
 
 import argparse
@@ -66,6 +67,9 @@ def parse_args():
                         "per half for gate/up and per expert for down, pointer tables")
     p.add_argument("--rounding", default="fp16", choices=["fp16", "e4m3"],
                    help="codebook rounding: fp16 values, or the EXLR8 E4M3 variant")
+    p.add_argument("--fp8", action="store_true",
+                   help="prefill: kind::f8f6f4 GEMM on E4M3 weights and per-token E4M3 "
+                        "activations (implies --rounding e4m3)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
@@ -150,6 +154,11 @@ def workload_spec(args):
     """Layers of one step as (in, out, bits), a description and the codebook rounding."""
     spec = _workload_spec(args)
     spec["rounding"] = args.rounding
+    spec["fp8"] = bool(args.fp8 and spec["kind"] == "prefill")
+    if spec["fp8"]:
+        spec["rounding"] = "e4m3"
+        spec["name"] += ", FP8 tensor cores (E4M3 weights, per-token E4M3 activations)"
+        return spec
     if args.rounding == "e4m3":
         spec["name"] += ", E4M3 codebook rounding"
     if args.norm and spec["kind"] == "mlp":
@@ -275,12 +284,80 @@ def run_reference_encode(args, spec):
     return 0
 
 
+def prefill_oracle_layer(spec):
+    """The prefill workload's first weight set, as the GPU leg builds it."""
+    k, n, b = spec["layers"][0]
+    return S.make_linear(np.random.default_rng(spec["seed"]), k, n, b)
+
+
+def prefill_oracle_sample(spec, lay, x, rng):
+    """The CPU oracle's prefill layer on one sample: the tokens x through one
+    128-column output block of the layer (fp16 or FP8 route); returns its flops."""
+    from oracle import escha_oracle as O
+    k, n, b = spec["layers"][0]
+    su = O.fold_scales(lay["rin"], lay["s_in"])
+    sv = O.fold_scales(lay["rout"], lay["s_out"])
+    blk = [int(rng.integers(n // 128))]
+    if spec["fp8"]:
+        O.linear_forward_fp8_columns(x, lay["code"], b, su, sv, blk)
+    else:
+        O.linear_forward_columns(x, lay["code"], b, su, sv, blk, rounding=spec["rounding"])
+    return WL.layer_flops(x.shape[0], k, 128)
+
+
+def prefill_oracle_rate(spec, m, seconds):
+    """(TFLOP/s, cores, sample) of the CPU oracle's prefill layer over `seconds`."""
+    lay = prefill_oracle_layer(spec)
+    rng = np.random.default_rng(spec["seed"] + 29)
+    rows = min(m, 256)
+    x = S.make_activations(rng, rows, spec["layers"][0][0])
+    t0 = time.perf_counter()
+    c0 = time.process_time()
+    flops, blocks = 0, 0
+    while True:
+        flops += prefill_oracle_sample(spec, lay, x, rng)
+        blocks += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    wall = time.perf_counter() - t0
+    return (flops / wall / 1e12, round((time.process_time() - c0) / wall, 2),
+            "%d tokens through %d random 128-output column blocks (full input depth), %.1f s"
+            % (rows, blocks, wall))
+
+
+def run_reference_prefill(args, spec):
+    """--impl reference for the prefill: the oracle's layer on a bounded sample per step."""
+    steps = args.steps if args.steps != 4000 else 5
+    warm = args.warmup if args.warmup != 50 else 3
+    budget = 120.0 / max(1, steps + warm)
+    prefill_oracle_rate(spec, args.m, min(budget, 2.0) * warm)
+    t0 = time.perf_counter()
+    c0 = time.process_time()
+    rates = [prefill_oracle_rate(spec, args.m, budget) for _ in range(steps)]
+    wall = time.perf_counter() - t0
+    cores = round((time.process_time() - c0) / wall, 2)
+    value = statistics.mean(r[0] for r in rates)
+    line = {"impl": "reference", "metric": "prefill TFLOP/s (2*M*in*out per step)",
+            "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": steps,
+            "warmup": warm, "ms_per_step": 1e3 * wall / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec["name"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + rates[-1][2]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, spec, rank):
     """--impl reference: the CPU oracle, as it stands, on a bounded sample per step."""
     if rank != 0:
         return 0
     if spec["kind"] == "encode":
         return run_reference_encode(args, spec)
+    if spec["kind"] == "prefill":
+        return run_reference_prefill(args, spec)
     from oracle import escha_oracle as O
     mats = instance_matrices(spec, make_instance(spec, spec["seed"]))
     rng = np.random.default_rng(11)
@@ -557,8 +634,12 @@ def run_prefill(args, spec, rank, world, local):
     y = torch.empty((m, n), dtype=torch.float16, device=dev)
     for lin in lins:
         lin.reserve(m)
+    fp8 = spec["fp8"]
+
+    def call(lin):
+        return lin.gemm_fp8(x, y) if fp8 else lin.gemm(x, y)
     for i in range(max(args.warmup, 3)):
-        lins[i % n_inst].gemm(x, y)
+        call(lins[i % n_inst])
     torch.cuda.synchronize()
     for lin in lins:
         if lin.check() != 0:
@@ -573,7 +654,7 @@ def run_prefill(args, spec, rank, world, local):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record()
     for i in range(args.steps):
-        lins[i % n_inst].gemm(x, y)
+        call(lins[i % n_inst])
     t1.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -599,7 +680,7 @@ def run_prefill(args, spec, rank, world, local):
     e0.record()
     for i in range(e_steps):
         x.copy_(x_host, non_blocking=True)
-        lins[i % n_inst].gemm(x, y)
+        call(lins[i % n_inst])
         y_host.copy_(y, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
@@ -609,12 +690,19 @@ def run_prefill(args, spec, rank, world, local):
             raise SystemExit("device error flag set")
     peaks, src = measured_peaks()
     peak = float(peaks["bf16_tflops"])
+    peak_note = (src + " (MEASURED_PEAKS.json bf16_tflops burst; fp16 has the same nominal "
+                 "dense rate)")
+    if fp8:
+        peak *= 2.0
+        peak_note = (src + " (MEASURED_PEAKS.json bf16_tflops burst x 2, the nominal dense "
+                     "E4M3 : bf16 ratio 4.5 : 2.25 PFLOP/s)")
     value = world * args.steps * flops / (ms / 1e3) / 1e12
     line = {
         "metric": "prefill TFLOP/s (2*M*in*out per step)", "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded uniform code words)",
+        "vs_baseline": None, "dtype": "e4m3" if fp8 else "f16",
+        "data": "synthetic (seeded uniform code words)",
         "config": {"workload": spec["name"], "tokens": m,
                    "l2": "4 rotating weight sets; activations %.0f MB, output %.0f MB per step"
                          % (m * k * 2 / 1e6, m * n * 2 / 1e6),
@@ -622,14 +710,17 @@ def run_prefill(args, spec, rank, world, local):
         "roofline": {"bound": "tensor", "kernel": "trellis_gemm", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak if achieved else None, "traffic": None,
-                     "peak_source": src + " (MEASURED_PEAKS.json bf16_tflops burst; fp16 has "
-                                    "the same nominal dense rate)"},
+                     "peak_source": peak_note},
         "e2e": {"value": e_steps * flops / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(y_host.numel() * 2)},
-        "gpu_launches": prefill_launches(m, k, n, props_sms(dev)) * args.steps,
+        "gpu_launches": prefill_launches(m, k, n, props_sms(dev), fp8) * args.steps,
         "clocks": clocks,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = prefill_oracle_rate(spec, m, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -774,11 +865,12 @@ def props_sms(dev):
     return torch.cuda.get_device_properties(dev).multi_processor_count
 
 
-def prefill_launches(m, k, n, sms):
-    """Launches of one prefill call: the input rotation, the GEMM, and the
-    fix-up kernel when stream-K splits a 512 x 128 tile between CTAs (the
-    GEMM's own rule: at least 16 K-blocks per CTA, at most one CTA per SM)."""
-    kb = k // 64
+def prefill_launches(m, k, n, sms, fp8=False):
+    """Launches of one prefill call: the input rotation (FP8: rotation and
+    quantisation), the GEMM, and the fix-up kernel when stream-K splits a
+    512 x 128 tile between CTAs (the GEMM's own rule: at least 16 K-blocks of
+    128 bytes per row per CTA, at most one CTA per SM)."""
+    kb = k // (128 if fp8 else 64)
     tiles = -(-m // 512) * (n // 128)
     units = tiles * kb
     grid = max(1, min(sms, units // 16))

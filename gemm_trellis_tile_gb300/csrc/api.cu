@@ -414,6 +414,35 @@ escha_status_t escha_linear_gemm(escha_linear_t h, const uint16_t* x, uint16_t* 
                       static_cast<cudaStream_t>(stream));
 }
 
+escha_status_t escha_linear_gemm_fp8(escha_linear_t h, const uint16_t* x, uint16_t* y, int M,
+                                     void* stream) {
+  if (!h || !x || !y) return ESCHA_ERR_INVALID_ARG;
+  if (M < 1) return ESCHA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return ESCHA_ERR_INVALID_ARG;
+  return after_launch(linear_gemm_fp8(h, x, y, M, static_cast<cudaStream_t>(stream)),
+                      static_cast<cudaStream_t>(stream));
+}
+
+escha_status_t escha_linear_gemm_fp8_codes(escha_linear_t h, const uint8_t* q, const float* d,
+                                           uint16_t* y, int M, void* stream) {
+  if (!h || !q || !d || !y) return ESCHA_ERR_INVALID_ARG;
+  if (M < 1) return ESCHA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(y) || (reinterpret_cast<uintptr_t>(d) & 3u))
+    return ESCHA_ERR_INVALID_ARG;
+  return after_launch(linear_gemm_fp8_codes(h, q, d, y, M, static_cast<cudaStream_t>(stream)),
+                      static_cast<cudaStream_t>(stream));
+}
+
+escha_status_t escha_quantize_e4m3_rows(const uint16_t* xh, uint8_t* q, float* d, int M, int K,
+                                        void* stream) {
+  if (!xh || !q || !d || M < 1 || K < 128 || K % 128 != 0) return ESCHA_ERR_INVALID_ARG;
+  if (escha::quantize_e4m3_smem_bytes(K) > escha::kMaxQuantSmem) return ESCHA_ERR_INVALID_ARG;
+  if (!aligned16(xh) || !aligned16(q) || !aligned16(d)) return ESCHA_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return after_launch(escha::from_cuda(escha::launch_quantize_e4m3_rows(xh, nullptr, q, d, M, K, st)),
+                      st);
+}
+
 escha_status_t escha_linear_reserve(escha_linear_t h, int max_m) {
   if (!h || max_m < 1) return ESCHA_ERR_INVALID_ARG;
   return linear_reserve(h, max_m);

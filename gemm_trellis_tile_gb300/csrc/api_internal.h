@@ -46,6 +46,8 @@ struct escha_linear_s {
   int* err = nullptr;         // device error word
   escha::GemvSchedule sched;  // one job: this matrix
   uint16_t* xh = nullptr;     // prefill workspace: rotated activations [xh_rows, K]
+                              // (FP8 prefill: their E4M3 codes, K bytes a row)
+  float* xd = nullptr;        // FP8 prefill: per-row activation scales [xh_rows]
   int xh_rows = 0;
   float* gemm_ws = nullptr;   // prefill partial sums of tiles shared between CTAs
   escha::Profiler prof;
@@ -153,6 +155,10 @@ escha_status_t linear_gemv_stage(escha_linear_s* h, int stage, const uint16_t* x
 escha_status_t linear_gemv(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
                            cudaStream_t st);
 escha_status_t linear_reserve(escha_linear_s* h, int rows);
+escha_status_t linear_gemm_fp8(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
+                               cudaStream_t st);
+escha_status_t linear_gemm_fp8_codes(escha_linear_s* h, const uint8_t* q, const float* d,
+                                     uint16_t* y, int M, cudaStream_t st);
 escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
                            cudaStream_t st);
 escha_status_t mlp_init(escha_mlp_s* m, escha_linear_s* gate, escha_linear_s* up,

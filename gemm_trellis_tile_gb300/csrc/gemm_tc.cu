@@ -27,6 +27,18 @@
 //               * sv, fp16 stores -- or the raw fp32 partial sums.
 // Every mbarrier wait is bounded; a wait that runs out sets the error word and
 // the CTA unwinds (TMEM is always released, in-flight copies are drained).
+// The kernel is launched as a programmatic dependent of the input rotation:
+// setup, code streaming and the first decodes overlap the rotation's tail;
+// the activation loads and the epilogue (which reads the FP8 scales and
+// writes y) wait for it first (griddepcontrol.wait).
+//
+// FP8 variant (EXLR8 format page: weights rounded to E4M3 are exact FP8, so
+// prefill can multiply on FP8 tensor cores).  The activations arrive as
+// per-token E4M3 codes q with fp32 scales d (xh ~ q * d); a block is 128 K
+// elements (still 128 bytes per row, so the swizzle, descriptors and ring
+// sizes are unchanged), the MMA is kind::f8f6f4 with E4M3 A and B (K = 32 per
+// instruction), each decoder warp decodes four tiles per block into E4M3
+// bytes, and the epilogue multiplies each row by its d.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,7 +55,7 @@ namespace {
 
 constexpr int kBM = 512;          // rows per tile (four M=128 accumulators)
 constexpr int kBN = 128;          // output channels per tile (= one Hadamard block)
-constexpr int kBK = 64;           // K per block (128 bytes of fp16)
+constexpr int kRowBytes = 128;    // bytes of one operand row per K block
 constexpr int kAStages = 2;
 constexpr int kBStages = 3;
 constexpr int kCStages = 4;
@@ -52,13 +64,23 @@ constexpr int kFirstDec = 3;
 constexpr int kThreadsG = (kFirstDec + kDecWarps) * 32;  // 608
 constexpr int kTmemCols = 512;
 
-constexpr int kABytes = kBM * kBK * 2;  // 64 KB
-constexpr int kBBytes = kBN * kBK * 2;  // 16 KB
-constexpr int kCBytes = 4 * 8 * 128;    // 4 k-tiles x 8 n-tiles, sized for 4 bits
+constexpr int kABytes = kBM * kRowBytes;  // 64 KB
+constexpr int kBBytes = kBN * kRowBytes;  // 16 KB
 constexpr int kOffB = kAStages * kABytes;
-constexpr int kOffC = kOffB + kBStages * kBBytes;
-constexpr int kOffBar = kOffC + kCStages * kCBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+
+// Per-operand-type geometry: fp16 blocks are 64 K elements (4 k-tiles), E4M3
+// blocks 128 (8 k-tiles); either way 128 bytes per operand row.
+template <bool FP8>
+struct BlockGeom {
+  static constexpr int kKE = FP8 ? 128 : 64;           // K elements per block
+  static constexpr int kKT = kKE / 16;                 // k-tiles per block
+  static constexpr int kTilesPerWarp = kKT * 8 / kDecWarps;
+  static constexpr int kCBytes = kKT * 8 * 128;        // code stage, sized for 4 bits
+  static constexpr int kOffC = kOffB + kBStages * kBBytes;
+  static constexpr int kOffBar = kOffC + kCStages * kCBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+};
+static_assert(BlockGeom<true>::kSmemBytes <= 227 * 1024, "FP8 ring does not fit");
 
 // barrier indices
 constexpr int kBarAFull = 0, kBarAEmpty = 2, kBarCFull = 4, kBarCEmpty = 8, kBarBFull = 12,
@@ -67,11 +89,12 @@ constexpr int kBarAFull = 0, kBarAEmpty = 2, kBarCFull = 4, kBarCEmpty = 8, kBar
 struct GemmArgs {
   const uint8_t* code;
   const float* sv;
+  const float* d;        // FP8: per-row activation scales [M]; else null
   uint16_t* y;
   float* ws;             // partial sums: [grid][2][kBM][kBN] fp32
   int M, N, K;
   int n_blocks;          // N / kBN
-  int kb_per_tile;       // K / kBK
+  int kb_per_tile;       // K / (K elements per block)
   long long units;       // tiles * kb_per_tile
   int grid;
   int* err;
@@ -128,6 +151,25 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= A * B with E4M3 A and B (K = 32 per instruction), fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Two fp16 values (low half first) to two E4M3 bytes (low byte first),
+// nearest even, saturating.
+__device__ __forceinline__ uint16_t e4m3x2_from_f16x2(uint32_t h2) {
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e) : "r"(h2));
+  return e;
 }
 
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread completes.
@@ -211,11 +253,12 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D,
-// M = 128, N = 128.
+// Instruction descriptor: fp32 D, A and B both K-major, M = 128, N = 128.
+// The A/B format fields read 0 for f16 under kind::f16 and for E4M3 under
+// kind::f8f6f4, so both kinds use the same word.
 constexpr uint32_t kIdesc = (1u << 4)              // D format: f32
-                            | (0u << 7)            // A format: f16
-                            | (0u << 10)           // B format: f16
+                            | (0u << 7)            // A format: f16 / E4M3
+                            | (0u << 10)           // B format: f16 / E4M3
                             | ((kBN >> 3) << 17)   // N / 8
                             | ((128 >> 4) << 24);  // M / 16
 
@@ -269,14 +312,16 @@ struct SegIter {
 
 // ---------------------------------------------------------------- kernel
 
-template <int BITS, bool E4M3>
+template <int BITS, bool E4M3, bool FP8>
 __global__ void __launch_bounds__(kThreadsG, 1)
     trellis_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs a) {
+  using G = BlockGeom<FP8>;
+  static_assert(!FP8 || E4M3, "the FP8 MMA needs E4M3 weights");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars + 1);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -324,6 +369,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       int armed[kAStages] = {-1, -1};
       bool ok = true;
       Ring<kAStages> ra;
+      pdl_wait();  // the activations are the previous kernel's output
       while (ok && it.next(seg)) {
         const int m0 = (seg.tile / a.n_blocks) * kBM;
         for (int kb = seg.kb0; kb < seg.kb1; ++kb, ra.advance()) {
@@ -336,8 +382,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           }
           mbar_arrive_expect_tx(bar(kBarAFull + s), kABytes);
           const uint32_t dst = base + s * kABytes;
-          tma_load_2d(dst, &tmap_a, kb * kBK, m0, bar(kBarAFull + s));
-          tma_load_2d(dst + kABytes / 2, &tmap_a, kb * kBK, m0 + kBM / 2, bar(kBarAFull + s));
+          tma_load_2d(dst, &tmap_a, kb * G::kKE, m0, bar(kBarAFull + s));
+          tma_load_2d(dst + kABytes / 2, &tmap_a, kb * G::kKE, m0 + kBM / 2, bar(kBarAFull + s));
           armed[s] = static_cast<int>(ph);
         }
       }
@@ -363,10 +409,10 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(kBarCFull + s), 4 * row_bytes);
-          const uint32_t dst = base + kOffC + s * kCBytes;
-          for (int r = 0; r < 4; ++r) {
-            const uint8_t* src = a.code + ((size_t)(4 * kb + r) * NT + 8 * nb) * T;
+          mbar_arrive_expect_tx(bar(kBarCFull + s), G::kKT * row_bytes);
+          const uint32_t dst = base + G::kOffC + s * G::kCBytes;
+          for (int r = 0; r < G::kKT; ++r) {
+            const uint8_t* src = a.code + ((size_t)(G::kKT * kb + r) * NT + 8 * nb) * T;
             bulk_g2s(dst + r * row_bytes, src, row_bytes, bar(kBarCFull + s));
           }
           armed[s] = static_cast<int>(ph);
@@ -407,11 +453,14 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 #pragma unroll
           for (int acc = 0; acc < 4; ++acc) {
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
+            for (int kk = 0; kk < kRowBytes / 32; ++kk) {  // 32 bytes of K per MMA
               const uint64_t ad = smem_desc_k128(as + acc * (kABytes / 4) + kk * 32);
               const uint64_t bd = smem_desc_k128(bs + kk * 32);
-              mma_f16(tmem_base + acc * kBN, ad, bd, kIdesc,
-                      (kb > seg.kb0 || kk > 0) ? 1u : 0u);
+              const uint32_t accum = (kb > seg.kb0 || kk > 0) ? 1u : 0u;
+              if constexpr (FP8)
+                mma_e4m3(tmem_base + acc * kBN, ad, bd, kIdesc, accum);
+              else
+                mma_f16(tmem_base + acc * kBN, ad, bd, kIdesc, accum);
             }
           }
           mma_commit(bar(kBarAEmpty + sa));
@@ -427,8 +476,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   } else {
     // ---------------------------------------------------------- decoders + epilogue
     const int dw = warp - kFirstDec;   // 0..15
-    const int kt_local = dw >> 2;      // k-tile row of the block this warp decodes
-    const int nt_base = (dw & 3) * 2;  // its two n-tiles
+    constexpr int NTW = G::kTilesPerWarp;  // n-tiles this warp decodes per block: 2 or 4
+    const int kt_local = dw / (8 / NTW);   // k-tile row of the block this warp decodes
+    const int nt_base = (dw % (8 / NTW)) * NTW;
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
     const int acc = dw >> 2;           // accumulator (128-row slice) it finishes
     const LaneWindow lw = lane_window<BITS>(lane);
@@ -451,21 +501,29 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           ok = false;
           break;
         }
-        const uint8_t* codes = smem + kOffC + sc * kCBytes;
+        const uint8_t* codes = smem + G::kOffC + sc * G::kCBytes;
         uint8_t* bt = smem + kOffB + sb * kBBytes;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NTW; ++i) {
           const int nt = nt_base + i;
           const uint32_t* tw = reinterpret_cast<const uint32_t*>(codes + (kt_local * 8 + nt) * T);
           uint32_t h[8];
-          decode8<BITS, E4M3>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
+          // symbols 2p, 2p+1 of the lane: input channels k, k+1 of output channel n
+          decode8<BITS, E4M3 && !FP8>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const int rh = p & 1, nh = p >> 1;
-            const int n = 16 * nt + g + 8 * nh;
-            const int chunk = (2 * kt_local + rh) ^ g;
+            const int n = 16 * nt + g + 8 * nh;   // n & 7 == g: the row's swizzle phase
             const uint32_t pair = __byte_perm(h[2 * p], h[2 * p + 1], 0x5410);
-            *reinterpret_cast<uint32_t*>(bt + n * 128 + chunk * 16 + 4 * t) = pair;
+            if constexpr (FP8) {
+              // k = 16 kt_local + 8 rh + 2t: byte k of the row, 16-byte chunk kt_local
+              const int chunk = kt_local ^ g;
+              *reinterpret_cast<uint16_t*>(bt + n * 128 + chunk * 16 + 8 * rh + 2 * t) =
+                  e4m3x2_from_f16x2(pair);
+            } else {
+              const int chunk = (2 * kt_local + rh) ^ g;
+              *reinterpret_cast<uint32_t*>(bt + n * 128 + chunk * 16 + 4 * t) = pair;
+            }
           }
         }
         fence_proxy_async_smem();
@@ -478,6 +536,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       if (!ok) break;
 
       // ---- epilogue of this segment: row acc*128 + quad*32 + lane of the tile
+      if (nseg == 0) pdl_wait();  // the scales d come from the previous kernel
       __syncwarp();
       if (!mbar_wait(bar(kBarAcc), nseg & 1, a.limit_ns)) {
         set_error(a.err, kDevErrTimeout);
@@ -493,6 +552,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           owner(t_first, a.units, a.grid) == owner(t_first + a.kb_per_tile - 1, a.units, a.grid);
       const int n0 = nb * kBN;
       if (fused) {
+        // FP8: the row's activation scale joins the output scale
+        const float dm = FP8 ? (m < a.M ? __ldg(a.d + m) : 0.f) : 1.f;
         // index bits 0..4: a 32-point transform on each 32-column chunk, in TMEM
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
@@ -532,8 +593,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
               uint32_t pk[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const float s0 = sc[2 * e] * kHadScale;
-                const float s1 = sc[2 * e + 1] * kHadScale;
+                const float s0 = sc[2 * e] * kHadScale * dm;
+                const float s1 = sc[2 * e + 1] * kHadScale * dm;
                 pk[e] = float_to_half_bits(w[2 * e] * s0) |
                         (uint32_t(float_to_half_bits(w[2 * e + 1] * s1)) << 16);
               }
@@ -578,6 +639,7 @@ constexpr int kMaxSplitTiles = 512;
 struct FixupArgs {
   const float* ws;
   const float* sv;
+  const float* d;  // per-row activation scales (FP8), or null
   uint16_t* y;
   int M, N, n_blocks, kb_per_tile, grid, count;
   long long units;
@@ -603,51 +665,54 @@ __global__ void gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
     for (int q = 0; q < 4; ++q) v[q] += wrow[lane + 32 * q];
   }
   fwht128_warp_strided(v, lane);
+  const float dm = f.d ? f.d[m] : 1.f;
   uint16_t* yr = f.y + (size_t)m * f.N + n0 + lane;
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    yr[32 * q] = float_to_half_bits(v[q] * kHadScale * f.sv[n0 + lane + 32 * q]);
+    yr[32 * q] = float_to_half_bits(v[q] * kHadScale * dm * f.sv[n0 + lane + 32 * q]);
 }
 
-template <int BITS, bool E4M3>
+template <int BITS, bool E4M3, bool FP8>
 cudaError_t launch_gemm_bits(const CUtensorMap& map, const GemmArgs& a, cudaStream_t st) {
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(trellis_gemm_kernel<BITS, E4M3>),
-                                 kSmemBytes);
+  constexpr int smem = BlockGeom<FP8>::kSmemBytes;
+  cudaError_t e =
+      set_smem_limit(reinterpret_cast<const void*>(trellis_gemm_kernel<BITS, E4M3, FP8>), smem);
   if (e != cudaSuccess) return e;
-  trellis_gemm_kernel<BITS, E4M3><<<a.grid, kThreadsG, kSmemBytes, st>>>(map, a);
-  return cudaGetLastError();
+  PdlLaunch dl(a.grid, kThreadsG, smem, st);
+  return cudaLaunchKernelEx(&dl.cfg, trellis_gemm_kernel<BITS, E4M3, FP8>, map, a);
 }
 
-}  // namespace
-
-size_t gemm_workspace_floats(int num_sms) { return (size_t)num_sms * 2 * kBM * kBN; }
-
-// xh: rotated activations fp16 [M, K] (16-byte aligned, K a multiple of 128);
-// ws: gemm_workspace_floats(num_sms) fp32.
-cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, bool e4m3,
-                                int M, int K, int N, const float* sv, uint16_t* y, float* ws,
-                                int num_sms, int* err, cudaStream_t st) {
+// Shared by both operand types: the activation tensor map (rows of K elements
+// of `esize` bytes, 128-byte boxes, 128B swizzle), the stream-K split, the list
+// of tiles shared between CTAs, the kernel and the fix-up launch.
+cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t* code, int bits,
+                        bool e4m3, int M, int K, int N, const float* sv, uint16_t* y, float* ws,
+                        int num_sms, int* err, cudaStream_t st) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
+  const int esize = fp8 ? 1 : 2;
+  const int ke = kRowBytes / esize;  // K elements per block
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t box[2] = {kBK, kBM / 2};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * esize};
+  const cuuint32_t box[2] = {(cuuint32_t)ke, kBM / 2};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xh), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   const_cast<void*>(act), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   GemmArgs a;
   a.code = reinterpret_cast<const uint8_t*>(code);
   a.sv = sv;
+  a.d = fp8 ? d : nullptr;
   a.y = y;
   a.ws = ws;
   a.M = M;
   a.N = N;
   a.K = K;
   a.n_blocks = N / kBN;
-  a.kb_per_tile = K / kBK;
+  a.kb_per_tile = K / ke;
   const long long tiles = (long long)((M + kBM - 1) / kBM) * a.n_blocks;
   a.units = tiles * a.kb_per_tile;
   // at least 16 K-blocks per CTA, at most one CTA per SM
@@ -661,6 +726,7 @@ cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bit
   FixupArgs f;
   f.ws = ws;
   f.sv = sv;
+  f.d = a.d;
   f.y = y;
   f.M = M;
   f.N = N;
@@ -678,10 +744,18 @@ cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bit
   }
 
   cudaError_t e;
-  switch (bits) {
-    case 2: e = e4m3 ? launch_gemm_bits<2, true>(map, a, st) : launch_gemm_bits<2, false>(map, a, st); break;
-    case 3: e = e4m3 ? launch_gemm_bits<3, true>(map, a, st) : launch_gemm_bits<3, false>(map, a, st); break;
-    default: e = e4m3 ? launch_gemm_bits<4, true>(map, a, st) : launch_gemm_bits<4, false>(map, a, st); break;
+  if (fp8) {
+    switch (bits) {
+      case 2: e = launch_gemm_bits<2, true, true>(map, a, st); break;
+      case 3: e = launch_gemm_bits<3, true, true>(map, a, st); break;
+      default: e = launch_gemm_bits<4, true, true>(map, a, st); break;
+    }
+  } else {
+    switch (bits) {
+      case 2: e = e4m3 ? launch_gemm_bits<2, true, false>(map, a, st) : launch_gemm_bits<2, false, false>(map, a, st); break;
+      case 3: e = e4m3 ? launch_gemm_bits<3, true, false>(map, a, st) : launch_gemm_bits<3, false, false>(map, a, st); break;
+      default: e = e4m3 ? launch_gemm_bits<4, true, false>(map, a, st) : launch_gemm_bits<4, false, false>(map, a, st); break;
+    }
   }
   if (e != cudaSuccess) return e;
   if (f.count > 0) {
@@ -690,6 +764,26 @@ cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bit
     e = cudaGetLastError();
   }
   return e;
+}
+
+}  // namespace
+
+size_t gemm_workspace_floats(int num_sms) { return (size_t)num_sms * 2 * kBM * kBN; }
+
+// xh: rotated activations fp16 [M, K] (16-byte aligned, K a multiple of 128);
+// ws: gemm_workspace_floats(num_sms) fp32.
+cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, bool e4m3,
+                                int M, int K, int N, const float* sv, uint16_t* y, float* ws,
+                                int num_sms, int* err, cudaStream_t st) {
+  return launch_gemm(xh, false, nullptr, code, bits, e4m3, M, K, N, sv, y, ws, num_sms, err, st);
+}
+
+// xq: E4M3 activation codes [M, K] (16-byte aligned, K a multiple of 128) with
+// per-row scales d [M]; the weights are decoded with the E4M3 rounding.
+cudaError_t launch_trellis_gemm_fp8(const uint8_t* xq, const float* d, const int16_t* code,
+                                    int bits, int M, int K, int N, const float* sv, uint16_t* y,
+                                    float* ws, int num_sms, int* err, cudaStream_t st) {
+  return launch_gemm(xq, true, d, code, bits, true, M, K, N, sv, y, ws, num_sms, err, st);
 }
 
 }  // namespace escha

@@ -108,6 +108,18 @@ size_t gemm_workspace_floats(int num_sms);
 cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, bool e4m3,
                                 int M, int K, int N, const float* sv, uint16_t* y, float* ws,
                                 int num_sms, int* err, cudaStream_t st);
+// FP8 prefill: xq E4M3 codes [M, K] with per-row scales d (xh ~ xq * d); the
+// weights are decoded with the E4M3 rounding and multiplied on kind::f8f6f4.
+cudaError_t launch_trellis_gemm_fp8(const uint8_t* xq, const float* d, const int16_t* code,
+                                    int bits, int M, int K, int N, const float* sv, uint16_t* y,
+                                    float* ws, int num_sms, int* err, cudaStream_t st);
+// Per-token E4M3 quantisation: q [M, K], d [M] from xh = fp16(had128(x * su))
+// (su != null) or from x itself (su == null).  K a multiple of 128; the block
+// keeps the row in quantize_e4m3_smem_bytes(K) of shared memory.
+size_t quantize_e4m3_smem_bytes(int K);
+constexpr size_t kMaxQuantSmem = 128 * 1024;  // K <= 65536
+cudaError_t launch_quantize_e4m3_rows(const uint16_t* x, const float* su, uint8_t* q, float* d,
+                                      int M, int K, cudaStream_t st);
 cudaError_t launch_decode(const int16_t* code, int bits, bool e4m3, int K, int N, uint16_t* w,
                           cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);

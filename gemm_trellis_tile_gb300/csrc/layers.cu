@@ -131,8 +131,10 @@ void linear_free(escha_linear_s* h) {
   cudaFree(h->err);
   cudaFree(h->sched.d_jobs);
   cudaFree(h->xh);
+  cudaFree(h->xd);
   cudaFree(h->gemm_ws);
   h->gemm_ws = nullptr;
+  h->xd = nullptr;
   h->su = h->sv = nullptr;
   h->xfrag = nullptr;
   h->tmap = nullptr;
@@ -187,11 +189,14 @@ escha_status_t linear_reserve(escha_linear_s* h, int rows) {
   if (h->xh) {
     if (cudaDeviceSynchronize() != cudaSuccess) return ESCHA_ERR_CUDA;
     cudaFree(h->xh);
+    cudaFree(h->xd);
     h->xh = nullptr;
+    h->xd = nullptr;
     h->xh_rows = 0;
   }
   escha_status_t s = dev_alloc(&h->xh, (size_t)rows * h->K);
   if (s != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->xd, (size_t)rows)) != ESCHA_OK) return s;
   h->xh_rows = rows;
   if (!h->gemm_ws && (s = dev_alloc(&h->gemm_ws, gemm_workspace_floats(h->num_sms))) != ESCHA_OK)
     return s;
@@ -208,6 +213,38 @@ escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, in
   e = launch_trellis_gemm(h->xh, h->code, h->bits, h->rounding == ESCHA_ROUND_E4M3, M, h->K,
                           h->N, h->sv, y, h->gemm_ws,
                           h->num_sms, h->err, st);
+  h->prof.end(st);
+  return from_cuda(e);
+}
+
+// FP8 prefill (E4M3-rounded layers only): per-token E4M3 activations from the
+// input rotation, then the kind::f8f6f4 GEMM; the codes reuse the rotated-
+// activation workspace (K bytes of its 2K per row).
+escha_status_t linear_gemm_fp8(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
+                               cudaStream_t st) {
+  if (h->rounding != ESCHA_ROUND_E4M3) return ESCHA_ERR_UNSUPPORTED;
+  if (quantize_e4m3_smem_bytes(h->K) > kMaxQuantSmem) return ESCHA_ERR_UNSUPPORTED;
+  escha_status_t s = linear_reserve(h, M);
+  if (s != ESCHA_OK) return s;
+  uint8_t* xq = reinterpret_cast<uint8_t*>(h->xh);
+  cudaError_t e = launch_quantize_e4m3_rows(x, h->su, xq, h->xd, M, h->K, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  h->prof.begin(st);
+  e = launch_trellis_gemm_fp8(xq, h->xd, h->code, h->bits, M, h->K, h->N, h->sv, y, h->gemm_ws,
+                              h->num_sms, h->err, st);
+  h->prof.end(st);
+  return from_cuda(e);
+}
+
+escha_status_t linear_gemm_fp8_codes(escha_linear_s* h, const uint8_t* q, const float* d,
+                                     uint16_t* y, int M, cudaStream_t st) {
+  if (h->rounding != ESCHA_ROUND_E4M3) return ESCHA_ERR_UNSUPPORTED;
+  escha_status_t s;
+  if (!h->gemm_ws && (s = dev_alloc(&h->gemm_ws, gemm_workspace_floats(h->num_sms))) != ESCHA_OK)
+    return s;
+  h->prof.begin(st);
+  cudaError_t e = launch_trellis_gemm_fp8(q, d, h->code, h->bits, M, h->K, h->N, h->sv, y,
+                                          h->gemm_ws, h->num_sms, h->err, st);
   h->prof.end(st);
   return from_cuda(e);
 }

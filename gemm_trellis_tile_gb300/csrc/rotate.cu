@@ -125,27 +125,138 @@ __global__ void fold_norm_kernel(const uint16_t* w, float offset, const float* s
   if (i < n) g[i] = (half_bits_to_float(w[i]) + offset) * su[i];
 }
 
+// Blocks of 128 channels a warp loads before it transforms any: with one
+// 256-byte load per warp in flight the prefill's rotations reached about a
+// third of HBM bandwidth.
+constexpr int kRotBatch = 4;
+
 // xh[m, k] = fp16(had128(x * su)), plain row-major (the GEMM's A operand).
+// One warp per token and kRotBatch consecutive 128-blocks.
 __global__ void rotate_in_plain_kernel(const uint16_t* x, const float* su, uint16_t* xh, int M,
                                        int K) {
+  pdl_trigger();  // the GEMM may set up; it waits for this kernel before loading xh
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int nb = K / kHad;
-  if (wid >= (long long)M * nb) return;
-  const int m = static_cast<int>(wid / nb);
-  const int kb = static_cast<int>(wid - (long long)m * nb);
-  const int k0 = kb * kHad + 4 * lane;
-  float v[4];
-  load4_half(x + (size_t)m * K + k0, v);
-  const float4 s = *reinterpret_cast<const float4*>(su + k0);
-  v[0] *= s.x;
-  v[1] *= s.y;
-  v[2] *= s.z;
-  v[3] *= s.w;
-  fwht128_warp(v, lane);
+  const int ng = (nb + kRotBatch - 1) / kRotBatch;
+  if (wid >= (long long)M * ng) return;
+  const int m = static_cast<int>(wid / ng);
+  const int b0 = static_cast<int>(wid - (long long)m * ng) * kRotBatch;
+  float v[kRotBatch][4];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) v[r] *= kHadScale;
-  store4_half(xh + (size_t)m * K + k0, v);
+  for (int i = 0; i < kRotBatch; ++i)
+    if (b0 + i < nb) load4_half(x + (size_t)m * K + (b0 + i) * kHad + 4 * lane, v[i]);
+#pragma unroll
+  for (int i = 0; i < kRotBatch; ++i) {
+    if (b0 + i >= nb) break;
+    const int k0 = (b0 + i) * kHad + 4 * lane;
+    const float4 s = *reinterpret_cast<const float4*>(su + k0);
+    v[i][0] *= s.x;
+    v[i][1] *= s.y;
+    v[i][2] *= s.z;
+    v[i][3] *= s.w;
+    fwht128_warp(v[i], lane);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v[i][r] *= kHadScale;
+    store4_half(xh + (size_t)m * K + k0, v[i]);
+  }
+}
+
+// Per-token E4M3 activations for the FP8 prefill (EXLR8 format page: weights
+// that are exact E4M3 values let prefill multiply on FP8 tensor cores; the
+// page leaves the activation side open, and this kernel scales each token by
+// its largest magnitude).  One block per token:
+//   xh   = fp16(had128(x * su))           (ROTATE; else x is xh already)
+//   amax = max |xh|,  inv = 448 / amax,  d = amax / 448   (IEEE-rounded fp32)
+//   q    = E4M3(xh * inv), nearest even, saturating  (the product rounded to fp32 first)
+// A row of zeros gives q = 0 and d = 0.  The row's xh waits in shared memory
+// (2K bytes) between the two passes.
+constexpr int kQuantThreads = 512;
+constexpr float kE4M3Max = 448.0f;
+
+// Two fp32 values to two E4M3 bytes: `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(e) : "f"(hi), "f"(lo));
+  return e;
+}
+
+template <bool ROTATE>
+__global__ void __launch_bounds__(kQuantThreads)
+    quantize_e4m3_rows_kernel(const uint16_t* x, const float* su, uint8_t* q, float* d, int K) {
+  extern __shared__ __align__(16) uint16_t xrow[];
+  __shared__ float part[kQuantThreads / 32];
+  constexpr int W = kQuantThreads / 32;
+  pdl_trigger();  // the GEMM may set up; it waits for this kernel before loading q or d
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int m = blockIdx.x;
+  const uint16_t* xr = x + (size_t)m * K;
+  const int nb = K / kHad;
+  float amax = 0.f;
+  // warp w takes blocks w, w + W, w + 2W, ..., loading kRotBatch of them at a time
+  for (int i0 = 0; warp + W * i0 < nb; i0 += kRotBatch) {
+    uint2 batch[kRotBatch];
+#pragma unroll
+    for (int i = 0; i < kRotBatch; ++i) {
+      const int b = warp + W * (i0 + i);
+      if (b < nb) batch[i] = *reinterpret_cast<const uint2*>(xr + b * kHad + 4 * lane);
+    }
+#pragma unroll
+    for (int i = 0; i < kRotBatch; ++i) {
+      const int b = warp + W * (i0 + i);
+      if (b >= nb) break;
+      const int k0 = b * kHad + 4 * lane;
+      uint2 raw = batch[i];
+      if (ROTATE) {
+        float v[4];
+        v[0] = half_bits_to_float(raw.x & 0xFFFF);
+        v[1] = half_bits_to_float(raw.x >> 16);
+        v[2] = half_bits_to_float(raw.y & 0xFFFF);
+        v[3] = half_bits_to_float(raw.y >> 16);
+        const float4 s = *reinterpret_cast<const float4*>(su + k0);
+        v[0] *= s.x;
+        v[1] *= s.y;
+        v[2] *= s.z;
+        v[3] *= s.w;
+        fwht128_warp(v, lane);
+        raw.x = float_to_half_bits(v[0] * kHadScale) |
+                (uint32_t(float_to_half_bits(v[1] * kHadScale)) << 16);
+        raw.y = float_to_half_bits(v[2] * kHadScale) |
+                (uint32_t(float_to_half_bits(v[3] * kHadScale)) << 16);
+      }
+      *reinterpret_cast<uint2*>(xrow + k0) = raw;
+      amax = fmaxf(amax, fabsf(half_bits_to_float(raw.x & 0xFFFF)));
+      amax = fmaxf(amax, fabsf(half_bits_to_float(raw.x >> 16)));
+      amax = fmaxf(amax, fabsf(half_bits_to_float(raw.y & 0xFFFF)));
+      amax = fmaxf(amax, fabsf(half_bits_to_float(raw.y >> 16)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if (lane == 0) part[warp] = amax;
+  __syncthreads();
+  amax = 0.f;
+#pragma unroll
+  for (int w = 0; w < W; ++w) amax = fmaxf(amax, part[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(kE4M3Max, amax) : 0.f;
+  if (threadIdx.x == 0) d[m] = amax > 0.f ? __fdiv_rn(amax, kE4M3Max) : 0.f;
+  uint8_t* qr = q + (size_t)m * K;
+  for (int k = 16 * threadIdx.x; k < K; k += 16 * kQuantThreads) {
+    const uint4 a = *reinterpret_cast<const uint4*>(xrow + k);
+    const uint4 b = *reinterpret_cast<const uint4*>(xrow + k + 8);
+    const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t w0 = h[2 * i], w1 = h[2 * i + 1];
+      const uint32_t lo = e4m3x2_from_f32(__fmul_rn(half_bits_to_float(w0 & 0xFFFF), inv),
+                                          __fmul_rn(half_bits_to_float(w0 >> 16), inv));
+      const uint32_t hi = e4m3x2_from_f32(__fmul_rn(half_bits_to_float(w1 & 0xFFFF), inv),
+                                          __fmul_rn(half_bits_to_float(w1 >> 16), inv));
+      out[i] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(qr + k) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
 }
 
 // y = fp16(had128(sum of partial slots) * sv).
@@ -258,8 +369,24 @@ cudaError_t launch_fold_norm(const uint16_t* w, float offset, const float* su, f
 
 cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t* xh, int M,
                                    int K, cudaStream_t st) {
-  const long long warps = (long long)M * (K / kHad);
+  const long long warps = (long long)M * ((K / kHad + kRotBatch - 1) / kRotBatch);
   rotate_in_plain_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(x, su, xh, M, K);
+  return cudaGetLastError();
+}
+
+size_t quantize_e4m3_smem_bytes(int K) { return (size_t)K * 2; }
+
+cudaError_t launch_quantize_e4m3_rows(const uint16_t* x, const float* su, uint8_t* q, float* d,
+                                      int M, int K, cudaStream_t st) {
+  const size_t smem = quantize_e4m3_smem_bytes(K);
+  const void* fn = su ? reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<true>)
+                      : reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<false>);
+  cudaError_t e = set_smem_limit(fn, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (su)
+    quantize_e4m3_rows_kernel<true><<<M, kQuantThreads, smem, st>>>(x, su, q, d, K);
+  else
+    quantize_e4m3_rows_kernel<false><<<M, kQuantThreads, smem, st>>>(x, nullptr, q, d, K);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,9 @@ _SIGS = {
     "escha_selftest_wait_timeout": (_I, [_I, _P]),
     "escha_trellis_encode": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "escha_linear_gemv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _P]),
+    "escha_linear_gemm_fp8": (_I, [_P, _P, _P, _I, _P]),
+    "escha_quantize_e4m3_rows": (_I, [_P, _P, _P, _I, _I, _P]),
+    "escha_linear_gemm_fp8_codes": (_I, [_P, _P, _P, _P, _I, _P]),
 }
 
 
@@ -214,6 +217,31 @@ class Linear:
             y = torch.empty((m, self.out_features), dtype=torch.float16, device=x.device)
         check(load().escha_linear_gemm(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
               "escha_linear_gemm")
+        return y
+
+    def gemm_fp8(self, x, y=None, stream=None):
+        """Prefill on FP8 tensor cores (E4M3-rounded handles): activations
+        quantised per token to E4M3 (escha_linear_gemm_fp8)."""
+        torch = _torch()
+        _dev(x, torch.float16)
+        m = x.shape[0]
+        if y is None:
+            y = torch.empty((m, self.out_features), dtype=torch.float16, device=x.device)
+        check(load().escha_linear_gemm_fp8(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
+              "escha_linear_gemm_fp8")
+        return y
+
+    def gemm_fp8_codes(self, q, d, y=None, stream=None):
+        """The FP8 prefill's contraction on given E4M3 codes q (uint8 [M, in]) and
+        per-row scales d (fp32 [M]) (escha_linear_gemm_fp8_codes)."""
+        torch = _torch()
+        _dev(q, torch.uint8)
+        m = q.shape[0]
+        _dev(d, torch.float32, (m,))
+        if y is None:
+            y = torch.empty((m, self.out_features), dtype=torch.float16, device=q.device)
+        check(load().escha_linear_gemm_fp8_codes(self.handle, _ptr(q), _ptr(d), _ptr(y), m,
+                                                 _stream(stream)), "escha_linear_gemm_fp8_codes")
         return y
 
     def reserve(self, max_m):
@@ -498,6 +526,19 @@ class MoEHalves(MoE):
 def selftest_wait_timeout(limit_us=10000, stream=None):
     """Run the bounded-wait self test; returns the status code (5 = timed out as designed)."""
     return load().escha_selftest_wait_timeout(int(limit_us), _stream(stream))
+
+
+def quantize_e4m3_rows(xh, stream=None):
+    """Per-token E4M3 codes and scales of fp16 activations xh [M, K] (CUDA):
+    returns (q uint8 [M, K] E4M3 bit patterns, d fp32 [M]); xh ~ q * d."""
+    torch = _torch()
+    _dev(xh, torch.float16)
+    m, k = xh.shape
+    q = torch.empty((m, k), dtype=torch.uint8, device=xh.device)
+    d = torch.empty((m,), dtype=torch.float32, device=xh.device)
+    check(load().escha_quantize_e4m3_rows(_ptr(xh), _ptr(q), _ptr(d), int(m), int(k),
+                                          _stream(stream)), "escha_quantize_e4m3_rows")
+    return q, d
 
 
 def trellis_encode(w, bits, rounding="fp16", sq_err=False, stream=None):

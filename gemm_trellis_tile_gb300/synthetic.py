@@ -43,6 +43,16 @@ def make_activations(rng, m, features):
     return rng.normal(0.0, 1.0, (m, features)).astype(np.float16)
 
 
+def make_activation_rows_mixed(rng, m, features):
+    """fp16 rows of N(0, 1) values times a per-row factor e^U(-8, 5), with row 0
+    all zeros and row 1 holding a single non-zero value (m >= 3)."""
+    x = rng.normal(0.0, 1.0, (m, features)) * np.exp(rng.uniform(-8, 5, size=(m, 1)))
+    x[0] = 0.0
+    x[1] = 0.0
+    x[1, rng.integers(features)] = rng.normal()
+    return x.astype(np.float16)
+
+
 def make_mlp(rng, hidden, inter, bits_gate, bits_up, bits_down):
     """Gated MLP down(silu(gate x) * up x) with the fp16 range guard on every matrix."""
     return dict(gate=make_linear(rng, hidden, inter, bits_gate, guard=True),

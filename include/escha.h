@@ -132,6 +132,49 @@ escha_status_t escha_linear_gemm(escha_linear_t h, const uint16_t* x, uint16_t* 
 escha_status_t escha_linear_reserve(escha_linear_t h, int max_m);
 
 /*
+ * FP8 prefill, for handles with ESCHA_ROUND_E4M3 (else ESCHA_ERR_UNSUPPORTED).
+ * The EXLR8 format page notes that weights rounded to E4M3 are exact FP8
+ * values, so prefill can multiply them on FP8 tensor cores; it leaves the
+ * activation side open.  Here each token's rotated activations
+ * xh = fp16(had(x * su)) are quantised per token as escha_quantize_e4m3_rows
+ * describes (codes q, scale d), and
+ *     y = fp16( had( d * (q @ W_inner) ) * sv )
+ * with tcgen05 kind::f8f6f4 MMAs (E4M3 x E4M3, fp32 TMEM accumulators).  The
+ * result differs from escha_linear_gemm's by the activation rounding (up to
+ * 2^-4 relative per activation).  x fp16 [M, in], y fp16 [M, out], M >= 1,
+ * in <= 65536 (else ESCHA_ERR_UNSUPPORTED); 16-byte aligned.  Uses the same
+ * workspace as escha_linear_gemm (codes in place of the rotated activations).
+ */
+escha_status_t escha_linear_gemm_fp8(escha_linear_t h, const uint16_t* x, uint16_t* y, int M,
+                                     void* stream);
+
+/*
+ * The FP8 prefill's contraction on activations the caller has quantised:
+ *     y = fp16( had( d * (q @ W_inner) ) * sv )
+ * q uint8 [M, in]: E4M3 bit patterns of the rotated activations (for example
+ * from escha_quantize_e4m3_rows); d fp32 [M]: their per-row scales.  Device
+ * pointers, q and y 16-byte aligned, d 4-byte aligned; M >= 1.  Same handle
+ * requirement (ESCHA_ROUND_E4M3) and workspace as escha_linear_gemm_fp8.
+ */
+escha_status_t escha_linear_gemm_fp8_codes(escha_linear_t h, const uint8_t* q, const float* d,
+                                           uint16_t* y, int M, void* stream);
+
+/*
+ * Per-token FP8 E4M3 quantisation of fp16 activations, the FP8 prefill's
+ * activation step on its own (a reading of the EXLR8 format page, which leaves
+ * it open).  For each row m of xh:
+ *     amax = max_k |xh[m, k]|,  inv = 448 / amax,  d[m] = amax / 448
+ *     q[m, k] = E4M3( xh[m, k] * inv )    nearest even, saturating at 448
+ * with both quotients and the product rounded to fp32 (IEEE, nearest); a row
+ * of zeros gives q = 0 and d = 0.  xh fp16 [M, K], q uint8 [M, K] (E4M3 bit
+ * patterns), d fp32 [M]; all device pointers, 16-byte aligned, owned by the
+ * caller.  K a multiple of 128 with 128 <= K <= 65536, M >= 1, else
+ * ESCHA_ERR_INVALID_ARG.  Asynchronous on `stream`.
+ */
+escha_status_t escha_quantize_e4m3_rows(const uint16_t* xh, uint8_t* q, float* d, int M, int K,
+                                        void* stream);
+
+/*
  * Gated MLP at decode: y = down( silu(gate(x)) * up(x) ), each matrix a dense
  * trellis layer with its own rin/rout/s_in/s_out.  gate and up map in -> inter,
  * down maps inter -> in.  The three handles are borrowed.  1 <= M <= 16.
@@ -295,9 +338,9 @@ escha_status_t escha_linear_moe_gemv_stage(escha_moe_t m, int stage, const uint1
 /*
  * Codebook rounding of a handle's weights.  ESCHA_ROUND_FP16 (default): each
  * weight is the codebook's fp16 value.  ESCHA_ROUND_E4M3: the EXLR8 variant
- * (EXLR8 format page: "Every value the codebook produces is rounded to E4M3
- * (round-to-nearest-even, saturating)"): the fp16 value is rounded to the
- * nearest FP8 E4M3 value, ties to even, magnitudes past 448 clamped to 448.
+ * (EXLR8 format page, the E4M3 rounding inside the Viterbi search): the fp16
+ * value is rounded to the nearest FP8 E4M3 value, ties to even, magnitudes
+ * past 448 clamped to 448.
  * Applies to every later decode, GEMV and GEMM of the handle (MoE: every
  * routed expert).  Synchronises the device.  A gated MLP takes each matrix's
  * rounding when it is created.  Other values: ESCHA_ERR_INVALID_ARG.

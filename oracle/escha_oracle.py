@@ -518,7 +518,16 @@ def linear_forward_fp8(x, w_inner, su, sv):
     two E4M3 operands and everything after it is fp64.
     """
     q, d = quantize_rows_e4m3(rotate_in_fp16(x, su))
-    y_pre = (q @ np.asarray(w_inner).astype(np.float64)) * d.astype(np.float64)[:, None]
+    return linear_forward_fp8_codes(q, d, w_inner, sv)
+
+
+def linear_forward_fp8_codes(q, d, w_inner, sv):
+    """The FP8 layer after quantisation: y = had(d * (q @ W_inner)) * sv, fp64.
+
+    q: [M, K] E4M3 activation values; d: [M] their per-row scales.
+    """
+    y_pre = (np.asarray(q, dtype=np.float64) @ np.asarray(w_inner).astype(np.float64))
+    y_pre = y_pre * np.asarray(d).astype(np.float64)[:, None]
     return had_blockwise(y_pre) * sv
 
 

@@ -59,6 +59,17 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
     assert lib.escha_trellis_encode(fake, 24, 16, 2, 0, fake, None, None) == 2   # not whole tiles
     assert lib.escha_trellis_encode(fake, 16, 16, 5, 0, fake, None, None) == 2   # bits
     assert lib.escha_trellis_encode(fake, 16, 16, 2, 3, fake, None, None) == 1   # rounding
+    assert lib.escha_linear_gemm_fp8(None, fake, fake, 1, None) == 1
+    assert lib.escha_linear_gemm_fp8(fake, fake, fake, 0, None) == 1
+    assert lib.escha_linear_gemm_fp8_codes(fake, None, fake, fake, 1, None) == 1
+    assert lib.escha_linear_gemm_fp8_codes(fake, fake, fake, fake, 0, None) == 1
+    assert lib.escha_linear_gemm_fp8_codes(fake, fake, ctypes.c_void_p(0x10002), fake, 1, None) == 1
+    assert lib.escha_quantize_e4m3_rows(None, fake, fake, 1, 128, None) == 1
+    assert lib.escha_quantize_e4m3_rows(fake, fake, fake, 0, 128, None) == 1
+    for k in (0, 64, 200, 65536 + 128):                  # K: multiple of 128, at most 65536
+        assert lib.escha_quantize_e4m3_rows(fake, fake, fake, 1, k, None) == 1, k
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.escha_quantize_e4m3_rows(fake, odd, fake, 1, 128, None) == 1    # alignment
 
 
 def test_bad_config_rejected_on_host(lib):
