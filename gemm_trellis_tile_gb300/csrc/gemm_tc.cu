@@ -90,6 +90,8 @@ struct GemmArgs {
   const uint8_t* code;
   const float* sv;
   const float* d;        // FP8: per-row activation scales [M]; else null
+  uint32_t mcg_mask;     // the codebook's mask and flip words, passed at run time so
+  uint32_t mcg_xor;      // that each state's mask-and-flip is one three-input logic op
   uint16_t* y;
   float* ws;             // partial sums: [grid][2][kBM][kBN] fp32
   int M, N, K;
@@ -162,6 +164,13 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Lane-wise fp16 sum of two fp16 pairs (round to nearest even).
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  const __half2 s = __hadd2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&s);
 }
 
 // Two fp16 values (low half first) to two E4M3 bytes (low byte first),
@@ -483,6 +492,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     const int acc = dw >> 2;           // accumulator (128-row slice) it finishes
     const LaneWindow lw = lane_window<BITS>(lane);
     const int g = lane >> 2, t = lane & 3;
+    const uint32_t mcg_mask = a.mcg_mask, mcg_xor = a.mcg_xor;
     bool ok = true;
     Ring<kCStages> rc;
     Ring<kBStages> rb;
@@ -507,22 +517,39 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         for (int i = 0; i < NTW; ++i) {
           const int nt = nt_base + i;
           const uint32_t* tw = reinterpret_cast<const uint32_t*>(codes + (kt_local * 8 + nt) * T);
-          uint32_t h[8];
-          // symbols 2p, 2p+1 of the lane: input channels k, k+1 of output channel n
-          decode8<BITS, E4M3 && !FP8>(tw[lw.i0], tw[lw.i1], lw.sh7, h);
+          uint32_t v[8];  // codebook words (fp16 lo, fp16 hi) of the lane's symbols
+          decode8_pairs<BITS>(tw[lw.i0], tw[lw.i1], lw.sh7, mcg_mask, mcg_xor, v);
+          // symbols 2p, 2p+1 (p = 2 nh + rh) are input channels k, k+1 of output
+          // channel n = 16 nt + g + 8 nh, k = 16 kt_local + 8 rh + 2t; one fp16
+          // addition per weight, two weights per instruction
+          uint32_t pair[4];
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const int rh = p & 1, nh = p >> 1;
-            const int n = 16 * nt + g + 8 * nh;   // n & 7 == g: the row's swizzle phase
-            const uint32_t pair = __byte_perm(h[2 * p], h[2 * p + 1], 0x5410);
-            if constexpr (FP8) {
-              // k = 16 kt_local + 8 rh + 2t: byte k of the row, 16-byte chunk kt_local
-              const int chunk = kt_local ^ g;
-              *reinterpret_cast<uint16_t*>(bt + n * 128 + chunk * 16 + 8 * rh + 2 * t) =
-                  e4m3x2_from_f16x2(pair);
-            } else {
+          for (int p = 0; p < 4; ++p)
+            pair[p] = hadd2_u32(__byte_perm(v[2 * p], v[2 * p + 1], 0x5410),
+                                __byte_perm(v[2 * p], v[2 * p + 1], 0x7632));
+          if constexpr (FP8) {
+            // Bytes k, k+1 of row n.  Lanes t and t^1 swap halves so that each
+            // stores one whole word: even t bytes 2t..2t+3 (rh = 0), odd t bytes
+            // 8 + 2(t-1) .. +3 (rh = 1), all in the row's 16-byte chunk kt_local.
+            const bool odd = t & 1;
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+              const uint32_t e0 = e4m3x2_from_f16x2(pair[2 * nh]);
+              const uint32_t e1 = e4m3x2_from_f16x2(pair[2 * nh + 1]);
+              const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? e0 : e1, 1);
+              const uint32_t word = odd ? (recv | (e1 << 16)) : (e0 | (recv << 16));
+              const int n = 16 * nt + g + 8 * nh;   // n & 7 == g: the row's swizzle phase
+              const int off = 8 * (t & 1) + 2 * (t & 2);
+              *reinterpret_cast<uint32_t*>(bt + n * 128 + (kt_local ^ g) * 16 + off) = word;
+            }
+          } else {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const int rh = p & 1, nh = p >> 1;
+              const int n = 16 * nt + g + 8 * nh;
               const int chunk = (2 * kt_local + rh) ^ g;
-              *reinterpret_cast<uint32_t*>(bt + n * 128 + chunk * 16 + 4 * t) = pair;
+              *reinterpret_cast<uint32_t*>(bt + n * 128 + chunk * 16 + 4 * t) =
+                  E4M3 ? round_e4m3x2(pair[p]) : pair[p];
             }
           }
         }
@@ -706,6 +733,8 @@ cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t
   a.code = reinterpret_cast<const uint8_t*>(code);
   a.sv = sv;
   a.d = fp8 ? d : nullptr;
+  a.mcg_mask = kMcgMask;
+  a.mcg_xor = kMcgXor;
   a.y = y;
   a.ws = ws;
   a.M = M;
