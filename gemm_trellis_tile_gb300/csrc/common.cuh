@@ -159,7 +159,9 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 // Fast Walsh-Hadamard transform of one 128-block held by a warp, four
 // consecutive elements per lane (element 4*lane + r in v[r]); natural
 // (Sylvester) order, unnormalised.  Two butterfly stages in registers, five
-// across lanes.
+// across lanes.  A cross-lane stage forms v + o in the lower lane and o - v in
+// the upper one as fma(+-1, v, o): the product by +-1 is exact, so this is the
+// same single rounding as the addition, in one instruction.
 __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
   const float a0 = v[0] + v[1], a1 = v[0] - v[1];
   const float a2 = v[2] + v[3], a3 = v[2] - v[3];
@@ -170,34 +172,13 @@ __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
 #pragma unroll
   for (int s = 0; s < 5; ++s) {
     const int m = 1 << s;
-    const bool upper = (lane & m) != 0;
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const float o = __shfl_xor_sync(0xffffffffu, v[r], m);
-      v[r] = upper ? (o - v[r]) : (v[r] + o);
+      v[r] = fmaf(sgn, v[r], o);
     }
   }
-}
-
-// Same transform with element lane + 32*r held in v[r]: the two highest index
-// bits are in registers, the five lowest across lanes.
-__device__ __forceinline__ void fwht128_warp_strided(float (&v)[4], int lane) {
-#pragma unroll
-  for (int s = 0; s < 5; ++s) {
-    const int m = 1 << s;
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[r], m);
-      v[r] = upper ? (o - v[r]) : (v[r] + o);
-    }
-  }
-  const float a0 = v[0] + v[1], a1 = v[0] - v[1];
-  const float a2 = v[2] + v[3], a3 = v[2] - v[3];
-  v[0] = a0 + a2;
-  v[2] = a0 - a2;
-  v[1] = a1 + a3;
-  v[3] = a1 - a3;
 }
 
 __device__ __forceinline__ float half_bits_to_float(uint16_t b) {

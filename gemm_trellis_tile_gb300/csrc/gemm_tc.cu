@@ -660,9 +660,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   }
 }
 
-// Fix-up for tiles shared by several CTAs: y = fp16(had128(sum of partials) * sv).
-// One warp per (listed tile, row); element lane + 32*q in v[q].
+// Fix-up for tiles shared by several CTAs: y = fp16(had128(d * sum of partials) * sv).
+// One warp per (listed tile, kFixRows consecutive rows); lane l holds columns
+// 4l..4l+3 of each row, and every partial-sum load of the warp is issued before
+// the first addition, so the loads' latencies overlap.
 constexpr int kMaxSplitTiles = 512;
+constexpr int kFixRows = 4;
+constexpr int kFixWarps = 8;
 struct FixupArgs {
   const float* ws;
   const float* sv;
@@ -673,30 +677,48 @@ struct FixupArgs {
   int tiles[kMaxSplitTiles];
 };
 
-__global__ void gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
+__global__ void __launch_bounds__(32 * kFixWarps)
+    gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int row0 = (blockIdx.y * kFixWarps + (threadIdx.x >> 5)) * kFixRows;  // row in the tile
   const int tile = f.tiles[blockIdx.x];
-  const int m = (tile / f.n_blocks) * kBM + row;
-  if (m >= f.M) return;
+  const int m0 = (tile / f.n_blocks) * kBM + row0;
+  if (m0 >= f.M) return;  // the whole warp: rows past M
   const int n0 = (tile % f.n_blocks) * kBN;
   const long long t_first = (long long)tile * f.kb_per_tile;
   const int c0 = owner(t_first, f.units, f.grid);
   const int c1 = owner(t_first + f.kb_per_tile - 1, f.units, f.grid);
-  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  float v[kFixRows][4] = {};
   for (int c = c0; c <= c1; ++c) {
     const long long cb = range_start(c, f.units, f.grid);
     const int which = (t_first <= cb) ? 0 : 1;
-    const float* wrow = f.ws + ((size_t)(2 * c + which) * kBM + row) * kBN;
+    const float* p = f.ws + ((size_t)(2 * c + which) * kBM + row0) * kBN + 4 * lane;
+    float4 q[kFixRows];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) v[q] += wrow[lane + 32 * q];
+    for (int i = 0; i < kFixRows; ++i) q[i] = *reinterpret_cast<const float4*>(p + i * kBN);
+#pragma unroll
+    for (int i = 0; i < kFixRows; ++i) {
+      v[i][0] += q[i].x;
+      v[i][1] += q[i].y;
+      v[i][2] += q[i].z;
+      v[i][3] += q[i].w;
+    }
   }
-  fwht128_warp_strided(v, lane);
-  const float dm = f.d ? f.d[m] : 1.f;
-  uint16_t* yr = f.y + (size_t)m * f.N + n0 + lane;
+  const float4 s = *reinterpret_cast<const float4*>(f.sv + n0 + 4 * lane);
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    yr[32 * q] = float_to_half_bits(v[q] * kHadScale * dm * f.sv[n0 + lane + 32 * q]);
+  for (int i = 0; i < kFixRows; ++i) {
+    fwht128_warp(v[i], lane);
+    const int m = m0 + i;
+    if (m < f.M) {
+      const float sc = kHadScale * (f.d ? f.d[m] : 1.f);
+      const float o[4] = {v[i][0] * sc * s.x, v[i][1] * sc * s.y, v[i][2] * sc * s.z,
+                          v[i][3] * sc * s.w};
+      uint2 raw;
+      raw.x = float_to_half_bits(o[0]) | (uint32_t(float_to_half_bits(o[1])) << 16);
+      raw.y = float_to_half_bits(o[2]) | (uint32_t(float_to_half_bits(o[3])) << 16);
+      *reinterpret_cast<uint2*>(f.y + (size_t)m * f.N + n0 + 4 * lane) = raw;
+    }
+  }
 }
 
 template <int BITS, bool E4M3, bool FP8>
@@ -788,8 +810,8 @@ cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t
   }
   if (e != cudaSuccess) return e;
   if (f.count > 0) {
-    dim3 grid(f.count, kBM / 8);
-    gemm_fixup_kernel<<<grid, 256, 0, st>>>(f);
+    dim3 grid(f.count, kBM / (kFixWarps * kFixRows));
+    gemm_fixup_kernel<<<grid, 32 * kFixWarps, 0, st>>>(f);
     e = cudaGetLastError();
   }
   return e;
