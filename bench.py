@@ -45,6 +45,12 @@ L2_FALLBACK_BYTES = 129 * 1024 * 1024
 GEMV_TRAFFIC_BYTES = {
     "dense gated MLP 5120->17408->5120, gate 2-bit / up 3-bit / down 3-bit, M=1": 44.69e6,
 }
+# The same for one prefill GEMM launch (the trellis_gemm kernel alone).
+PREFILL_TRAFFIC_BYTES = {
+    "prefill GEMM 5120x17408 3-bit, M=2048 tokens": 129.93e6,
+    "prefill GEMM 5120x17408 3-bit, M=2048 tokens, FP8 tensor cores (E4M3 weights, "
+    "per-token E4M3 activations)": 120.54e6,
+}
 
 
 def parse_args():
@@ -709,7 +715,8 @@ def run_prefill(args, spec, rank, world, local):
                    "timing": "CUDA events around back-to-back public API calls"},
         "roofline": {"bound": "tensor", "kernel": "trellis_gemm", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak if achieved else None, "traffic": None,
+                     "frac": achieved / peak if achieved else None,
+                     "traffic": PREFILL_TRAFFIC_BYTES.get(spec["name"]),
                      "peak_source": peak_note},
         "e2e": {"value": e_steps * flops / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
