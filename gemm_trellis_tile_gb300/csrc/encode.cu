@@ -1,10 +1,11 @@
 // Trellis encoder: the Viterbi search that picks each tile's code.
 //
-// EXLR8 format page: "A 16x16 tile is encoded jointly ... The Viterbi search
-// picks the path minimizing the tile's squared error, with per-step values
-// drawn from the mcg codebook"; the E4M3 variant rounds every codebook value
-// inside the search.  The stream is circular (tail-biting, "Escha-W2 runs on
-// Metal": code i is the 16-bit window at offset i*K, circular).
+// EXLR8 format page, the Viterbi search: each 16x16 tile is coded as a whole,
+// by the trellis path whose decoded values (the mcg codebook's value of each
+// step's state) have the least squared error against the tile; the E4M3
+// variant rounds every codebook value inside the search.  The stream is
+// circular (tail-biting; "Escha-W2 runs on Metal": code i is the 16-bit window
+// at offset i*K, wrapping around).
 //
 // State s of symbol i is its 16-bit window; the next state is
 // ((s << K) | new K bits) & 0xFFFF, so the predecessors of state s are the

@@ -191,8 +191,8 @@ escha_status_t escha_mlp_gemv(escha_mlp_t m, const uint16_t* x, uint16_t* y, int
  * paragraph): after this call escha_mlp_gemv computes
  *     n = x / sqrt(mean(x^2) + eps) * w,   y = down( silu(gate(n)) * up(n) )
  * per token, the norm fused into the input rotations (one launch per call, as
- * before).  norm_w: DEVICE fp16 [in], the weight as stored; escha stores
- * RMSNorm weights centred on zero, so with stored_minus_one != 0 the weight
+ * before).  norm_w: DEVICE fp16 [in], the weight as stored; escha keeps
+ * its RMSNorm weights minus one, so with stored_minus_one != 0 the weight
  * applied is norm_w + 1 (the gated norms inside a linear-attention block carry
  * no offset: pass 0).  norm_w is read during this call only (folded with the
  * gate and up input scales); eps in [0, 1).  norm_w = NULL removes the norm.
@@ -233,8 +233,8 @@ escha_status_t escha_moe_create(escha_moe_t* out, int num_experts, int hidden, i
  * expert matrix is split into H = inter/128 halves of 128 intermediate
  * channels.  Gate and up are split along their output channels and each half
  * has its own width; down is split along its input channels and has one width
- * per expert.  Kernels get a pointer table ptr[e][h] instead of one pointer per
- * matrix, and the table is re-read at every launch.  Everything else (shared
+ * per expert.  The kernels read a device table of half pointers, ptr[e][h], in
+ * place of one pointer per matrix, fetching it anew on every launch.  Everything else (shared
  * hidden-side rotation, side vectors, the call escha_linear_moe_gemv and its
  * stages, rounding, check) is as for escha_moe_create.
  *   gate_half, up_half  DEVICE arrays [E * H] of device pointers: entry

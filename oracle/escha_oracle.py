@@ -131,7 +131,7 @@ def tile_states_k2_printed(tile_code):
 
     Lane L handles symbols t = 8L .. 8L+7.  It forms a 64-bit value from the
     word pair (i0, i1), shifts it right by 16 when bit 3 of t is clear, and
-    symbol t+j is the 16-bit window at shift 14-2j.  Independent of the stream
+    takes symbol t+j as the 16 bits that sit 14-2j bits above the bottom.  Independent of the stream
     model above; the two must agree.
     """
     u32 = tile_u32_words(tile_code)
@@ -193,8 +193,8 @@ def codebook_value(states):
 
 
 # ----------------------------------------------------------------------------
-# E4M3 rounding of codebook values  ([EXLR8] "Every value the codebook produces
-# is rounded to E4M3 (round-to-nearest-even, saturating)")
+# E4M3 rounding of codebook values  ([EXLR8]: each codebook output is rounded
+# to FP8 E4M3, nearest even, saturating)
 # ----------------------------------------------------------------------------
 
 E4M3_MAX = 448.0        # largest finite FP8 E4M3 value: 1.75 * 2^8
@@ -233,8 +233,8 @@ def codebook(states, rounding="fp16"):
 
 
 # ----------------------------------------------------------------------------
-# Trellis encoder: Viterbi search  ([EXLR8] "The Viterbi search picks the path
-# minimizing the tile's squared error"; [MLX] tail-biting windows)
+# Trellis encoder: Viterbi search  ([EXLR8]: the code of a tile is the trellis
+# path of least squared error; [MLX] tail-biting windows)
 # ----------------------------------------------------------------------------
 
 def _viterbi_pass(values, bits, cvals, start_ok=None, end_ok=None):
@@ -392,8 +392,8 @@ def decode_row_halves(halves, bits, rounding="fp16"):
     """W_inner [128*H, out] of a matrix stored by halves along its input side.
 
     [EXLR8] manifest paragraph: down's halves are 128 of its input (intermediate)
-    channels, and down has one width per expert ("its width must be uniform
-    across the expert").  halves[h] is the code int16 [8, out/16, 16*bits] of
+    channels, and down has one width per expert (the error feedback of its
+    calibrated rounding crosses halves).  halves[h] is the code int16 [8, out/16, 16*bits] of
     input channels 128h .. 128h+127; the matrix is the halves' decoded rows
     stacked in order.
     """
@@ -543,8 +543,8 @@ def linear_forward_fp8_columns(x, code, bits, su, sv, blocks):
 def rms_norm(x, w_stored, eps, stored_minus_one=True):
     """RMSNorm of each row of x: x / sqrt(mean(x^2) + eps) * w, fp64.
 
-    "Escha-W2 runs on Metal", model-loading paragraph: escha stores RMSNorm
-    weights centred on zero (w - 1), so the weight applied is stored + 1 --
+    "Escha-W2 runs on Metal", model-loading paragraph: the checkpoint keeps
+    RMSNorm weights minus one (w - 1), so the weight applied is stored + 1 --
     except the gated norms inside the linear-attention block, which are
     stored as they are (stored_minus_one=False).
     """

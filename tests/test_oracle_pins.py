@@ -158,7 +158,7 @@ def test_stream_model_equals_printed_k2_decoder():
 
 @pytest.mark.parametrize("bits", [2, 3, 4])
 def test_overlap_invariant_including_wrap(bits):
-    """Low 16-bits bits of state t equal the high 16-bits bits of state t+1 (255 -> 0 too)."""
+    """State t+1 begins with state t's last 16-bits bits (including 255 -> 0)."""
     rng = np.random.default_rng(3 + bits)
     st = O.tile_states(random_tiles(rng, 256, bits), bits).astype(np.int64)
     nxt = np.roll(st, -1, axis=-1)
@@ -759,9 +759,9 @@ def test_encoder_path_is_locally_optimal(bits):
 
 @pytest.mark.parametrize("bits", [2, 3])
 def test_encoder_sits_near_the_shannon_bound(bits):
-    """Gaussian source at rate R: relative Frobenius error >= 2^-R (no code can
-    beat it), and trellis coding comes close ([MLX]: "within a few percent" on
-    the model's Hadamard-rotated weights; on 8 random Gaussian tiles this
+    """Gaussian weights coded at R bits each: no code gets the relative
+    Frobenius error below 2^-R, and trellis coding comes close ([MLX] puts it a
+    few percent above the bound on the model's Hadamard-rotated weights; on 8 random Gaussian tiles this
     encoder lands 9-10 % above the bound at 2 and 3 bits)."""
     rng = np.random.default_rng(930 + bits)
     num, den = 0.0, 0.0
