@@ -873,19 +873,11 @@ def props_sms(dev):
 
 
 def prefill_launches(m, k, n, sms, fp8=False):
-    """Launches of one prefill call: the input rotation (FP8: rotation and
-    quantisation), the GEMM, and the fix-up kernel when stream-K splits a
-    512 x 128 tile between CTAs (the GEMM's own rule: at least 16 K-blocks of
-    128 bytes per row per CTA, at most one CTA per SM)."""
-    kb = k // (128 if fp8 else 64)
-    tiles = -(-m // 512) * (n // 128)
-    units = tiles * kb
-    grid = max(1, min(sms, units // 16))
-
-    def owner(u):
-        return ((u + 1) * grid - 1) // units
-    split = any(owner(t * kb) != owner(t * kb + kb - 1) for t in range(tiles))
-    return 3 if split else 2
+    """Kernels of one prefill call: the input rotation (FP8: rotation and
+    quantisation) and the GEMM, which finishes tiles shared between CTAs
+    itself.  (The call also clears the shared tiles' arrival counters with a
+    cudaMemsetAsync, which is not a kernel of this library.)"""
+    return 2
 
 
 def make_handles(spec, inst):

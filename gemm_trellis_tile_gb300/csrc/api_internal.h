@@ -50,6 +50,8 @@ struct escha_linear_s {
   float* xd = nullptr;        // FP8 prefill: per-row activation scales [xh_rows]
   int xh_rows = 0;
   float* gemm_ws = nullptr;   // prefill partial sums of tiles shared between CTAs
+  int* gemm_cnt = nullptr;    // prefill arrival counters of shared tiles, cleared per call
+  size_t gemm_cnt_ints = 0;
   escha::Profiler prof;
 };
 

@@ -7,9 +7,12 @@
 // TMEM (all 512 columns) share one decoded 128 x 64 B block per K step, so each
 // weight is decoded once per 512 rows.  The kernel is persistent: the grid's
 // CTAs split the (tile, K-block) units evenly and contiguously (stream-K).  A
-// CTA whose range covers a whole tile runs the fused epilogue; where a tile is
-// shared between CTAs each writes its fp32 partial sums and a fix-up kernel
-// sums them and applies the epilogue.
+// CTA whose range covers a whole tile runs the fused epilogue.  Where a tile is
+// shared between CTAs, each decoder warp of each CTA either writes its rows'
+// fp32 partial sums and counts itself in (a counter per tile and warp), or, if
+// it is the last to get there, sums every CTA's partials in CTA order into its
+// accumulators and runs the epilogue.  No CTA waits for another, and the sum
+// does not depend on which CTA finishes.
 //
 // Warp roles (19 warps):
 //   warp 0      A producer: TMA tiled loads of the 512 x 64 activation block
@@ -94,6 +97,7 @@ struct GemmArgs {
   uint32_t mcg_xor;      // that each state's mask-and-flip is one three-input logic op
   uint16_t* y;
   float* ws;             // partial sums: [grid][2][kBM][kBN] fp32
+  int* tile_cnt;         // [tiles][kDecWarps] arrival counters, zero at launch
   int M, N, K;
   int n_blocks;          // N / kBN
   int kb_per_tile;       // K / (K elements per block)
@@ -173,6 +177,12 @@ __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t*>(&s);
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Two fp16 values (low half first) to two E4M3 bytes (low byte first),
 // nearest even, saturating.
 __device__ __forceinline__ uint16_t e4m3x2_from_f16x2(uint32_t h2) {
@@ -242,6 +252,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                   taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -575,10 +593,77 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       const int row = acc * 128 + quad * 32 + lane;
       const int m = m0 + row;
       const long long t_first = (long long)seg.tile * a.kb_per_tile;
-      const bool fused =
-          owner(t_first, a.units, a.grid) == owner(t_first + a.kb_per_tile - 1, a.units, a.grid);
+      const int c_first = owner(t_first, a.units, a.grid);
+      const int c_last = owner(t_first + a.kb_per_tile - 1, a.units, a.grid);
       const int n0 = nb * kBN;
-      if (fused) {
+      bool finish = c_first == c_last;  // this CTA holds the whole tile
+      if (!finish) {
+        // A shared tile.  This warp's rows of it are finished by the last of the
+        // tile's c_last - c_first + 1 CTAs to arrive here; the others leave their
+        // partial sums (slot 0: a CTA's first tile, slot 1: a later one).
+        int* cnt = a.tile_cnt + (size_t)seg.tile * kDecWarps + dw;
+        const int others = c_last - c_first;
+        int is_last = 0;
+        if (lane == 0) is_last = ld_acquire_gpu(cnt) == others;
+        is_last = __shfl_sync(0xFFFFFFFFu, is_last, 0);
+        if (!is_last) {
+          const int which = (t_first <= u_begin) ? 0 : 1;
+          float* wrow = a.ws + ((size_t)(2 * c + which) * kBM + row) * kBN;
+#pragma unroll 1
+          for (int c16 = 0; c16 < kBN; c16 += 16) {
+            float u[16];
+            tmem_ld16(tl + c16, u);
+            tmem_wait_ld();
+            float4* dst = reinterpret_cast<float4*>(wrow + c16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();  // the warp's partial sums before its count
+            is_last = atomicAdd(cnt, 1) == others;
+          }
+          is_last = __shfl_sync(0xFFFFFFFFu, is_last, 0);
+        }
+        if (is_last && lane == 0) __threadfence();  // every other partial is visible
+        __syncwarp();
+        finish = is_last != 0;
+      }
+      if (finish && c_first != c_last) {
+        // the last arrival: accumulators <- the CTAs' partial sums added in CTA
+        // order (this CTA's own from its accumulators), 8 columns at a time
+#pragma unroll 1
+        for (int c8 = 0; c8 < kBN; c8 += 8) {
+          float w[8], s[8];
+          tmem_ld8(tl + c8, w);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s[j] = 0.f;
+          for (int cc = c_first; cc <= c_last; ++cc) {
+            if (cc == c) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) s[j] += w[j];
+            } else {
+              const int wh = (t_first <= range_start(cc, a.units, a.grid)) ? 0 : 1;
+              const float4* src = reinterpret_cast<const float4*>(
+                  a.ws + ((size_t)(2 * cc + wh) * kBM + row) * kBN + c8);
+              const float4 p0 = src[0], p1 = src[1];
+              s[0] += p0.x;
+              s[1] += p0.y;
+              s[2] += p0.z;
+              s[3] += p0.w;
+              s[4] += p1.x;
+              s[5] += p1.y;
+              s[6] += p1.z;
+              s[7] += p1.w;
+            }
+          }
+          tmem_st8(tl + c8, s);
+        }
+        tmem_wait_st();
+      }
+      if (finish) {
         // FP8: the row's activation scale joins the output scale
         const float dm = FP8 ? (m < a.M ? __ldg(a.d + m) : 0.f) : 1.f;
         // index bits 0..4: a 32-point transform on each 32-column chunk, in TMEM
@@ -630,20 +715,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             }
           }
         }
-      } else {
-        // partial sums of a shared tile: slot 0 = this CTA's first tile, slot 1 = a later one
-        const int which = (t_first <= u_begin) ? 0 : 1;
-        float* wrow = a.ws + ((size_t)(2 * c + which) * kBM + row) * kBN;
-#pragma unroll 1
-        for (int c16 = 0; c16 < kBN; c16 += 16) {
-          float u[16];
-          tmem_ld16(tl + c16, u);
-          tmem_wait_ld();
-          float4* d = reinterpret_cast<float4*>(wrow + c16);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d[q] = make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
-        }
       }
       tc_fence_before();
       __syncwarp();
@@ -660,67 +731,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   }
 }
 
-// Fix-up for tiles shared by several CTAs: y = fp16(had128(d * sum of partials) * sv).
-// One warp per (listed tile, kFixRows consecutive rows); lane l holds columns
-// 4l..4l+3 of each row, and every partial-sum load of the warp is issued before
-// the first addition, so the loads' latencies overlap.
-constexpr int kMaxSplitTiles = 512;
-constexpr int kFixRows = 4;
-constexpr int kFixWarps = 8;
-struct FixupArgs {
-  const float* ws;
-  const float* sv;
-  const float* d;  // per-row activation scales (FP8), or null
-  uint16_t* y;
-  int M, N, n_blocks, kb_per_tile, grid, count;
-  long long units;
-  int tiles[kMaxSplitTiles];
-};
-
-__global__ void __launch_bounds__(32 * kFixWarps)
-    gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
-  const int lane = threadIdx.x & 31;
-  const int row0 = (blockIdx.y * kFixWarps + (threadIdx.x >> 5)) * kFixRows;  // row in the tile
-  const int tile = f.tiles[blockIdx.x];
-  const int m0 = (tile / f.n_blocks) * kBM + row0;
-  if (m0 >= f.M) return;  // the whole warp: rows past M
-  const int n0 = (tile % f.n_blocks) * kBN;
-  const long long t_first = (long long)tile * f.kb_per_tile;
-  const int c0 = owner(t_first, f.units, f.grid);
-  const int c1 = owner(t_first + f.kb_per_tile - 1, f.units, f.grid);
-  float v[kFixRows][4] = {};
-  for (int c = c0; c <= c1; ++c) {
-    const long long cb = range_start(c, f.units, f.grid);
-    const int which = (t_first <= cb) ? 0 : 1;
-    const float* p = f.ws + ((size_t)(2 * c + which) * kBM + row0) * kBN + 4 * lane;
-    float4 q[kFixRows];
-#pragma unroll
-    for (int i = 0; i < kFixRows; ++i) q[i] = *reinterpret_cast<const float4*>(p + i * kBN);
-#pragma unroll
-    for (int i = 0; i < kFixRows; ++i) {
-      v[i][0] += q[i].x;
-      v[i][1] += q[i].y;
-      v[i][2] += q[i].z;
-      v[i][3] += q[i].w;
-    }
-  }
-  const float4 s = *reinterpret_cast<const float4*>(f.sv + n0 + 4 * lane);
-#pragma unroll
-  for (int i = 0; i < kFixRows; ++i) {
-    fwht128_warp(v[i], lane);
-    const int m = m0 + i;
-    if (m < f.M) {
-      const float sc = kHadScale * (f.d ? f.d[m] : 1.f);
-      const float o[4] = {v[i][0] * sc * s.x, v[i][1] * sc * s.y, v[i][2] * sc * s.z,
-                          v[i][3] * sc * s.w};
-      uint2 raw;
-      raw.x = float_to_half_bits(o[0]) | (uint32_t(float_to_half_bits(o[1])) << 16);
-      raw.y = float_to_half_bits(o[2]) | (uint32_t(float_to_half_bits(o[3])) << 16);
-      *reinterpret_cast<uint2*>(f.y + (size_t)m * f.N + n0 + 4 * lane) = raw;
-    }
-  }
-}
-
 template <int BITS, bool E4M3, bool FP8>
 cudaError_t launch_gemm_bits(const CUtensorMap& map, const GemmArgs& a, cudaStream_t st) {
   constexpr int smem = BlockGeom<FP8>::kSmemBytes;
@@ -732,11 +742,11 @@ cudaError_t launch_gemm_bits(const CUtensorMap& map, const GemmArgs& a, cudaStre
 }
 
 // Shared by both operand types: the activation tensor map (rows of K elements
-// of `esize` bytes, 128-byte boxes, 128B swizzle), the stream-K split, the list
-// of tiles shared between CTAs, the kernel and the fix-up launch.
+// of `esize` bytes, 128-byte boxes, 128B swizzle), the stream-K split and the
+// kernel launch.
 cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t* code, int bits,
                         bool e4m3, int M, int K, int N, const float* sv, uint16_t* y, float* ws,
-                        int num_sms, int* err, cudaStream_t st) {
+                        int* tile_cnt, int num_sms, int* err, cudaStream_t st) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
   const int esize = fp8 ? 1 : 2;
@@ -759,6 +769,7 @@ cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t
   a.mcg_xor = kMcgXor;
   a.y = y;
   a.ws = ws;
+  a.tile_cnt = tile_cnt;
   a.M = M;
   a.N = N;
   a.K = K;
@@ -774,26 +785,6 @@ cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t
   a.err = err;
   a.limit_ns = kWaitLimitNs;
 
-  FixupArgs f;
-  f.ws = ws;
-  f.sv = sv;
-  f.d = a.d;
-  f.y = y;
-  f.M = M;
-  f.N = N;
-  f.n_blocks = a.n_blocks;
-  f.kb_per_tile = a.kb_per_tile;
-  f.grid = a.grid;
-  f.units = a.units;
-  f.count = 0;
-  for (long long t = 0; t < tiles; ++t) {
-    const long long t0 = t * a.kb_per_tile;
-    if (owner(t0, a.units, a.grid) != owner(t0 + a.kb_per_tile - 1, a.units, a.grid)) {
-      if (f.count >= kMaxSplitTiles) return cudaErrorInvalidValue;
-      f.tiles[f.count++] = static_cast<int>(t);
-    }
-  }
-
   cudaError_t e;
   if (fp8) {
     switch (bits) {
@@ -808,12 +799,6 @@ cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t
       default: e = e4m3 ? launch_gemm_bits<4, true, false>(map, a, st) : launch_gemm_bits<4, false, false>(map, a, st); break;
     }
   }
-  if (e != cudaSuccess) return e;
-  if (f.count > 0) {
-    dim3 grid(f.count, kBM / (kFixWarps * kFixRows));
-    gemm_fixup_kernel<<<grid, 32 * kFixWarps, 0, st>>>(f);
-    e = cudaGetLastError();
-  }
   return e;
 }
 
@@ -821,20 +806,27 @@ cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t
 
 size_t gemm_workspace_floats(int num_sms) { return (size_t)num_sms * 2 * kBM * kBN; }
 
+size_t gemm_counter_ints(int M, int N) {
+  return (size_t)((M + kBM - 1) / kBM) * (N / kBN) * kDecWarps;
+}
+
 // xh: rotated activations fp16 [M, K] (16-byte aligned, K a multiple of 128);
 // ws: gemm_workspace_floats(num_sms) fp32.
 cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, bool e4m3,
                                 int M, int K, int N, const float* sv, uint16_t* y, float* ws,
-                                int num_sms, int* err, cudaStream_t st) {
-  return launch_gemm(xh, false, nullptr, code, bits, e4m3, M, K, N, sv, y, ws, num_sms, err, st);
+                                int* tile_cnt, int num_sms, int* err, cudaStream_t st) {
+  return launch_gemm(xh, false, nullptr, code, bits, e4m3, M, K, N, sv, y, ws, tile_cnt, num_sms,
+                     err, st);
 }
 
 // xq: E4M3 activation codes [M, K] (16-byte aligned, K a multiple of 128) with
 // per-row scales d [M]; the weights are decoded with the E4M3 rounding.
 cudaError_t launch_trellis_gemm_fp8(const uint8_t* xq, const float* d, const int16_t* code,
                                     int bits, int M, int K, int N, const float* sv, uint16_t* y,
-                                    float* ws, int num_sms, int* err, cudaStream_t st) {
-  return launch_gemm(xq, true, d, code, bits, true, M, K, N, sv, y, ws, num_sms, err, st);
+                                    float* ws, int* tile_cnt, int num_sms, int* err,
+                                    cudaStream_t st) {
+  return launch_gemm(xq, true, d, code, bits, true, M, K, N, sv, y, ws, tile_cnt, num_sms, err,
+                     st);
 }
 
 }  // namespace escha

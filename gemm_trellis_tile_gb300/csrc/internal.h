@@ -103,16 +103,19 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
                                         bool maps_from_device = false, int layout = kGemvWhole);
 // Prefill GEMM on tcgen05: y = fp16(had128(xh @ W_inner) * sv) for any M >= 1;
 // xh is fp16 [M, K], 16-byte aligned; ws holds gemm_workspace_floats(num_sms)
-// fp32 for tiles shared between CTAs.
+// fp32 for tiles shared between CTAs; tile_cnt holds gemm_counter_ints(M, N)
+// ints that are zero when the kernel starts (the caller clears them first).
 size_t gemm_workspace_floats(int num_sms);
+size_t gemm_counter_ints(int M, int N);
 cudaError_t launch_trellis_gemm(const uint16_t* xh, const int16_t* code, int bits, bool e4m3,
                                 int M, int K, int N, const float* sv, uint16_t* y, float* ws,
-                                int num_sms, int* err, cudaStream_t st);
+                                int* tile_cnt, int num_sms, int* err, cudaStream_t st);
 // FP8 prefill: xq E4M3 codes [M, K] with per-row scales d (xh ~ xq * d); the
 // weights are decoded with the E4M3 rounding and multiplied on kind::f8f6f4.
 cudaError_t launch_trellis_gemm_fp8(const uint8_t* xq, const float* d, const int16_t* code,
                                     int bits, int M, int K, int N, const float* sv, uint16_t* y,
-                                    float* ws, int num_sms, int* err, cudaStream_t st);
+                                    float* ws, int* tile_cnt, int num_sms, int* err,
+                                    cudaStream_t st);
 // Per-token E4M3 quantisation: q [M, K], d [M] from xh = fp16(had128(x * su))
 // (su != null) or from x itself (su == null).  K a multiple of 128; the block
 // keeps the row in quantize_e4m3_smem_bytes(K) of shared memory.

@@ -133,7 +133,10 @@ void linear_free(escha_linear_s* h) {
   cudaFree(h->xh);
   cudaFree(h->xd);
   cudaFree(h->gemm_ws);
+  cudaFree(h->gemm_cnt);
   h->gemm_ws = nullptr;
+  h->gemm_cnt = nullptr;
+  h->gemm_cnt_ints = 0;
   h->xd = nullptr;
   h->su = h->sv = nullptr;
   h->xfrag = nullptr;
@@ -184,6 +187,23 @@ escha_status_t linear_set_rounding(escha_linear_s* h, int rounding) {
   return upload_jobs(h->sched);
 }
 
+// Arrival counters for M-row prefill calls; a larger array replaces the old
+// one after the device has finished with it.
+escha_status_t reserve_counters(escha_linear_s* h, int M) {
+  const size_t need = gemm_counter_ints(M, h->N);
+  if (need <= h->gemm_cnt_ints) return ESCHA_OK;
+  if (h->gemm_cnt) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return ESCHA_ERR_CUDA;
+    cudaFree(h->gemm_cnt);
+    h->gemm_cnt = nullptr;
+    h->gemm_cnt_ints = 0;
+  }
+  escha_status_t s = dev_alloc(&h->gemm_cnt, need);
+  if (s != ESCHA_OK) return s;
+  h->gemm_cnt_ints = need;
+  return ESCHA_OK;
+}
+
 escha_status_t linear_reserve(escha_linear_s* h, int rows) {
   if (rows <= h->xh_rows) return ESCHA_OK;
   if (h->xh) {
@@ -200,18 +220,32 @@ escha_status_t linear_reserve(escha_linear_s* h, int rows) {
   h->xh_rows = rows;
   if (!h->gemm_ws && (s = dev_alloc(&h->gemm_ws, gemm_workspace_floats(h->num_sms))) != ESCHA_OK)
     return s;
-  return ESCHA_OK;
+  return reserve_counters(h, rows);
+}
+
+// The prefill GEMM's split-tile workspace for M rows: partial sums (fixed size)
+// and arrival counters (grown on demand), the counters cleared on `st`.  Called
+// before the call's first launch, so the clear is not between the rotation and
+// the GEMM that overlaps it.
+escha_status_t gemm_prepare(escha_linear_s* h, int M, cudaStream_t st) {
+  escha_status_t s;
+  if (!h->gemm_ws && (s = dev_alloc(&h->gemm_ws, gemm_workspace_floats(h->num_sms))) != ESCHA_OK)
+    return s;
+  if ((s = reserve_counters(h, M)) != ESCHA_OK) return s;
+  return from_cuda(
+      cudaMemsetAsync(h->gemm_cnt, 0, gemm_counter_ints(M, h->N) * sizeof(int), st));
 }
 
 escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, int M,
                            cudaStream_t st) {
   escha_status_t s = linear_reserve(h, M);
   if (s != ESCHA_OK) return s;
+  if ((s = gemm_prepare(h, M, st)) != ESCHA_OK) return s;
   cudaError_t e = launch_rotate_in_plain(x, h->su, h->xh, M, h->K, st);
   if (e != cudaSuccess) return from_cuda(e);
   h->prof.begin(st);
   e = launch_trellis_gemm(h->xh, h->code, h->bits, h->rounding == ESCHA_ROUND_E4M3, M, h->K,
-                          h->N, h->sv, y, h->gemm_ws,
+                          h->N, h->sv, y, h->gemm_ws, h->gemm_cnt,
                           h->num_sms, h->err, st);
   h->prof.end(st);
   return from_cuda(e);
@@ -226,12 +260,13 @@ escha_status_t linear_gemm_fp8(escha_linear_s* h, const uint16_t* x, uint16_t* y
   if (quantize_e4m3_smem_bytes(h->K) > kMaxQuantSmem) return ESCHA_ERR_UNSUPPORTED;
   escha_status_t s = linear_reserve(h, M);
   if (s != ESCHA_OK) return s;
+  if ((s = gemm_prepare(h, M, st)) != ESCHA_OK) return s;
   uint8_t* xq = reinterpret_cast<uint8_t*>(h->xh);
   cudaError_t e = launch_quantize_e4m3_rows(x, h->su, xq, h->xd, M, h->K, st);
   if (e != cudaSuccess) return from_cuda(e);
   h->prof.begin(st);
   e = launch_trellis_gemm_fp8(xq, h->xd, h->code, h->bits, M, h->K, h->N, h->sv, y, h->gemm_ws,
-                              h->num_sms, h->err, st);
+                              h->gemm_cnt, h->num_sms, h->err, st);
   h->prof.end(st);
   return from_cuda(e);
 }
@@ -239,12 +274,11 @@ escha_status_t linear_gemm_fp8(escha_linear_s* h, const uint16_t* x, uint16_t* y
 escha_status_t linear_gemm_fp8_codes(escha_linear_s* h, const uint8_t* q, const float* d,
                                      uint16_t* y, int M, cudaStream_t st) {
   if (h->rounding != ESCHA_ROUND_E4M3) return ESCHA_ERR_UNSUPPORTED;
-  escha_status_t s;
-  if (!h->gemm_ws && (s = dev_alloc(&h->gemm_ws, gemm_workspace_floats(h->num_sms))) != ESCHA_OK)
-    return s;
+  escha_status_t s = gemm_prepare(h, M, st);
+  if (s != ESCHA_OK) return s;
   h->prof.begin(st);
   cudaError_t e = launch_trellis_gemm_fp8(q, d, h->code, h->bits, M, h->K, h->N, h->sv, y,
-                                          h->gemm_ws, h->num_sms, h->err, st);
+                                          h->gemm_ws, h->gemm_cnt, h->num_sms, h->err, st);
   h->prof.end(st);
   return from_cuda(e);
 }

@@ -48,8 +48,10 @@ def test_quantize_rows_bit_exact(m, k):
 
 @pytest.mark.parametrize("m,k,n,bits", [(256, 128, 128, 2), (300, 512, 384, 3), (1, 256, 256, 4),
                                         (600, 1920, 1280, 2), (517, 2048, 1280, 4),
-                                        (64, 384, 256, 3)])
+                                        (64, 384, 256, 3), (64, 8192, 256, 3)])
 def test_gemm_fp8_matches_oracle(m, k, n, bits):
+    """(600, 1920, 1280): tiles split between two CTAs; (64, 8192, 256): each
+    of the two tiles shared by four."""
     rng = np.random.default_rng(9200 + m + k + bits)
     layer = S.make_linear(rng, k, n, bits)
     lin, _ = make_linear_handle(layer)

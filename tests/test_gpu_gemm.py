@@ -29,8 +29,9 @@ def built():
 
 @pytest.mark.parametrize("m,k,n,bits", [(256, 128, 128, 2), (300, 512, 384, 3), (1, 256, 256, 4),
                                         (1000, 1024, 640, 2), (517, 2048, 1280, 4),
-                                        (64, 384, 256, 3)])
+                                        (64, 384, 256, 3), (64, 17408, 256, 2)])
 def test_gemm_matches_oracle(m, k, n, bits):
+    """(64, 17408, 256): each of the two tiles is shared by 17 CTAs."""
     rng = np.random.default_rng(5000 + m + k + bits)
     layer = S.make_linear(rng, k, n, bits)
     lin, _ = make_linear_handle(layer)
@@ -41,6 +42,20 @@ def test_gemm_matches_oracle(m, k, n, bits):
     got = y.cpu().numpy()
     assert np.all(np.isfinite(got))
     assert rel_l2(got, oracle_linear(layer, x)) <= REL_L2_TOL
+
+
+def test_gemm_is_bit_reproducible_with_shared_tiles():
+    """Shared tiles are finished by whichever CTA arrives last, always summing
+    the CTAs' partials in CTA order: repeated calls give the same bits."""
+    rng = np.random.default_rng(5050)
+    layer = S.make_linear(rng, 2048, 1280, 3)
+    lin, _ = make_linear_handle(layer)
+    x = torch.from_numpy(S.make_activations(rng, 517, 2048)).cuda()
+    first = lin.gemm(x).cpu().numpy().view(np.uint16)
+    for _ in range(4):
+        again = lin.gemm(x).cpu().numpy().view(np.uint16)
+        assert np.array_equal(first, again)
+    assert lin.check() == 0
 
 
 def test_gemm_agrees_with_gemv_and_grows_workspace():
