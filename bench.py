@@ -90,6 +90,52 @@ def dist_env():
     return rank, world, local
 
 
+class Replicas:
+    """N independent replicas of the workload, one process per GPU (launched by
+    torchrun): each rank builds its own rank-seeded weight sets and inputs, the
+    timed region has a barrier on both sides, and its time is the slowest
+    rank's.  Nothing is exchanged on the data path.  With world == 1 there is
+    no process group and the barriers and reduction do nothing."""
+
+    def __init__(self, rank, world, local, backend="nccl"):
+        self.rank, self.world = rank, world
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+            if backend == "nccl":
+                import torch
+                torch.cuda.set_device(local)
+            dist.init_process_group(backend)
+            self.dist = dist
+
+    def seed(self, base, inst=0):
+        """Seed of weight set `inst` on this rank (distinct across ranks and sets)."""
+        return base + 7919 * inst + 1000003 * self.rank
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def slowest(self, ms, device):
+        """The largest of the ranks' times; every rank gets it."""
+        if self.dist is None:
+            return ms
+        import torch
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def emit(self, line):
+        """The job's one JSON line, from rank 0."""
+        if self.rank == 0:
+            print(json.dumps(line), flush=True)
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -422,18 +468,14 @@ def run_moe(args, spec, rank, world, local):
     hidden vectors, activations), over 64 cycled seeded routings."""
     import torch
     from gemm_trellis_tile_gb300 import build, escha
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+    rep = Replicas(rank, world, local)
     build.build()
     escha.load()
     dev = torch.device("cuda", torch.cuda.current_device())
     E, hidden, inter, m = 256, 6144, 2048, args.m
     halves = spec.get("halves", False)
     H = inter // 128
-    seed = spec["seed"] + 1000003 * rank
+    seed = rep.seed(spec["seed"])
     mspec = (S.make_moe_half_spec if halves else S.make_moe_spec)(seed, E, hidden, inter)
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
@@ -527,8 +569,7 @@ def run_moe(args, spec, rank, world, local):
     def timed(g, reps, sampler=None):
         if sampler is not None:
             sampler.start()
-        if dist is not None:
-            dist.barrier()
+        rep.barrier()
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
@@ -538,11 +579,9 @@ def run_moe(args, spec, rank, world, local):
         t1.record()
         torch.cuda.synchronize()
         clk = sampler.stop() if sampler is not None else None
+        rep.barrier()
         elapsed = t0.elapsed_time(t1)
-        if dist is not None:
-            tt = torch.tensor([elapsed], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            elapsed = float(tt.item())
+        elapsed = rep.slowest(elapsed, dev)
         return elapsed, clk
 
     reps = max(1, args.steps // R)
@@ -607,10 +646,8 @@ def run_moe(args, spec, rank, world, local):
         "gpu_launches": 5 * steps,
         "clocks": clocks,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    rep.emit(line)
+    rep.close()
     return 0
 
 
@@ -618,11 +655,7 @@ def run_prefill(args, spec, rank, world, local):
     """Prefill GEMM: TFLOP/s of 2*M*in*out per step against the tensor peak."""
     import torch
     from gemm_trellis_tile_gb300 import build, escha
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+    rep = Replicas(rank, world, local)
     build.build()
     escha.load()
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -632,7 +665,7 @@ def run_prefill(args, spec, rank, world, local):
     lins = []
     for r in range(n_inst):
         lins.append(escha.Linear.from_arrays(S.make_linear(np.random.default_rng(
-            spec["seed"] + 7919 * r + 1000003 * rank), k, n, b)))
+            rep.seed(spec["seed"], r)), k, n, b)))
         lins[-1].set_rounding(spec["rounding"])
     rng = np.random.default_rng(spec["seed"] + 17)
     x_host = torch.from_numpy(S.make_activations(rng, m, k)).pin_memory()
@@ -653,8 +686,7 @@ def run_prefill(args, spec, rank, world, local):
         lin.profile(True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
-    if dist is not None:
-        dist.barrier()
+    rep.barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -664,11 +696,9 @@ def run_prefill(args, spec, rank, world, local):
     t1.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    rep.barrier()
     ms = t0.elapsed_time(t1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = rep.slowest(ms, dev)
     k_ms, k_n = 0.0, 0
     for lin in lins:
         a, c = lin.collect()
@@ -728,10 +758,8 @@ def run_prefill(args, spec, rank, world, local):
         v, cores, sample = prefill_oracle_rate(spec, m, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    rep.emit(line)
+    rep.close()
     return 0
 
 
@@ -767,16 +795,12 @@ def run_encode(args, spec, rank, world, local):
     """Viterbi trellis encoder: weights encoded per second (whole tiles)."""
     import torch
     from gemm_trellis_tile_gb300 import build, escha
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+    rep = Replicas(rank, world, local)
     build.build()
     escha.load()
     dev = torch.device("cuda", torch.cuda.current_device())
     k, n, bits = spec["layers"][0]
-    rng = np.random.default_rng(spec["seed"] + 1000003 * rank)
+    rng = np.random.default_rng(rep.seed(spec["seed"]))
     w_host_np = (rng.standard_normal((k, n)) * S.CODEBOOK_STD).astype(np.float32)
     w_host = torch.from_numpy(w_host_np).pin_memory()
     w = w_host.to(dev)
@@ -795,8 +819,7 @@ def run_encode(args, spec, rank, world, local):
     torch.cuda.synchronize()
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
-    if dist is not None:
-        dist.barrier()
+    rep.barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -806,11 +829,9 @@ def run_encode(args, spec, rank, world, local):
     t1.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    rep.barrier()
     ms = t0.elapsed_time(t1)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = rep.slowest(ms, dev)
     tiles = (k // 16) * (n // 16)
     weights = k * n
     # e2e: host matrix in, host code out, through the C ABI
@@ -860,10 +881,8 @@ def run_encode(args, spec, rank, world, local):
         v, cores, sample, _ = encode_oracle_rate(w_host_np, bits, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "weights/s", "cores": cores,
                                 "kind": "oracle", "sample": sample}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    rep.emit(line)
+    rep.close()
     return 0
 
 
@@ -911,11 +930,7 @@ def main():
 
     import torch
     from gemm_trellis_tile_gb300 import build, escha
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+    rep = Replicas(rank, world, local)
     build.build()
     escha.load()
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -933,7 +948,7 @@ def main():
     n_inst = max(2, int(np.ceil(4.0 * l2 / code_per_inst)))
     handles = []
     for r in range(n_inst):
-        inst = make_instance(spec, spec["seed"] + 7919 * r + 1000003 * rank)
+        inst = make_instance(spec, rep.seed(spec["seed"], r))
         handles.append(make_handles(spec, inst))
         if spec.get("norm"):
             nrng = np.random.default_rng(spec["seed"] + 31 * r)
@@ -973,8 +988,7 @@ def main():
     def timed_replays(graphs, sampler=None):
         if sampler is not None:
             sampler.start()
-        if dist is not None:
-            dist.barrier()
+        rep.barrier()
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
@@ -984,13 +998,9 @@ def main():
         t1.record()
         torch.cuda.synchronize()
         clk = sampler.stop() if sampler is not None else None
-        if dist is not None:
-            dist.barrier()
+        rep.barrier()
         elapsed = t0.elapsed_time(t1)
-        if dist is not None:
-            t = torch.tensor([elapsed], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            elapsed = float(t.item())
+        elapsed = rep.slowest(elapsed, dev)
         return elapsed, clk
 
     per_graph = n_inst
@@ -1076,10 +1086,8 @@ def main():
         v, cores, sample = oracle_sample_rate(spec, m, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    rep.emit(line)
+    rep.close()
     return 0
 
 
