@@ -64,8 +64,9 @@ constexpr int kMoeMaxDistinct = kMoeMaxTokens * kMoeMaxTopk;
 constexpr int kMoeMaxExperts = 4096;
 constexpr int kMinUnitsPerCta = 8;
 
-// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
-// device, once per (kernel, device, bytes); thread-safe.
+// Make sure a kernel may take `bytes` of dynamic shared memory on the current
+// device: the limit is raised when `bytes` exceeds every earlier request for
+// that kernel and device, never lowered; thread-safe.
 cudaError_t set_smem_limit(const void* func, int bytes);
 
 int gemv_ranges_per_sm();

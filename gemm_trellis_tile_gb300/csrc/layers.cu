@@ -12,9 +12,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
-#include <set>
-#include <tuple>
+#include <utility>
 
 #include "api_internal.h"
 
@@ -24,13 +24,16 @@ cudaError_t set_smem_limit(const void* func, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  // The largest limit set so far per (kernel, device): a launch with less
+  // dynamic shared memory than the limit is fine, so the limit only rises
+  // (kernels whose shared memory depends on the layer see several sizes).
   static std::mutex mu;
-  static std::set<std::tuple<const void*, int, int>> done;
+  static std::map<std::pair<const void*, int>, int> limit;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_tuple(func, dev, bytes);
-  if (done.count(key)) return cudaSuccess;
+  int& cur = limit[std::make_pair(func, dev)];
+  if (bytes <= cur) return cudaSuccess;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert(key);
+  if (e == cudaSuccess) cur = bytes;
   return e;
 }
 

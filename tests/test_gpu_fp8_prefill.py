@@ -46,6 +46,20 @@ def test_quantize_rows_bit_exact(m, k):
     assert np.array_equal(d.cpu().numpy(), d_ref)
 
 
+def test_quantize_rows_wide_after_narrow():
+    """The quantiser's shared memory grows with K (2K bytes): a wide row (64 KB,
+    above the default 48 KB limit) after a narrow one must still launch."""
+    from gemm_trellis_tile_gb300 import escha
+    rng = np.random.default_rng(9150)
+    for k in (32768, 128, 32768):
+        xh = S.make_activations(rng, 2, k)
+        q, d = escha.quantize_e4m3_rows(torch.from_numpy(xh).cuda())
+        torch.cuda.synchronize()
+        q_ref, d_ref = O.quantize_rows_e4m3(xh)
+        assert np.array_equal(_e4m3_values(q), q_ref), k
+        assert np.array_equal(d.cpu().numpy(), d_ref), k
+
+
 @pytest.mark.parametrize("m,k,n,bits", [(256, 128, 128, 2), (300, 512, 384, 3), (1, 256, 256, 4),
                                         (600, 1920, 1280, 2), (517, 2048, 1280, 4),
                                         (64, 384, 256, 3), (64, 8192, 256, 3)])
