@@ -125,7 +125,11 @@ escha_status_t escha_linear_gemv(escha_linear_t h, const uint16_t* x, uint16_t* 
  * accumulators) and the output rotation fused into the epilogue.
  * The handle keeps a workspace for the rotated activations; it grows on demand
  * (a call with a larger M than any before allocates).  escha_linear_reserve()
- * sizes it up front.
+ * sizes it up front.  Tiles that the kernel's even split shares between CTAs
+ * are finished by the last CTA to reach them, summing the CTAs' partial sums
+ * in CTA order, so repeated calls give the same bits; each call clears the
+ * handle's arrival counters for this with a cudaMemsetAsync on `stream`
+ * (capturable in a CUDA graph).  Calls that share a handle must be ordered.
  */
 escha_status_t escha_linear_gemm(escha_linear_t h, const uint16_t* x, uint16_t* y, int M,
                                  void* stream);
