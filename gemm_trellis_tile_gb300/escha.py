@@ -151,6 +151,22 @@ def _dev(t, dtype, shape=None):
     return t
 
 
+def _rows(t, width, what):
+    """Row count of a [M, width] tensor; the kernels read whole rows of `width`
+    elements, so any other shape is refused before it reaches them."""
+    if t.dim() != 2 or t.shape[1] != width:
+        raise ValueError("%s must be [M, %d], got %s" % (what, width, tuple(t.shape)))
+    return t.shape[0]
+
+
+def _out(y, m, width, device):
+    """The caller's fp16 output [m, width], or a new one."""
+    torch = _torch()
+    if y is None:
+        return torch.empty((m, width), dtype=torch.float16, device=device)
+    return _dev(y, torch.float16, (m, width))
+
+
 def _collect(handle, kind):
     ms = ctypes.c_double()
     n = _I()
@@ -198,9 +214,8 @@ class Linear:
     def gemv(self, x, y=None, stream=None, stage=None):
         torch = _torch()
         _dev(x, torch.float16)
-        m = x.shape[0]
-        if y is None:
-            y = torch.empty((m, self.out_features), dtype=torch.float16, device=x.device)
+        m = _rows(x, self.in_features, "x")
+        y = _out(y, m, self.out_features, x.device)
         if stage is None:
             check(load().escha_linear_gemv(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
                   "escha_linear_gemv")
@@ -212,9 +227,8 @@ class Linear:
     def gemm(self, x, y=None, stream=None):
         torch = _torch()
         _dev(x, torch.float16)
-        m = x.shape[0]
-        if y is None:
-            y = torch.empty((m, self.out_features), dtype=torch.float16, device=x.device)
+        m = _rows(x, self.in_features, "x")
+        y = _out(y, m, self.out_features, x.device)
         check(load().escha_linear_gemm(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
               "escha_linear_gemm")
         return y
@@ -224,9 +238,8 @@ class Linear:
         quantised per token to E4M3 (escha_linear_gemm_fp8)."""
         torch = _torch()
         _dev(x, torch.float16)
-        m = x.shape[0]
-        if y is None:
-            y = torch.empty((m, self.out_features), dtype=torch.float16, device=x.device)
+        m = _rows(x, self.in_features, "x")
+        y = _out(y, m, self.out_features, x.device)
         check(load().escha_linear_gemm_fp8(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
               "escha_linear_gemm_fp8")
         return y
@@ -236,10 +249,9 @@ class Linear:
         per-row scales d (fp32 [M]) (escha_linear_gemm_fp8_codes)."""
         torch = _torch()
         _dev(q, torch.uint8)
-        m = q.shape[0]
+        m = _rows(q, self.in_features, "q")
         _dev(d, torch.float32, (m,))
-        if y is None:
-            y = torch.empty((m, self.out_features), dtype=torch.float16, device=q.device)
+        y = _out(y, m, self.out_features, q.device)
         check(load().escha_linear_gemm_fp8_codes(self.handle, _ptr(q), _ptr(d), _ptr(y), m,
                                                  _stream(stream)), "escha_linear_gemm_fp8_codes")
         return y
@@ -295,9 +307,8 @@ class MLP:
     def gemv(self, x, y=None, stream=None, stage=None):
         torch = _torch()
         _dev(x, torch.float16)
-        m = x.shape[0]
-        if y is None:
-            y = torch.empty((m, self.hidden), dtype=torch.float16, device=x.device)
+        m = _rows(x, self.hidden, "x")
+        y = _out(y, m, self.hidden, x.device)
         if stage is None:
             check(load().escha_mlp_gemv(self.handle, _ptr(x), _ptr(y), m, _stream(stream)),
                   "escha_mlp_gemv")
@@ -399,11 +410,14 @@ class MoE:
     def gemv(self, x, expert_ids, expert_w, y=None, stream=None, stage=None):
         torch = _torch()
         _dev(x, torch.float16)
+        m = _rows(x, self.hidden, "x")
         _dev(expert_ids, torch.int32)
-        _dev(expert_w, torch.float32)
-        m, topk = expert_ids.shape
-        if y is None:
-            y = torch.empty((m, self.hidden), dtype=torch.float16, device=x.device)
+        if expert_ids.dim() != 2 or expert_ids.shape[0] != m:
+            raise ValueError("expert_ids must be [M, topk] with M = %d, got %s"
+                             % (m, tuple(expert_ids.shape)))
+        topk = expert_ids.shape[1]
+        _dev(expert_w, torch.float32, (m, topk))
+        y = _out(y, m, self.hidden, x.device)
         if stage is None:
             check(load().escha_linear_moe_gemv(self.handle, _ptr(x), _ptr(expert_ids),
                                                _ptr(expert_w), _ptr(y), m, topk, _stream(stream)),
@@ -533,6 +547,8 @@ def quantize_e4m3_rows(xh, stream=None):
     returns (q uint8 [M, K] E4M3 bit patterns, d fp32 [M]); xh ~ q * d."""
     torch = _torch()
     _dev(xh, torch.float16)
+    if xh.dim() != 2:
+        raise ValueError("xh must be [M, K], got %s" % (tuple(xh.shape),))
     m, k = xh.shape
     q = torch.empty((m, k), dtype=torch.uint8, device=xh.device)
     d = torch.empty((m,), dtype=torch.float32, device=xh.device)
@@ -549,6 +565,8 @@ def trellis_encode(w, bits, rounding="fp16", sq_err=False, stream=None):
     """
     torch = _torch()
     _dev(w, torch.float32)
+    if w.dim() != 2:
+        raise ValueError("w must be [in, out], got %s" % (tuple(w.shape),))
     k, n = w.shape
     code = torch.empty((k // 16, n // 16, 16 * bits), dtype=torch.int16, device=w.device)
     err = torch.empty((k // 16, n // 16), dtype=torch.float32, device=w.device) if sq_err else None

@@ -186,6 +186,25 @@ def test_argument_errors_on_gpu():
     assert e.value.status == 2
 
 
+def test_binding_refuses_wrong_widths_before_any_launch():
+    """Kernels read whole rows of the layer's width: other shapes stop in the binding."""
+    rng = np.random.default_rng(33)
+    layer = S.make_linear(rng, 256, 384, 2)
+    lin, _ = make_linear_handle(layer)
+    for bad in (torch.zeros((2, 128), dtype=torch.float16, device="cuda"),
+                torch.zeros((256,), dtype=torch.float16, device="cuda")):
+        for call in (lin.gemv, lin.gemm):
+            with pytest.raises(ValueError):
+                call(bad)
+    x = torch.zeros((2, 256), dtype=torch.float16, device="cuda")
+    with pytest.raises(ValueError):
+        lin.gemv(x, torch.zeros((2, 256), dtype=torch.float16, device="cuda"))   # y width
+    with pytest.raises(ValueError):
+        lin.gemm_fp8_codes(torch.zeros((2, 128), dtype=torch.uint8, device="cuda"),
+                           torch.zeros((2,), dtype=torch.float32, device="cuda"))
+    assert lin.check() == 0
+
+
 def test_bounded_wait_times_out_and_context_survives():
     from gemm_trellis_tile_gb300 import escha
     assert escha.selftest_wait_timeout(20000) == 5
