@@ -697,6 +697,54 @@ def test_linear_fp8_differs_from_fp16_layer_by_the_activation_rounding():
     assert 1e-3 < rel < 2.0 ** -4 / np.sqrt(3)
 
 
+def test_linear_fp8_brute_force_loops():
+    """Per-element loops on a 128x128 E4M3 layer, two tokens: the Hadamard from
+    its sign formula, fp16 and fp32 roundings through struct (IEEE half and
+    single), the E4M3 code by searching the whole table (ties to the even
+    mantissa), then explicit sums."""
+    import struct
+
+    def f16(v):
+        return struct.unpack("e", struct.pack("e", v))[0]
+
+    def f32(v):
+        return struct.unpack("f", struct.pack("f", v))[0]
+
+    table = _e4m3_table()
+
+    def even_mantissa(v):
+        a = abs(v)
+        if a < 2.0 ** -6:
+            return int(round(a / 2.0 ** -9)) % 2 == 0
+        return int(round((a / 2.0 ** np.floor(np.log2(a)) - 1) * 8)) % 2 == 0
+
+    def e4m3(v):
+        dist = np.abs(table - v)
+        best = table[dist == dist.min()]
+        if best.size == 1:
+            return float(best[0])
+        return float([t for t in best if even_mantissa(t)][0])
+
+    rng = np.random.default_rng(907)
+    k = n = 128
+    code = rng.integers(-32768, 32768, size=(k // 16, n // 16, 48), dtype=np.int16)
+    w8 = O.decode_matrix(code, 3, rounding="e4m3").astype(np.float64)
+    su = rng.uniform(0.5, 1.5, size=k)
+    sv = rng.uniform(0.5, 1.5, size=n)
+    x = rng.normal(size=(2, k)) * np.array([[0.01], [30.0]])
+    H = [[(-1.0) ** bin(a & b).count("1") / np.sqrt(128) for b in range(128)] for a in range(128)]
+    ref = []
+    for row in x:
+        xh = [f16(sum(row[a] * su[a] * H[a][j] for a in range(k))) for j in range(k)]
+        amax = max(abs(v) for v in xh)
+        inv, d = f32(448.0 / amax), f32(amax / 448.0)
+        q = [e4m3(f32(v * inv)) for v in xh]
+        yp = [d * sum(q[j] * w8[j, c] for j in range(k)) for c in range(n)]
+        ref.append([sum(yp[b] * H[b][c] for b in range(n)) * sv[c] for c in range(n)])
+    got = O.linear_forward_fp8(x, w8, su, sv)
+    assert np.allclose(got, np.array(ref), rtol=1e-10, atol=1e-12 * np.max(np.abs(ref)))
+
+
 def test_linear_fp8_columns_match_full_layer():
     rng = np.random.default_rng(906)
     k, n = 256, 512
