@@ -244,20 +244,21 @@ def test_stages_compose_to_the_full_call():
         x = S.make_activations(rng, m, 768)
         xt = torch.from_numpy(x).cuda()
         full = lin.gemv(xt)
-        staged = torch.empty_like(full)
+        ylin = torch.empty_like(full)
         for s in range(escha.Linear.STAGES):
-            lin.gemv(xt, staged, stage=s)
-        assert torch.equal(full, staged)
-        assert rel_l2(staged.cpu().numpy(), oracle_linear(layer, x)) <= REL_L2_TOL
+            lin.gemv(xt, ylin, stage=s)
+        assert torch.equal(full, ylin)
+        assert rel_l2(ylin.cpu().numpy(), oracle_linear(layer, x)) <= REL_L2_TOL
         xm = torch.from_numpy(S.make_activations(rng, m, 512)).cuda()
         full = handle.gemv(xm)
-        staged = torch.empty_like(full)
+        ymlp = torch.empty_like(full)
         for s in range(escha.MLP.STAGES):
-            handle.gemv(xm, staged, stage=s)
-        assert torch.equal(full, staged)
+            handle.gemv(xm, ymlp, stage=s)
+        assert torch.equal(full, ymlp)
+    assert ylin.shape == (11, 1280)
     for bad in (-1, escha.Linear.STAGES):
         with pytest.raises(escha.EschaError) as e:
-            lin.gemv(xt, staged[:, :1280], stage=bad)
+            lin.gemv(xt, ylin, stage=bad)
         assert e.value.status == 1
 
 

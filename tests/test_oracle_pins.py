@@ -379,6 +379,51 @@ def test_moe_single_output_rotation_by_linearity():
     assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
 
 
+def test_mlp_brute_force_loops_gate_takes_the_silu():
+    """down(silu(gate(x)) * up(x)) on a 128 -> 256 -> 128 MLP, two tokens, by
+    per-element loops: Hadamard entries from their sign formula, each layer by
+    the activation route, SiLU as z / (1 + e^-z) with math.exp.  Gate and up
+    are distinct matrices scaled so that their outputs are O(1), where SiLU is
+    far from linear; swapping their roles, or another activation, moves the
+    result by O(1) relative."""
+    import math
+    rng = np.random.default_rng(14)
+
+    def layer(k, n, b, scale):
+        code, rin, rout, s_in, s_out = make_small_layer(rng, k, n, b)
+        return dict(w=O.decode_matrix(code, b).astype(np.float64), su=O.fold_scales(rin, s_in),
+                    sv=O.fold_scales(rout, s_out) * scale)
+    gate, up, down = layer(128, 256, 2, 1 / 16), layer(128, 256, 3, 1 / 16), layer(256, 128, 4, 1.0)
+    x = rng.normal(size=(2, 128))
+    H = [[(-1.0) ** bin(a & b).count("1") / math.sqrt(128) for b in range(128)] for a in range(128)]
+
+    def had(v):
+        out = [0.0] * len(v)
+        for b0 in range(0, len(v), 128):
+            for k in range(128):
+                out[b0 + k] = sum(v[b0 + a] * H[a][k] for a in range(128))
+        return out
+
+    def lin(v, L):
+        k_in, n_out = L["w"].shape
+        xh = had([v[a] * L["su"][a] for a in range(k_in)])
+        yp = [sum(xh[k] * L["w"][k, n] for k in range(k_in)) for n in range(n_out)]
+        return [t * L["sv"][n] for n, t in enumerate(had(yp))]
+
+    def mlp_loops(v, first, second):
+        g, u = lin(v, first), lin(v, second)
+        return lin([g[j] / (1.0 + math.exp(-g[j])) * u[j] for j in range(len(g))], down)
+
+    ours = O.mlp_forward(x, gate, up, down)
+    for t in range(2):
+        ref = np.array(mlp_loops(list(x[t]), gate, up))
+        assert np.allclose(ours[t], ref, rtol=1e-10, atol=1e-10 * np.abs(ref).max())
+        swapped = np.array(mlp_loops(list(x[t]), up, gate))
+        assert np.linalg.norm(swapped - ref) > 0.1 * np.linalg.norm(ref)
+    g = O.linear_forward(x, gate["w"], gate["su"], gate["sv"])
+    assert 0.3 < np.std(g) < 3.0           # SiLU acts in its curved range
+
+
 def test_moe_forward_reduces_to_mlp():
     rng = np.random.default_rng(13)
 
