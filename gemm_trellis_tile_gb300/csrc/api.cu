@@ -155,7 +155,7 @@ escha_status_t upload_jobs(GemvSchedule& s) {
 // ESCHA_SYNC_DEBUG=1 in the environment (read once): every compute call
 // synchronises its stream after launching and reports an asynchronous CUDA
 // error at that call instead of a later one.
-static bool sync_debug() {
+bool sync_debug() {
   static const bool on = [] {
     const char* v = std::getenv("ESCHA_SYNC_DEBUG");
     return v != nullptr && v[0] == '1';

@@ -27,6 +27,8 @@ bool aligned16(const void* p);
 escha_status_t device_info(int* dev, int* sms);
 escha_status_t upload_jobs(GemvSchedule& s);
 escha_status_t read_and_clear_error(int* d_err, cudaStream_t st);
+escha_status_t after_launch(escha_status_t s, cudaStream_t st);
+bool sync_debug();
 template <typename T>
 escha_status_t dev_alloc(T** p, size_t count);
 

@@ -16,6 +16,12 @@
 // behind; everything a call reads is rewritten by that call first.  Two calls
 // whose work overlaps on the GPU (other streams, other host threads) race on
 // the array.
+//
+// With no handle there is no error flag for the caller to read later, so a
+// bounded wait of the GEMV that runs out marks the call's own output instead:
+// a last small kernel sees the scratch error word set and fills y with fp16
+// NaN.  With ESCHA_SYNC_DEBUG=1 the call also synchronises and returns
+// ESCHA_ERR_TIMEOUT.
 
 #include <cuda_runtime.h>
 
@@ -53,6 +59,15 @@ __global__ void put_job_kernel(GemvJob job, GemvJob* dst, const __grid_constant_
   *dst = job;
   *map_dst = map;
   tensormap_release();
+}
+
+// Runs last: if a bounded wait of this call ran out (error word set), every
+// element of y becomes fp16 NaN, so the failure reaches the caller's data.
+__global__ void mark_failed_output_kernel(const int* err, uint16_t* y, size_t count) {
+  if (*reinterpret_cast<const volatile int*>(err) == 0) return;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count;
+       i += (size_t)gridDim.x * blockDim.x)
+    y[i] = 0x7E00u;
 }
 
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -161,5 +176,10 @@ extern "C" escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const u
   pr.KT = s.sched.jobs[0].KT;
   pr.N = N;
   e = launch_rotate_out(pr, s.sched.units, s.sched.grid, sv, y, M, kGemvMaxTokens, st);
-  return from_cuda(e);
+  if (e != cudaSuccess) return from_cuda(e);
+  mark_failed_output_kernel<<<1, 256, 0, st>>>(err, y, (size_t)M * N);
+  if ((e = cudaGetLastError()) != cudaSuccess) return from_cuda(e);
+  escha_status_t status = after_launch(ESCHA_OK, st);
+  if (status == ESCHA_OK && sync_debug()) status = read_and_clear_error(err, st);
+  return status;
 }

@@ -401,8 +401,11 @@ escha_status_t escha_profile_collect(void* handle, int kind, double* ms_total, i
  * the array's device address; make that first call before any stream capture.
  * Every call reuses the same array: calls whose work overlaps on the GPU (on
  * other streams or from other host threads) race and must be ordered by the
- * caller.  The call is asynchronous on `stream`; it reports argument and
- * launch errors only (there is no handle whose error flag could be read).
+ * caller.  The call is asynchronous on `stream` and returns argument and
+ * launch errors.  There is no handle whose error flag could be read later, so
+ * if a bounded device wait of the GEMV runs out, the call writes fp16 NaN to
+ * every element of y; with ESCHA_SYNC_DEBUG=1 it also synchronises `stream`
+ * and returns ESCHA_ERR_TIMEOUT (or ESCHA_ERR_CUDA for an asynchronous error).
  */
 #define ESCHA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 escha_status_t escha_linear_gemv_noalloc(const int16_t* code, const uint16_t* rin,

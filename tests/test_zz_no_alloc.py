@@ -102,6 +102,49 @@ def test_noalloc_refuses_layers_larger_than_its_scratch():
     assert rel_l2(y.cpu().numpy(), oracle_linear(layer, x_np)) <= REL_L2_TOL
 
 
+_SYNC_DEBUG_NOALLOC = r"""
+import ctypes, hashlib, sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+from gemm_trellis_tile_gb300 import escha, synthetic as S
+lib = escha.load()
+rng = np.random.default_rng(77)
+layer = S.make_linear(rng, 512, 768, 3)
+d = {k: torch.from_numpy(layer[k]).cuda() for k in ("code", "rin", "rout", "s_in", "s_out")}
+p = lambda t: ctypes.c_void_p(t.data_ptr())
+out = b""
+for m in (3, 16):
+    x = torch.from_numpy(S.make_activations(rng, m, 512)).cuda()
+    y = torch.empty((m, 768), dtype=torch.float16, device="cuda")
+    st = lib.escha_linear_gemv_noalloc(p(d["code"]), p(d["rin"]), p(d["rout"]), p(d["s_in"]),
+                                       p(d["s_out"]), 512, 768, 3, p(x), p(y), m,
+                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, st
+    out += y.cpu().numpy().tobytes()
+print(hashlib.sha256(out).hexdigest())
+"""
+
+
+@pytest.mark.gpu
+def test_noalloc_sync_debug_mode_gives_the_same_results():
+    """With ESCHA_SYNC_DEBUG=1 the entry point synchronises and reads its error
+    word after each call; the results are the same bits as without it."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for flag in ("0", "1"):
+        env = dict(os.environ, ESCHA_SYNC_DEBUG=flag)
+        r = subprocess.run([sys.executable, "-c", _SYNC_DEBUG_NOALLOC, root], env=env,
+                           capture_output=True, text=True, timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs.append(r.stdout.strip().splitlines()[-1])
+    assert outs[0] == outs[1]
+
+
 def escha_scratch_bytes():
     import re
     from gemm_trellis_tile_gb300 import escha
