@@ -9,9 +9,13 @@ SiLU-gate middle, the output rotation) on device-resident inputs.
 Prints ONE JSON line.  `value` is decode GEMV throughput in GB/s of
 algorithmic bytes (code words + side vectors + activations) per step;
 `roofline` rates the dominant kernel (the trellis GEMV) against the measured
-HBM copy bandwidth; `e2e` is the same metric through the C ABI with host
-buffers and the copies inside the timed region; `cpu_baseline` is the CPU
-oracle on a bounded sample of the same workload.
+HBM copy bandwidth and `roofline_issue` against the instruction-issue bound
+of its decode; `e2e` is the same metric through the C ABI with host buffers
+and the copies inside the timed region; `cpu_baseline` is the CPU oracle on a
+bounded sample of the same workload.  The `prefill` object holds the other
+half of the metric, measured in the same process: the tcgen05 prefill GEMM at
+2048 tokens, 5120 -> 17408 at 3 bits, in TFLOP/s against the tensor peak.
+The timed region (K steps) is repeated and its median reported.
 
 Other workloads print the same line for their own shapes and metric:
 --workload linear512 | sweep (--m, --shape) | moe (--m, --halves, --shared)
@@ -39,6 +43,20 @@ from gemm_trellis_tile_gb300 import workloads as WL  # noqa: E402
 
 L2_FALLBACK_BYTES = 129 * 1024 * 1024
 
+# One metric string per kind of line, the same in both arms.
+METRIC_DECODE = "decode GEMV compressed-weight GB/s vs HBM peak (\u00b5s/layer); prefill TFLOP/s"
+METRIC_PREFILL = "prefill TFLOP/s (2*M*in*out per step)"
+METRIC_ENCODE = "trellis encode weights/s (Viterbi search, whole tiles)"
+BYTES_NOTE = "algorithmic bytes: code words + side vectors + activations"
+
+# The prefill half of the default line: 2048 tokens through 5120 -> 17408 at 3 bits.
+PREFILL_DEFAULT = dict(m=2048, shape="5120x17408")
+
+# Timed-region repeats: at least this many, and enough for this much device time.
+MIN_REPEATS = 5
+MAX_REPEATS = 200
+REPEAT_SECONDS = 0.25
+
 # DRAM bytes per contraction launch (dram__bytes_read.sum + dram__bytes_write.sum
 # from one ncu capture of this kernel, averaged over the step's launches), by
 # workload at M=1; None where no capture of the current kernel exists.
@@ -51,6 +69,48 @@ PREFILL_TRAFFIC_BYTES = {
     "prefill GEMM 5120x17408 3-bit, M=2048 tokens, FP8 tensor cores (E4M3 weights, "
     "per-token E4M3 activations)": 153.60e6,
 }
+
+
+# Instruction mix of the trellis GEMV per decoded weight, by workload at M=1:
+# lane-instructions (warp instructions x 32) per weight over the step's
+# contraction launches, from one ncu capture of this kernel
+# (smsp__inst_executed.sum and smsp__inst_executed_pipe_alu.sum); None where no
+# capture of the current kernel exists.
+GEMV_ISSUE_MIX = {
+    "dense gated MLP 5120->17408->5120, gate 2-bit / up 3-bit / down 3-bit, M=1":
+        {"issue": 6.04, "alu": 2.74},
+}
+# Per SM sub-partition and clock: one warp instruction issued, 16 lanes of the
+# integer ALU pipe (a warp instruction holds it for two cycles: ncu's
+# sm__pipe_alu_cycles_active / sm__inst_executed_pipe_alu = 2.0 on this kernel).
+ISSUE_LANES_PER_CLK = 32
+ALU_LANES_PER_CLK = 16
+SMSP_PER_SM = 4
+
+
+def issue_roofline(name, weights_per_s, sms, clocks):
+    """The GEMV against the instruction-issue bound of its decode: with I lane-
+    instructions per weight (the capture's mix), an SM issues at most
+    4 x 32 / I weights per clock, and the ALU pipe allows 4 x 16 / A (A = ALU
+    lane-instructions per weight); the bound is the smaller, at the median SM
+    clock sampled during the timed region (else the maximum clock)."""
+    mix = GEMV_ISSUE_MIX.get(name) if name else None
+    if mix is None:
+        return None
+    peaks, _ = measured_peaks()
+    mhz = (clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    f = sms * SMSP_PER_SM * mhz * 1e6
+    by_issue = f * ISSUE_LANES_PER_CLK / mix["issue"]
+    by_alu = f * ALU_LANES_PER_CLK / mix["alu"]
+    peak = min(by_issue, by_alu)
+    return {"bound": "alu", "pipe": "issue" if by_issue <= by_alu else "alu",
+            "kernel": "trellis_gemv", "achieved": weights_per_s / 1e12, "peak": peak / 1e12,
+            "unit": "T weights/s", "frac": weights_per_s / peak,
+            "lane_instr_per_weight": mix["issue"], "alu_lane_instr_per_weight": mix["alu"],
+            "peak_source": "derived: %d SMs x 4 sub-partitions x %.0f MHz x min(32 issue "
+                           "lanes / %.2f, 16 ALU lanes / %.2f) lane-instructions per weight "
+                           "(ncu counters of this kernel)" % (sms, mhz, mix["issue"],
+                                                              mix["alu"])}
 
 
 def parse_args():
@@ -77,6 +137,10 @@ def parse_args():
                    help="prefill: kind::f8f6f4 GEMM on E4M3 weights and per-token E4M3 "
                         "activations (implies --rounding e4m3)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="default line: leave out the prefill half of the metric")
+    p.add_argument("--repeats", type=int, default=0,
+                   help="repeats of the K-step timed region (median reported); 0 = automatic")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     return p.parse_args()
 
@@ -143,6 +207,37 @@ def measured_peaks():
             d = json.load(f)
         return d, "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def repeats_for(first_ms, asked=0):
+    """Repeats of a timed region whose first run took `first_ms`."""
+    if asked > 0:
+        return asked
+    want = int(np.ceil(REPEAT_SECONDS * 1e3 / max(first_ms, 1e-3)))
+    return max(MIN_REPEATS, min(MAX_REPEATS, want))
+
+
+def median_region(run, rep, dev, asked=0):
+    """Time `run()` (K steps launched on the current stream) between CUDA
+    events, a barrier and a synchronize on both sides, repeatedly; returns
+    (median ms, repeats, min ms, max ms), each repeat the slowest rank's."""
+    import torch
+
+    def once():
+        rep.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        run()
+        t1.record()
+        torch.cuda.synchronize()
+        rep.barrier()
+        return rep.slowest(t0.elapsed_time(t1), dev)
+    times = [once()]
+    for _ in range(repeats_for(times[0], asked) - 1):
+        times.append(once())
+    return statistics.median(times), len(times), min(times), max(times)
 
 
 class ClockSampler:
@@ -322,7 +417,7 @@ def run_reference_encode(args, spec):
     wall = time.perf_counter() - t0
     cores = round((time.process_time() - c0) / wall, 2)
     value = done / wall
-    line = {"impl": "reference", "metric": "trellis encode weights/s (Viterbi search, whole tiles)",
+    line = {"impl": "reference", "metric": METRIC_ENCODE,
             "value": value, "unit": "weights/s", "n_gpus": args.gpus, "steps": steps,
             "warmup": warm, "ms_per_step": 1e3 * wall / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -389,7 +484,7 @@ def run_reference_prefill(args, spec):
     wall = time.perf_counter() - t0
     cores = round((time.process_time() - c0) / wall, 2)
     value = statistics.mean(r[0] for r in rates)
-    line = {"impl": "reference", "metric": "prefill TFLOP/s (2*M*in*out per step)",
+    line = {"impl": "reference", "metric": METRIC_PREFILL,
             "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": steps,
             "warmup": warm, "ms_per_step": 1e3 * wall / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -447,7 +542,7 @@ def run_reference(args, spec, rank):
     depth = min(ktiles, max(lay["in_features"] // 16 for lay in mats))
     sample = ("per step: one 128-output column block of one matrix (cycling through the "
               "workload's matrices), %d k-tiles deep" % depth)
-    line = {"impl": "reference", "metric": "decode GEMV compressed-weight GB/s", "value": value,
+    line = {"impl": "reference", "metric": METRIC_DECODE, "value": value,
             "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -456,6 +551,13 @@ def run_reference(args, spec, rank):
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+    if spec["kind"] == "mlp" and not args.no_prefill and args.workload == "mlp":
+        pspec = prefill_spec(args)
+        pv, pcores, psample = prefill_oracle_rate(pspec, PREFILL_DEFAULT["m"], args.cpu_seconds)
+        line["prefill"] = {"workload": pspec["name"], "metric": METRIC_PREFILL, "value": pv,
+                           "unit": "TFLOP/s", "dtype": "f64",
+                           "cpu_baseline": {"value": pv, "unit": "TFLOP/s", "cores": pcores,
+                                            "kind": "oracle", "sample": psample}}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -626,12 +728,13 @@ def run_moe(args, spec, rank, world, local):
     peak = float(peaks["hbm_gbs"])
     value = world * reps * per_pass / (ms / 1e3) / 1e9
     line = {
-        "metric": "decode GEMV compressed-weight GB/s (algorithmic bytes of the routed experts)",
+        "metric": METRIC_DECODE,
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded device-generated code "
         "words, 64 cycled uniform top-8 routings)",
         "config": {"workload": spec["name"], "tokens": m, "bytes_per_step": per_pass / R,
+                   "bytes": BYTES_NOTE + " of each step's distinct routed experts",
                    "l2": "256 experts, %.1f GB of code words; 64 routings cycled"
                          % (sum(c.numel() * 2 for cc in codes for part in cc
                                 for c in (part if isinstance(part, list) else [part])) / 1e9),
@@ -651,15 +754,23 @@ def run_moe(args, spec, rank, world, local):
     return 0
 
 
-def run_prefill(args, spec, rank, world, local):
-    """Prefill GEMM: TFLOP/s of 2*M*in*out per step against the tensor peak."""
+def prefill_spec(args):
+    """The prefill workload of the default line (2048 tokens, 5120 -> 17408, 3-bit)."""
+    import argparse as _ap
+    pa = _ap.Namespace(**vars(args))
+    pa.workload, pa.m, pa.shape, pa.fp8 = "prefill", PREFILL_DEFAULT["m"], PREFILL_DEFAULT["shape"], False
+    pa.rounding = "fp16"
+    return workload_spec(pa)
+
+
+def measure_prefill(args, spec, rep, dev, m, want_cpu):
+    """Prefill GEMM of `spec` at m tokens: TFLOP/s of 2*m*in*out per step (median
+    over repeats of the K-step region), its roofline against the tensor peak,
+    e2e through the C ABI with host buffers, and the CPU oracle's rate."""
     import torch
     from gemm_trellis_tile_gb300 import build, escha
-    rep = Replicas(rank, world, local)
     build.build()
     escha.load()
-    dev = torch.device("cuda", torch.cuda.current_device())
-    m = args.m
     k, n, b = spec["layers"][0]
     n_inst = 4   # rotating weight sets: 4 x code + activations + outputs > L2
     lins = []
@@ -683,22 +794,19 @@ def run_prefill(args, spec, rank, world, local):
     for lin in lins:
         if lin.check() != 0:
             raise SystemExit("device error flag set during warm-up")
-        lin.profile(True)
+
+    def run():
+        for i in range(args.steps):
+            call(lins[i % n_inst])
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
-    rep.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for i in range(args.steps):
-        call(lins[i % n_inst])
-    t1.record()
-    torch.cuda.synchronize()
+    ms, n_rep, lo, hi = median_region(run, rep, dev, args.repeats)
     clocks = sampler.stop()
-    rep.barrier()
-    ms = t0.elapsed_time(t1)
-    ms = rep.slowest(ms, dev)
+    # dominant kernel: the GEMM launches alone, from the handles' own event pairs
+    for lin in lins:
+        lin.profile(True)
+    run()
+    torch.cuda.synchronize()
     k_ms, k_n = 0.0, 0
     for lin in lins:
         a, c = lin.collect()
@@ -732,18 +840,19 @@ def run_prefill(args, spec, rank, world, local):
         peak *= 2.0
         peak_note = (src + " (MEASURED_PEAKS.json bf16_tflops burst x 2, the nominal dense "
                      "E4M3 : bf16 ratio 4.5 : 2.25 PFLOP/s)")
-    value = world * args.steps * flops / (ms / 1e3) / 1e12
-    line = {
-        "metric": "prefill TFLOP/s (2*M*in*out per step)", "value": value, "unit": "TFLOP/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3" if fp8 else "f16",
-        "data": "synthetic (seeded uniform code words)",
-        "config": {"workload": spec["name"], "tokens": m,
-                   "l2": "4 rotating weight sets; activations %.0f MB, output %.0f MB per step"
-                         % (m * k * 2 / 1e6, m * n * 2 / 1e6),
-                   "timing": "CUDA events around back-to-back public API calls"},
+    world = rep.world
+    out = {
+        "workload": spec["name"], "metric": METRIC_PREFILL,
+        "value": world * args.steps * flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        "ms_per_step": ms / args.steps, "steps": args.steps,
+        "dtype": "e4m3" if fp8 else "f16", "tokens": m,
+        "l2": "4 rotating weight sets; activations %.0f MB, output %.0f MB per step"
+              % (m * k * 2 / 1e6, m * n * 2 / 1e6),
+        "timing": "CUDA events around back-to-back public API calls; median of %d repeats "
+                  "of the %d-step region (min %.4f, max %.4f ms per step)"
+                  % (n_rep, args.steps, lo / args.steps, hi / args.steps),
         "roofline": {"bound": "tensor", "kernel": "trellis_gemm", "achieved": achieved,
+                     "launch_us": 1e3 * k_ms / k_n if k_n else None,
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak if achieved else None,
                      "traffic": PREFILL_TRAFFIC_BYTES.get(spec["name"]),
@@ -754,10 +863,33 @@ def run_prefill(args, spec, rank, world, local):
         "gpu_launches": prefill_launches(m, k, n, props_sms(dev), fp8) * args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if want_cpu:
         v, cores, sample = prefill_oracle_rate(spec, m, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                                "sample": sample}
+        out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                               "sample": sample}
+    return out
+
+
+def run_prefill(args, spec, rank, world, local):
+    """Prefill GEMM: TFLOP/s of 2*M*in*out per step against the tensor peak."""
+    import torch
+    rep = Replicas(rank, world, local)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    p = measure_prefill(args, spec, rep, dev, args.m,
+                        want_cpu=(rank == 0 and world == 1 and not args.no_cpu_baseline))
+    line = {
+        "metric": METRIC_PREFILL, "value": p["value"], "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": p["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": p["dtype"],
+        "data": "synthetic (seeded uniform code words)",
+        "config": {"workload": spec["name"], "tokens": args.m, "l2": p["l2"],
+                   "timing": p["timing"]},
+        "roofline": p["roofline"], "e2e": p["e2e"], "gpu_launches": p["gpu_launches"],
+        "clocks": p["clocks"],
+    }
+    if "cpu_baseline" in p:
+        line["cpu_baseline"] = p["cpu_baseline"]
     rep.emit(line)
     rep.close()
     return 0
@@ -856,7 +988,7 @@ def run_encode(args, spec, rank, world, local):
     peak_edges = sms * 128 * sm_mhz * 1e6 / ENCODE_FP32_OPS_PER_EDGE
     achieved_edges = steps * tiles * ENCODE_EDGES_PER_TILE / (ms / 1e3)
     line = {
-        "metric": "trellis encode weights/s (Viterbi search, whole tiles)",
+        "metric": METRIC_ENCODE,
         "value": world * steps * weights / (ms / 1e3), "unit": "weights/s", "n_gpus": world,
         "steps": steps, "warmup": warm, "ms_per_step": ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded "
@@ -986,22 +1118,16 @@ def main():
         return g
 
     def timed_replays(graphs, sampler=None):
+        """Median over repeats of the K-step region (replays of `graphs`)."""
         if sampler is not None:
             sampler.start()
-        rep.barrier()
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for g in graphs:
-            g.replay()
-        t1.record()
-        torch.cuda.synchronize()
+
+        def run():
+            for g in graphs:
+                g.replay()
+        med, n, lo, hi = median_region(run, rep, dev, args.repeats)
         clk = sampler.stop() if sampler is not None else None
-        rep.barrier()
-        elapsed = t0.elapsed_time(t1)
-        elapsed = rep.slowest(elapsed, dev)
-        return elapsed, clk
+        return med, clk, (n, lo, hi)
 
     per_graph = n_inst
     full, rem = divmod(args.steps, per_graph)
@@ -1011,8 +1137,8 @@ def main():
     for i in range(3):
         g_main.replay()
     torch.cuda.synchronize()
-    ms, clocks = timed_replays([g_main] * full + ([g_rem] if g_rem else []),
-                               ClockSampler(dev.index if dev.index is not None else 0))
+    ms, clocks, reps_info = timed_replays([g_main] * full + ([g_rem] if g_rem else []),
+                                          ClockSampler(dev.index if dev.index is not None else 0))
 
     # Dominant kernel: the same steps with only the trellis contraction stage(s)
     # of each call (escha_*_gemv_stage), K steps between two CUDA events on the
@@ -1029,7 +1155,7 @@ def main():
     for i in range(3):
         gk_main.replay()
     torch.cuda.synchronize()
-    k_ms, _ = timed_replays([gk_main] * full + ([gk_rem] if gk_rem else []))
+    k_ms, _, _ = timed_replays([gk_main] * full + ([gk_rem] if gk_rem else []))
     k_n = gemv_launches_per_step * args.steps
     k_bytes = WL.gemv_kernel_bytes(m, spec["layers"]) * args.steps
     achieved = k_bytes / (k_ms / 1e3) / 1e9 if k_ms > 0 else None
@@ -1058,18 +1184,23 @@ def main():
     value = world * args.steps * sbytes / (ms / 1e3) / 1e9
     peaks, peak_src = measured_peaks()
     peak = float(peaks["hbm_gbs"])
+    k_launch_s = k_ms / 1e3 / k_n
+    weights_per_launch = sum(i * o for i, o, _ in spec["layers"]) / gemv_launches_per_step
     line = {
-        "metric": "decode GEMV compressed-weight GB/s (algorithmic bytes: codes + side vectors + activations)",
+        "metric": METRIC_DECODE,
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "us_per_layer": 1e3 * ms / args.steps / len(spec["layers"]),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded uniform code words, N(1,0.1) scales, N(0,1) activations)",
         "config": {"workload": spec["name"], "tokens": m,
-                   "bytes_per_step": sbytes,
+                   "bytes_per_step": sbytes, "bytes": BYTES_NOTE,
                    "l2": "%d rotating weight sets, %.0f MB of code words (> 4x L2)"
                          % (n_inst, n_inst * code_per_inst / 1e6),
-                   "timing": "CUDA graphs of the public API calls, CUDA events"},
+                   "timing": "CUDA graphs of the public API calls, CUDA events; median of %d "
+                             "repeats of the %d-step region (min %.4f, max %.4f ms per step)"
+                             % (reps_info[0], args.steps, reps_info[1] / args.steps,
+                                reps_info[2] / args.steps)},
         "roofline": {"bound": "hbm", "kernel": "trellis_gemv",
                      "launch_us": 1e3 * k_ms / k_n,
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -1082,10 +1213,19 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    issue = issue_roofline(spec["name"] if m == 1 else None, weights_per_launch / k_launch_s,
+                           props.multi_processor_count, clocks)
+    if issue is not None:
+        line["roofline_issue"] = issue
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_sample_rate(spec, m, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
+    if spec["kind"] == "mlp" and not args.no_prefill and args.workload == "mlp":
+        pspec = prefill_spec(args)
+        line["prefill"] = measure_prefill(args, pspec, rep, dev, PREFILL_DEFAULT["m"],
+                                          want_cpu=(rank == 0 and world == 1
+                                                    and not args.no_cpu_baseline))
     rep.emit(line)
     rep.close()
     return 0

@@ -13,6 +13,17 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / np.linalg.norm(b))
 
 
+def worst_rel_l2(a, b):
+    """The larger of the whole-output relative L2 error and the worst single
+    token's (row's): a wrong token or block cannot hide in the whole-output norm."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    err = rel_l2(a, b)
+    if a.ndim == 2 and a.shape[0] > 1:
+        err = max(err, max(rel_l2(a[r], b[r]) for r in range(a.shape[0])))
+    return err
+
+
 def cuda_layer(layer):
     import torch
     d = {}

@@ -58,3 +58,39 @@ def test_every_workload_parses(monkeypatch):
     for wl in ("mlp", "linear512", "sweep", "prefill", "moe", "encode"):
         _, spec = _spec(monkeypatch, "--workload", wl)
         assert spec["name"] and spec["layers"]
+
+
+def test_timed_region_repeats():
+    assert bench.repeats_for(1.4) == 179          # 20 steps of 70 us: about 0.25 s in all
+    assert bench.repeats_for(0.01) == bench.MAX_REPEATS
+    assert bench.repeats_for(1000.0) == bench.MIN_REPEATS
+    assert bench.repeats_for(10.0) == 25
+    assert bench.repeats_for(5.0, asked=3) == 3
+
+
+def test_issue_roofline_is_the_tighter_of_issue_and_alu(monkeypatch):
+    _, spec = _spec(monkeypatch)
+    r = bench.issue_roofline(spec["name"], 4.0e12, 152, {"sm_mhz": 2000.0})
+    mix = bench.GEMV_ISSUE_MIX[spec["name"]]
+    f = 152 * 4 * 2000e6
+    assert abs(r["peak"] * 1e12 - min(f * 32 / mix["issue"], f * 16 / mix["alu"])) < 1e3
+    assert abs(r["frac"] - 4.0e12 / (r["peak"] * 1e12)) < 1e-12
+    assert bench.issue_roofline(None, 1.0, 152, None) is None
+    assert bench.issue_roofline("no capture of this workload", 1.0, 152, None) is None
+
+
+def test_default_line_prefill_half_is_the_2048_token_gemm(monkeypatch):
+    args, spec = _spec(monkeypatch)
+    p = bench.prefill_spec(args)
+    assert p["kind"] == "prefill" and p["layers"] == [(5120, 17408, 3)]
+    assert not p["fp8"] and p["rounding"] == "fp16" and "M=2048" in p["name"]
+    assert bench.PREFILL_TRAFFIC_BYTES.get(p["name"]) is not None
+    assert args.workload == "mlp" and args.m == 1          # the decode half is unchanged
+
+
+def test_both_arms_print_one_metric_string_per_kind():
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    # every "metric" key of either arm takes one of the three shared strings
+    import re
+    vals = re.findall(r'"metric": ([A-Za-z_"][^,]*),', src)
+    assert vals and set(vals) <= {"METRIC_DECODE", "METRIC_PREFILL", "METRIC_ENCODE"}

@@ -13,7 +13,8 @@ import pytest
 
 from gemm_trellis_tile_gb300 import synthetic as S
 from oracle import escha_oracle as O
-from tests.helpers import REL_L2_TOL, make_linear_handle, oracle_layer_dict, oracle_linear, rel_l2
+from tests.helpers import (REL_L2_TOL, make_linear_handle, oracle_layer_dict, oracle_linear,
+                           rel_l2, worst_rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,13 +57,13 @@ def test_gemv_and_gemm_e4m3_match_oracle(bits, k, n):
         xt = torch.from_numpy(x).cuda()
         ref = oracle_linear(layer, x, w8)
         y = lin.gemv(xt).cpu().numpy()
-        assert rel_l2(y, ref) <= REL_L2_TOL, m
+        assert worst_rel_l2(y, ref) <= REL_L2_TOL, m
         # the rounding is visible: the fp16 weights are far outside the tolerance
         assert rel_l2(oracle_linear(layer, x, w16), ref) > 5 * REL_L2_TOL
         yg = lin.gemm(xt).cpu().numpy()
-        assert rel_l2(yg, ref) <= REL_L2_TOL, m
+        assert worst_rel_l2(yg, ref) <= REL_L2_TOL, m
     x = S.make_activations(rng, 300, k)
-    assert rel_l2(lin.gemm(torch.from_numpy(x).cuda()).cpu().numpy(),
+    assert worst_rel_l2(lin.gemm(torch.from_numpy(x).cuda()).cpu().numpy(),
                   oracle_linear(layer, x, w8)) <= REL_L2_TOL
 
 
@@ -81,7 +82,7 @@ def test_mlp_takes_each_matrix_rounding():
     ref = O.mlp_forward(x, oracle_layer_dict(mlp["gate"], rounding="e4m3"),
                         oracle_layer_dict(mlp["up"], rounding="e4m3"),
                         oracle_layer_dict(mlp["down"], rounding="e4m3"))
-    assert rel_l2(y, ref) <= REL_L2_TOL
+    assert worst_rel_l2(y, ref) <= REL_L2_TOL
 
 
 def test_moe_e4m3_matches_oracle():
@@ -111,7 +112,7 @@ def test_moe_e4m3_matches_oracle():
         y = moe.gemv(torch.from_numpy(x).cuda(), torch.from_numpy(ids).cuda(),
                      torch.from_numpy(w).cuda()).cpu().numpy()
         assert moe.check() == 0
-        assert rel_l2(y, O.moe_forward(x, experts, ids, w)) <= REL_L2_TOL
+        assert worst_rel_l2(y, O.moe_forward(x, experts, ids, w)) <= REL_L2_TOL
 
 
 def test_set_rounding_rejects_unknown_modes():

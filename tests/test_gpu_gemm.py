@@ -11,7 +11,8 @@ import pytest
 
 from gemm_trellis_tile_gb300 import synthetic as S
 from oracle import escha_oracle as O
-from tests.helpers import REL_L2_TOL, make_linear_handle, oracle_linear, oracle_scales, rel_l2
+from tests.helpers import (REL_L2_TOL, make_linear_handle, oracle_linear, oracle_scales,
+                           worst_rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +42,7 @@ def test_gemm_matches_oracle(m, k, n, bits):
     assert lin.check() == 0
     got = y.cpu().numpy()
     assert np.all(np.isfinite(got))
-    assert rel_l2(got, oracle_linear(layer, x)) <= REL_L2_TOL
+    assert worst_rel_l2(got, oracle_linear(layer, x)) <= REL_L2_TOL
 
 
 def test_gemm_is_bit_reproducible_with_shared_tiles():
@@ -68,13 +69,13 @@ def test_gemm_agrees_with_gemv_and_grows_workspace():
         xt = torch.from_numpy(x).cuda()
         yg = lin.gemm(xt).cpu().numpy()
         ref = oracle_linear(layer, x, w)
-        assert rel_l2(yg, ref) <= REL_L2_TOL, m
+        assert worst_rel_l2(yg, ref) <= REL_L2_TOL, m
         if m <= 16:
             yv = lin.gemv(xt).cpu().numpy()
-            assert rel_l2(yg, yv) <= REL_L2_TOL
+            assert worst_rel_l2(yg, yv) <= REL_L2_TOL
     lin.reserve(4096)
     x = S.make_activations(rng, 5, 1024)
-    assert rel_l2(lin.gemm(torch.from_numpy(x).cuda()).cpu().numpy(),
+    assert worst_rel_l2(lin.gemm(torch.from_numpy(x).cuda()).cpu().numpy(),
                   oracle_linear(layer, x, w)) <= REL_L2_TOL
 
 
@@ -92,4 +93,4 @@ def test_gemm_prefill_full_size_sampled(k, n, blocks):
     assert np.all(np.isfinite(got))
     su, sv = oracle_scales(layer)
     cols, ref = O.linear_forward_columns(x, layer["code"], 3, su, sv, blocks)
-    assert rel_l2(got[:, cols], ref) <= REL_L2_TOL
+    assert worst_rel_l2(got[:, cols], ref) <= REL_L2_TOL

@@ -8,7 +8,7 @@ import pytest
 
 from gemm_trellis_tile_gb300 import synthetic as S
 from oracle import escha_oracle as O
-from tests.helpers import REL_L2_TOL, oracle_layer_dict, rel_l2
+from tests.helpers import REL_L2_TOL, oracle_layer_dict, worst_rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def test_mlp_input_norm_matches_oracle(m, offset):
     y = mlp.gemv(torch.from_numpy(x).cuda()).cpu().numpy()
     assert mlp.check() == 0
     ref = _oracle(spec, O.rms_norm(x, w, eps, stored_minus_one=offset))
-    assert rel_l2(y, ref) <= REL_L2_TOL
+    assert worst_rel_l2(y, ref) <= REL_L2_TOL
 
 
 def test_mlp_input_norm_removed_restores_the_plain_mlp():
@@ -79,4 +79,4 @@ def test_mlp_input_norm_full_width_stages_compose():
     torch.cuda.synchronize()
     assert torch.equal(full, staged)
     ref = _oracle(spec, O.rms_norm(x, w, 1e-6))
-    assert rel_l2(full.cpu().numpy(), ref) <= REL_L2_TOL
+    assert worst_rel_l2(full.cpu().numpy(), ref) <= REL_L2_TOL

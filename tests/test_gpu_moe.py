@@ -11,7 +11,7 @@ import pytest
 
 from gemm_trellis_tile_gb300 import synthetic as S
 from oracle import escha_oracle as O
-from tests.helpers import REL_L2_TOL, rel_l2
+from tests.helpers import REL_L2_TOL, worst_rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +67,7 @@ def test_moe_small_matches_oracle(m, topk):
     y = _run(moe, x, ids, w)
     assert moe.check() == 0
     ref = O.moe_forward(x, experts, ids, w)
-    assert rel_l2(y, ref) <= REL_L2_TOL
+    assert worst_rel_l2(y, ref) <= REL_L2_TOL
 
 
 def test_moe_repeated_calls_with_different_routing():
@@ -78,7 +78,7 @@ def test_moe_repeated_calls_with_different_routing():
         x = S.make_activations(rng, m, spec["hidden"])
         ids, w = S.make_routing(rng, m, spec["num_experts"], 8)
         y = _run(moe, x, ids, w)
-        assert rel_l2(y, O.moe_forward(x, experts, ids, w)) <= REL_L2_TOL
+        assert worst_rel_l2(y, O.moe_forward(x, experts, ids, w)) <= REL_L2_TOL
 
 
 def test_moe_duplicate_ids_are_summed():
@@ -88,7 +88,7 @@ def test_moe_duplicate_ids_are_summed():
     ids = np.array([[3, 3, 5, 7], [1, 2, 3, 3]], dtype=np.int32)
     w = np.array([[0.25, 0.5, 0.125, 0.125], [0.1, 0.2, 0.3, 0.4]], dtype=np.float32)
     y = _run(moe, x, ids, w)
-    assert rel_l2(y, O.moe_forward(x, experts, ids, w)) <= REL_L2_TOL
+    assert worst_rel_l2(y, O.moe_forward(x, experts, ids, w)) <= REL_L2_TOL
 
 
 def test_moe_out_of_range_id_is_skipped_and_flagged():
@@ -100,7 +100,7 @@ def test_moe_out_of_range_id_is_skipped_and_flagged():
     y = _run(moe, x, ids, w)
     assert moe.check() == 1                       # ESCHA_ERR_INVALID_ARG, flag cleared
     ref = O.moe_forward(x, experts, np.array([[2, 4]]), np.array([[0.4, 0.2]]))
-    assert rel_l2(y, ref) <= REL_L2_TOL
+    assert worst_rel_l2(y, ref) <= REL_L2_TOL
     assert moe.check() == 0
 
 
@@ -153,7 +153,7 @@ def test_moe_glm_shape_full_size_sampled():
                                                                   spec["s_in_down"][e]),
                                          sv_h, blocks)
         ref += float(w[0, k]) * yd[0]
-    assert rel_l2(y[0, cols], ref) <= REL_L2_TOL
+    assert worst_rel_l2(y[0, cols], ref) <= REL_L2_TOL
 
 
 def test_moe_stages_compose_to_the_full_call():
@@ -216,7 +216,7 @@ def test_moe_shared_expert_matches_oracle(m, topk):
     assert moe.check() == 0
     experts = {e: _expert_layers(spec, e, codes[e]) for e in used}
     ref = O.moe_forward_shared(x, experts, ids, w, _shared_layers(spec, sh))
-    assert rel_l2(y, ref) <= REL_L2_TOL
+    assert worst_rel_l2(y, ref) <= REL_L2_TOL
     del keep
 
 

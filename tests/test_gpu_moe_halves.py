@@ -12,7 +12,7 @@ import pytest
 
 from gemm_trellis_tile_gb300 import synthetic as S
 from oracle import escha_oracle as O
-from tests.helpers import REL_L2_TOL, rel_l2
+from tests.helpers import REL_L2_TOL, rel_l2, worst_rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +67,7 @@ def test_moe_halves_small_matches_oracle(m, topk):
     assert moe.check() == 0
     experts = {e: _expert(spec, e, codes[e]) for e in set(ids.reshape(-1).tolist())}
     ref = O.moe_forward(x, experts, ids, w)
-    assert rel_l2(y, ref) <= REL_L2_TOL
+    assert worst_rel_l2(y, ref) <= REL_L2_TOL
 
 
 def test_moe_halves_with_uniform_widths_equals_whole_matrix_storage():
@@ -99,7 +99,7 @@ def test_moe_halves_with_uniform_widths_equals_whole_matrix_storage():
         assert a.check() == 0 and b.check() == 0
         experts = {e: _expert(hspec, e, halves[e]) for e in set(ids.reshape(-1).tolist())}
         ref = O.moe_forward(x, experts, ids, w)
-        assert rel_l2(yb, ref) <= REL_L2_TOL
+        assert worst_rel_l2(yb, ref) <= REL_L2_TOL
         assert rel_l2(yb, ya) <= 2e-4          # the same sums, grouped differently in fp32
 
 
@@ -115,7 +115,7 @@ def test_moe_halves_table_is_reread_every_call():
     y0 = _run(moe, x, ids, w)
     assert moe.check() == 0
     ref0 = O.moe_forward(x, {e: _expert(spec, e, codes[e]) for e in range(12)}, ids, w)
-    assert rel_l2(y0, ref0) <= REL_L2_TOL
+    assert worst_rel_l2(y0, ref0) <= REL_L2_TOL
 
     t = moe.tables
     fresh = rng.integers(-32768, 32768, size=(spec["hidden"] // 16, 8, 64), dtype=np.int16)
@@ -139,7 +139,7 @@ def test_moe_halves_table_is_reread_every_call():
     codes2 = dict(codes)
     codes2[3] = ([g7[0], fresh] + list(g7[2:]), codes[3][1], d7)
     ref1 = O.moe_forward(x, {e: _expert(spec2, e, codes2[e]) for e in range(12)}, ids, w)
-    assert rel_l2(y1, ref1) <= REL_L2_TOL
+    assert worst_rel_l2(y1, ref1) <= REL_L2_TOL
     assert rel_l2(y1, y0) > 0.05
 
 
@@ -181,7 +181,7 @@ def test_moe_halves_bad_table_entry_is_flagged_not_read(what):
     y = _run(moe, x, ids, w)
     assert moe.check() == 0
     ref = O.moe_forward(x, {e: _expert(spec, e, codes[e]) for e in (2, 5, 6, 8)}, ids, w)
-    assert rel_l2(y, ref) <= REL_L2_TOL
+    assert worst_rel_l2(y, ref) <= REL_L2_TOL
 
 
 def test_moe_halves_e4m3_rounding():
@@ -193,7 +193,7 @@ def test_moe_halves_e4m3_rounding():
     y = _run(moe, x, ids, w)
     assert moe.check() == 0
     experts = {e: _expert(spec, e, codes[e], "e4m3") for e in set(ids.reshape(-1).tolist())}
-    assert rel_l2(y, O.moe_forward(x, experts, ids, w)) <= REL_L2_TOL
+    assert worst_rel_l2(y, O.moe_forward(x, experts, ids, w)) <= REL_L2_TOL
 
 
 def test_moe_halves_stages_compose_to_the_full_call():
@@ -243,4 +243,4 @@ def test_moe_halves_glm_shape_full_size_sampled(m):
                             axis=0)
         xh = O.had_blockwise(h * O.fold_scales(spec["rin_down"][e], spec["s_in_down"][e]))
         ref += float(w[0, k]) * (O.had_blockwise(xh @ wd.astype(np.float64)) * sv_h[cols])[0]
-    assert rel_l2(y[0, cols], ref) <= REL_L2_TOL
+    assert worst_rel_l2(y[0, cols], ref) <= REL_L2_TOL
