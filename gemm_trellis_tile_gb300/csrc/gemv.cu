@@ -164,6 +164,33 @@ struct ChunkIter {
     g = static_cast<int>(rel / KT);
     kt = static_cast<int>(rel - (long long)g * KT);
   }
+  // The next segment: the units of the range in the current (job, group),
+  // from the current position on.
+  __device__ __forceinline__ bool next_segment(const GemvJob* jobs, Chunk& ch) {
+    if (u >= u1) return false;
+    while (u >= ue) {  // entered the next job: it starts at its group 0, k-tile 0
+      ++j;
+      load(jobs);
+      g = 0;
+      kt = 0;
+    }
+    const long long left = u1 - u;
+    int n = KT - kt;
+    if ((long long)n > left) n = static_cast<int>(left);
+    ch.g = g;
+    ch.kt = kt;
+    ch.n = n;
+    ch.seg_end = true;
+    u += n;
+    kt += n;
+    if (kt == KT) {
+      kt = 0;
+      ++g;
+    }
+    return true;
+  }
+  // The next stage-sized chunk (the producer's walk; within a segment it
+  // splits the units exactly as the consumers' run_segment does).
   // rpu: the launch's k-tile rows per unit (1 or 8).
   __device__ __forceinline__ bool next(const GemvJob* jobs, Chunk& ch, int rpu) {
     if (u >= u1) return false;
@@ -223,60 +250,92 @@ __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t*
   }
 }
 
-// One stage: n units (k-tile rows of 8 tiles); this warp owns tile column w.
-// The stage holds fragments for the M real tokens only.  A lane whose token
-// (8 tb + g) is at or past M reads token M-1's fragment instead: MMA output
-// column g depends on B column g alone, and those columns are never stored.
-// MC > 0: the token count M is the compile-time MC (activation fragment
-// addresses become immediate offsets); MC = 0: M at run time.
-template <int BITS, int TB, bool E4M3, int MC = 0>
-__device__ __forceinline__ void consume_chunk(const uint8_t* codes_s, const uint4* xf_s, int n,
-                                              int w, int lane, int M_rt, uint32_t mask,
-                                              uint32_t xr, float (&acc)[TB][4]) {
+// A consumer group's view of its ring stages (stage s serves group s % kGroups).
+struct GroupRing {
+  const uint8_t* codes;  // stage code words, kCodeStageBytes each
+  const uint8_t* xfs;    // stage activation fragments
+  uint64_t* bars;        // [0, S): full barriers; [S, 2S): empty barriers
+  int q;                 // group
+  int slot;              // next stage index within the group's stages
+  uint32_t phase;
+};
+
+// One segment: n consecutive units of one job and one 128-channel output
+// group, streamed through the group's stages (kUPS k-tile rows per full
+// stage); this warp owns tile column wt.  Everything that does not change
+// from stage to stage (the lane's word offsets, its funnel shift, its
+// activation-fragment offsets) is set up once per segment.  The stage holds
+// fragments for the M real tokens only; a lane whose token (8 tb + g) is at or
+// past M reads token M-1's fragment instead: MMA output column g depends on B
+// column g alone, and those columns are never stored.  MC > 0: the token
+// count is the compile-time MC (fragment addresses become immediate offsets).
+// Returns false if a bounded wait ran out.
+template <int BITS, int TB, bool E4M3, int MC, int STAGES, int RPU>
+__device__ __forceinline__ bool run_segment(GroupRing& rg, int n, int wt, int lane, int M_rt,
+                                            const GemvArgs& a, float (&acc)[TB][4]) {
   const int M = MC > 0 ? MC : M_rt;
-  constexpr int T = 32 * BITS;
-  constexpr int kRowWords = kCW * T / 4;  // uint32 words per unit in the stage
+  constexpr int T = 32 * BITS;            // bytes per tile
+  constexpr int kRowWords = kCW * T / 4;  // uint32 words per k-tile row of the stage
+  constexpr int cap = kUPS / RPU;         // units per full stage
   const LaneWindow lw = lane_window<BITS>(lane);
-  const uint32_t* base = reinterpret_cast<const uint32_t*>(codes_s + w * T);
-  const uint32_t* p0 = base + lw.i0;
-  const uint32_t* p1 = base + lw.i1;
+  const int o0 = wt * (T / 4) + lw.i0;
+  const int o1 = wt * (T / 4) + lw.i1;
   const int g = lane >> 2;
-  const int xstride = 4 * M;  // uint4 per unit
-  const uint4* xq[TB];
+  const int xstride = 4 * M;  // uint4 per k-tile row
+  int xo[TB];
 #pragma unroll
-  for (int tb = 0; tb < TB; ++tb) xq[tb] = xf_s + 4 * min(8 * tb + g, M - 1) + (lane & 3);
-  if (n == kUPS) {
-    for (int h = 0; h < kUPS; h += 8) {
+  for (int tb = 0; tb < TB; ++tb) xo[tb] = 4 * min(8 * tb + g, M - 1) + (lane & 3);
+  const uint32_t mask = a.cb_mask, xr = a.cb_xor;
+  for (int left = n; left > 0;) {
+    const int nu = left < cap ? left : cap;
+    const int stage = rg.q + kGroups * rg.slot;
+    if (!mbar_wait(smem_u32(&rg.bars[stage]), rg.phase, a.limit_ns)) return false;
+    const uint32_t* cw = reinterpret_cast<const uint32_t*>(rg.codes + stage * kCodeStageBytes);
+    const uint4* xs = reinterpret_cast<const uint4*>(rg.xfs + stage * xf_stage_bytes<TB>());
+    const uint32_t* p0 = cw + o0;
+    const uint32_t* p1 = cw + o1;
+    const uint4* xq[TB];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        consume_unit<BITS, TB, E4M3>(p0 + (h + i) * kRowWords, p1 + (h + i) * kRowWords, xq,
-                                     lw.sh7, mask, xr, acc);
+    for (int tb = 0; tb < TB; ++tb) xq[tb] = xs + xo[tb];
+    const int rows = nu * RPU;
+    if (rows == kUPS) {
+#pragma unroll
+      for (int i = 0; i < kUPS; ++i) {
+        consume_unit<BITS, TB, E4M3>(p0 + i * kRowWords, p1 + i * kRowWords, xq, lw.sh7, mask, xr,
+                                     acc);
+#pragma unroll
+        for (int tb = 0; tb < TB; ++tb) xq[tb] += xstride;
+      }
+    } else {
+      for (int i = 0; i < rows; ++i) {
+        consume_unit<BITS, TB, E4M3>(p0 + i * kRowWords, p1 + i * kRowWords, xq, lw.sh7, mask, xr,
+                                     acc);
 #pragma unroll
         for (int tb = 0; tb < TB; ++tb) xq[tb] += xstride;
       }
     }
-  } else {
-    for (int i = 0; i < n; ++i) {
-      consume_unit<BITS, TB, E4M3>(p0 + i * kRowWords, p1 + i * kRowWords, xq, lw.sh7, mask, xr,
-                                   acc);
-#pragma unroll
-      for (int tb = 0; tb < TB; ++tb) xq[tb] += xstride;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&rg.bars[STAGES + stage]));
+    if (++rg.slot == STAGES / kGroups) {
+      rg.slot = 0;
+      rg.phase ^= 1u;
     }
+    left -= nu;
   }
+  return true;
 }
 
-// The chunk's decode at its width and rounding (key = bits + 8 * e4m3).
-template <int TB, int MC>
-__device__ __forceinline__ void consume_dispatch(int key, const uint8_t* cs, const uint4* xs,
-                                                 int rows, int wt, int lane, int M, uint32_t mask,
-                                                 uint32_t xr, float (&acc)[TB][4]) {
+// The segment's decode at its width and rounding (key = bits + 8 * e4m3).
+template <int TB, int MC, int STAGES, int RPU>
+__device__ __forceinline__ bool segment_dispatch(int key, GroupRing& rg, int n, int wt, int lane,
+                                                 int M, const GemvArgs& a, float (&acc)[TB][4]) {
   switch (key) {
-    case 2: consume_chunk<2, TB, false, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
-    case 3: consume_chunk<3, TB, false, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
-    case 4: consume_chunk<4, TB, false, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
-    case 10: consume_chunk<2, TB, true, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
-    case 11: consume_chunk<3, TB, true, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
-    default: consume_chunk<4, TB, true, MC>(cs, xs, rows, wt, lane, M, mask, xr, acc); break;
+    case 2: return run_segment<2, TB, false, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
+    case 3: return run_segment<3, TB, false, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
+    case 4: return run_segment<4, TB, false, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
+    case 10: return run_segment<2, TB, true, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
+    case 11: return run_segment<3, TB, true, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
+    default: return run_segment<4, TB, true, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
   }
 }
 
@@ -428,55 +487,43 @@ __global__ void __launch_bounds__(threads_for<MODE>(), 1)
   if (r >= G) return;
   ChunkIter it;
   it.init(jobs, cta_start(r, U, G), cta_start(r + 1, U, G), a.job_units);
-  Chunk ch;
+  Chunk sg;
   float acc[TB][4];
 #pragma unroll
   for (int tb = 0; tb < TB; ++tb)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[tb][i] = 0.f;
-  int slot = 0;  // next stage index within the group's stages
-  uint32_t phase = 0;
-  while (it.next(jobs, ch, RPU)) {
-    const int stage = q + kGroups * slot;
-    if (!mbar_wait(smem_u32(&bars[stage]), phase, a.limit_ns)) {
+  GroupRing rg{codes, xfs, bars, q, 0, 0u};
+  // The range walks its units as segments, one per (job, 128-channel group)
+  // it touches; each ends with the group's partial sums for this range.
+  while (it.next_segment(jobs, sg)) {
+    const int key = it.bits + 8 * it.e4m3;
+    const bool ok = (TB == 1 && a.M == 1)  // one token: the common decode case, specialised
+                        ? segment_dispatch<TB, 1, kStages, RPU>(key, rg, sg.n, wt, lane, 1, a, acc)
+                        : segment_dispatch<TB, 0, kStages, RPU>(key, rg, sg.n, wt, lane, a.M, a,
+                                                                acc);
+    if (!ok) {
       set_error(a.err, kDevErrTimeout);
       break;
     }
-    const uint8_t* cs = codes + stage * kCodeStageBytes;
-    const uint4* xs = reinterpret_cast<const uint4*>(xfs + stage * xf_stage_bytes<TB>());
-    const int rows = ch.n * RPU;  // k-tile rows of the stage
-    if (TB == 1 && a.M == 1)  // one token: the common decode case, specialised
-      consume_dispatch<TB, 1>(it.bits + 8 * it.e4m3, cs, xs, rows, wt, lane, 1, a.cb_mask,
-                              a.cb_xor, acc);
-    else
-      consume_dispatch<TB, 0>(it.bits + 8 * it.e4m3, cs, xs, rows, wt, lane, a.M, a.cb_mask,
-                              a.cb_xor, acc);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + stage]));
-    if (++slot == kStages / kGroups) {
-      slot = 0;
-      phase ^= 1u;
-    }
-    if (ch.seg_end) {
-      const long long gb = it.ub + (long long)ch.g * it.KT;
-      const int ps = r - cta_of_unit(gb, U, G);  // partial-sum slot
-      const int n0 = 128 * ch.g + 16 * wt + (lane >> 2);
-      const int t2 = 2 * (lane & 3);
-      const float f = it.e4m3 ? 0.5f : 1.0f;  // the E4M3 path's MMAs form 2*w*x
+    const long long gb = it.ub + (long long)sg.g * it.KT;
+    const int ps = r - cta_of_unit(gb, U, G);  // partial-sum slot
+    const int n0 = 128 * sg.g + 16 * wt + (lane >> 2);
+    const int t2 = 2 * (lane & 3);
+    const float f = it.e4m3 ? 0.5f : 1.0f;  // the E4M3 path's MMAs form 2*w*x
 #pragma unroll
-      for (int tb = 0; tb < TB; ++tb) {
+    for (int tb = 0; tb < TB; ++tb) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int tok = 8 * tb + t2 + i;
-          if (tok < a.M) {
-            float* row = it.part + ((size_t)ps * a.mpad + tok) * it.N;
-            row[n0] = acc[tb][i] * f;
-            row[n0 + 8] = acc[tb][2 + i] * f;
-          }
+      for (int i = 0; i < 2; ++i) {
+        const int tok = 8 * tb + t2 + i;
+        if (tok < a.M) {
+          float* row = it.part + ((size_t)ps * a.mpad + tok) * it.N;
+          row[n0] = acc[tb][i] * f;
+          row[n0 + 8] = acc[tb][2 + i] * f;
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[tb][i] = 0.f;
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[tb][i] = 0.f;
     }
   }
 }
