@@ -65,9 +65,9 @@ GEMV_TRAFFIC_BYTES = {
 }
 # The same for one prefill GEMM launch (the trellis_gemm kernel alone).
 PREFILL_TRAFFIC_BYTES = {
-    "prefill GEMM 5120x17408 3-bit, M=2048 tokens": 171.01e6,
+    "prefill GEMM 5120x17408 3-bit, M=2048 tokens": 149.77e6,
     "prefill GEMM 5120x17408 3-bit, M=2048 tokens, FP8 tensor cores (E4M3 weights, "
-    "per-token E4M3 activations)": 153.60e6,
+    "per-token E4M3 activations)": None,
 }
 
 

@@ -397,6 +397,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       bool ok = true;
       Ring<kAStages> ra;
       pdl_wait();  // the activations are the previous kernel's output
+      // Every tile of a 512-row block reads the same activations: keep them in
+      // L2 ahead of the code words and outputs, which are touched once.
+      const uint64_t keep = policy_evict_last();
       while (ok && it.next(seg)) {
         const int m0 = (seg.tile / a.n_blocks) * kBM;
         for (int kb = seg.kb0; kb < seg.kb1; ++kb, ra.advance()) {
@@ -409,8 +412,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           }
           mbar_arrive_expect_tx(bar(kBarAFull + s), kABytes);
           const uint32_t dst = base + s * kABytes;
-          tma_load_2d(dst, &tmap_a, kb * G::kKE, m0, bar(kBarAFull + s));
-          tma_load_2d(dst + kABytes / 2, &tmap_a, kb * G::kKE, m0 + kBM / 2, bar(kBarAFull + s));
+          tma_load_2d_hint(dst, &tmap_a, kb * G::kKE, m0, bar(kBarAFull + s), keep);
+          tma_load_2d_hint(dst + kABytes / 2, &tmap_a, kb * G::kKE, m0 + kBM / 2,
+                           bar(kBarAFull + s), keep);
           armed[s] = static_cast<int>(ph);
         }
       }
@@ -426,6 +430,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       bool ok = true;
       Ring<kCStages> rc;
       const uint32_t row_bytes = 8 * T;
+      const uint64_t once = policy_evict_first();
       while (ok && it.next(seg)) {
         const int nb = seg.tile % a.n_blocks;
         for (int kb = seg.kb0; kb < seg.kb1; ++kb, rc.advance()) {
@@ -440,7 +445,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           const uint32_t dst = base + G::kOffC + s * G::kCBytes;
           for (int r = 0; r < G::kKT; ++r) {
             const uint8_t* src = a.code + ((size_t)(G::kKT * kb + r) * NT + 8 * nb) * T;
-            bulk_g2s(dst + r * row_bytes, src, row_bytes, bar(kBarCFull + s));
+            bulk_g2s_evict_first(dst + r * row_bytes, src, row_bytes, bar(kBarCFull + s), once);
           }
           armed[s] = static_cast<int>(ph);
         }

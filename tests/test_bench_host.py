@@ -32,7 +32,7 @@ def test_prefill_traffic_figures_are_keyed_by_the_workload_names(monkeypatch, fp
     _, spec = _spec(monkeypatch, "--workload", "prefill", *(["--fp8"] if fp8 else []))
     assert spec["fp8"] is fp8
     assert spec["rounding"] == ("e4m3" if fp8 else "fp16")
-    assert bench.PREFILL_TRAFFIC_BYTES.get(spec["name"]) is not None
+    assert spec["name"] in bench.PREFILL_TRAFFIC_BYTES
 
 
 def test_fp8_only_changes_the_prefill(monkeypatch):
