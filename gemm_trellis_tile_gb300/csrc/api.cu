@@ -439,7 +439,7 @@ escha_status_t escha_quantize_e4m3_rows(const uint16_t* xh, uint8_t* q, float* d
   if (escha::quantize_e4m3_smem_bytes(K) > escha::kMaxQuantSmem) return ESCHA_ERR_INVALID_ARG;
   if (!aligned16(xh) || !aligned16(q) || !aligned16(d)) return ESCHA_ERR_INVALID_ARG;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return after_launch(escha::from_cuda(escha::launch_quantize_e4m3_rows(xh, nullptr, q, d, M, K, st)),
+  return after_launch(escha::from_cuda(escha::launch_quantize_e4m3_rows(xh, nullptr, q, d, M, K, nullptr, 0, st)),
                       st);
 }
 

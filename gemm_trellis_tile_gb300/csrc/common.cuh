@@ -187,6 +187,35 @@ __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
   }
 }
 
+// The same transform with eight consecutive elements per lane: a 128-block
+// per half-warp (element 8*(lane & 15) + r in v[r]).  Three butterfly stages
+// in registers, four across the half-warp's lanes, in the same order of index
+// bits and with the same operations as fwht128_warp, so the results are
+// bit-identical.  Every lane of the warp must take part.
+__device__ __forceinline__ void fwht128_halfwarp(float (&v)[8], int lane) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const float p = v[i], q = v[i + h];
+        v[i] = p + q;
+        v[i + h] = p - q;
+      }
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int m = 1 << s;
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[r], m);
+      v[r] = fmaf(sgn, v[r], o);
+    }
+  }
+}
+
 __device__ __forceinline__ float half_bits_to_float(uint16_t b) {
   return __half2float(__ushort_as_half(b));
 }

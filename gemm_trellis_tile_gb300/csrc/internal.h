@@ -122,8 +122,9 @@ cudaError_t launch_trellis_gemm_fp8(const uint8_t* xq, const float* d, const int
 // keeps the row in quantize_e4m3_smem_bytes(K) of shared memory.
 size_t quantize_e4m3_smem_bytes(int K);
 constexpr size_t kMaxQuantSmem = 128 * 1024;  // K <= 65536
+// cnt/ncnt: the prefill GEMM's arrival counters, zeroed by the kernel (null/0: none).
 cudaError_t launch_quantize_e4m3_rows(const uint16_t* x, const float* su, uint8_t* q, float* d,
-                                      int M, int K, cudaStream_t st);
+                                      int M, int K, int* cnt, int ncnt, cudaStream_t st);
 cudaError_t launch_decode(const int16_t* code, int bits, bool e4m3, int K, int N, uint16_t* w,
                           cudaStream_t st);
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t st);
@@ -181,8 +182,9 @@ cudaError_t launch_rotate_in_norm(const uint16_t* x, const float* g_gate, const 
                                   cudaStream_t st);
 cudaError_t launch_fold_norm(const uint16_t* w, float offset, const float* su, float* g, int n,
                              cudaStream_t st);
+// cnt/ncnt: the prefill GEMM's arrival counters, zeroed by the kernel.
 cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t* xh, int M,
-                                   int K, cudaStream_t st);
+                                   int K, int* cnt, int ncnt, cudaStream_t st);
 cudaError_t launch_rotate_out(const PartRef& pr, long long units, int grid, const float* sv,
                               uint16_t* y, int M, int mpad, cudaStream_t st);
 cudaError_t launch_mlp_mid(const PartRef& gate, const PartRef& up, long long units, int grid,

@@ -227,14 +227,15 @@ escha_status_t linear_reserve(escha_linear_s* h, int rows) {
 }
 
 // The prefill GEMM's split-tile workspace for M rows: partial sums (fixed size)
-// and arrival counters (grown on demand), the counters cleared on `st`.  Called
-// before the call's first launch, so the clear is not between the rotation and
-// the GEMM that overlaps it.
-escha_status_t gemm_prepare(escha_linear_s* h, int M, cudaStream_t st) {
+// and arrival counters (grown on demand).  The counters must be zero when the
+// GEMM starts: the activation kernel that precedes it clears them, or, with
+// clear set (no such kernel), a clear on `st` here.
+escha_status_t gemm_prepare(escha_linear_s* h, int M, cudaStream_t st, bool clear) {
   escha_status_t s;
   if (!h->gemm_ws && (s = dev_alloc(&h->gemm_ws, gemm_workspace_floats(h->num_sms))) != ESCHA_OK)
     return s;
   if ((s = reserve_counters(h, M)) != ESCHA_OK) return s;
+  if (!clear) return ESCHA_OK;
   return from_cuda(
       cudaMemsetAsync(h->gemm_cnt, 0, gemm_counter_ints(M, h->N) * sizeof(int), st));
 }
@@ -243,8 +244,9 @@ escha_status_t linear_gemm(escha_linear_s* h, const uint16_t* x, uint16_t* y, in
                            cudaStream_t st) {
   escha_status_t s = linear_reserve(h, M);
   if (s != ESCHA_OK) return s;
-  if ((s = gemm_prepare(h, M, st)) != ESCHA_OK) return s;
-  cudaError_t e = launch_rotate_in_plain(x, h->su, h->xh, M, h->K, st);
+  if ((s = gemm_prepare(h, M, st, false)) != ESCHA_OK) return s;
+  cudaError_t e = launch_rotate_in_plain(x, h->su, h->xh, M, h->K, h->gemm_cnt,
+                                         static_cast<int>(gemm_counter_ints(M, h->N)), st);
   if (e != cudaSuccess) return from_cuda(e);
   h->prof.begin(st);
   e = launch_trellis_gemm(h->xh, h->code, h->bits, h->rounding == ESCHA_ROUND_E4M3, M, h->K,
@@ -263,9 +265,10 @@ escha_status_t linear_gemm_fp8(escha_linear_s* h, const uint16_t* x, uint16_t* y
   if (quantize_e4m3_smem_bytes(h->K) > kMaxQuantSmem) return ESCHA_ERR_UNSUPPORTED;
   escha_status_t s = linear_reserve(h, M);
   if (s != ESCHA_OK) return s;
-  if ((s = gemm_prepare(h, M, st)) != ESCHA_OK) return s;
+  if ((s = gemm_prepare(h, M, st, false)) != ESCHA_OK) return s;
   uint8_t* xq = reinterpret_cast<uint8_t*>(h->xh);
-  cudaError_t e = launch_quantize_e4m3_rows(x, h->su, xq, h->xd, M, h->K, st);
+  cudaError_t e = launch_quantize_e4m3_rows(x, h->su, xq, h->xd, M, h->K, h->gemm_cnt,
+                                            static_cast<int>(gemm_counter_ints(M, h->N)), st);
   if (e != cudaSuccess) return from_cuda(e);
   h->prof.begin(st);
   e = launch_trellis_gemm_fp8(xq, h->xd, h->code, h->bits, M, h->K, h->N, h->sv, y, h->gemm_ws,
@@ -277,7 +280,7 @@ escha_status_t linear_gemm_fp8(escha_linear_s* h, const uint16_t* x, uint16_t* y
 escha_status_t linear_gemm_fp8_codes(escha_linear_s* h, const uint8_t* q, const float* d,
                                      uint16_t* y, int M, cudaStream_t st) {
   if (h->rounding != ESCHA_ROUND_E4M3) return ESCHA_ERR_UNSUPPORTED;
-  escha_status_t s = gemm_prepare(h, M, st);
+  escha_status_t s = gemm_prepare(h, M, st, true);
   if (s != ESCHA_OK) return s;
   h->prof.begin(st);
   cudaError_t e = launch_trellis_gemm_fp8(q, d, h->code, h->bits, M, h->K, h->N, h->sv, y,

@@ -125,40 +125,79 @@ __global__ void fold_norm_kernel(const uint16_t* w, float offset, const float* s
   if (i < n) g[i] = (half_bits_to_float(w[i]) + offset) * su[i];
 }
 
-// Blocks of 128 channels a warp loads before it transforms any: with one
-// 256-byte load per warp in flight the prefill's rotations reached about a
-// third of HBM bandwidth.
+// Loads (16 bytes per lane: a pair of 128-blocks per warp) the E4M3 quantiser
+// keeps in flight per warp before it transforms any.
 constexpr int kRotBatch = 4;
 
-// xh[m, k] = fp16(had128(x * su)), plain row-major (the GEMM's A operand).
-// One warp per token and kRotBatch consecutive 128-blocks.
+// Zero the prefill GEMM's shared-tile arrival counters.  The kernels that
+// produce the GEMM's activations do it: the GEMM reads the counters only after
+// waiting for its predecessor (griddepcontrol.wait), and these kernels are
+// launched in plain stream order after the previous GEMM, so no separate clear
+// is needed between calls.
+__device__ __forceinline__ void clear_counters(int* cnt, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    cnt[i] = 0;
+}
+
+constexpr int kPlainPairs = 4;  // pairs of 128-blocks per warp in rotate_in_plain
+
+// xh = fp16(had128(x * su)), row-major [M, K] (the prefill GEMM's A operand).
+// One warp per token and 2 * kPlainPairs consecutive 128-blocks: each lane
+// loads 16 bytes of each pair (half-warp h holds block 2i + h), all loads in
+// flight before the transforms; 16-byte stores.
 __global__ void rotate_in_plain_kernel(const uint16_t* x, const float* su, uint16_t* xh, int M,
-                                       int K) {
+                                       int K, int* cnt, int ncnt) {
   pdl_trigger();  // the GEMM may set up; it waits for this kernel before loading xh
+  clear_counters(cnt, ncnt);
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int nb = K / kHad;
-  const int ng = (nb + kRotBatch - 1) / kRotBatch;
+  constexpr int kPer = 2 * kPlainPairs;
+  const int ng = (nb + kPer - 1) / kPer;
   if (wid >= (long long)M * ng) return;
   const int m = static_cast<int>(wid / ng);
-  const int b0 = static_cast<int>(wid - (long long)m * ng) * kRotBatch;
-  float v[kRotBatch][4];
+  const int b0 = static_cast<int>(wid - (long long)m * ng) * kPer + (lane >> 4);
+  const int e = 8 * (lane & 15);
+  const uint16_t* xr = x + (size_t)m * K;
+  uint4 raw[kPlainPairs];
 #pragma unroll
-  for (int i = 0; i < kRotBatch; ++i)
-    if (b0 + i < nb) load4_half(x + (size_t)m * K + (b0 + i) * kHad + 4 * lane, v[i]);
+  for (int i = 0; i < kPlainPairs; ++i) {
+    const int b = b0 + 2 * i;
+    raw[i] = b < nb ? *reinterpret_cast<const uint4*>(xr + b * kHad + e) : make_uint4(0, 0, 0, 0);
+  }
 #pragma unroll
-  for (int i = 0; i < kRotBatch; ++i) {
-    if (b0 + i >= nb) break;
-    const int k0 = (b0 + i) * kHad + 4 * lane;
-    const float4 s = *reinterpret_cast<const float4*>(su + k0);
-    v[i][0] *= s.x;
-    v[i][1] *= s.y;
-    v[i][2] *= s.z;
-    v[i][3] *= s.w;
-    fwht128_warp(v[i], lane);
+  for (int i = 0; i < kPlainPairs; ++i) {
+    const int b = b0 + 2 * i;
+    const bool valid = b < nb;
+    const int k0 = b * kHad + e;
+    float v[8];
+    const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
-    for (int r = 0; r < 4; ++r) v[i][r] *= kHadScale;
-    store4_half(xh + (size_t)m * K + k0, v[i]);
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = half_bits_to_float(w[j] & 0xFFFF);
+      v[2 * j + 1] = half_bits_to_float(w[j] >> 16);
+    }
+    if (valid) {
+      const float4 s0 = *reinterpret_cast<const float4*>(su + k0);
+      const float4 s1 = *reinterpret_cast<const float4*>(su + k0 + 4);
+      v[0] *= s0.x;
+      v[1] *= s0.y;
+      v[2] *= s0.z;
+      v[3] *= s0.w;
+      v[4] *= s1.x;
+      v[5] *= s1.y;
+      v[6] *= s1.z;
+      v[7] *= s1.w;
+    }
+    fwht128_halfwarp(v, lane);  // every lane, valid or not
+    if (valid) {
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = float_to_half_bits(v[2 * j] * kHadScale) |
+               (uint32_t(float_to_half_bits(v[2 * j + 1] * kHadScale)) << 16);
+      *reinterpret_cast<uint4*>(xh + (size_t)m * K + k0) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -171,7 +210,8 @@ __global__ void rotate_in_plain_kernel(const uint16_t* x, const float* su, uint1
 //   q    = E4M3(xh * inv), nearest even, saturating  (the product rounded to fp32 first)
 // A row of zeros gives q = 0 and d = 0.  The row's xh waits in shared memory
 // (2K bytes) between the two passes.
-constexpr int kQuantThreads = 512;
+constexpr int kQuantThreads = 128;
+constexpr int kQuantWarps = kQuantThreads / 32;
 constexpr float kE4M3Max = 448.0f;
 
 // Two fp32 values to two E4M3 bytes: `lo` in the low byte.
@@ -181,54 +221,77 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
   return e;
 }
 
+// One block of kQuantThreads per token (16 blocks per SM, so 2048 tokens are
+// one wave).  Warp w takes the pairs of 128-blocks w, w + 4, ...: each lane
+// loads 16 bytes of a pair (half-warp h holds block 2p + h), up to
+// kRotBatch pairs in flight, then the half-warp transforms.
 template <bool ROTATE>
 __global__ void __launch_bounds__(kQuantThreads)
-    quantize_e4m3_rows_kernel(const uint16_t* x, const float* su, uint8_t* q, float* d, int K) {
+    quantize_e4m3_rows_kernel(const uint16_t* x, const float* su, uint8_t* q, float* d, int K,
+                              int* cnt, int ncnt) {
   extern __shared__ __align__(16) uint16_t xrow[];
-  __shared__ float part[kQuantThreads / 32];
-  constexpr int W = kQuantThreads / 32;
+  __shared__ float part[kQuantWarps];
   pdl_trigger();  // the GEMM may set up; it waits for this kernel before loading q or d
+  clear_counters(cnt, ncnt);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int m = blockIdx.x;
   const uint16_t* xr = x + (size_t)m * K;
   const int nb = K / kHad;
+  const int np = (nb + 1) / 2;  // pairs of blocks (the last may hold one)
+  const int e = 8 * (lane & 15);
   float amax = 0.f;
-  // warp w takes blocks w, w + W, w + 2W, ..., loading kRotBatch of them at a time
-  for (int i0 = 0; warp + W * i0 < nb; i0 += kRotBatch) {
-    uint2 batch[kRotBatch];
+  for (int p0 = warp; p0 < np; p0 += kQuantWarps * kRotBatch) {
+    uint4 batch[kRotBatch];
 #pragma unroll
     for (int i = 0; i < kRotBatch; ++i) {
-      const int b = warp + W * (i0 + i);
-      if (b < nb) batch[i] = *reinterpret_cast<const uint2*>(xr + b * kHad + 4 * lane);
+      const int b = 2 * (p0 + kQuantWarps * i) + (lane >> 4);
+      batch[i] = b < nb ? *reinterpret_cast<const uint4*>(xr + b * kHad + e) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < kRotBatch; ++i) {
-      const int b = warp + W * (i0 + i);
-      if (b >= nb) break;
-      const int k0 = b * kHad + 4 * lane;
-      uint2 raw = batch[i];
+      const int p = p0 + kQuantWarps * i;
+      if (p >= np) break;  // uniform across the warp
+      const int b = 2 * p + (lane >> 4);
+      const bool valid = b < nb;
+      const int k0 = b * kHad + e;
+      uint4 raw = batch[i];
       if (ROTATE) {
-        float v[4];
-        v[0] = half_bits_to_float(raw.x & 0xFFFF);
-        v[1] = half_bits_to_float(raw.x >> 16);
-        v[2] = half_bits_to_float(raw.y & 0xFFFF);
-        v[3] = half_bits_to_float(raw.y >> 16);
-        const float4 s = *reinterpret_cast<const float4*>(su + k0);
-        v[0] *= s.x;
-        v[1] *= s.y;
-        v[2] *= s.z;
-        v[3] *= s.w;
-        fwht128_warp(v, lane);
-        raw.x = float_to_half_bits(v[0] * kHadScale) |
-                (uint32_t(float_to_half_bits(v[1] * kHadScale)) << 16);
-        raw.y = float_to_half_bits(v[2] * kHadScale) |
-                (uint32_t(float_to_half_bits(v[3] * kHadScale)) << 16);
+        float v[8];
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[2 * j] = half_bits_to_float(w[j] & 0xFFFF);
+          v[2 * j + 1] = half_bits_to_float(w[j] >> 16);
+        }
+        if (valid) {
+          const float4 s0 = *reinterpret_cast<const float4*>(su + k0);
+          const float4 s1 = *reinterpret_cast<const float4*>(su + k0 + 4);
+          v[0] *= s0.x;
+          v[1] *= s0.y;
+          v[2] *= s0.z;
+          v[3] *= s0.w;
+          v[4] *= s1.x;
+          v[5] *= s1.y;
+          v[6] *= s1.z;
+          v[7] *= s1.w;
+        }
+        fwht128_halfwarp(v, lane);  // every lane of the warp
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = float_to_half_bits(v[2 * j] * kHadScale) |
+                 (uint32_t(float_to_half_bits(v[2 * j + 1] * kHadScale)) << 16);
+        raw = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      *reinterpret_cast<uint2*>(xrow + k0) = raw;
-      amax = fmaxf(amax, fabsf(half_bits_to_float(raw.x & 0xFFFF)));
-      amax = fmaxf(amax, fabsf(half_bits_to_float(raw.x >> 16)));
-      amax = fmaxf(amax, fabsf(half_bits_to_float(raw.y & 0xFFFF)));
-      amax = fmaxf(amax, fabsf(half_bits_to_float(raw.y >> 16)));
+      if (valid) {
+        *reinterpret_cast<uint4*>(xrow + k0) = raw;
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          amax = fmaxf(amax, fabsf(half_bits_to_float(w[j] & 0xFFFF)));
+          amax = fmaxf(amax, fabsf(half_bits_to_float(w[j] >> 16)));
+        }
+      }
     }
   }
 #pragma unroll
@@ -237,7 +300,7 @@ __global__ void __launch_bounds__(kQuantThreads)
   __syncthreads();
   amax = 0.f;
 #pragma unroll
-  for (int w = 0; w < W; ++w) amax = fmaxf(amax, part[w]);
+  for (int w = 0; w < kQuantWarps; ++w) amax = fmaxf(amax, part[w]);
   const float inv = amax > 0.f ? __fdiv_rn(kE4M3Max, amax) : 0.f;
   if (threadIdx.x == 0) d[m] = amax > 0.f ? __fdiv_rn(amax, kE4M3Max) : 0.f;
   uint8_t* qr = q + (size_t)m * K;
@@ -368,25 +431,27 @@ cudaError_t launch_fold_norm(const uint16_t* w, float offset, const float* su, f
 }
 
 cudaError_t launch_rotate_in_plain(const uint16_t* x, const float* su, uint16_t* xh, int M,
-                                   int K, cudaStream_t st) {
-  const long long warps = (long long)M * ((K / kHad + kRotBatch - 1) / kRotBatch);
-  rotate_in_plain_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(x, su, xh, M, K);
+                                   int K, int* cnt, int ncnt, cudaStream_t st) {
+  const long long warps = (long long)M * ((K / kHad + 2 * kPlainPairs - 1) / (2 * kPlainPairs));
+  rotate_in_plain_kernel<<<blocks_for(warps), 32 * kWarpsPerBlock, 0, st>>>(x, su, xh, M, K, cnt,
+                                                                           ncnt);
   return cudaGetLastError();
 }
 
 size_t quantize_e4m3_smem_bytes(int K) { return (size_t)K * 2; }
 
 cudaError_t launch_quantize_e4m3_rows(const uint16_t* x, const float* su, uint8_t* q, float* d,
-                                      int M, int K, cudaStream_t st) {
+                                      int M, int K, int* cnt, int ncnt, cudaStream_t st) {
   const size_t smem = quantize_e4m3_smem_bytes(K);
   const void* fn = su ? reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<true>)
                       : reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<false>);
   cudaError_t e = set_smem_limit(fn, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (su)
-    quantize_e4m3_rows_kernel<true><<<M, kQuantThreads, smem, st>>>(x, su, q, d, K);
+    quantize_e4m3_rows_kernel<true><<<M, kQuantThreads, smem, st>>>(x, su, q, d, K, cnt, ncnt);
   else
-    quantize_e4m3_rows_kernel<false><<<M, kQuantThreads, smem, st>>>(x, nullptr, q, d, K);
+    quantize_e4m3_rows_kernel<false><<<M, kQuantThreads, smem, st>>>(x, nullptr, q, d, K, cnt,
+                                                                      ncnt);
   return cudaGetLastError();
 }
 
