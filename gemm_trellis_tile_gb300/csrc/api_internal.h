@@ -108,7 +108,8 @@ struct escha_moe_s {
   const int* gate_bits = nullptr;             // [E][H]
   const int* up_bits = nullptr;               // [E][H]
   const int* down_bits = nullptr;             // [E]
-  CUtensorMap* half_maps = nullptr;     // [kMoeMaxDistinct][H] down-half maps, written per call
+  CUtensorMap* half_maps = nullptr;     // [E][H] down-half maps, rewritten when a half's entry changes
+  unsigned long long* half_map_key = nullptr;  // [E][H] pointer | bits each map was written for (0: none)
   CUtensorMap* half_map_tmpl = nullptr; // [3] down-half map templates for 2/3/4 bits
   uint8_t* stand_in = nullptr;          // zero code replacing table entries that fail checks
   unsigned char* route = nullptr;       // device routing state

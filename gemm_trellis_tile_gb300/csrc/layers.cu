@@ -57,6 +57,7 @@ template escha_status_t dev_alloc<GemvJob>(GemvJob**, size_t);
 template escha_status_t dev_alloc<const uint8_t*>(const uint8_t***, size_t);
 template escha_status_t dev_alloc<unsigned char>(unsigned char**, size_t);
 template escha_status_t dev_alloc<CUtensorMap>(CUtensorMap**, size_t);
+template escha_status_t dev_alloc<unsigned long long>(unsigned long long**, size_t);
 
 namespace {
 

@@ -254,7 +254,8 @@ struct MoeHalvesPlanArgs {
   const int* up_bits;               // [E][H]
   const int* down_bits;             // [E]
   const CUtensorMap* tmpl;          // [3]: down-half maps for 2, 3, 4 bits
-  CUtensorMap* half_maps;           // [kMoeMaxDistinct][H]
+  CUtensorMap* half_maps;           // [E][H]
+  unsigned long long* half_map_key; // [E][H]: pointer | bits of each map (0: not written)
   const uint8_t* stand_in;          // zero code used in place of a failing entry
   int e4m3;
   const uint32_t* xfrag_hidden;
@@ -311,26 +312,34 @@ __global__ void moe_plan_halves_kernel(const MoeHalvesPlanArgs a, const MoeRotIn
     a.jobs1[q] = make_job(p, nullptr, a.xfrag_hidden, a.part1 + dm * a.part1_stride + 128 * h,
                           (long long)q * KTg, b, KTg, 1, a.inter, a.e4m3);
   }
-  // down: the tensor map of every half of every distinct expert
+  // down: the tensor map of every half of every distinct expert, kept per
+  // (expert, half) and rewritten only when the table's pointer or the
+  // expert's width differs from what the map was written for (the tables are
+  // re-read every call, so a caller may swap halves between calls)
   for (int q = threadIdx.x; q < nd * H; q += blockDim.x) {
     const int d = q / H, h = q - d * H;
     const int e = r->expert[d];
     const int b = checked_bits(a.down_bits[e], a.err);
     const uint8_t* p = checked_half(a.down_half[(size_t)e * H + h], a.stand_in, a.err);
+    const size_t slot = (size_t)e * H + h;
+    const unsigned long long key = reinterpret_cast<unsigned long long>(p) | (unsigned)b;
+    if (a.half_map_key[slot] == key) continue;
     const uint4* src = reinterpret_cast<const uint4*>(a.tmpl + (b - 2));
-    uint4* dst = reinterpret_cast<uint4*>(a.half_maps + q);
+    uint4* dst = reinterpret_cast<uint4*>(a.half_maps + slot);
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = src[i];
     asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst),
                  "l"(reinterpret_cast<uint64_t>(p))
                  : "memory");
     tensormap_release();
+    a.half_map_key[slot] = key;
   }
   for (int d = threadIdx.x; d < nd; d += blockDim.x) {
-    const int b = checked_bits(a.down_bits[r->expert[d]], a.err);
+    const int e = r->expert[d];
+    const int b = checked_bits(a.down_bits[e], a.err);
     GemvJob j = make_job(nullptr, nullptr, a.xfrag_down + d * a.xdown_stride,
                          a.part2 + d * a.part2_stride, d * ud, b, H, NGd, a.hidden, a.e4m3);
-    j.row_maps = a.half_maps + (size_t)d * H;
+    j.row_maps = a.half_maps + (size_t)e * H;
     a.jobs2[d] = j;
   }
   if (threadIdx.x == 0) {
@@ -615,7 +624,10 @@ escha_status_t moe_init_halves(escha_moe_s* h, int E, int hidden, int inter,
       if (!encode_gemv_half_map(&tm[b - 2], h->stand_in, b, hidden / 16)) return ESCHA_ERR_CUDA;
     if ((s = upload(&h->half_map_tmpl, tm, 3)) != ESCHA_OK) return s;
   }
-  if ((s = dev_alloc(&h->half_maps, (size_t)kMoeMaxDistinct * h->H)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->half_maps, (size_t)E * h->H)) != ESCHA_OK) return s;
+  if ((s = dev_alloc(&h->half_map_key, (size_t)E * h->H)) != ESCHA_OK) return s;
+  if (cudaMemset(h->half_map_key, 0, (size_t)E * h->H * sizeof(unsigned long long)) != cudaSuccess)
+    return ESCHA_ERR_CUDA;
   return moe_init_common(h, rin_hidden, s_in_hidden, rout_gate, s_out_gate, rout_up, s_out_up,
                          rin_down, s_in_down, rout_hidden, s_out_hidden,
                          (size_t)2 * kMoeMaxDistinct * h->H, st);
@@ -659,6 +671,7 @@ escha_status_t moe_set_shared_expert(escha_moe_s* h, const int16_t* gate_code,
 
 void moe_free(escha_moe_s* h) {
   cudaFree(h->half_maps);
+  cudaFree(h->half_map_key);
   cudaFree(h->half_map_tmpl);
   cudaFree(h->stand_in);
   cudaFree(h->code_maps);
@@ -707,6 +720,7 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
         pa.down_bits = h->down_bits;
         pa.tmpl = h->half_map_tmpl;
         pa.half_maps = h->half_maps;
+        pa.half_map_key = h->half_map_key;
         pa.stand_in = h->stand_in;
         pa.e4m3 = h->rounding == ESCHA_ROUND_E4M3 ? 1 : 0;
         pa.xfrag_hidden = h->xfrag_hidden;
