@@ -421,59 +421,48 @@ struct MoeOutArgs {
   int M, topk, hidden;
 };
 
-// One warp per (token m, 128-channel group g of the hidden side).
-__global__ void moe_out_kernel(const MoeOutArgs a) {
+// One block per (token m, 128-channel group g of the hidden side), one warp
+// per expert slot of the token: warp k < topk sums routed expert k's partial
+// slots, warp kMoeMaxTopk the shared expert's, all at once (each is a chain
+// of dependent loads: route, job, partial sums); then warp 0 adds them in
+// routing order (the shared expert last, weight 1), transforms and scales.
+constexpr int kOutWarps = kMoeMaxTopk + 1;
+__global__ void __launch_bounds__(32 * kOutWarps) moe_out_kernel(const MoeOutArgs a) {
+  __shared__ float4 ps[kOutWarps][32];
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, k = threadIdx.x >> 5;
   const int NG = a.hidden / kHad;
-  if (wid >= (long long)a.M * NG) return;
-  const int m = static_cast<int>(wid / NG);
-  const int g = static_cast<int>(wid - (long long)m * NG);
+  const int m = blockIdx.x / NG;
+  const int g = blockIdx.x - m * NG;
   const MoeRoute* r = a.route;
+  const int d = k < a.topk ? r->route[m * a.topk + k] : (k == kMoeMaxTopk ? r->shared_slot : -1);
+  float p[4] = {0.f, 0.f, 0.f, 0.f};
+  if (d >= 0) {
+    const GemvJob& j = a.jobs2[d];
+    sum_slots<kMoeSlots>(j.part, j.unit_begin, j.KT, j.N, r->units2, r->grid2, kMoeMaxTokens, m, g,
+                         lane, p);
+  }
+  ps[k][lane] = make_float4(p[0], p[1], p[2], p[3]);
+  __syncthreads();
+  if (k != 0) return;
   const int n0 = g * kHad + 4 * lane;
   const float4 s = load4_f32(a.sv_hidden + n0);
-  // Routes, weights and job fields of all routed experts first (independent
-  // loads), then their partial sums two experts at a time; the experts are
-  // still added in routing order.
-  int dk[kMoeMaxTopk];
-  float wk[kMoeMaxTopk];
-#pragma unroll
-  for (int k = 0; k < kMoeMaxTopk; ++k) {
-    dk[k] = k < a.topk ? r->route[m * a.topk + k] : -1;
-    wk[k] = k < a.topk ? a.expert_w[m * a.topk + k] : 0.f;
-  }
   float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int k = 0; k < kMoeMaxTopk; k += 2) {
-    const int d0 = dk[k], d1 = dk[k + 1];
-    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-    if (d0 >= 0 && d1 >= 0) {
-      const GemvJob& j0 = a.jobs2[d0];
-      const GemvJob& j1 = a.jobs2[d1];
-      sum_slots_pair<kMoeSlots>(j0.part, j0.unit_begin, j1.part, j1.unit_begin, j0.KT, j0.N,
-                                r->units2, r->grid2, kMoeMaxTokens, m, g, lane, p0, p1);
-    } else if (d0 >= 0 || d1 >= 0) {
-      const GemvJob& j = a.jobs2[d0 >= 0 ? d0 : d1];
-      sum_slots<kMoeSlots>(j.part, j.unit_begin, j.KT, j.N, r->units2, r->grid2, kMoeMaxTokens, m,
-                           g, lane, d0 >= 0 ? p0 : p1);
-    }
-    if (d0 >= 0) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] += wk[k] * p0[q];
-    }
-    if (d1 >= 0) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] += wk[k + 1] * p1[q];
-    }
+  for (int kk = 0; kk < a.topk; ++kk) {
+    if (r->route[m * a.topk + kk] < 0) continue;
+    const float w = a.expert_w[m * a.topk + kk];
+    const float4 q = ps[kk][lane];
+    v[0] += w * q.x;
+    v[1] += w * q.y;
+    v[2] += w * q.z;
+    v[3] += w * q.w;
   }
-  if (r->shared_slot >= 0) {  // the shared expert, weight 1, after the routed ones
-    const GemvJob& j = a.jobs2[r->shared_slot];
-    float ps[4];
-    sum_slots<kMoeSlots>(j.part, j.unit_begin, j.KT, j.N, r->units2, r->grid2, kMoeMaxTokens, m, g,
-                         lane, ps);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) v[q] += ps[q];
+  if (r->shared_slot >= 0) {
+    const float4 q = ps[kMoeMaxTopk][lane];
+    v[0] += q.x;
+    v[1] += q.y;
+    v[2] += q.z;
+    v[3] += q.w;
   }
   fwht128_warp(v, lane);
   v[0] *= kHadScale * s.x;
@@ -819,8 +808,7 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
       oa.M = M;
       oa.topk = topk;
       oa.hidden = h->hidden;
-      const long long out_warps = (long long)M * (h->hidden / kHad);
-      PdlLaunch pl(blocks_for(out_warps), 32 * kWarpsPerBlock, 0, st);
+      PdlLaunch pl(static_cast<unsigned>(M * (h->hidden / kHad)), 32 * kOutWarps, 0, st);
       e = cudaLaunchKernelEx(&pl.cfg, moe_out_kernel, oa);
       break;
     }
