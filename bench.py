@@ -61,13 +61,13 @@ REPEAT_SECONDS = 0.25
 # from one ncu capture of this kernel, averaged over the step's launches), by
 # workload at M=1; None where no capture of the current kernel exists.
 GEMV_TRAFFIC_BYTES = {
-    "dense gated MLP 5120->17408->5120, gate 2-bit / up 3-bit / down 3-bit, M=1": 44.69e6,
+    "dense gated MLP 5120->17408->5120, gate 2-bit / up 3-bit / down 3-bit, M=1": 44.71e6,
 }
 # The same for one prefill GEMM launch (the trellis_gemm kernel alone).
 PREFILL_TRAFFIC_BYTES = {
-    "prefill GEMM 5120x17408 3-bit, M=2048 tokens": 149.77e6,
+    "prefill GEMM 5120x17408 3-bit, M=2048 tokens": 146.01e6,
     "prefill GEMM 5120x17408 3-bit, M=2048 tokens, FP8 tensor cores (E4M3 weights, "
-    "per-token E4M3 activations)": None,
+    "per-token E4M3 activations)": 119.87e6,
 }
 
 
@@ -78,7 +78,7 @@ PREFILL_TRAFFIC_BYTES = {
 # capture of the current kernel exists.
 GEMV_ISSUE_MIX = {
     "dense gated MLP 5120->17408->5120, gate 2-bit / up 3-bit / down 3-bit, M=1":
-        {"issue": 6.04, "alu": 2.74},
+        {"issue": 5.52, "alu": 2.57},
 }
 # Per SM sub-partition and clock: one warp instruction issued, 16 lanes of the
 # integer ALU pipe (a warp instruction holds it for two cycles: ncu's
