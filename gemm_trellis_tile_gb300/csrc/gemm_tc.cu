@@ -87,7 +87,8 @@ static_assert(BlockGeom<true>::kSmemBytes <= 227 * 1024, "FP8 ring does not fit"
 
 // barrier indices
 constexpr int kBarAFull = 0, kBarAEmpty = 2, kBarCFull = 4, kBarCEmpty = 8, kBarBFull = 12,
-              kBarBEmpty = 15, kBarAcc = 18, kBarTmemFree = 19, kBarDrain = 20, kNumBars = 21;
+              kBarBEmpty = 15, kBarAcc = 18, kBarTmemFree = 19, kBarDrain = 20, kBarEpi = 21,
+              kNumBars = 22;
 
 struct GemmArgs {
   const uint8_t* code;
@@ -367,6 +368,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     mbar_init(bar(kBarAcc), 1);
     mbar_init(bar(kBarTmemFree), kDecWarps);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarEpi), kDecWarps);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -603,17 +605,19 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         if (lane == 0) is_last = ld_acquire_gpu(cnt) == others;
         is_last = __shfl_sync(0xFFFFFFFFu, is_last, 0);
         if (!is_last) {
+          // partial sums as [slot][column / 4][row][4]: a warp's 32 rows of
+          // four columns are 512 contiguous bytes
           const int which = (t_first <= u_begin) ? 0 : 1;
-          float* wrow = a.ws + ((size_t)(2 * c + which) * kBM + row) * kBN;
+          float4* wslot = reinterpret_cast<float4*>(a.ws) + (size_t)(2 * c + which) * (kBN / 4) * kBM;
 #pragma unroll 1
           for (int c16 = 0; c16 < kBN; c16 += 16) {
             float u[16];
             tmem_ld16(tl + c16, u);
             tmem_wait_ld();
-            float4* dst = reinterpret_cast<float4*>(wrow + c16);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              dst[q] = make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+              wslot[(size_t)(c16 / 4 + q) * kBM + row] =
+                  make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
           }
           __syncwarp();
           if (lane == 0) {
@@ -642,9 +646,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
               for (int j = 0; j < 8; ++j) s[j] += w[j];
             } else {
               const int wh = (t_first <= range_start(cc, a.units, a.grid)) ? 0 : 1;
-              const float4* src = reinterpret_cast<const float4*>(
-                  a.ws + ((size_t)(2 * cc + wh) * kBM + row) * kBN + c8);
-              const float4 p0 = src[0], p1 = src[1];
+              const float4* src = reinterpret_cast<const float4*>(a.ws) +
+                                  (size_t)(2 * cc + wh) * (kBN / 4) * kBM + (size_t)(c8 / 4) * kBM + row;
+              const float4 p0 = src[0], p1 = src[kBM];
               s[0] += p0.x;
               s[1] += p0.y;
               s[2] += p0.z;
@@ -662,17 +666,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       if (finish) {
         // FP8: the row's activation scale joins the output scale
         const float dm = FP8 ? (m < a.M ? __ldg(a.d + m) : 0.f) : 1.f;
-        // index bits 0..4: a 32-point transform on each 32-column chunk, in TMEM
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          float w[32];
-          tmem_ld32(tl + 32 * q, w);
-          tmem_wait_ld();
-          fwht32_regs(w);
-          tmem_st32(tl + 32 * q, w);
-        }
-        tmem_wait_st();
-        // index bits 5 and 6 across the four chunks, then * sv / sqrt(128), fp16
+        // index bits 5 and 6 across the four 32-column chunks, in TMEM
 #pragma unroll 1
         for (int c8 = 0; c8 < 32; c8 += 8) {
           float x0[8], x1[8], x2[8], x3[8];
@@ -681,36 +675,72 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           tmem_ld8(tl + c8 + 64, x2);
           tmem_ld8(tl + c8 + 96, x3);
           tmem_wait_ld();
-          if (m < a.M) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float a0 = x0[j] + x1[j], a1 = x0[j] - x1[j];
-              const float a2 = x2[j] + x3[j], a3 = x2[j] - x3[j];
-              x0[j] = a0 + a2;
-              x2[j] = a0 - a2;
-              x1[j] = a1 + a3;
-              x3[j] = a1 - a3;
-            }
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const float(&w)[8] = qq == 0 ? x0 : (qq == 1 ? x1 : (qq == 2 ? x2 : x3));
-              const int col = n0 + c8 + 32 * qq;
-              const float4 sa = __ldg(reinterpret_cast<const float4*>(a.sv + col));
-              const float4 sb = __ldg(reinterpret_cast<const float4*>(a.sv + col + 4));
-              const float sc[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-              uint32_t pk[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float s0 = sc[2 * e] * kHadScale * dm;
-                const float s1 = sc[2 * e + 1] * kHadScale * dm;
-                pk[e] = float_to_half_bits(w[2 * e] * s0) |
-                        (uint32_t(float_to_half_bits(w[2 * e + 1] * s1)) << 16);
-              }
-              *reinterpret_cast<uint4*>(a.y + (size_t)m * a.N + col) =
-                  make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
+          for (int j = 0; j < 8; ++j) {
+            const float a0 = x0[j] + x1[j], a1 = x0[j] - x1[j];
+            const float a2 = x2[j] + x3[j], a3 = x2[j] - x3[j];
+            x0[j] = a0 + a2;
+            x2[j] = a0 - a2;
+            x1[j] = a1 + a3;
+            x3[j] = a1 - a3;
           }
+          tmem_st8(tl + c8, x0);
+          tmem_st8(tl + c8 + 32, x1);
+          tmem_st8(tl + c8 + 64, x2);
+          tmem_st8(tl + c8 + 96, x3);
         }
+        tmem_wait_st();
+        // Index bits 0..4 on each chunk in registers, * sv / sqrt(128), fp16:
+        // each lane then holds 64 contiguous bytes of its row.  They go out
+        // through this warp's 2 KB slot of the decoded-B ring (idle during the
+        // epilogue: every MMA of the segment has completed, and no decoder
+        // writes it again before all have passed the barrier below), read
+        // back so that four lanes store one row's 64 bytes: eight rows per
+        // store instruction instead of 32 scattered 16-byte pieces.
+        uint8_t* scr = smem + kOffB + dw * 2048;
+        const int qj = lane & 3, qb = lane & ~3;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          float4 sc4[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            sc4[i] = __ldg(reinterpret_cast<const float4*>(a.sv + n0 + 32 * q) + i);
+          float w[32];
+          tmem_ld32(tl + 32 * q, w);
+          tmem_wait_ld();
+          fwht32_regs(w);
+          const float* scv = reinterpret_cast<const float*>(sc4);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = float_to_half_bits(w[2 * e] * (scv[2 * e] * kHadScale * dm)) |
+                    (uint32_t(float_to_half_bits(w[2 * e + 1] * (scv[2 * e + 1] * kHadScale * dm)))
+                     << 16);
+          // row `lane`, 16-byte piece p at chunk p ^ ((lane >> 1) & 3): conflict-free
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+            *reinterpret_cast<uint4*>(scr + lane * 64 + 16 * (p ^ ((lane >> 1) & 3))) =
+                make_uint4(pk[4 * p], pk[4 * p + 1], pk[4 * p + 2], pk[4 * p + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = qb + i;  // this warp's row written by the lane's quad
+            const uint4 v = *reinterpret_cast<const uint4*>(scr + r * 64 + 16 * (qj ^ ((r >> 1) & 3)));
+            const int mr = m0 + acc * 128 + quad * 32 + r;
+            if (mr < a.M)
+              *reinterpret_cast<uint4*>(a.y + (size_t)mr * a.N + n0 + 32 * q + 8 * qj) = v;
+          }
+          __syncwarp();
+        }
+      }
+      // no decoder writes the decoded-B ring (used above as scratch) before
+      // every decoder warp has finished this epilogue (a bounded wait: a warp
+      // that gave up earlier never arrives)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarEpi));
+      if (!mbar_wait(bar(kBarEpi), nseg & 1, a.limit_ns)) {
+        set_error(a.err, kDevErrTimeout);
+        ok = false;
       }
       tc_fence_before();
       __syncwarp();
