@@ -81,7 +81,8 @@ struct BlockGeom {
   static constexpr int kCBytes = kKT * 8 * 128;        // code stage, sized for 4 bits
   static constexpr int kOffC = kOffB + kBStages * kBBytes;
   static constexpr int kOffBar = kOffC + kCStages * kCBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+  static constexpr int kOffSv = kOffBar + 256;  // per decoder warp: the tile's 128 output scales
+  static constexpr int kSmemBytes = kOffSv + kDecWarps * kBN * 4 + 1024;  // + alignment slack
 };
 static_assert(BlockGeom<true>::kSmemBytes <= 227 * 1024, "FP8 ring does not fit");
 
@@ -580,6 +581,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 
       // ---- epilogue of this segment: row acc*128 + quad*32 + lane of the tile
       if (nseg == 0) pdl_wait();  // the scales d come from the previous kernel
+      // the tile's 128 output scales, staged in this warp's slot while the
+      // segment's last MMAs run (read back below as broadcasts)
+      float* svs = reinterpret_cast<float*>(smem + G::kOffSv) + dw * kBN;
+      reinterpret_cast<float4*>(svs)[lane] =
+          __ldg(reinterpret_cast<const float4*>(a.sv + nb * kBN) + lane);
       __syncwarp();
       if (!mbar_wait(bar(kBarAcc), nseg & 1, a.limit_ns)) {
         set_error(a.err, kDevErrTimeout);
@@ -632,34 +638,38 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       }
       if (finish && c_first != c_last) {
         // the last arrival: accumulators <- the CTAs' partial sums added in CTA
-        // order (this CTA's own from its accumulators), 8 columns at a time
+        // order (this CTA's own from its accumulators), 16 columns at a time
+        // with each other CTA's loads in flight together
 #pragma unroll 1
-        for (int c8 = 0; c8 < kBN; c8 += 8) {
-          float w[8], s[8];
-          tmem_ld8(tl + c8, w);
-          tmem_wait_ld();
+        for (int c16 = 0; c16 < kBN; c16 += 16) {
+          float w[16], sacc[16];
+          tmem_ld16(tl + c16, w);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s[j] = 0.f;
+          for (int j = 0; j < 16; ++j) sacc[j] = 0.f;
+          tmem_wait_ld();
           for (int cc = c_first; cc <= c_last; ++cc) {
             if (cc == c) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) s[j] += w[j];
+              for (int j = 0; j < 16; ++j) sacc[j] += w[j];
             } else {
               const int wh = (t_first <= range_start(cc, a.units, a.grid)) ? 0 : 1;
               const float4* src = reinterpret_cast<const float4*>(a.ws) +
-                                  (size_t)(2 * cc + wh) * (kBN / 4) * kBM + (size_t)(c8 / 4) * kBM + row;
-              const float4 p0 = src[0], p1 = src[kBM];
-              s[0] += p0.x;
-              s[1] += p0.y;
-              s[2] += p0.z;
-              s[3] += p0.w;
-              s[4] += p1.x;
-              s[5] += p1.y;
-              s[6] += p1.z;
-              s[7] += p1.w;
+                                  (size_t)(2 * cc + wh) * (kBN / 4) * kBM + (size_t)(c16 / 4) * kBM +
+                                  row;
+              float4 p[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) p[q] = src[(size_t)q * kBM];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                sacc[4 * q] += p[q].x;
+                sacc[4 * q + 1] += p[q].y;
+                sacc[4 * q + 2] += p[q].z;
+                sacc[4 * q + 3] += p[q].w;
+              }
             }
           }
-          tmem_st8(tl + c8, s);
+          tmem_st8(tl + c16, reinterpret_cast<const float(&)[8]>(sacc[0]));
+          tmem_st8(tl + c16 + 8, reinterpret_cast<const float(&)[8]>(sacc[8]));
         }
         tmem_wait_st();
       }
@@ -701,15 +711,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         const int qj = lane & 3, qb = lane & ~3;
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
-          float4 sc4[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            sc4[i] = __ldg(reinterpret_cast<const float4*>(a.sv + n0 + 32 * q) + i);
           float w[32];
           tmem_ld32(tl + 32 * q, w);
           tmem_wait_ld();
           fwht32_regs(w);
-          const float* scv = reinterpret_cast<const float*>(sc4);
+          const float* scv = svs + 32 * q;
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
