@@ -282,19 +282,54 @@ constexpr uint32_t kIdesc = (1u << 4)              // D format: f32
                             | ((kBN >> 3) << 17)   // N / 8
                             | ((128 >> 4) << 24);  // M / 16
 
+// Two fp32 additions / subtractions / products in one instruction (each
+// lane rounded exactly as the scalar operation).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Butterfly (p, q) -> (p + q, p - q) on neighbouring pairs of values.
+__device__ __forceinline__ void f2_butterfly(float& p0, float& p1, float& q0, float& q1) {
+  const uint64_t p = f2_pack(p0, p1), q = f2_pack(q0, q1);
+  f2_unpack(f2_add(p, q), p0, p1);
+  f2_unpack(f2_sub(p, q), q0, q1);
+}
+
 // Walsh-Hadamard butterflies (natural order, unnormalised) over 32 values
-// held in registers.
+// held in registers: index bit 0 as scalar operations, bits 1..4 two
+// butterflies per instruction pair (the same roundings).
 __device__ __forceinline__ void fwht32_regs(float (&v)[32]) {
 #pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
+  for (int i = 0; i < 32; i += 2) {
+    const float p = v[i], q = v[i + 1];
+    v[i] = p + q;
+    v[i + 1] = p - q;
+  }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if ((i & h) == 0) {
-        const float p = v[i], q = v[i + h];
-        v[i] = p + q;
-        v[i + h] = p - q;
-      }
-    }
+  for (int h = 2; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2)
+      if ((i & h) == 0) f2_butterfly(v[i], v[i + 1], v[i + h], v[i + h + 1]);
   }
 }
 
@@ -584,8 +619,14 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       // the tile's 128 output scales, staged in this warp's slot while the
       // segment's last MMAs run (read back below as broadcasts)
       float* svs = reinterpret_cast<float*>(smem + G::kOffSv) + dw * kBN;
-      reinterpret_cast<float4*>(svs)[lane] =
-          __ldg(reinterpret_cast<const float4*>(a.sv + nb * kBN) + lane);
+      {
+        float4 sv4 = __ldg(reinterpret_cast<const float4*>(a.sv + nb * kBN) + lane);
+        sv4.x *= kHadScale;  // 1/sqrt(128) folded in, as the products below take it
+        sv4.y *= kHadScale;
+        sv4.z *= kHadScale;
+        sv4.w *= kHadScale;
+        reinterpret_cast<float4*>(svs)[lane] = sv4;
+      }
       __syncwarp();
       if (!mbar_wait(bar(kBarAcc), nseg & 1, a.limit_ns)) {
         set_error(a.err, kDevErrTimeout);
@@ -686,13 +727,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           tmem_ld8(tl + c8 + 96, x3);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float a0 = x0[j] + x1[j], a1 = x0[j] - x1[j];
-            const float a2 = x2[j] + x3[j], a3 = x2[j] - x3[j];
-            x0[j] = a0 + a2;
-            x2[j] = a0 - a2;
-            x1[j] = a1 + a3;
-            x3[j] = a1 - a3;
+          for (int j = 0; j < 8; j += 2) {
+            f2_butterfly(x0[j], x0[j + 1], x1[j], x1[j + 1]);  // bit 5
+            f2_butterfly(x2[j], x2[j + 1], x3[j], x3[j + 1]);
+            f2_butterfly(x0[j], x0[j + 1], x2[j], x2[j + 1]);  // bit 6
+            f2_butterfly(x1[j], x1[j + 1], x3[j], x3[j + 1]);
           }
           tmem_st8(tl + c8, x0);
           tmem_st8(tl + c8 + 32, x1);
@@ -718,10 +757,14 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           const float* scv = svs + 32 * q;
           uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = float_to_half_bits(w[2 * e] * (scv[2 * e] * kHadScale * dm)) |
-                    (uint32_t(float_to_half_bits(w[2 * e + 1] * (scv[2 * e + 1] * kHadScale * dm)))
-                     << 16);
+          for (int e = 0; e < 16; ++e) {
+            const uint64_t sc = FP8 ? f2_pack(scv[2 * e] * dm, scv[2 * e + 1] * dm)
+                                    : f2_pack(scv[2 * e], scv[2 * e + 1]);
+            float o0, o1;
+            f2_unpack(f2_mul(f2_pack(w[2 * e], w[2 * e + 1]), sc), o0, o1);
+            const __half2 h = __floats2half2_rn(o0, o1);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&h);
+          }
           // row `lane`, 16-byte piece p at chunk p ^ ((lane >> 1) & 3): conflict-free
 #pragma unroll
           for (int p = 0; p < 4; ++p)
