@@ -237,11 +237,22 @@ template <int BITS, int TB, bool E4M3>
 __device__ __forceinline__ void consume_unit(const uint32_t* p0, const uint32_t* p1,
                                              const uint4* const (&xq)[TB], int sh7, uint32_t mask,
                                              uint32_t xr, float (&acc)[TB][4]) {
+  if (E4M3) {
+    // E4M3 weights as plain fp16 A fragments (one weight per half): one MMA
+    // per tile against (x[2t], x[2t+1]) and (x[2t+8], x[2t+9]), taken from
+    // the repeated-activation fragment words by one byte permute each
+    uint32_t fa[4];
+    decode8_e4m3_frag<BITS>(*p0, *p1, sh7, mask, xr, fa);
+#pragma unroll
+    for (int tb = 0; tb < TB; ++tb) {
+      const uint4 xf = *xq[tb];
+      mma16816(acc[tb], fa[0], fa[1], fa[2], fa[3], __byte_perm(xf.x, xf.z, 0x5410),
+               __byte_perm(xf.y, xf.w, 0x5410));
+    }
+    return;
+  }
   uint32_t h[8];
-  if (E4M3)
-    decode8_e4m3_dup<BITS>(*p0, *p1, sh7, mask, xr, h);  // MMA forms 2*w*x
-  else
-    decode8_pairs<BITS>(*p0, *p1, sh7, mask, xr, h);
+  decode8_pairs<BITS>(*p0, *p1, sh7, mask, xr, h);
 #pragma unroll
   for (int tb = 0; tb < TB; ++tb) {
     const uint4 xf = *xq[tb];
@@ -326,9 +337,18 @@ __device__ __forceinline__ bool run_segment(GroupRing& rg, int n, int wt, int la
 }
 
 // The segment's decode at its width and rounding (key = bits + 8 * e4m3).
-template <int TB, int MC, int STAGES, int RPU>
+// F16_ONLY: the launch holds no E4M3-rounded job, so only the three fp16
+// decodes are compiled in.
+template <int TB, int MC, int STAGES, int RPU, bool F16_ONLY>
 __device__ __forceinline__ bool segment_dispatch(int key, GroupRing& rg, int n, int wt, int lane,
                                                  int M, const GemvArgs& a, float (&acc)[TB][4]) {
+  if (F16_ONLY) {
+    switch (key) {
+      case 2: return run_segment<2, TB, false, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
+      case 3: return run_segment<3, TB, false, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
+      default: return run_segment<4, TB, false, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
+    }
+  }
   switch (key) {
     case 2: return run_segment<2, TB, false, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
     case 3: return run_segment<3, TB, false, MC, STAGES, RPU>(rg, n, wt, lane, M, a, acc);
@@ -345,7 +365,7 @@ __device__ __forceinline__ bool segment_dispatch(int key, GroupRing& rg, int n, 
 // whose stage rows are contiguous (one 1-D bulk copy); kModeRowHalves, every
 // job is stored by input halves (one unit = 8 k-tile rows, one 2-D copy per
 // unit through the half's tensor map).
-template <int TB, int MODE>
+template <int TB, int MODE, bool F16_ONLY>
 __global__ void __launch_bounds__(threads_for<MODE>(), 1)
     trellis_gemv_kernel(const __grid_constant__ GemvArgs a) {
   constexpr int RPU = MODE == kModeRowHalves ? 8 : 1;  // k-tile rows per unit
@@ -499,9 +519,10 @@ __global__ void __launch_bounds__(threads_for<MODE>(), 1)
   while (it.next_segment(jobs, sg)) {
     const int key = it.bits + 8 * it.e4m3;
     const bool ok = (TB == 1 && a.M == 1)  // one token: the common decode case, specialised
-                        ? segment_dispatch<TB, 1, kStages, RPU>(key, rg, sg.n, wt, lane, 1, a, acc)
-                        : segment_dispatch<TB, 0, kStages, RPU>(key, rg, sg.n, wt, lane, a.M, a,
-                                                                acc);
+                        ? segment_dispatch<TB, 1, kStages, RPU, F16_ONLY>(key, rg, sg.n, wt,
+                                                                          lane, 1, a, acc)
+                        : segment_dispatch<TB, 0, kStages, RPU, F16_ONLY>(key, rg, sg.n, wt,
+                                                                          lane, a.M, a, acc);
     if (!ok) {
       set_error(a.err, kDevErrTimeout);
       break;
@@ -510,7 +531,6 @@ __global__ void __launch_bounds__(threads_for<MODE>(), 1)
     const int ps = r - cta_of_unit(gb, U, G);  // partial-sum slot
     const int n0 = 128 * sg.g + 16 * wt + (lane >> 2);
     const int t2 = 2 * (lane & 3);
-    const float f = it.e4m3 ? 0.5f : 1.0f;  // the E4M3 path's MMAs form 2*w*x
 #pragma unroll
     for (int tb = 0; tb < TB; ++tb) {
 #pragma unroll
@@ -518,8 +538,8 @@ __global__ void __launch_bounds__(threads_for<MODE>(), 1)
         const int tok = 8 * tb + t2 + i;
         if (tok < a.M) {
           float* row = it.part + ((size_t)ps * a.mpad + tok) * it.N;
-          row[n0] = acc[tb][i] * f;
-          row[n0 + 8] = acc[tb][2 + i] * f;
+          row[n0] = acc[tb][i];
+          row[n0 + 8] = acc[tb][2 + i];
         }
       }
 #pragma unroll
@@ -563,9 +583,10 @@ __global__ void wait_selftest_kernel(int* err, uint64_t limit_ns) {
   }
 }
 
-template <int TB>
+template <int TB, bool F16_ONLY>
 cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t st) {
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(trellis_gemv_kernel<TB, kModeWhole>),
+  const auto kern = trellis_gemv_kernel<TB, kModeWhole, F16_ONLY>;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern),
                                  gemv_smem_bytes<TB, kModeWhole>());
   if (e != cudaSuccess) return e;
   GemvArgs a;
@@ -597,7 +618,7 @@ cudaError_t launch_gemv_tb(const GemvSchedule& s, int M, int* err, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, trellis_gemv_kernel<TB, kModeWhole>, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace
@@ -630,11 +651,11 @@ bool encode_gemv_half_map(CUtensorMap* map, const void* code, int bits, int NT) 
 
 int gemv_ranges_per_sm() {
   int n = 0;
-  if (cudaFuncSetAttribute(trellis_gemv_kernel<2, kModeWhole>,
+  if (cudaFuncSetAttribute(trellis_gemv_kernel<2, kModeWhole, false>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            gemv_smem_bytes<2, kModeWhole>()) != cudaSuccess)
     return kGroups;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, trellis_gemv_kernel<2, kModeWhole>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, trellis_gemv_kernel<2, kModeWhole, false>,
                                                     threads_for<kModeWhole>(),
                                                     gemv_smem_bytes<2, kModeWhole>()) != cudaSuccess)
     return kGroups;
@@ -666,17 +687,25 @@ int gemv_slots_for_group(const GemvSchedule& s, int job, int g) {
 }
 
 cudaError_t launch_gemv(const GemvSchedule& s, int M, int* err, cudaStream_t st) {
-  if (M <= 8) return launch_gemv_tb<1>(s, M, err, st);
-  return launch_gemv_tb<2>(s, M, err, st);
+  bool f16 = true;
+  for (const GemvJob& j : s.jobs) f16 = f16 && !j.e4m3;
+  if (M <= 8)
+    return f16 ? launch_gemv_tb<1, true>(s, M, err, st) : launch_gemv_tb<1, false>(s, M, err, st);
+  return f16 ? launch_gemv_tb<2, true>(s, M, err, st) : launch_gemv_tb<2, false>(s, M, err, st);
 }
 
 cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* d_units,
                                         const int* d_grid, int max_grid, int M, int mpad,
                                         int* err, cudaStream_t st, long long job_units,
-                                        bool maps_from_device, int layout) {
-  auto kern = layout == kGemvColHalves   ? trellis_gemv_kernel<1, kModeColHalves>
-              : layout == kGemvRowHalves ? trellis_gemv_kernel<1, kModeRowHalves>
-                                         : trellis_gemv_kernel<1, kModeWhole>;
+                                        bool maps_from_device, int layout, bool e4m3) {
+  auto kern = layout == kGemvColHalves
+                  ? (e4m3 ? trellis_gemv_kernel<1, kModeColHalves, false>
+                          : trellis_gemv_kernel<1, kModeColHalves, true>)
+              : layout == kGemvRowHalves
+                  ? (e4m3 ? trellis_gemv_kernel<1, kModeRowHalves, false>
+                          : trellis_gemv_kernel<1, kModeRowHalves, true>)
+                  : (e4m3 ? trellis_gemv_kernel<1, kModeWhole, false>
+                          : trellis_gemv_kernel<1, kModeWhole, true>);
   const int smem = layout == kGemvWhole ? gemv_smem_bytes<1, kModeWhole>()
                                         : gemv_smem_bytes<1, kModeColHalves>();
   const int threads = layout == kGemvWhole ? threads_for<kModeWhole>()

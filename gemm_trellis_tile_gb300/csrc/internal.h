@@ -94,14 +94,16 @@ bool encode_gemv_half_map(CUtensorMap* map, const void* code, int bits, int NT);
 // launch is stored -- kGemvWhole (whole matrices, tensor maps in `tmap`),
 // kGemvColHalves (each job one 128-channel column half: NG = 1, contiguous
 // rows, no tensor map), kGemvRowHalves (input halves through row_maps; one
-// unit = 8 k-tile rows).
+// unit = 8 k-tile rows).  e4m3: some job may be E4M3-rounded; false promises
+// that none is and launches the kernel built with the fp16 decodes only.
 constexpr int kGemvWhole = 0;
 constexpr int kGemvColHalves = 1;
 constexpr int kGemvRowHalves = 2;
 cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* d_units,
                                         const int* d_grid, int max_grid, int M, int mpad,
                                         int* err, cudaStream_t st, long long job_units = 0,
-                                        bool maps_from_device = false, int layout = kGemvWhole);
+                                        bool maps_from_device = false, int layout = kGemvWhole,
+                                        bool e4m3 = true);
 // Prefill GEMM on tcgen05: y = fp16(had128(xh @ W_inner) * sv) for any M >= 1;
 // xh is fp16 [M, K], 16-byte aligned; ws holds gemm_workspace_floats(num_sms)
 // fp32 for tiles shared between CTAs; tile_cnt holds gemm_counter_ints(M, N)

@@ -767,7 +767,8 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
                                       kMoeMaxTokens, h->err, st,
                                       h->halves ? (long long)(h->hidden / 16)
                                                 : (long long)(h->hidden / 16) * (h->inter / 128),
-                                      false, h->halves ? kGemvColHalves : kGemvWhole);
+                                      false, h->halves ? kGemvColHalves : kGemvWhole,
+                                      h->rounding == ESCHA_ROUND_E4M3);
       h->prof.end(st);
       break;
     case 2: {
@@ -795,7 +796,8 @@ escha_status_t moe_gemv_stage(escha_moe_s* h, int stage, const uint16_t* x, cons
                                       kMoeMaxTokens, h->err, st,
                                       h->halves ? (long long)h->H * (h->hidden / 128)
                                                 : (long long)(h->inter / 16) * (h->hidden / 128),
-                                      h->halves != 0, h->halves ? kGemvRowHalves : kGemvWhole);
+                                      h->halves != 0, h->halves ? kGemvRowHalves : kGemvWhole,
+                                      h->rounding == ESCHA_ROUND_E4M3);
       h->prof.end(st);
       break;
     case 4: {

@@ -127,22 +127,33 @@ __device__ __forceinline__ void decode8(uint32_t w0, uint32_t w1, int sh7, uint3
   }
 }
 
-// E4M3 variant for the GEMV: the rounded value in both halves, with the mask
-// and flip constants as run-time values (see mcg_pair).  Against activations
-// repeated in both halves an MMA forms 2*w*x, exactly twice the product.
+// E4M3 variant for the GEMV in the m16n8k16 A-fragment layout: the lane's
+// eight weights as four registers of two weights each (a0 <- symbols 0,1,
+// a1 <- 4,5, a2 <- 2,3, a3 <- 6,7: two input channels of one output channel),
+// each the codebook's fp16 sum rounded to E4M3 (and held exactly in fp16).
+// Per pair of states: one HADD2 each with its operands' halves broadcast
+// ((lo, lo) + (hi, hi), no separate permute), one byte permute joins the two
+// sums, one conversion pair rounds both to E4M3.
 template <int BITS>
-__device__ __forceinline__ void decode8_e4m3_dup(uint32_t w0, uint32_t w1, int sh7, uint32_t mask,
-                                                 uint32_t xr, uint32_t (&out)[8]) {
+__device__ __forceinline__ void decode8_e4m3_frag(uint32_t w0, uint32_t w1, int sh7, uint32_t mask,
+                                                  uint32_t xr, uint32_t (&a)[4]) {
   const uint32_t lo = __funnelshift_r(w1, w0, sh7);
   const uint32_t hi = w0 >> sh7;
   uint32_t st[8];
   lane_states<BITS>(lo, hi, st);
+  uint32_t v[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t v = mcg_pair(st[j], mask, xr);
-    const __half2 h = *reinterpret_cast<const __half2*>(&v);
-    const __half2 s = __hadd2(__low2half2(h), __high2half2(h));
-    out[j] = round_e4m3x2(*reinterpret_cast<const uint32_t*>(&s));
+  for (int j = 0; j < 8; ++j) v[j] = mcg_pair(st[j], mask, xr);
+  constexpr int first[4] = {0, 4, 2, 6};  // a0..a3
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int j = first[r];
+    const __half2 h0 = *reinterpret_cast<const __half2*>(&v[j]);
+    const __half2 h1 = *reinterpret_cast<const __half2*>(&v[j + 1]);
+    const __half2 s0 = __hadd2(__low2half2(h0), __high2half2(h0));
+    const __half2 s1 = __hadd2(__low2half2(h1), __high2half2(h1));
+    a[r] = round_e4m3x2(__byte_perm(*reinterpret_cast<const uint32_t*>(&s0),
+                                    *reinterpret_cast<const uint32_t*>(&s1), 0x5410));
   }
 }
 
