@@ -141,24 +141,29 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], fp16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem desc] * B[smem desc], fp16 inputs, fp32 accumulate;
+// issued by one elected lane of a converged warp (the whole warp runs the
+// issue loop, so its descriptor arithmetic is warp-uniform).
+__device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// D[tmem] (+)= A * B with E4M3 A and B (K = 32 per instruction), fp32 accumulate.
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A * B with E4M3 A and B (K = 32 per instruction), fp32
+// accumulate; one elected lane.
+__device__ __forceinline__ void mma_e4m3_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -184,11 +189,17 @@ __device__ __forceinline__ uint16_t e4m3x2_from_f16x2(uint32_t h2) {
   return e;
 }
 
-// Arrive on `bar` once every tcgen05 operation issued so far by this thread completes.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+// Arrive on `bar` once every tcgen05 operation issued so far by the issuing
+// thread completes; from one elected lane of a converged warp (the lane that
+// issued the MMAs: elect.sync picks the same lane while the warp stays
+// converged).
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -229,23 +240,6 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
                    taddr),
@@ -486,14 +480,18 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the loop (waits and descriptor arithmetic are
+    // warp-uniform); one elected lane issues each MMA and commit.  Every wait
+    // result is made warp-uniform so that the warp never splits.
+    {
       bool ok = true;
       Ring<kAStages> ra;
       Ring<kBStages> rb;
       int nseg = 0;
       while (ok && it.next(seg)) {
-        if (nseg > 0 && !mbar_wait(bar(kBarTmemFree), (nseg - 1) & 1, a.limit_ns)) {
-          set_error(a.err, kDevErrTimeout);
+        if (nseg > 0 &&
+            !__all_sync(0xFFFFFFFFu, mbar_wait(bar(kBarTmemFree), (nseg - 1) & 1, a.limit_ns))) {
+          if (lane == 0) set_error(a.err, kDevErrTimeout);
           break;
         }
         tc_fence_after();
@@ -502,36 +500,41 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           const uint32_t pa = ra.phase;
           const int sb = rb.stage;
           const uint32_t pb = rb.phase;
-          if (!mbar_wait(bar(kBarAFull + sa), pa, a.limit_ns) ||
-              !mbar_wait(bar(kBarBFull + sb), pb, a.limit_ns)) {
-            set_error(a.err, kDevErrTimeout);
+          const bool got = mbar_wait(bar(kBarAFull + sa), pa, a.limit_ns) &&
+                           mbar_wait(bar(kBarBFull + sb), pb, a.limit_ns);
+          if (!__all_sync(0xFFFFFFFFu, got)) {
+            if (lane == 0) set_error(a.err, kDevErrTimeout);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t as = base + sa * kABytes;
-          const uint32_t bs = base + kOffB + sb * kBBytes;
+          // Descriptors of the stage's first A and B rows; an operand
+          // further into the stage adds its byte offset / 16 to the start
+          // address field (shared memory is below 256 KB, so no carry).
+          const uint64_t ad0 = smem_desc_k128(base + sa * kABytes);
+          const uint64_t bd0 = smem_desc_k128(base + kOffB + sb * kBBytes);
+          const uint32_t cont = kb > seg.kb0 ? 1u : 0u;
 #pragma unroll
           for (int acc = 0; acc < 4; ++acc) {
 #pragma unroll
             for (int kk = 0; kk < kRowBytes / 32; ++kk) {  // 32 bytes of K per MMA
-              const uint64_t ad = smem_desc_k128(as + acc * (kABytes / 4) + kk * 32);
-              const uint64_t bd = smem_desc_k128(bs + kk * 32);
-              const uint32_t accum = (kb > seg.kb0 || kk > 0) ? 1u : 0u;
+              const uint64_t ad = ad0 + (uint64_t)((acc * (kABytes / 4) + kk * 32) >> 4);
+              const uint64_t bd = bd0 + (uint64_t)((kk * 32) >> 4);
+              const uint32_t accum = kk > 0 ? 1u : cont;
               if constexpr (FP8)
-                mma_e4m3(tmem_base + acc * kBN, ad, bd, kIdesc, accum);
+                mma_e4m3_elect(tmem_base + acc * kBN, ad, bd, kIdesc, accum);
               else
-                mma_f16(tmem_base + acc * kBN, ad, bd, kIdesc, accum);
+                mma_f16_elect(tmem_base + acc * kBN, ad, bd, kIdesc, accum);
             }
           }
-          mma_commit(bar(kBarAEmpty + sa));
-          mma_commit(bar(kBarBEmpty + sb));
+          mma_commit_elect(bar(kBarAEmpty + sa));
+          mma_commit_elect(bar(kBarBEmpty + sb));
         }
         if (!ok) break;
-        mma_commit(bar(kBarAcc));  // this segment's accumulators are complete
+        mma_commit_elect(bar(kBarAcc));  // this segment's accumulators are complete
         ++nseg;
       }
-      mma_commit(bar(kBarDrain));
+      mma_commit_elect(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, a.limit_ns);  // nothing in flight before TMEM is released
     }
   } else {

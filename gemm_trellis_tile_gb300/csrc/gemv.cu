@@ -300,7 +300,9 @@ __device__ __forceinline__ bool run_segment(GroupRing& rg, int n, int wt, int la
   for (int left = n; left > 0;) {
     const int nu = left < cap ? left : cap;
     const int stage = rg.q + kGroups * rg.slot;
-    if (!mbar_wait(smem_u32(&rg.bars[stage]), rg.phase, a.limit_ns)) return false;
+    // warp-uniform: the MMAs below need every lane
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&rg.bars[stage]), rg.phase, a.limit_ns)))
+      return false;
     const uint32_t* cw = reinterpret_cast<const uint32_t*>(rg.codes + stage * kCodeStageBytes);
     const uint4* xs = reinterpret_cast<const uint4*>(rg.xfs + stage * xf_stage_bytes<TB>());
     const uint32_t* p0 = cw + o0;
