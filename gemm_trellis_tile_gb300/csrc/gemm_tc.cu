@@ -194,6 +194,13 @@ __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t*>(&s);
 }
 
+// fp16(lo + hi) of a codebook word, in both halves (round to nearest even).
+__device__ __forceinline__ uint32_t hsum_dup(uint32_t w) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&w);
+  const __half2 s = __hadd2(__low2half2(h), __high2half2(h));
+  return *reinterpret_cast<const uint32_t*>(&s);
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -586,13 +593,21 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           uint32_t v[8];  // codebook words (fp16 lo, fp16 hi) of the lane's symbols
           decode8_pairs<BITS>(tw[lw.i0], tw[lw.i1], lw.sh7, mcg_mask, mcg_xor, v);
           // symbols 2p, 2p+1 (p = 2 nh + rh) are input channels k, k+1 of output
-          // channel n = 16 nt + g + 8 nh, k = 16 kt_local + 8 rh + 2t; one fp16
-          // addition per weight, two weights per instruction
+          // channel n = 16 nt + g + 8 nh, k = 16 kt_local + 8 rh + 2t.  fp16:
+          // two byte permutes gather the pair's (lo, lo) and (hi, hi), one
+          // addition forms both weights.  FP8, whose decoders keep the integer
+          // pipe busier: one addition per weight with its operands' halves
+          // broadcast, then one permute per pair (measured 3 % faster there,
+          // 4 % slower at fp16).
           uint32_t pair[4];
 #pragma unroll
-          for (int p = 0; p < 4; ++p)
-            pair[p] = hadd2_u32(__byte_perm(v[2 * p], v[2 * p + 1], 0x5410),
-                                __byte_perm(v[2 * p], v[2 * p + 1], 0x7632));
+          for (int p = 0; p < 4; ++p) {
+            if constexpr (FP8)
+              pair[p] = __byte_perm(hsum_dup(v[2 * p]), hsum_dup(v[2 * p + 1]), 0x5410);
+            else
+              pair[p] = hadd2_u32(__byte_perm(v[2 * p], v[2 * p + 1], 0x5410),
+                                  __byte_perm(v[2 * p], v[2 * p + 1], 0x7632));
+          }
           if constexpr (FP8) {
             // Bytes k, k+1 of row n.  Lanes t and t^1 swap halves so that each
             // stores one whole word: even t bytes 2t..2t+3 (rh = 0), odd t bytes
