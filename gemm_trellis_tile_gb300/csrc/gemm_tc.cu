@@ -609,19 +609,15 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                                   __byte_perm(v[2 * p], v[2 * p + 1], 0x7632));
           }
           if constexpr (FP8) {
-            // Bytes k, k+1 of row n.  Lanes t and t^1 swap halves so that each
-            // stores one whole word: even t bytes 2t..2t+3 (rh = 0), odd t bytes
-            // 8 + 2(t-1) .. +3 (rh = 1), all in the row's 16-byte chunk kt_local.
-            const bool odd = t & 1;
+            // Bytes k, k+1 of row n, one 16-bit store per pair: rh = 0 at
+            // bytes 2t, 2t+1 and rh = 1 at 8 + 2t of the row's 16-byte chunk
+            // kt_local (no exchange between lanes).
 #pragma unroll
             for (int nh = 0; nh < 2; ++nh) {
-              const uint32_t e0 = e4m3x2_from_f16x2(pair[2 * nh]);
-              const uint32_t e1 = e4m3x2_from_f16x2(pair[2 * nh + 1]);
-              const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? e0 : e1, 1);
-              const uint32_t word = odd ? (recv | (e1 << 16)) : (e0 | (recv << 16));
               const int n = 16 * nt + g + 8 * nh;   // n & 7 == g: the row's swizzle phase
-              const int off = 8 * (t & 1) + 2 * (t & 2);
-              *reinterpret_cast<uint32_t*>(bt + n * 128 + (kt_local ^ g) * 16 + off) = word;
+              uint8_t* row = bt + n * 128 + (kt_local ^ g) * 16 + 2 * t;
+              *reinterpret_cast<uint16_t*>(row) = e4m3x2_from_f16x2(pair[2 * nh]);
+              *reinterpret_cast<uint16_t*>(row + 8) = e4m3x2_from_f16x2(pair[2 * nh + 1]);
             }
           } else {
 #pragma unroll
