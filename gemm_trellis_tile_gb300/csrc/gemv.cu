@@ -13,12 +13,14 @@
 //               a shared-memory ring, completing on mbarriers.
 //   warps 3..26 consumers, three groups of eight.  Each group owns one of the
 //               launch's contiguous unit ranges (CTA b of C: ranges b, b + C,
-//               b + 2C) and three ring stages (two with 9..16 tokens); in a
+//               b + 2C) and three ring stages (four when every job is 2-bit,
+//               two with 9..16 tokens); in a
 //               group, warp w owns output tile column w of the current
 //               128-channel group.  Per unit it reads its tile's two words per
 //               lane, decodes eight weights per lane, and issues m16n8k16 MMAs
 //               with the weight tile as A (rows = output channels) and up to 8
-//               tokens as B; a second token block handles 9..16 tokens.
+//               tokens as B (E4M3-rounded weights: one weight per half and
+//               one MMA per tile); a second token block handles 9..16 tokens.
 // The three groups share one CTA rather than running as three CTAs per SM:
 // separate CTAs on one SM drift apart (the warp scheduler favours the oldest
 // CTA, whose ring runs ahead while the youngest one's work piles up at the end
