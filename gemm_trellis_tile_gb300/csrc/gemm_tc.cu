@@ -109,6 +109,7 @@ struct GemmArgs {
   int kb_per_tile;       // K / (K elements per block)
   long long units;       // tiles * kb_per_tile
   int grid;
+  int parts_last;        // walk each CTA's whole tiles before its shared parts (SegIter)
   int* err;
   uint64_t limit_ns;
 };
@@ -358,16 +359,53 @@ struct Segment {
   int tile, kb0, kb1;
 };
 
+// A CTA's range [u, u1) is at most: the end part of one tile (if u is not at a
+// tile start), whole tiles, and the start part of another (if u1 is not).
+// The parts are shared with the neighbouring CTAs.  parts_last: the whole
+// tiles are walked first and the two parts last, so that both CTAs of a
+// shared tile reach it near the end of the launch and the partial sums are
+// still in L2 when the last of them merges them; otherwise range order.
 struct SegIter {
-  long long u, u1;
+  int ta, ka, tb, kb;  // the range starts at K block ka of tile ta, ends before kb of tb
   int KB;
+  int parts_last;
+  int step;  // segments handed out so far
+  __device__ __forceinline__ SegIter(long long u, long long u1, int kb_per_tile, int last_mode)
+      : KB(kb_per_tile), parts_last(last_mode), step(u < u1 ? 0 : -1) {
+    ta = static_cast<int>(u / KB);
+    ka = static_cast<int>(u - (long long)ta * KB);
+    tb = static_cast<int>(u1 / KB);
+    kb = static_cast<int>(u1 - (long long)tb * KB);
+  }
   __device__ __forceinline__ bool next(Segment& s) {
-    if (u >= u1) return false;
-    s.tile = static_cast<int>(u / KB);
-    s.kb0 = static_cast<int>(u - (long long)s.tile * KB);
-    const long long left = u1 - u;
-    s.kb1 = (left >= KB - s.kb0) ? KB : s.kb0 + static_cast<int>(left);
-    u += s.kb1 - s.kb0;
+    if (step < 0) return false;  // empty range
+    const int i = step++;
+    if (ta == tb) {  // inside one tile
+      if (i > 0) return false;
+      s.tile = ta;
+      s.kb0 = ka;
+      s.kb1 = kb;
+      return true;
+    }
+    const int first = ka > 0 ? 1 : 0, last = kb > 0 ? 1 : 0;
+    const int w0 = ta + first;  // whole tiles [w0, tb)
+    const int nwhole = tb - w0;
+    const int n = first + nwhole + last;
+    if (i >= n) return false;
+    const int k = !parts_last ? i : i < nwhole ? i + first : (i == nwhole && first) ? 0 : n - 1;
+    if (first && k == 0) {
+      s.tile = ta;
+      s.kb0 = ka;
+      s.kb1 = KB;
+    } else if (last && k == n - 1) {
+      s.tile = tb;
+      s.kb0 = 0;
+      s.kb1 = kb;
+    } else {
+      s.tile = w0 + k - first;
+      s.kb0 = 0;
+      s.kb1 = KB;
+    }
     return true;
   }
 };
@@ -423,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  SegIter it{u_begin, u_end, a.kb_per_tile};
+  SegIter it(u_begin, u_end, a.kb_per_tile, a.parts_last);
   Segment seg;
 
   if (warp == 0) {
@@ -882,6 +920,10 @@ cudaError_t launch_gemm(const void* act, bool fp8, const float* d, const int16_t
   if (g < 1) g = 1;
   if (g > num_sms) g = num_sms;
   a.grid = static_cast<int>(g);
+  // With two or more tiles per CTA, shared parts last: measured 2.9 % faster at
+  // 5120 -> 17408 (M = 2048) with the DRAM traffic down to the algorithmic
+  // bytes; with about one tile per CTA (17408 -> 5120) range order is 2 % faster.
+  a.parts_last = tiles >= 2LL * g ? 1 : 0;
   a.err = err;
   a.limit_ns = kWaitLimitNs;
 
