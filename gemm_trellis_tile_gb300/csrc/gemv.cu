@@ -46,14 +46,14 @@ constexpr int kModeWhole = kGemvWhole;
 constexpr int kModeColHalves = kGemvColHalves;
 constexpr int kModeRowHalves = kGemvRowHalves;
 
-// Per layout, measured: whole matrices run best with one producer warp per
-// consumer group and, with one token block, three ring stages per group
-// (216 KB); the two layouts of experts stored by halves, whose jobs change
-// every few stages, with one producer warp (a lane per group) and two stages
-// per group.  Stage s serves group s % kGroups.
+// Per layout, measured: whole matrices and experts' column halves run best
+// with one producer warp per consumer group and, with one token block, three
+// ring stages per group (216 KB); experts stored by input halves (a 2-D copy
+// per half-unit, a tensor map acquired per half) with one producer warp (a
+// lane per group) and two stages per group.  Stage s serves group s % kGroups.
 template <int MODE>
 __host__ __device__ constexpr int producer_warps() {
-  return MODE == kModeWhole ? kGroups : 1;
+  return MODE == kModeRowHalves ? 1 : kGroups;
 }
 // NARROW (one token block): every job of the launch is 2 bits wide, so a
 // stage's code words take half the bytes and the ring has 12 stages (four per
@@ -61,7 +61,7 @@ __host__ __device__ constexpr int producer_warps() {
 // token blocks a 9-stage narrow ring measured no faster than six stages.)
 template <int TB, int MODE, bool NARROW = false>
 __host__ __device__ constexpr int stages_for() {
-  return MODE != kModeWhole ? 6 : TB == 1 ? (NARROW ? 12 : 9) : 6;
+  return MODE == kModeRowHalves ? 6 : TB == 1 ? (NARROW && MODE == kModeWhole ? 12 : 9) : 6;
 }
 constexpr int kConsumers = kCW * kGroups * 32;
 template <int MODE>
@@ -737,10 +737,12 @@ cudaError_t launch_gemv_device_schedule(const GemvJob* d_jobs, const long long* 
                           : trellis_gemv_kernel<1, kModeRowHalves, true>)
                   : (e4m3 ? trellis_gemv_kernel<1, kModeWhole, false>
                           : trellis_gemv_kernel<1, kModeWhole, true>);
-  const int smem = layout == kGemvWhole ? gemv_smem_bytes<1, kModeWhole>()
-                                        : gemv_smem_bytes<1, kModeColHalves>();
-  const int threads = layout == kGemvWhole ? threads_for<kModeWhole>()
-                                           : threads_for<kModeColHalves>();
+  const int smem = layout == kGemvColHalves   ? gemv_smem_bytes<1, kModeColHalves>()
+                   : layout == kGemvRowHalves ? gemv_smem_bytes<1, kModeRowHalves>()
+                                              : gemv_smem_bytes<1, kModeWhole>();
+  const int threads = layout == kGemvColHalves   ? threads_for<kModeColHalves>()
+                      : layout == kGemvRowHalves ? threads_for<kModeRowHalves>()
+                                                 : threads_for<kModeWhole>();
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   GemvArgs a;
