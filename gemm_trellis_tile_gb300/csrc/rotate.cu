@@ -210,8 +210,12 @@ __global__ void rotate_in_plain_kernel(const uint16_t* x, const float* su, uint1
 //   q    = E4M3(xh * inv), nearest even, saturating  (the product rounded to fp32 first)
 // A row of zeros gives q = 0 and d = 0.  The row's xh waits in shared memory
 // (2K bytes) between the two passes.
-constexpr int kQuantThreads = 128;
-constexpr int kQuantWarps = kQuantThreads / 32;
+// Threads per block: eight warps for long rows, four for short ones (each
+// measured faster in its range).
+constexpr int kQuantThreadsLong = 256;
+constexpr int kQuantThreadsShort = 128;
+constexpr int kQuantLongK = 8192;
+constexpr int kQuantWarpsMax = kQuantThreadsLong / 32;
 constexpr float kE4M3Max = 448.0f;
 
 // Two fp32 values to two E4M3 bytes: `lo` in the low byte.
@@ -221,16 +225,18 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
   return e;
 }
 
-// One block of kQuantThreads per token (16 blocks per SM, so 2048 tokens are
-// one wave).  Warp w takes the pairs of 128-blocks w, w + 4, ...: each lane
-// loads 16 bytes of a pair (half-warp h holds block 2p + h), up to
-// kRotBatch pairs in flight, then the half-warp transforms.
-template <bool ROTATE>
-__global__ void __launch_bounds__(kQuantThreads)
+// One block of THREADS per token (as many blocks per SM as threads and the
+// row's 2K bytes of shared memory allow).  Warp w of W takes the pairs of
+// 128-blocks w, w + W, ...: each lane loads 16 bytes of a pair (half-warp h
+// holds block 2p + h) and their scales, up to kRotBatch pairs in flight, then
+// the half-warp transforms.
+template <bool ROTATE, int THREADS>
+__global__ void __launch_bounds__(THREADS)
     quantize_e4m3_rows_kernel(const uint16_t* x, const float* su, uint8_t* q, float* d, int K,
                               int* cnt, int ncnt) {
   extern __shared__ __align__(16) uint16_t xrow[];
-  __shared__ float part[kQuantWarps];
+  constexpr int kQuantWarps = THREADS / 32;
+  __shared__ float part[kQuantWarpsMax];
   pdl_trigger();  // the GEMM may set up; it waits for this kernel before loading q or d
   clear_counters(cnt, ncnt);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -241,11 +247,19 @@ __global__ void __launch_bounds__(kQuantThreads)
   const int e = 8 * (lane & 15);
   float amax = 0.f;
   for (int p0 = warp; p0 < np; p0 += kQuantWarps * kRotBatch) {
+    // the batch's activations and scales all in flight before the first transform
     uint4 batch[kRotBatch];
+    float4 sc[kRotBatch][2];
 #pragma unroll
     for (int i = 0; i < kRotBatch; ++i) {
       const int b = 2 * (p0 + kQuantWarps * i) + (lane >> 4);
-      batch[i] = b < nb ? *reinterpret_cast<const uint4*>(xr + b * kHad + e) : make_uint4(0, 0, 0, 0);
+      const bool in = b < nb && p0 + kQuantWarps * i < np;
+      batch[i] = in ? *reinterpret_cast<const uint4*>(xr + b * kHad + e) : make_uint4(0, 0, 0, 0);
+      if (ROTATE) {
+        sc[i][0] = in ? *reinterpret_cast<const float4*>(su + b * kHad + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        sc[i][1] = in ? *reinterpret_cast<const float4*>(su + b * kHad + e + 4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
     for (int i = 0; i < kRotBatch; ++i) {
@@ -264,8 +278,8 @@ __global__ void __launch_bounds__(kQuantThreads)
           v[2 * j + 1] = half_bits_to_float(w[j] >> 16);
         }
         if (valid) {
-          const float4 s0 = *reinterpret_cast<const float4*>(su + k0);
-          const float4 s1 = *reinterpret_cast<const float4*>(su + k0 + 4);
+          const float4 s0 = sc[i][0];
+          const float4 s1 = sc[i][1];
           v[0] *= s0.x;
           v[1] *= s0.y;
           v[2] *= s0.z;
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(kQuantThreads)
   const float inv = amax > 0.f ? __fdiv_rn(kE4M3Max, amax) : 0.f;
   if (threadIdx.x == 0) d[m] = amax > 0.f ? __fdiv_rn(amax, kE4M3Max) : 0.f;
   uint8_t* qr = q + (size_t)m * K;
-  for (int k = 16 * threadIdx.x; k < K; k += 16 * kQuantThreads) {
+  for (int k = 16 * threadIdx.x; k < K; k += 16 * THREADS) {
     const uint4 a = *reinterpret_cast<const uint4*>(xrow + k);
     const uint4 b = *reinterpret_cast<const uint4*>(xrow + k + 8);
     const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -443,15 +457,18 @@ size_t quantize_e4m3_smem_bytes(int K) { return (size_t)K * 2; }
 cudaError_t launch_quantize_e4m3_rows(const uint16_t* x, const float* su, uint8_t* q, float* d,
                                       int M, int K, int* cnt, int ncnt, cudaStream_t st) {
   const size_t smem = quantize_e4m3_smem_bytes(K);
-  const void* fn = su ? reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<true>)
-                      : reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<false>);
+  const bool lng = K >= kQuantLongK;
+  const void* fn =
+      su ? (lng ? reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<true, kQuantThreadsLong>)
+                : reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<true, kQuantThreadsShort>))
+         : (lng ? reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<false, kQuantThreadsLong>)
+                : reinterpret_cast<const void*>(quantize_e4m3_rows_kernel<false, kQuantThreadsShort>));
   cudaError_t e = set_smem_limit(fn, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  if (su)
-    quantize_e4m3_rows_kernel<true><<<M, kQuantThreads, smem, st>>>(x, su, q, d, K, cnt, ncnt);
-  else
-    quantize_e4m3_rows_kernel<false><<<M, kQuantThreads, smem, st>>>(x, nullptr, q, d, K, cnt,
-                                                                      ncnt);
+  const int threads = lng ? kQuantThreadsLong : kQuantThreadsShort;
+  void* args[] = {const_cast<uint16_t**>(&x), const_cast<float**>(&su), &q, &d, &K, &cnt, &ncnt};
+  e = cudaLaunchKernel(fn, dim3(M), dim3(threads), args, smem, st);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
