@@ -91,9 +91,15 @@ struct BlockGeom {
 static_assert(BlockGeom<true>::kSmemBytes <= 227 * 1024, "FP8 ring does not fit");
 
 // barrier indices
-constexpr int kBarAFull = 0, kBarAEmpty = 2, kBarCFull = 4, kBarCEmpty = 8, kBarBFull = 12,
-              kBarBEmpty = 15, kBarAcc = 18, kBarTmemFree = 19, kBarDrain = 20, kBarEpi = 21,
-              kNumBars = 22;
+// An activation stage has one full barrier and one empty barrier per 256-row
+// half (index 2 * stage + half): at fp16 the half that accumulators 0 and 1
+// read is refilled as soon as their MMAs are done (17408 -> 5120: 283.5 ->
+// 266.6 us), while the MMA warp still waits once per stage; the FP8 route
+// frees the whole stage at once (splitting measured 1 % slower there).
+constexpr int kBarAFull = 0, kBarAEmpty = 2, kBarCFull = 6, kBarCEmpty = 10, kBarBFull = 14,
+              kBarBEmpty = 17, kBarAcc = 20, kBarTmemFree = 21, kBarDrain = 22, kBarEpi = 23,
+              kNumBars = 24;
+static_assert((kNumBars + 2) * 8 <= 256, "barriers and the TMEM slot fit their 256 bytes");
 
 struct GemmArgs {
   const uint8_t* code;
@@ -434,10 +440,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   const long long u_end = range_start(c + 1, a.units, a.grid);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kAStages; ++s) {
-      mbar_init(bar(kBarAFull + s), 1);
-      mbar_init(bar(kBarAEmpty + s), 1);
-    }
+    for (int s = 0; s < kAStages; ++s) mbar_init(bar(kBarAFull + s), 1);
+    for (int s = 0; s < 2 * kAStages; ++s) mbar_init(bar(kBarAEmpty + s), 1);
     for (int s = 0; s < kCStages; ++s) {
       mbar_init(bar(kBarCFull + s), 1);
       mbar_init(bar(kBarCEmpty + s), kDecWarps);
@@ -479,17 +483,27 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         for (int kb = seg.kb0; kb < seg.kb1; ++kb, ra.advance()) {
           const int s = ra.stage;
           const uint32_t ph = ra.phase;
-          if (!mbar_wait(bar(kBarAEmpty + s), ph ^ 1u, a.limit_ns)) {
+          // fp16: each half has its own empty barrier; FP8: the second half's
+          // barrier frees the whole stage (the first is not used)
+          if (!mbar_wait(bar(kBarAEmpty + 2 * s + (FP8 ? 1 : 0)), ph ^ 1u, a.limit_ns)) {
             set_error(a.err, kDevErrTimeout);
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(bar(kBarAFull + s), kABytes);
+          armed[s] = static_cast<int>(ph);
           const uint32_t dst = base + s * kABytes;
           tma_load_2d_hint(dst, &tmap_a, kb * G::kKE, m0, bar(kBarAFull + s), keep);
+          // On a timeout the second half is still loaded (the result is
+          // flagged as wrong), so that the stage's full barrier completes and
+          // the drain below can wait for every copy in flight.
+          if (!FP8 && !mbar_wait(bar(kBarAEmpty + 2 * s + 1), ph ^ 1u, a.limit_ns)) {
+            set_error(a.err, kDevErrTimeout);
+            ok = false;
+          }
           tma_load_2d_hint(dst + kABytes / 2, &tmap_a, kb * G::kKE, m0 + kBM / 2,
                            bar(kBarAFull + s), keep);
-          armed[s] = static_cast<int>(ph);
+          if (!ok) break;
         }
       }
       if (!ok)
@@ -578,8 +592,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                 else
                   mma_f16(tmem_base + acc * kBN, ad, bd, kIdesc, accum);
               }
+              // accumulators 0 and 1 read the stage's first 256 rows (fp16:
+              // that half is freed here)
+              if (!FP8 && acc == 1) mma_commit(bar(kBarAEmpty + 2 * sa));
             }
-            mma_commit(bar(kBarAEmpty + sa));
+            mma_commit(bar(kBarAEmpty + 2 * sa + 1));
             mma_commit(bar(kBarBEmpty + sb));
           }
           __syncwarp();
