@@ -17,7 +17,8 @@
 // Warp roles (19 warps):
 //   warp 0      A producer: TMA tiled loads of the 512 x 64 activation block
 //               (two 256-row boxes, 128B swizzle, rows past M zero-filled)
-//               into a 2-stage ring.
+//               into a 2-stage ring; at fp16 each box is reloaded as soon as
+//               the two accumulators that read it are done.
 //   warp 1      code producer: 1-D bulk copies of the block's 4 x 8 code tiles
 //               into a 4-stage ring.
 //   warp 2      owns TMEM; the whole warp walks the MMA loop (its waits and
