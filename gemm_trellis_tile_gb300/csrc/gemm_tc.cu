@@ -30,9 +30,11 @@
 //   warps 3-18  decoders: two tiles per warp per block, decoded in registers
 //               and stored as fp16 pairs into the canonical K-major 128B-swizzled
 //               B layout (3-stage ring); then, per tile, the epilogue: the
-//               128-point Hadamard over each row is done in registers (two
-//               64-point halves written back to TMEM, then the last stage),
-//               * sv, fp16 stores -- or the raw fp32 partial sums.
+//               128-point Hadamard over each row (the last two stages across
+//               the four 32-column chunks through TMEM, then each chunk in
+//               registers), * sv, fp16 stores -- or the raw fp32 partial sums.
+//               fp16: the next segment's first two blocks are decoded before
+//               the epilogue, and each warp frees TMEM after its last read.
 // Every mbarrier wait is bounded; a wait that runs out sets the error word and
 // the CTA unwinds (TMEM is always released, in-flight copies are drained).
 // The kernel is launched as a programmatic dependent of the input rotation:
@@ -87,9 +89,16 @@ struct BlockGeom {
   static constexpr int kOffC = kOffB + kBStages * kBBytes;
   static constexpr int kOffBar = kOffC + kCStages * kCBytes;
   static constexpr int kOffSv = kOffBar + 256;  // per decoder warp: the tile's 128 output scales
-  static constexpr int kSmemBytes = kOffSv + kDecWarps * kBN * 4 + 1024;  // + alignment slack
+  // fp16: each decoder warp stages its output rows in a 1 KB slot of its own,
+  // so the decoded-B ring stays free during an epilogue and the decoders fill
+  // kLookahead blocks of the next segment before it.  FP8 (no room) stages
+  // them in the ring, which is idle during its epilogues.
+  static constexpr int kOffScr = kOffSv + kDecWarps * kBN * 4;
+  static constexpr int kLookahead = FP8 ? 0 : 2;
+  static constexpr int kSmemBytes = kOffScr + (FP8 ? 0 : kDecWarps * 1024) + 1024;  // + slack
 };
 static_assert(BlockGeom<true>::kSmemBytes <= 227 * 1024, "FP8 ring does not fit");
+static_assert(BlockGeom<false>::kSmemBytes <= 227 * 1024, "fp16 ring does not fit");
 
 // barrier indices
 // An activation stage has one full barrier and one empty barrier per 256-row
@@ -626,10 +635,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     Ring<kCStages> rc;
     Ring<kBStages> rb;
     int nseg = 0;
-    while (ok && it.next(seg)) {
-      const int nb = seg.tile % a.n_blocks;
-      const int m0 = (seg.tile / a.n_blocks) * kBM;
-      for (int kb = seg.kb0; kb < seg.kb1; ++kb, rc.advance(), rb.advance()) {
+    // Decode the next code stage into the next decoded-B stage.
+    auto decode_block = [&]() -> bool {
         const int sc = rc.stage;
         const uint32_t pc = rc.phase;
         const int sb = rb.stage;
@@ -637,8 +644,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         if (!mbar_wait(bar(kBarCFull + sc), pc, a.limit_ns) ||
             !mbar_wait(bar(kBarBEmpty + sb), pb ^ 1u, a.limit_ns)) {
           set_error(a.err, kDevErrTimeout);
-          ok = false;
-          break;
+          return false;
         }
         const uint8_t* codes = smem + G::kOffC + sc * G::kCBytes;
         uint8_t* bt = smem + kOffB + sb * kBBytes;
@@ -691,6 +697,35 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         if (lane == 0) {
           mbar_arrive(bar(kBarBFull + sb));
           mbar_arrive(bar(kBarCEmpty + sc));
+        }
+        return true;
+    };
+    int pre = 0;  // K blocks of the current segment decoded ahead of its loop
+    while (ok && it.next(seg)) {
+      const int nb = seg.tile % a.n_blocks;
+      const int m0 = (seg.tile / a.n_blocks) * kBM;
+      for (int kb = seg.kb0 + pre; kb < seg.kb1; ++kb, rc.advance(), rb.advance()) {
+        if (!decode_block()) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+      // fp16: the next segment's first blocks are decoded while this one's
+      // last MMAs run (their ring stages free up as those MMAs complete), so
+      // that the MMA warp finds them ready once the epilogue frees TMEM.
+      pre = 0;
+      if (G::kLookahead > 0) {
+        SegIter peek = it;
+        Segment nx;
+        if (peek.next(nx)) {
+          const int la = min(G::kLookahead, nx.kb1 - nx.kb0);
+          for (; pre < la; ++pre, rc.advance(), rb.advance()) {
+            if (!decode_block()) {
+              ok = false;
+              break;
+            }
+          }
         }
       }
       if (!ok) break;
@@ -753,6 +788,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             is_last = atomicAdd(cnt, 1) == others;
           }
           is_last = __shfl_sync(0xFFFFFFFFu, is_last, 0);
+          if (G::kLookahead > 0 && !is_last) {
+            // fp16: this warp is done with TMEM for the segment
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarTmemFree));
+          }
         }
         if (is_last && lane == 0) __threadfence();  // every other partial is visible
         __syncwarp();
@@ -822,18 +863,27 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         tmem_wait_st();
         // Index bits 0..4 on each chunk in registers, * sv / sqrt(128), fp16:
         // each lane then holds 64 contiguous bytes of its row.  They go out
-        // through this warp's 2 KB slot of the decoded-B ring (idle during the
-        // epilogue: every MMA of the segment has completed, and no decoder
-        // writes it again before all have passed the barrier below), read
-        // back so that four lanes store one row's 64 bytes: eight rows per
-        // store instruction instead of 32 scattered 16-byte pieces.
-        uint8_t* scr = smem + kOffB + dw * 2048;
+        // through a shared-memory slot of this warp and are read back so that
+        // several lanes store each row's bytes together instead of 32 lanes
+        // writing scattered 16-byte pieces.  fp16: the warp's own 1 KB slot,
+        // 16 rows at a time (two lanes per row, 32 contiguous bytes each),
+        // with TMEM freed as soon as the last chunk is read.  FP8: 2 KB of the
+        // decoded-B ring (idle during the epilogue: every MMA of the segment
+        // has completed, and no decoder writes it again before all have passed
+        // the barrier below), 32 rows at a time (four lanes per row).
+        constexpr bool kOwnSlot = G::kLookahead > 0;
+        uint8_t* scr = kOwnSlot ? smem + G::kOffScr + dw * 1024 : smem + kOffB + dw * 2048;
         const int qj = lane & 3, qb = lane & ~3;
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
           float w[32];
           tmem_ld32(tl + 32 * q, w);
           tmem_wait_ld();
+          if (kOwnSlot && q == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarTmemFree));
+          }
           fwht32_regs(w);
           const float* scv = svs + 32 * q;
           uint32_t pk[16];
@@ -846,35 +896,65 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             const __half2 h = __floats2half2_rn(o0, o1);
             pk[e] = *reinterpret_cast<const uint32_t*>(&h);
           }
-          // row `lane`, 16-byte piece p at chunk p ^ ((lane >> 1) & 3): conflict-free
+          if (kOwnSlot) {
 #pragma unroll
-          for (int p = 0; p < 4; ++p)
-            *reinterpret_cast<uint4*>(scr + lane * 64 + 16 * (p ^ ((lane >> 1) & 3))) =
-                make_uint4(pk[4 * p], pk[4 * p + 1], pk[4 * p + 2], pk[4 * p + 3]);
-          __syncwarp();
+            for (int hr = 0; hr < 2; ++hr) {
+              // rows 16 hr .. 16 hr + 15: row lane & 15 written by lane
+              // 16 hr + (lane & 15), 16-byte piece p at chunk p ^ ((row >> 1) & 3)
+              if ((lane >> 4) == hr) {
+                const int lr = lane & 15;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = qb + i;  // this warp's row written by the lane's quad
-            const uint4 v = *reinterpret_cast<const uint4*>(scr + r * 64 + 16 * (qj ^ ((r >> 1) & 3)));
-            const int mr = m0 + acc * 128 + quad * 32 + r;
-            if (mr < a.M)
-              *reinterpret_cast<uint4*>(a.y + (size_t)mr * a.N + n0 + 32 * q + 8 * qj) = v;
+                for (int p = 0; p < 4; ++p)
+                  *reinterpret_cast<uint4*>(scr + lr * 64 + 16 * (p ^ ((lr >> 1) & 3))) =
+                      make_uint4(pk[4 * p], pk[4 * p + 1], pk[4 * p + 2], pk[4 * p + 3]);
+              }
+              __syncwarp();
+              const int lr = lane >> 1, hf = lane & 1;
+              const int mr = m0 + acc * 128 + quad * 32 + 16 * hr + lr;
+#pragma unroll
+              for (int jj = 0; jj < 2; ++jj) {
+                const int p = 2 * jj + hf;  // lanes 2lr, 2lr+1: 32 contiguous bytes
+                const uint4 v =
+                    *reinterpret_cast<const uint4*>(scr + lr * 64 + 16 * (p ^ ((lr >> 1) & 3)));
+                if (mr < a.M)
+                  *reinterpret_cast<uint4*>(a.y + (size_t)mr * a.N + n0 + 32 * q + 8 * p) = v;
+              }
+              __syncwarp();
+            }
+          } else {
+            // row `lane`, 16-byte piece p at chunk p ^ ((lane >> 1) & 3): conflict-free
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+              *reinterpret_cast<uint4*>(scr + lane * 64 + 16 * (p ^ ((lane >> 1) & 3))) =
+                  make_uint4(pk[4 * p], pk[4 * p + 1], pk[4 * p + 2], pk[4 * p + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = qb + i;  // this warp's row written by the lane's quad
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(scr + r * 64 + 16 * (qj ^ ((r >> 1) & 3)));
+              const int mr = m0 + acc * 128 + quad * 32 + r;
+              if (mr < a.M)
+                *reinterpret_cast<uint4*>(a.y + (size_t)mr * a.N + n0 + 32 * q + 8 * qj) = v;
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
-      // no decoder writes the decoded-B ring (used above as scratch) before
-      // every decoder warp has finished this epilogue (a bounded wait: a warp
-      // that gave up earlier never arrives)
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarEpi));
-      if (!mbar_wait(bar(kBarEpi), nseg & 1, a.limit_ns)) {
-        set_error(a.err, kDevErrTimeout);
-        ok = false;
+      if (G::kLookahead == 0) {
+        // FP8: no decoder writes the decoded-B ring (used above as scratch)
+        // before every decoder warp has finished this epilogue (a bounded
+        // wait: a warp that gave up earlier never arrives); then TMEM is free
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarEpi));
+        if (!mbar_wait(bar(kBarEpi), nseg & 1, a.limit_ns)) {
+          set_error(a.err, kDevErrTimeout);
+          ok = false;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarTmemFree));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarTmemFree));
       ++nseg;
     }
   }
