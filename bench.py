@@ -68,9 +68,9 @@ GEMV_TRAFFIC_BYTES = {
 }
 # The same for one prefill GEMM launch (the trellis_gemm kernel alone).
 PREFILL_TRAFFIC_BYTES = {
-    "prefill GEMM 5120x17408 3-bit, M=2048 tokens": 121.50e6,
+    "prefill GEMM 5120x17408 3-bit, M=2048 tokens": 125.26e6,
     "prefill GEMM 5120x17408 3-bit, M=2048 tokens, FP8 tensor cores (E4M3 weights, "
-    "per-token E4M3 activations)": 103.66e6,
+    "per-token E4M3 activations)": 103.69e6,
 }
 
 
