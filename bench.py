@@ -766,6 +766,21 @@ def prefill_spec(args):
     return workload_spec(pa)
 
 
+def tensor_peak(peaks, src, region_s, steps, fp8):
+    """The tensor peak a prefill region is compared with, and its note.  A
+    timed region of SUSTAINED_REGION_S or more runs the GEMM back to back
+    under the power cap: the sustained bf16 peak; a shorter one: the burst
+    peak.  fp16 has the bf16 nominal rate; E4M3 twice it (4.5 : 2.25 PFLOP/s)."""
+    key = "bf16_tflops_sustained" if region_s >= SUSTAINED_REGION_S else "bf16_tflops"
+    peak = float(peaks[key])
+    if fp8:
+        return 2.0 * peak, (src + " (MEASURED_PEAKS.json %s x 2, the nominal dense E4M3 : bf16 "
+                            "ratio 4.5 : 2.25 PFLOP/s; the %s-step region lasts %.2f s)"
+                            % (key, steps, region_s))
+    return peak, (src + " (MEASURED_PEAKS.json %s: the %s-step region lasts %.2f s; fp16 has "
+                  "the same nominal dense rate)" % (key, steps, region_s))
+
+
 def measure_prefill(args, spec, rep, dev, m, want_cpu):
     """Prefill GEMM of `spec` at m tokens: TFLOP/s of 2*m*in*out per step (median
     over repeats of the K-step region), its roofline against the tensor peak,
@@ -836,19 +851,7 @@ def measure_prefill(args, spec, rep, dev, m, want_cpu):
         if lin.check() != 0:
             raise SystemExit("device error flag set")
     peaks, src = measured_peaks()
-    # A timed region of a second or more runs the GEMM back to back under the
-    # power cap: it is compared with the sustained peak, a shorter one with
-    # the burst peak.
-    sustained = ms / 1e3 >= SUSTAINED_REGION_S
-    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
-    peak = float(peaks[key])
-    peak_note = (src + " (MEASURED_PEAKS.json %s: the %s-step region lasts %.2f s; fp16 has "
-                 "the same nominal dense rate)" % (key, args.steps, ms / 1e3))
-    if fp8:
-        peak *= 2.0
-        peak_note = (src + " (MEASURED_PEAKS.json %s x 2, the nominal dense E4M3 : bf16 ratio "
-                     "4.5 : 2.25 PFLOP/s; the %s-step region lasts %.2f s)"
-                     % (key, args.steps, ms / 1e3))
+    peak, peak_note = tensor_peak(peaks, src, ms / 1e3, args.steps, fp8)
     world = rep.world
     out = {
         "workload": spec["name"], "metric": METRIC_PREFILL,

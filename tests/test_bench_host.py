@@ -94,3 +94,15 @@ def test_both_arms_print_one_metric_string_per_kind():
     import re
     vals = re.findall(r'"metric": ([A-Za-z_"][^,]*),', src)
     assert vals and set(vals) <= {"METRIC_DECODE", "METRIC_PREFILL", "METRIC_ENCODE"}
+
+
+def test_prefill_peak_is_sustained_for_long_regions():
+    """A region of half a second or more is compared with the sustained tensor
+    peak, a shorter one with the burst peak; E4M3 doubles either."""
+    import bench
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    assert bench.tensor_peak(peaks, "measured", 1.2, 4000, False)[0] == 1700.0
+    assert bench.tensor_peak(peaks, "measured", 0.006, 20, False)[0] == 1900.0
+    assert bench.tensor_peak(peaks, "measured", 1.2, 4000, True)[0] == 3400.0
+    peak, note = bench.tensor_peak(peaks, "measured", 0.006, 20, True)
+    assert peak == 3800.0 and "bf16_tflops x 2" in note
